@@ -1,0 +1,430 @@
+/*
+ * flashloop_oracle.c -- plain CPU oracle of the FlashLoop lazy loop step.
+ *
+ * TEST INFRASTRUCTURE, not product code. Only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg load this file. It shares no
+ * source, header, table or helper with the CUDA library, and it includes
+ * nothing from it.
+ *
+ * Method source: the rit.work page "FlashLoop: Fast and Memory-Efficient
+ * Looped Transformers via Lazy Updates" (a summary of the Yang & Liu
+ * preprint), in particular
+ *   [P2-late]  section "Later loops change only part of the state"
+ *              (each loop has its own KV cache; few tokens keep changing and
+ *              the active group narrows and nests; a small stable key group
+ *              drives the loop-to-loop change of attention; neighbouring KV
+ *              sets differ less than whole states, so base + small deltas);
+ *   [P2-three] section "FlashLoop combines three kinds of saving"
+ *              (dense early loops; rank tokens by how much their hidden
+ *              state changed and recompute only the active ones, the rest
+ *              reuse state and KV entries; choose keys from the previous
+ *              loop's statistics and keep the selected group's total
+ *              probability mass; KV cache = compressed base + a sequence of
+ *              compressed deltas, a low-bit delta for active tokens and no
+ *              entry for inactive ones, 4-bit deltas).
+ * Where the page leaves a step open, the plain readings used here are:
+ *   R1  previous-loop probability of row i, key j:
+ *       p_ij = exp(qhat_i . krec_j / sqrt(d) - Z_i) with the row's last
+ *       query qhat_i and log-normaliser Z_i (state that persists).
+ *   R2  one key set S per (sequence, head), ranked by column mass c_j.
+ *   R3  causal: S_i = {j in S : j <= i}; a row with S_i empty (or whose
+ *       old mass m_i is below FLT_MIN) keeps its O, Z and qhat.
+ *   R4  attention reads the reconstructed cache: base + dequantised deltas
+ *       in ascending loop order, fp32, rounded RNE to bf16.
+ *   R6  quantiser: symmetric int4 codes in [-7, 7], one fp16 scale per 32
+ *       contiguous elements, scale = fp16_rne(amax / 7) (fp32 divide),
+ *       code = rint_even(delta / scale) clamped to +-7, zero scale -> zero
+ *       codes; element 2t in the low nibble of byte t.
+ *   R7  R = ceil(r N), K = ceil(k N), clamped to [1, N]; ties in every
+ *       ranking go to the lower index; index lists ascending.
+ * Build with gcc -O2 -ffp-contract=off so every fp32 expression rounds
+ * exactly as written. Attention and norms accumulate in double.
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ */
+/* number formats (IEEE 754 binary16 and bfloat16, round to nearest even) */
+
+float orc_bf16_to_f32(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+uint16_t orc_f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (uint16_t)((u >> 16) | 0x40u); /* quiet NaN */
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+float orc_f16_to_f32(uint16_t h) {
+    uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+    uint32_t e = (h >> 10) & 0x1Fu, m = h & 0x3FFu;
+    float f;
+    if (e == 0) {               /* zero or subnormal: m * 2^-24 */
+        f = (float)m * 5.9604644775390625e-8f;
+        return sign ? -f : f;
+    }
+    uint32_t u;
+    if (e == 31) u = sign | 0x7F800000u | (m << 13);
+    else u = sign | ((e - 15u + 127u) << 23) | (m << 13);
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+uint16_t orc_f32_to_f16(float f) {
+    uint32_t x;
+    memcpy(&x, &f, 4);
+    uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    uint32_t ax = x & 0x7FFFFFFFu;
+    if (ax > 0x7F800000u) return sign | 0x7E00u;          /* NaN */
+    if (ax >= 0x477FF000u) return sign | 0x7C00u;         /* >= 65520 rounds to inf */
+    if (ax < 0x38800000u) {                               /* below 2^-14: subnormal */
+        float v;
+        memcpy(&v, &ax, 4);
+        double q = nearbyint((double)v * 16777216.0);     /* units of 2^-24, ties to even */
+        return (uint16_t)(sign | (uint16_t)q);
+    }
+    uint32_t e = (ax >> 23) - 127u + 15u;
+    uint32_t m = ax & 0x7FFFFFu;
+    uint32_t h = (e << 10) | (m >> 13);
+    uint32_t rem = m & 0x1FFFu;
+    if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) h += 1u;
+    return (uint16_t)(sign | h);
+}
+
+/* ------------------------------------------------------------------ */
+/* [P2-three] "rank tokens by how much their hidden states changed":
+ * score_i = || h_cur_i - h_prev_i ||_2^2 over the D hidden features.
+ * Ranking by the square is ranking by the norm. Exact up to double rounding. */
+void orc_token_scores(const uint16_t *h_prev, const uint16_t *h_cur,
+                      int64_t B, int64_t N, int64_t D, double *score) {
+#pragma omp parallel for schedule(static)
+    for (int64_t row = 0; row < B * N; ++row) {
+        const uint16_t *a = h_prev + row * D, *b = h_cur + row * D;
+        double s = 0.0;
+        for (int64_t x = 0; x < D; ++x) {
+            double dx = (double)orc_bf16_to_f32(b[x]) - (double)orc_bf16_to_f32(a[x]);
+            s += dx * dx;
+        }
+        score[row] = s;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* [P2-three] keep the top-k of a ranking (tokens by change, keys by the
+ * previous loop's column statistics). R7: ties go to the lower index; the
+ * kept indices are returned in ascending order. Plain sort, row by row. */
+typedef struct { double s; int32_t i; } orc_item;
+
+static int orc_by_score_desc(const void *pa, const void *pb) {
+    const orc_item *a = (const orc_item *)pa, *b = (const orc_item *)pb;
+    if (a->s > b->s) return -1;
+    if (a->s < b->s) return 1;
+    return (a->i > b->i) - (a->i < b->i);
+}
+
+static int orc_by_i32(const void *pa, const void *pb) {
+    int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    return (a > b) - (a < b);
+}
+
+void orc_topk_rows(const double *score, int64_t rows, int64_t n, int64_t k, int32_t *out) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < rows; ++r) {
+        orc_item *it = (orc_item *)malloc(sizeof(orc_item) * (size_t)n);
+        for (int64_t j = 0; j < n; ++j) { it[j].s = score[r * n + j]; it[j].i = (int32_t)j; }
+        qsort(it, (size_t)n, sizeof(orc_item), orc_by_score_desc);
+        int32_t *o = out + r * k;
+        for (int64_t t = 0; t < k; ++t) o[t] = it[t].i;
+        qsort(o, (size_t)k, sizeof(int32_t), orc_by_i32);
+        free(it);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* KV cache as [P2-three] describes it: a base plus a sequence of deltas.
+ * A delta layer holds, per sequence b, `cnt` entries with ascending token
+ * indices idx[b][e], int4 codes [b][e][h][d/2] and fp16 scales [b][e][h][d/32]. */
+typedef struct {
+    const int32_t *idx;
+    const uint8_t *codes;
+    const uint16_t *scales;
+    int64_t cnt;
+} orc_layer;
+
+static int64_t orc_find(const int32_t *idx, int64_t cnt, int64_t j) {
+    int64_t lo = 0, hi = cnt - 1;
+    while (lo <= hi) {
+        int64_t mid = (lo + hi) / 2;
+        if (idx[mid] == j) return mid;
+        if (idx[mid] < j) lo = mid + 1; else hi = mid - 1;
+    }
+    return -1;
+}
+
+static int orc_code(const uint8_t *codes, int64_t x) {
+    uint8_t byte = codes[x / 2];
+    int v = (x & 1) ? (byte >> 4) : (byte & 0xF);
+    return v >= 8 ? v - 16 : v;
+}
+
+/* R4: fp32 reconstruction of token j, head h: base, then each delta layer
+ * in ascending order that holds an entry for j adds scale * code. */
+static void orc_recon(const uint16_t *base, int64_t Nk, int64_t H, int64_t d,
+                      const orc_layer *L, int nl, int64_t b, int64_t j, int64_t h, float *out) {
+    const uint16_t *src = base + ((b * Nk + j) * H + h) * d;
+    for (int64_t x = 0; x < d; ++x) out[x] = orc_bf16_to_f32(src[x]);
+    for (int m = 0; m < nl; ++m) {
+        int64_t e = orc_find(L[m].idx + b * L[m].cnt, L[m].cnt, j);
+        if (e < 0) continue;
+        const uint8_t *cd = L[m].codes + ((b * L[m].cnt + e) * H + h) * (d / 2);
+        const uint16_t *sc = L[m].scales + ((b * L[m].cnt + e) * H + h) * (d / 32);
+        for (int64_t x = 0; x < d; ++x) {
+            float s = orc_f16_to_f32(sc[x / 32]);
+            float t = s * (float)orc_code(cd, x);
+            out[x] = out[x] + t;
+        }
+    }
+}
+
+static void orc_pack_layers(orc_layer *L, int nl, const int32_t *const *idx,
+                            const uint8_t *const *codes, const uint16_t *const *scales,
+                            const int64_t *cnt) {
+    for (int m = 0; m < nl; ++m) {
+        L[m].idx = idx[m]; L[m].codes = codes[m]; L[m].scales = scales[m]; L[m].cnt = cnt[m];
+    }
+}
+
+/* R6 applied to one group of 32 fp32 deltas. */
+static void orc_quant_group(const float *delta, uint16_t *scale_out, int *q) {
+    float amax = 0.0f;
+    for (int e = 0; e < 32; ++e) {
+        float a = fabsf(delta[e]);
+        if (a > amax) amax = a;
+    }
+    float sf = amax / 7.0f;
+    uint16_t sh = orc_f32_to_f16(sf);
+    float s = orc_f16_to_f32(sh);
+    *scale_out = sh;
+    for (int e = 0; e < 32; ++e) {
+        int v = 0;
+        if (s > 0.0f) {
+            float t = delta[e] / s;
+            v = (int)nearbyintf(t);
+            if (v > 7) v = 7;
+            if (v < -7) v = -7;
+        }
+        q[e] = v;
+    }
+}
+
+/* [P2-three] "for tokens that stay active, write the low-bit difference
+ * from the previous state; inactive tokens get no new entry"; 4-bit deltas.
+ * For every active token i of sequence b and every head, the delta of the
+ * loop-l tensor x_l against the previous loop's reconstruction is quantised
+ * per 32-element group (R6). Writes the new layer's entries in the order of
+ * `active` (ascending). `x_l` and `base` are [B,Nk,H,d] bf16. */
+void orc_kv_delta_append(const uint16_t *x_l, const uint16_t *base,
+                         int nl, const int32_t *const *idx, const uint8_t *const *codes,
+                         const uint16_t *const *scales, const int64_t *cnt,
+                         int64_t B, int64_t Nk, int64_t H, int64_t d,
+                         const int32_t *active, int64_t R,
+                         int32_t *out_idx, uint8_t *out_codes, uint16_t *out_scales) {
+    orc_layer L[64];
+    orc_pack_layers(L, nl, idx, codes, scales, cnt);
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t e = 0; e < R; ++e) {
+            int64_t i = active[b * R + e];
+            out_idx[b * R + e] = (int32_t)i;
+            float rec[512], delta[512];
+            int q[32];
+            for (int64_t h = 0; h < H; ++h) {
+                orc_recon(base, Nk, H, d, L, nl, b, i, h, rec);
+                const uint16_t *src = x_l + ((b * Nk + i) * H + h) * d;
+                for (int64_t x = 0; x < d; ++x) delta[x] = orc_bf16_to_f32(src[x]) - rec[x];
+                uint8_t *cd = out_codes + ((b * R + e) * H + h) * (d / 2);
+                uint16_t *sc = out_scales + ((b * R + e) * H + h) * (d / 32);
+                for (int64_t g = 0; g < d / 32; ++g) {
+                    orc_quant_group(delta + g * 32, &sc[g], q);
+                    for (int t = 0; t < 16; ++t)
+                        cd[g * 16 + t] = (uint8_t)((q[2 * t] & 0xF) | ((q[2 * t + 1] & 0xF) << 4));
+                }
+            }
+        }
+    }
+}
+
+/* R4: reconstruct every token of the cache (base + `nl` delta layers) as
+ * fp32 (out_f32, may be NULL) and rounded RNE to bf16 (out_bf16, may be NULL). */
+void orc_reconstruct(const uint16_t *base, int nl, const int32_t *const *idx,
+                     const uint8_t *const *codes, const uint16_t *const *scales, const int64_t *cnt,
+                     int64_t B, int64_t Nk, int64_t H, int64_t d,
+                     float *out_f32, uint16_t *out_bf16) {
+    orc_layer L[64];
+    orc_pack_layers(L, nl, idx, codes, scales, cnt);
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t j = 0; j < Nk; ++j) {
+            float rec[512];
+            for (int64_t h = 0; h < H; ++h) {
+                orc_recon(base, Nk, H, d, L, nl, b, j, h, rec);
+                int64_t off = ((b * Nk + j) * H + h) * d;
+                for (int64_t x = 0; x < d; ++x) {
+                    if (out_f32) out_f32[off + x] = rec[x];
+                    if (out_bf16) out_bf16[off + x] = orc_f32_to_bf16(rec[x]);
+                }
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* [P2-three] lazy attention with preserved probability mass, in double.
+ *
+ * For each sequence b, head h, and row r (key position pos_i, state slot s):
+ *   S_i   = {j in S[b,h] : j <= pos_i}                       (R3)
+ *   p_j   = exp(qhat_s . kold_j / sqrt(d) - Z_s)             (R1)
+ *   m     = sum_{S_i} p_j,   u = sum_{S_i} p_j vold_j
+ *   tau_j = q_s . knew_j / sqrt(d),  lam = logsumexp_{S_i} tau
+ *   w     = sum_{S_i} exp(tau_j - lam) vnew_j
+ *   O_s  <- O_s - u + m w,  Z_s <- lam - ln m,  qhat_s <- q_s
+ *   c_j  += m exp(tau_j - lam) - p_j                         (column mass)
+ * so the selected keys keep the old total mass m instead of being
+ * renormalised to one. `first` is the first dense loop: no previous state,
+ * m := 1, u := 0, p := 0, and c is overwritten rather than updated.
+ * Rows are processed per (b, h) independently; `bh_mask` (may be NULL)
+ * restricts the work to a subset of (b, h) pairs.
+ * Shapes: q, qhat [B,Ns,H,d] bf16; o [B,Ns,H,d] f32; z [B,H,Ns] f32;
+ * c [B,H,Nk] f32; S [B,H,K] i32; k/v old/new [B,Nk,H,d] bf16;
+ * pos, slot [B,R] i32; m_out [B,H,R] double (may be NULL; NaN when skipped). */
+void orc_attention(int first, int64_t B, int64_t H, int64_t d, int64_t Nk, int64_t Ns,
+                   int64_t R, const int32_t *pos, const int32_t *slot,
+                   const uint16_t *q, uint16_t *qhat, float *o, float *z, float *c,
+                   int64_t K, const int32_t *S,
+                   const uint16_t *k_old, const uint16_t *v_old,
+                   const uint16_t *k_new, const uint16_t *v_new,
+                   const uint8_t *bh_mask, double *m_out) {
+    const double inv_sqrt_d = 1.0 / sqrt((double)d);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t h = 0; h < H; ++h) {
+            if (bh_mask && !bh_mask[b * H + h]) continue;
+            const int32_t *Sb = S + (b * H + h) * K;
+            double *dc = (double *)calloc((size_t)K, sizeof(double));
+            double *p = (double *)malloc(sizeof(double) * (size_t)K);
+            double *tau = (double *)malloc(sizeof(double) * (size_t)K);
+            double *u = (double *)malloc(sizeof(double) * (size_t)d);
+            double *w = (double *)malloc(sizeof(double) * (size_t)d);
+            for (int64_t r = 0; r < R; ++r) {
+                int64_t i = pos[b * R + r], s = slot[b * R + r];
+                if (m_out) m_out[(b * H + h) * R + r] = NAN;
+                int64_t ns = 0;                     /* |S_i|: S is ascending */
+                while (ns < K && Sb[ns] <= i) ++ns;
+                if (ns == 0) continue;
+                const uint16_t *qs = q + ((b * Ns + s) * H + h) * d;
+                const uint16_t *qh = qhat + ((b * Ns + s) * H + h) * d;
+                float *os = o + ((b * Ns + s) * H + h) * d;
+                float *zs = z + (b * H + h) * Ns + s;
+                double m = 0.0;
+                for (int64_t x = 0; x < d; ++x) u[x] = 0.0;
+                if (first) {
+                    m = 1.0;
+                    for (int64_t t = 0; t < ns; ++t) p[t] = 0.0;
+                } else {
+                    for (int64_t t = 0; t < ns; ++t) {
+                        int64_t j = Sb[t];
+                        const uint16_t *kj = k_old + ((b * Nk + j) * H + h) * d;
+                        const uint16_t *vj = v_old + ((b * Nk + j) * H + h) * d;
+                        double dot = 0.0;
+                        for (int64_t x = 0; x < d; ++x)
+                            dot += (double)orc_bf16_to_f32(qh[x]) * (double)orc_bf16_to_f32(kj[x]);
+                        p[t] = exp(dot * inv_sqrt_d - (double)*zs);
+                        m += p[t];
+                        for (int64_t x = 0; x < d; ++x) u[x] += p[t] * (double)orc_bf16_to_f32(vj[x]);
+                    }
+                    if (!(m >= (double)FLT_MIN)) continue;     /* R3: old mass underflowed */
+                }
+                double mx = -INFINITY;
+                for (int64_t t = 0; t < ns; ++t) {
+                    int64_t j = Sb[t];
+                    const uint16_t *kj = k_new + ((b * Nk + j) * H + h) * d;
+                    double dot = 0.0;
+                    for (int64_t x = 0; x < d; ++x)
+                        dot += (double)orc_bf16_to_f32(qs[x]) * (double)orc_bf16_to_f32(kj[x]);
+                    tau[t] = dot * inv_sqrt_d;
+                    if (tau[t] > mx) mx = tau[t];
+                }
+                double sum = 0.0;
+                for (int64_t t = 0; t < ns; ++t) sum += exp(tau[t] - mx);
+                double lam = mx + log(sum);
+                for (int64_t x = 0; x < d; ++x) w[x] = 0.0;
+                for (int64_t t = 0; t < ns; ++t) {
+                    int64_t j = Sb[t];
+                    const uint16_t *vj = v_new + ((b * Nk + j) * H + h) * d;
+                    double a = exp(tau[t] - lam);
+                    for (int64_t x = 0; x < d; ++x) w[x] += a * (double)orc_bf16_to_f32(vj[x]);
+                    dc[t] += m * a - p[t];
+                }
+                for (int64_t x = 0; x < d; ++x) {
+                    double prev = first ? 0.0 : (double)os[x];
+                    os[x] = (float)(prev - u[x] + m * w[x]);
+                }
+                *zs = (float)(lam - log(m));
+                uint16_t *qw = qhat + ((b * Ns + s) * H + h) * d;
+                for (int64_t x = 0; x < d; ++x) qw[x] = qs[x];
+                if (m_out) m_out[(b * H + h) * R + r] = m;
+            }
+            float *cb = c + (b * H + h) * Nk;
+            if (first) for (int64_t j = 0; j < Nk; ++j) cb[j] = 0.0f;
+            for (int64_t t = 0; t < K; ++t) cb[Sb[t]] = (float)((double)cb[Sb[t]] + dc[t]);
+            free(dc); free(p); free(tau); free(u); free(w);
+        }
+    }
+}
+
+/* Textbook causal softmax attention in double (used to pin the lazy
+ * attention above in its full-set special case). q,k,v [B,N,H,d] bf16;
+ * o [B,N,H,d] double; lse [B,H,N] double. */
+void orc_softmax_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                           int64_t B, int64_t N, int64_t H, int64_t d, double *o, double *lse) {
+    const double sc = 1.0 / sqrt((double)d);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t h = 0; h < H; ++h) {
+            double *lg = (double *)malloc(sizeof(double) * (size_t)N);
+            for (int64_t i = 0; i < N; ++i) {
+                const uint16_t *qi = q + ((b * N + i) * H + h) * d;
+                double mx = -INFINITY;
+                for (int64_t j = 0; j <= i; ++j) {
+                    const uint16_t *kj = k + ((b * N + j) * H + h) * d;
+                    double dot = 0.0;
+                    for (int64_t x = 0; x < d; ++x)
+                        dot += (double)orc_bf16_to_f32(qi[x]) * (double)orc_bf16_to_f32(kj[x]);
+                    lg[j] = dot * sc;
+                    if (lg[j] > mx) mx = lg[j];
+                }
+                double den = 0.0;
+                for (int64_t j = 0; j <= i; ++j) den += exp(lg[j] - mx);
+                double *oi = o + ((b * N + i) * H + h) * d;
+                for (int64_t x = 0; x < d; ++x) oi[x] = 0.0;
+                for (int64_t j = 0; j <= i; ++j) {
+                    const uint16_t *vj = v + ((b * N + j) * H + h) * d;
+                    double pj = exp(lg[j] - mx) / den;
+                    for (int64_t x = 0; x < d; ++x) oi[x] += pj * (double)orc_bf16_to_f32(vj[x]);
+                }
+                lse[(b * H + h) * N + i] = mx + log(den);
+            }
+            free(lg);
+        }
+    }
+}
