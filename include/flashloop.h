@@ -1,0 +1,269 @@
+/*
+ * flashloop.h -- C ABI of the FlashLoop lazy loop step on one B300 (sm_103a).
+ *
+ * The operations follow the rit.work page "FlashLoop: Fast and
+ * Memory-Efficient Looped Transformers via Lazy Updates" (a summary of the
+ * Yang & Liu preprint):
+ *   - section "Later loops change only part of the state": every loop of a
+ *     looped transformer makes its own KV cache; few tokens keep changing and
+ *     that group narrows and nests; a small, stable group of keys drives the
+ *     loop-to-loop change of attention; neighbouring KV sets differ less than
+ *     whole states, so a base plus small deltas compresses better;
+ *   - section "FlashLoop combines three kinds of saving": early loops run in
+ *     full; later loops rank tokens by how much their hidden state changed
+ *     and recompute only the active ones (the rest reuse state and KV
+ *     entries); keys are chosen from the previous loop's statistics and the
+ *     chosen group keeps its total probability mass; the KV cache is a
+ *     compressed base plus a sequence of compressed deltas, a low-bit delta
+ *     for active tokens and no entry for inactive ones (4-bit deltas); the
+ *     selected data is gathered into dense buffers.
+ *
+ * Conventions for every call below
+ *   - Pointers are DEVICE pointers owned by the caller, 16-byte aligned, to
+ *     contiguous row-major arrays with the shapes given. bf16 and fp16
+ *     values travel as uint16_t bit patterns.
+ *   - No call allocates, frees or synchronises the device unless its comment
+ *     says so. Work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and the call returns.
+ *   - Host-side validation failures return an error status and enqueue
+ *     nothing. A failed launch returns FLASHLOOP_ERR_CUDA. The detail of the
+ *     last failure on the calling thread is in flashloop_last_error().
+ *   - Index lists are int32, ascending, and ties in every ranking go to the
+ *     lower index.
+ *   - Calls are reentrant; calls that write the same buffers on different
+ *     streams without ordering race.
+ */
+#ifndef FLASHLOOP_H
+#define FLASHLOOP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *flashloop_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    FLASHLOOP_OK = 0,
+    FLASHLOOP_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad size or count */
+    FLASHLOOP_ERR_UNSUPPORTED = -2, /* head dim not in {64, 96, 128}, or not an sm_103 device */
+    FLASHLOOP_ERR_CAPACITY = -3,    /* cache or delta layer too small for the request */
+    FLASHLOOP_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
+    FLASHLOOP_ERR_WORKSPACE = -5,   /* workspace missing or smaller than required */
+    FLASHLOOP_ERR_DEVICE = -6       /* a kernel reported a failure (see flashloop_device_status) */
+} flashloop_status_t;
+
+#define FLASHLOOP_MAX_LOOPS 32
+
+/* Problem sizes. B sequences, N_cap key positions per sequence (prefill
+ * tokens plus room for decode tokens), H heads of dimension d (64, 96 or
+ * 128), D = H*d. R active tokens per sequence and K key columns per
+ * (sequence, head) per lazy loop. T loops of which the first T_dense are
+ * dense. R_cap = entries per delta layer and sequence (>= R). */
+typedef struct {
+    int32_t B, N_cap, H, d;
+    int32_t R, K;
+    int32_t T, T_dense;
+    int32_t R_cap;
+} flashloop_dims_t;
+
+/* Per-loop KV cache ("a compressed base plus a sequence of compressed
+ * deltas"). Dense loop t (1..T_dense) owns a full bf16 layer; the base is
+ * layer T_dense. Lazy loop l (T_dense < l <= T) owns delta layer
+ * l - T_dense - 1 holding, per sequence b, count[] entries:
+ *   idx    [B, R_cap]            token index of each entry, ascending
+ *   slot   [B, N_cap]            entry of each token, -1 = no entry
+ *   codes  [B, R_cap, H, d/2]    int4 two's-complement codes; element 2t is
+ *                                the low nibble of byte t
+ *   scales [B, R_cap, H, d/32]   fp16 scale of each 32-element group
+ * for K and V separately. The reconstruction of token j at loop l is the
+ * base plus, in ascending loop order, scale*code of every delta layer up to
+ * l that holds j, summed in fp32 without fused multiply-add.
+ * All pointers are carved from one caller buffer by flashloop_kv_cache_init;
+ * `count` and `n_tokens` are host-side and updated by the calls that append. */
+typedef struct {
+    flashloop_dims_t dims;
+    int32_t n_tokens;                        /* key positions in use */
+    uint16_t *k_dense[FLASHLOOP_MAX_LOOPS];  /* [B, N_cap, H, d] bf16 */
+    uint16_t *v_dense[FLASHLOOP_MAX_LOOPS];
+    int32_t *idx[FLASHLOOP_MAX_LOOPS];
+    int32_t *slot[FLASHLOOP_MAX_LOOPS];
+    uint8_t *k_codes[FLASHLOOP_MAX_LOOPS];
+    uint16_t *k_scales[FLASHLOOP_MAX_LOOPS];
+    uint8_t *v_codes[FLASHLOOP_MAX_LOOPS];
+    uint16_t *v_scales[FLASHLOOP_MAX_LOOPS];
+    int32_t count[FLASHLOOP_MAX_LOOPS];
+} flashloop_kv_cache_t;
+
+typedef enum {
+    FLASHLOOP_ATTN_FIRST_DENSE = 0, /* loop 1: every row and key, no previous state (m = 1, u = 0) */
+    FLASHLOOP_ATTN_DENSE = 1,       /* a later dense loop: every row and key, previous state used */
+    FLASHLOOP_ATTN_LAZY = 2         /* listed rows, selected key columns, preserved mass */
+} flashloop_attn_mode_t;
+
+/* Lazy attention with preserved probability mass. For every listed row i
+ * (key position pos_i, state slot s) and head h, with S_i = {j in S : j <= i}
+ * and scale 1/sqrt(d):
+ *   p_j   = exp(qhat_s . k_j^(l-1) * scale - Z_s)        previous-loop probability
+ *   m     = sum_{S_i} p_j,   u = sum_{S_i} p_j v_j^(l-1)
+ *   tau_j = q_s . k_j^(l) * scale,  lam = logsumexp_{S_i} tau
+ *   w     = sum_{S_i} exp(tau_j - lam) v_j^(l)
+ *   O_s <- O_s - u + m w,  Z_s <- lam - ln m,  qhat_s <- q_s,
+ *   c_j += m exp(tau_j - lam) - p_j  for j in S_i.
+ * k^(t), v^(t) are the cache's reconstructions rounded to bf16. Rows with
+ * S_i empty, or with m below FLT_MIN, keep O, Z and qhat. FIRST_DENSE uses
+ * m = 1, u = 0, p = 0 and overwrites c with the column sums. DENSE and
+ * FIRST_DENSE take every key and every row (row_pos is ignored, R = n_state
+ * = n_keys). The dense layer of loop `loop` must already hold K/V.
+ * Precision: bf16 operands, fp32 accumulation and softmax. */
+typedef struct {
+    int32_t mode;             /* flashloop_attn_mode_t */
+    int32_t loop;             /* l, 1-based */
+    int32_t n_keys;           /* key positions 0..n_keys-1 of the cache */
+    int32_t n_state;          /* state rows per sequence */
+    int32_t R;                /* listed rows per sequence */
+    const int32_t *row_pos;   /* [B, R] key position of each row, ascending */
+    const int32_t *row_slot;  /* [B, R] state row of each row; NULL = row_pos */
+    int32_t K;                /* selected key columns per (b, h) (LAZY) */
+    const int32_t *key_idx;   /* [B, H, K] ascending (LAZY) */
+    const uint16_t *q;        /* [B, n_state, H, d] bf16, loop-l queries */
+    uint16_t *q_hat;          /* [B, n_state, H, d] bf16 state (in/out) */
+    float *o;                 /* [B, n_state, H, d] state (in/out) */
+    float *z;                 /* [B, H, n_state] log-normaliser state (in/out) */
+    float *c;                 /* [B, H, n_keys] column mass (in/out) */
+    const flashloop_kv_cache_t *cache;
+    void *workspace;
+    size_t workspace_bytes;
+} flashloop_attn_args_t;
+
+/* One loop of the looped model, fused: for a dense loop (l <= T_dense) it
+ * stores K/V as dense layer l and runs dense attention; for a lazy loop it
+ * runs select_tokens on (h_prev, h_cur), kv_delta_append of K and V for the
+ * active tokens, select_keys on c, and lazy attention. `decode` = 1 runs the
+ * same loop for ONE new token per sequence at key position cache->n_tokens-1
+ * (the caller counts it in n_tokens before loop 1): state arrays then have
+ * one row, the token is always active, and h_prev/h_cur are unused. */
+typedef struct {
+    int32_t loop;
+    int32_t decode;
+    const uint16_t *h_prev;   /* [B, N, D] bf16, loop l-1 hidden states (prefill, lazy) */
+    const uint16_t *h_cur;    /* [B, N, D] bf16, loop l hidden states */
+    const uint16_t *q;        /* [B, N, H, d] bf16 (decode: [B, 1, H, d]) */
+    const uint16_t *k;
+    const uint16_t *v;
+    uint16_t *q_hat;          /* state, as in flashloop_attn_args_t */
+    float *o;
+    float *z;
+    float *c;                 /* [B, H, n_keys] */
+    flashloop_kv_cache_t *cache;
+    int32_t *active_idx;      /* [B, R] out (prefill lazy loops) */
+    int32_t *key_idx;         /* [B, H, K] out (lazy loops) */
+    float *scores;            /* [B, N] out, or NULL */
+    void *workspace;
+    size_t workspace_bytes;
+} flashloop_step_args_t;
+
+/* ---- sizes and set-up ------------------------------------------------- */
+
+/* Bytes of workspace every call below needs for these dims (prefill and
+ * decode). Returns 0 for invalid dims. */
+size_t flashloop_workspace_bytes(const flashloop_dims_t *dims);
+
+/* Bytes of the single device buffer that holds the whole KV cache. */
+size_t flashloop_kv_cache_bytes(const flashloop_dims_t *dims);
+
+/* Carves `dev_buf` (>= flashloop_kv_cache_bytes, 256-byte aligned) into the
+ * cache layers and enqueues the reset of every slot map to -1 on `stream`.
+ * Counts and n_tokens start at zero. */
+flashloop_status_t flashloop_kv_cache_init(flashloop_kv_cache_t *cache, void *dev_buf, size_t bytes,
+                                           const flashloop_dims_t *dims, flashloop_stream_t stream);
+
+/* ---- the steps of a lazy loop ----------------------------------------- */
+
+/* Token selection ("rank tokens by how much their hidden states changed
+ * and recompute only the active ones"): score_i = sum_x (h_cur - h_prev)^2
+ * in fp32 over the D features of token i, then the R largest per sequence
+ * (ties to the lower index), ascending.
+ * h_prev, h_cur [B, N, D] bf16; active_idx [B, R] out; scores [B, N] out
+ * or NULL. Workspace: flashloop_workspace_bytes (holds the scores when
+ * `scores` is NULL). 1 <= R <= N; D % 8 == 0. */
+flashloop_status_t flashloop_select_tokens(const uint16_t *h_prev, const uint16_t *h_cur,
+                                           int32_t B, int32_t N, int32_t D, int32_t R,
+                                           int32_t *active_idx, float *scores,
+                                           void *workspace, size_t workspace_bytes,
+                                           flashloop_stream_t stream);
+
+/* Gather of selected rows into a dense buffer ("the selected data is
+ * gathered into dense buffers"): dst[b, r, :] = src[b, idx[b, r], :].
+ * src [B, N, row_bytes], idx [B, R] in [0, N), dst [B, R, row_bytes];
+ * row_bytes % 16 == 0. */
+flashloop_status_t flashloop_gather(const void *src, int32_t B, int32_t N, int32_t row_bytes,
+                                    const int32_t *idx, int32_t R, void *dst,
+                                    flashloop_stream_t stream);
+
+/* Delta append ("for tokens that stay active, write a low-bit difference
+ * from the previous state; inactive tokens get no new entry"; 4-bit). For
+ * lazy loop `loop` and every active token i and head: delta = bf16 input
+ * minus the loop-(l-1) reconstruction (fp32); per 32-element group
+ * scale = fp16_rne(amax / 7) and code = rint_even(delta / scale) clamped to
+ * [-7, 7] (zero scale gives zero codes). Writes entries [at, at + R) of
+ * the loop's K and V delta layers, their idx and slot entries, and sets
+ * count = at + R. at == 0 starts the layer afresh (its slot map is reset
+ * first); at == count appends (decode). k_l, v_l are bf16, either
+ * [B, n_tokens, H, d] indexed by token (rows_are_tokens = 1) or [B, R, H, d]
+ * with one row per listed token (rows_are_tokens = 0, as for a decode token). */
+flashloop_status_t flashloop_kv_delta_append(flashloop_kv_cache_t *cache, int32_t loop,
+                                             const uint16_t *k_l, const uint16_t *v_l,
+                                             int32_t rows_are_tokens,
+                                             const int32_t *active_idx, int32_t R, int32_t at,
+                                             flashloop_stream_t stream);
+
+/* Stores K/V rows as (part of) dense layer `loop` (loop <= T_dense):
+ * layer[b, pos0 + r] = k[b, r] for r < n_rows. k, v [B, n_rows, H, d]. */
+flashloop_status_t flashloop_kv_dense_store(flashloop_kv_cache_t *cache, int32_t loop,
+                                            const uint16_t *k, const uint16_t *v,
+                                            int32_t pos0, int32_t n_rows, flashloop_stream_t stream);
+
+/* Key-column selection ("keys are chosen from the previous loop's
+ * statistics"): the K largest col_stats per (b, h), ties to the lower index,
+ * ascending. col_stats [B, H, N] fp32; key_idx [B, H, K] out. */
+flashloop_status_t flashloop_select_keys(const float *col_stats, int32_t B, int32_t H, int32_t N, int32_t K,
+                                         int32_t *key_idx, void *workspace, size_t workspace_bytes,
+                                         flashloop_stream_t stream);
+
+/* Reconstruct-gather of the selected keys: for j = key_idx[b, h, r],
+ * k_old/v_old[b, h, r, :] = bf16_rne(reconstruction at loop-1) and
+ * k_new/v_new[b, h, r, :] = bf16_rne(reconstruction at loop). Outputs
+ * [B, H, K, d] bf16 each. */
+flashloop_status_t flashloop_reconstruct_keys(const flashloop_kv_cache_t *cache, int32_t loop,
+                                              const int32_t *key_idx, int32_t K,
+                                              uint16_t *k_old, uint16_t *v_old,
+                                              uint16_t *k_new, uint16_t *v_new,
+                                              flashloop_stream_t stream);
+
+/* Lazy (or dense) attention, see flashloop_attn_args_t. */
+flashloop_status_t flashloop_lazy_attention(const flashloop_attn_args_t *args, flashloop_stream_t stream);
+
+/* One fused loop, see flashloop_step_args_t. Graph-capturable: it only
+ * enqueues kernels and memsets on `stream`. */
+flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *args, flashloop_stream_t stream);
+
+/* ---- diagnostics -------------------------------------------------------- */
+
+const char *flashloop_status_string(flashloop_status_t status);
+const char *flashloop_last_error(void);
+
+/* Reads and clears the device-side failure word that kernels set when a
+ * bounded wait gives up (0 = none). SYNCHRONISES the current device. */
+flashloop_status_t flashloop_device_status(int32_t *word);
+
+/* Number of kernel launches this library has enqueued from the calling
+ * process (a counter for benchmarks). */
+int64_t flashloop_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLASHLOOP_H */

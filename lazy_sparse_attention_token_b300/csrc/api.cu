@@ -1,0 +1,519 @@
+// api.cu -- the C ABI declared in include/flashloop.h: argument checks,
+// cache and workspace layout, and the order of the kernels in one loop.
+//
+// Loop order (rit.work page "FlashLoop: Fast and Memory-Efficient Looped
+// Transformers via Lazy Updates", section "FlashLoop combines three kinds of
+// saving"): early loops run in full; a later loop ranks tokens by change and
+// keeps the active ones, writes their low-bit KV deltas, picks key columns
+// from the previous loop's statistics and runs mass-preserving attention
+// over them.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+
+namespace fl {
+
+namespace {
+thread_local std::string g_last_error;
+std::atomic<long long> g_launches{0};
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+__global__ void fill_rows_kernel(int32_t *pos, int32_t *slot, int B, int value) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B) {
+        pos[b] = value;
+        slot[b] = 0;
+    }
+}
+}  // namespace
+
+void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+flashloop_status_t set_error(flashloop_status_t st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+static flashloop_status_t cuda_fail(cudaError_t e, const char *what) {
+    return set_error(FLASHLOOP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Every compute entry point runs only on an sm_103 device.
+static flashloop_status_t check_device() {
+    static std::mutex mu;
+    static int cached_dev = -1;
+    static bool cached_ok = false;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev != cached_dev) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cached_ok = (major == 10 && minor == 3);
+        cached_dev = dev;
+    }
+    if (!cached_ok) return set_error(FLASHLOOP_ERR_UNSUPPORTED, "device is not sm_103 (B300)");
+    return FLASHLOOP_OK;
+}
+
+static bool head_dim_ok(int d) { return d == 64 || d == 96 || d == 128; }
+
+static flashloop_status_t check_dims(const flashloop_dims_t *dm) {
+    if (!dm) return set_error(FLASHLOOP_ERR_INVALID_ARG, "dims is NULL");
+    if (dm->B < 1 || dm->N_cap < 1 || dm->H < 1 || dm->T < 1 || dm->T_dense < 1 || dm->T_dense > dm->T ||
+        dm->T > FLASHLOOP_MAX_LOOPS || dm->R < 1 || dm->R > dm->N_cap || dm->K < 1 || dm->K > dm->N_cap ||
+        dm->R_cap < dm->R || dm->R_cap > dm->N_cap)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad dims (B=%d N_cap=%d H=%d R=%d K=%d T=%d T_dense=%d R_cap=%d)",
+                         dm->B, dm->N_cap, dm->H, dm->R, dm->K, dm->T, dm->T_dense, dm->R_cap);
+    if (!head_dim_ok(dm->d)) return set_error(FLASHLOOP_ERR_UNSUPPORTED, "head dim %d not in {64, 96, 128}", dm->d);
+    return FLASHLOOP_OK;
+}
+
+struct WsLayout {
+    size_t scores, kv, rows, slots, total;
+};
+
+static WsLayout ws_layout(const flashloop_dims_t *dm) {
+    WsLayout w;
+    size_t off = 0;
+    w.scores = off;
+    off += align_up((size_t)dm->B * dm->N_cap * sizeof(float));
+    w.kv = off;
+    off += 4 * align_up((size_t)dm->B * dm->H * dm->K * dm->d * 2);
+    w.rows = off;
+    off += align_up((size_t)dm->B * sizeof(int32_t));
+    w.slots = off;
+    off += align_up((size_t)dm->B * sizeof(int32_t));
+    w.total = off;
+    return w;
+}
+
+struct CacheLayout {
+    size_t dense_layer, idx, slot, codes, scales, total;
+};
+
+static CacheLayout cache_layout(const flashloop_dims_t *dm) {
+    CacheLayout c;
+    c.dense_layer = align_up((size_t)dm->B * dm->N_cap * dm->H * dm->d * 2);
+    c.idx = align_up((size_t)dm->B * dm->R_cap * 4);
+    c.slot = align_up((size_t)dm->B * dm->N_cap * 4);
+    c.codes = align_up((size_t)dm->B * dm->R_cap * dm->H * (dm->d / 2));
+    c.scales = align_up((size_t)dm->B * dm->R_cap * dm->H * (dm->d / 32) * 2);
+    const size_t n_delta = (size_t)(dm->T - dm->T_dense);
+    c.total = 2 * dm->T_dense * c.dense_layer + n_delta * (c.idx + c.slot + 2 * c.codes + 2 * c.scales);
+    return c;
+}
+
+// Reconstruction of loop `loop` = base (last dense layer) + delta layers up to `loop`.
+static DeltaView make_view(const flashloop_kv_cache_t *c, int loop) {
+    DeltaView v;
+    memset(&v, 0, sizeof v);
+    const int td = c->dims.T_dense;
+    if (loop <= td) {
+        v.k_base = c->k_dense[loop - 1];
+        v.v_base = c->v_dense[loop - 1];
+        v.n_layers = 0;
+        return v;
+    }
+    v.k_base = c->k_dense[td - 1];
+    v.v_base = c->v_dense[td - 1];
+    v.n_layers = loop - td;
+    for (int m = 0; m < v.n_layers; ++m) {
+        v.slot[m] = c->slot[m];
+        v.k_codes[m] = c->k_codes[m];
+        v.k_scales[m] = c->k_scales[m];
+        v.v_codes[m] = c->v_codes[m];
+        v.v_scales[m] = c->v_scales[m];
+    }
+    return v;
+}
+
+static flashloop_status_t check_cache(const flashloop_kv_cache_t *c) {
+    if (!c) return set_error(FLASHLOOP_ERR_INVALID_ARG, "cache is NULL");
+    flashloop_status_t st = check_dims(&c->dims);
+    if (st != FLASHLOOP_OK) return st;
+    for (int t = 0; t < c->dims.T_dense; ++t)
+        if (!c->k_dense[t] || !c->v_dense[t]) return set_error(FLASHLOOP_ERR_INVALID_ARG, "cache is not initialised");
+    return FLASHLOOP_OK;
+}
+
+}  // namespace fl
+
+using namespace fl;
+
+extern "C" {
+
+const char *flashloop_status_string(flashloop_status_t s) {
+    switch (s) {
+        case FLASHLOOP_OK: return "ok";
+        case FLASHLOOP_ERR_INVALID_ARG: return "invalid argument";
+        case FLASHLOOP_ERR_UNSUPPORTED: return "unsupported";
+        case FLASHLOOP_ERR_CAPACITY: return "capacity exceeded";
+        case FLASHLOOP_ERR_CUDA: return "CUDA error";
+        case FLASHLOOP_ERR_WORKSPACE: return "workspace too small";
+        case FLASHLOOP_ERR_DEVICE: return "device-side failure";
+    }
+    return "unknown status";
+}
+
+const char *flashloop_last_error(void) { return g_last_error.c_str(); }
+
+int64_t flashloop_launch_count(void) { return g_launches.load(); }
+
+size_t flashloop_workspace_bytes(const flashloop_dims_t *dims) {
+    if (check_dims(dims) != FLASHLOOP_OK) return 0;
+    return ws_layout(dims).total;
+}
+
+size_t flashloop_kv_cache_bytes(const flashloop_dims_t *dims) {
+    if (check_dims(dims) != FLASHLOOP_OK) return 0;
+    return cache_layout(dims).total;
+}
+
+flashloop_status_t flashloop_kv_cache_init(flashloop_kv_cache_t *cache, void *dev_buf, size_t bytes,
+                                           const flashloop_dims_t *dims, flashloop_stream_t stream) {
+    if (!cache || !dev_buf) return set_error(FLASHLOOP_ERR_INVALID_ARG, "cache or buffer is NULL");
+    flashloop_status_t st = check_dims(dims);
+    if (st != FLASHLOOP_OK) return st;
+    if (reinterpret_cast<uintptr_t>(dev_buf) % kAlign)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "cache buffer must be 256-byte aligned");
+    const CacheLayout L = cache_layout(dims);
+    if (bytes < L.total) return set_error(FLASHLOOP_ERR_CAPACITY, "cache buffer %zu < %zu bytes", bytes, L.total);
+    if ((st = check_device()) != FLASHLOOP_OK) return st;
+    memset(cache, 0, sizeof *cache);
+    cache->dims = *dims;
+    uint8_t *p = static_cast<uint8_t *>(dev_buf);
+    for (int t = 0; t < dims->T_dense; ++t) {
+        cache->k_dense[t] = reinterpret_cast<uint16_t *>(p); p += L.dense_layer;
+        cache->v_dense[t] = reinterpret_cast<uint16_t *>(p); p += L.dense_layer;
+    }
+    for (int m = 0; m < dims->T - dims->T_dense; ++m) {
+        cache->idx[m] = reinterpret_cast<int32_t *>(p); p += L.idx;
+        cache->slot[m] = reinterpret_cast<int32_t *>(p); p += L.slot;
+        cache->k_codes[m] = p; p += L.codes;
+        cache->k_scales[m] = reinterpret_cast<uint16_t *>(p); p += L.scales;
+        cache->v_codes[m] = p; p += L.codes;
+        cache->v_scales[m] = reinterpret_cast<uint16_t *>(p); p += L.scales;
+        cudaError_t e = cudaMemsetAsync(cache->slot[m], 0xFF, (size_t)dims->B * dims->N_cap * 4, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(slot)");
+    }
+    return FLASHLOOP_OK;
+}
+
+flashloop_status_t flashloop_select_tokens(const uint16_t *h_prev, const uint16_t *h_cur, int32_t B, int32_t N,
+                                           int32_t D, int32_t R, int32_t *active_idx, float *scores,
+                                           void *workspace, size_t workspace_bytes, flashloop_stream_t stream) {
+    if (!h_prev || !h_cur || !active_idx) return set_error(FLASHLOOP_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(h_prev) || !aligned16(h_cur)) return set_error(FLASHLOOP_ERR_INVALID_ARG, "inputs must be 16-byte aligned");
+    if (B < 1 || N < 1 || D < 8 || D % 8 || R < 1 || R > N)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad sizes (B=%d N=%d D=%d R=%d)", B, N, D, R);
+    float *sc = scores;
+    if (!sc) {
+        if (!workspace || workspace_bytes < (size_t)B * N * sizeof(float))
+            return set_error(FLASHLOOP_ERR_WORKSPACE, "workspace needs %zu bytes for scores", (size_t)B * N * 4);
+        sc = static_cast<float *>(workspace);
+    }
+    flashloop_status_t st = check_device();
+    if (st != FLASHLOOP_OK) return st;
+    cudaError_t e = launch_token_scores(h_prev, h_cur, B, N, D, sc, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "token_scores");
+    e = launch_topk_rows(sc, B, N, R, active_idx, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "topk(tokens)");
+    return FLASHLOOP_OK;
+}
+
+flashloop_status_t flashloop_gather(const void *src, int32_t B, int32_t N, int32_t row_bytes, const int32_t *idx,
+                                    int32_t R, void *dst, flashloop_stream_t stream) {
+    if (!src || !idx || !dst) return set_error(FLASHLOOP_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(src) || !aligned16(dst)) return set_error(FLASHLOOP_ERR_INVALID_ARG, "src/dst must be 16-byte aligned");
+    if (B < 1 || N < 1 || R < 0 || row_bytes < 16 || row_bytes % 16)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad sizes (B=%d N=%d R=%d row_bytes=%d)", B, N, R, row_bytes);
+    flashloop_status_t st = check_device();
+    if (st != FLASHLOOP_OK) return st;
+    cudaError_t e = launch_gather_rows(src, B, N, row_bytes, idx, R, dst, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "gather");
+    return FLASHLOOP_OK;
+}
+
+flashloop_status_t flashloop_kv_delta_append(flashloop_kv_cache_t *cache, int32_t loop, const uint16_t *k_l,
+                                             const uint16_t *v_l, int32_t rows_are_tokens,
+                                             const int32_t *active_idx, int32_t R, int32_t at,
+                                             flashloop_stream_t stream) {
+    flashloop_status_t st = check_cache(cache);
+    if (st != FLASHLOOP_OK) return st;
+    const flashloop_dims_t &dm = cache->dims;
+    if (loop <= dm.T_dense || loop > dm.T)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "loop %d is not a lazy loop (T_dense=%d, T=%d)", loop, dm.T_dense, dm.T);
+    if (!k_l || !v_l || !active_idx) return set_error(FLASHLOOP_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(k_l) || !aligned16(v_l)) return set_error(FLASHLOOP_ERR_INVALID_ARG, "K/V must be 16-byte aligned");
+    const int m = loop - dm.T_dense - 1;
+    if (R < 1 || at < 0 || (at != 0 && at != cache->count[m]))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "R=%d at=%d (layer holds %d)", R, at, cache->count[m]);
+    if (at + R > dm.R_cap) return set_error(FLASHLOOP_ERR_CAPACITY, "delta layer full (%d + %d > %d)", at, R, dm.R_cap);
+    if ((st = check_device()) != FLASHLOOP_OK) return st;
+    if (at == 0) {
+        cudaError_t e = cudaMemsetAsync(cache->slot[m], 0xFF, (size_t)dm.B * dm.N_cap * 4, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(slot)");
+    }
+    const DeltaView view = make_view(cache, loop - 1);
+    if (rows_are_tokens && (cache->n_tokens < 1 || cache->n_tokens > dm.N_cap))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "rows_are_tokens needs 1 <= cache n_tokens <= N_cap");
+    const int src_rows = rows_are_tokens ? cache->n_tokens : R;
+    cudaError_t e = launch_delta_append(view, k_l, v_l, rows_are_tokens, src_rows, active_idx, R, at, dm.B, dm.N_cap,
+                                        dm.H, dm.d, dm.R_cap, cache->idx[m], cache->slot[m], cache->k_codes[m],
+                                        cache->k_scales[m], cache->v_codes[m], cache->v_scales[m], stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kv_delta_append");
+    cache->count[m] = at + R;
+    return FLASHLOOP_OK;
+}
+
+flashloop_status_t flashloop_kv_dense_store(flashloop_kv_cache_t *cache, int32_t loop, const uint16_t *k,
+                                            const uint16_t *v, int32_t pos0, int32_t n_rows,
+                                            flashloop_stream_t stream) {
+    flashloop_status_t st = check_cache(cache);
+    if (st != FLASHLOOP_OK) return st;
+    const flashloop_dims_t &dm = cache->dims;
+    if (loop < 1 || loop > dm.T_dense)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "loop %d is not a dense loop (T_dense=%d)", loop, dm.T_dense);
+    if (!k || !v || !aligned16(k) || !aligned16(v)) return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad K/V pointer");
+    if (pos0 < 0 || n_rows < 1 || pos0 + n_rows > dm.N_cap)
+        return set_error(FLASHLOOP_ERR_CAPACITY, "rows [%d, %d) exceed N_cap=%d", pos0, pos0 + n_rows, dm.N_cap);
+    if ((st = check_device()) != FLASHLOOP_OK) return st;
+    const int row = dm.H * dm.d;
+    cudaError_t e = launch_store_rows(k, dm.B, n_rows, row, cache->k_dense[loop - 1], dm.N_cap, pos0, stream);
+    if (e == cudaSuccess) e = launch_store_rows(v, dm.B, n_rows, row, cache->v_dense[loop - 1], dm.N_cap, pos0, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kv_dense_store");
+    return FLASHLOOP_OK;
+}
+
+flashloop_status_t flashloop_select_keys(const float *col_stats, int32_t B, int32_t H, int32_t N, int32_t K,
+                                         int32_t *key_idx, void *workspace, size_t workspace_bytes,
+                                         flashloop_stream_t stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    if (!col_stats || !key_idx) return set_error(FLASHLOOP_ERR_INVALID_ARG, "NULL pointer");
+    if (B < 1 || H < 1 || N < 1 || K < 1 || K > N)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad sizes (B=%d H=%d N=%d K=%d)", B, H, N, K);
+    flashloop_status_t st = check_device();
+    if (st != FLASHLOOP_OK) return st;
+    cudaError_t e = launch_topk_rows(col_stats, B * H, N, K, key_idx, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "topk(keys)");
+    return FLASHLOOP_OK;
+}
+
+flashloop_status_t flashloop_reconstruct_keys(const flashloop_kv_cache_t *cache, int32_t loop, const int32_t *key_idx,
+                                              int32_t K, uint16_t *k_old, uint16_t *v_old, uint16_t *k_new,
+                                              uint16_t *v_new, flashloop_stream_t stream) {
+    flashloop_status_t st = check_cache(cache);
+    if (st != FLASHLOOP_OK) return st;
+    const flashloop_dims_t &dm = cache->dims;
+    if (loop <= dm.T_dense || loop > dm.T)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "loop %d is not a lazy loop", loop);
+    if (!key_idx || !k_old || !v_old || !k_new || !v_new) return set_error(FLASHLOOP_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(k_old) || !aligned16(v_old) || !aligned16(k_new) || !aligned16(v_new))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "outputs must be 16-byte aligned");
+    if (K < 1 || K > dm.N_cap) return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad K=%d", K);
+    if ((st = check_device()) != FLASHLOOP_OK) return st;
+    cudaError_t e = launch_reconstruct_keys(make_view(cache, loop - 1), make_view(cache, loop), key_idx, dm.B, dm.H, K,
+                                            dm.N_cap, dm.d, dm.R_cap, k_old, v_old, k_new, v_new, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reconstruct_keys");
+    return FLASHLOOP_OK;
+}
+
+flashloop_status_t flashloop_lazy_attention(const flashloop_attn_args_t *a, flashloop_stream_t stream) {
+    if (!a) return set_error(FLASHLOOP_ERR_INVALID_ARG, "args is NULL");
+    flashloop_status_t st = check_cache(a->cache);
+    if (st != FLASHLOOP_OK) return st;
+    const flashloop_kv_cache_t *c = a->cache;
+    const flashloop_dims_t &dm = c->dims;
+    const bool lazy = a->mode == FLASHLOOP_ATTN_LAZY;
+    if (a->mode < 0 || a->mode > 2) return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad mode %d", a->mode);
+    if (a->loop < 1 || a->loop > dm.T) return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad loop %d", a->loop);
+    if ((a->mode == FLASHLOOP_ATTN_FIRST_DENSE) != (a->loop == 1))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "FIRST_DENSE is loop 1 and only loop 1");
+    if (lazy != (a->loop > dm.T_dense))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "loop %d is %s but mode is %d", a->loop,
+                         a->loop > dm.T_dense ? "lazy" : "dense", a->mode);
+    if (!a->q || !a->q_hat || !a->o || !a->z || !a->c) return set_error(FLASHLOOP_ERR_INVALID_ARG, "NULL state pointer");
+    if (!aligned16(a->q) || !aligned16(a->q_hat) || !aligned16(a->o))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "q/q_hat/o must be 16-byte aligned");
+    if (a->n_keys < 1 || a->n_keys > dm.N_cap || a->n_state < 1 || a->R < 0)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad n_keys/n_state/R");
+    const bool few_rows = a->row_pos != nullptr && a->R <= 8;
+    if (!few_rows && a->R > 0 && a->n_state != a->n_keys)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "prefill attention needs n_state == n_keys");
+    if (lazy) {
+        if (!a->key_idx || a->K < 1 || a->K > a->n_keys)
+            return set_error(FLASHLOOP_ERR_INVALID_ARG, "lazy attention needs key_idx and 1 <= K <= n_keys");
+        if (!a->row_pos && a->R > 0) return set_error(FLASHLOOP_ERR_INVALID_ARG, "lazy attention needs row_pos");
+    } else if (!few_rows && a->R != a->n_keys) {
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "dense prefill attention covers every row (R == n_keys)");
+    }
+    if ((st = check_device()) != FLASHLOOP_OK) return st;
+    cudaError_t e;
+    if (a->mode == FLASHLOOP_ATTN_FIRST_DENSE) {
+        e = cudaMemsetAsync(a->c, 0, (size_t)dm.B * dm.H * a->n_keys * sizeof(float), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(c)");
+    }
+    if (a->R == 0) return FLASHLOOP_OK;
+    if (few_rows) {
+        DecodeAttnParams p;
+        memset(&p, 0, sizeof p);
+        p.mode = a->mode;
+        p.B = dm.B; p.H = dm.H; p.d = dm.d;
+        p.n_keys = a->n_keys; p.n_state = a->n_state; p.R = a->R;
+        p.row_pos = a->row_pos; p.row_slot = a->row_slot;
+        p.K = lazy ? a->K : a->n_keys;
+        p.key_idx = lazy ? a->key_idx : nullptr;
+        p.q = a->q; p.q_hat = a->q_hat; p.o = a->o; p.z = a->z; p.c = a->c;
+        p.new_view = make_view(c, a->loop);
+        if (a->loop > 1) p.old_view = make_view(c, a->loop - 1);
+        p.N_cap = dm.N_cap; p.R_cap = dm.R_cap;
+        e = launch_decode_attention(p, stream);
+        if (e == cudaErrorInvalidValue)
+            return set_error(FLASHLOOP_ERR_UNSUPPORTED, "decode attention: %d keys exceed its shared-memory limit",
+                             p.K);
+        if (e != cudaSuccess) return cuda_fail(e, "decode_attention");
+        return FLASHLOOP_OK;
+    }
+    TcAttnParams p;
+    memset(&p, 0, sizeof p);
+    p.mode = a->mode;
+    p.B = dm.B; p.H = dm.H; p.d = dm.d;
+    p.n_keys = a->n_keys; p.n_state = a->n_state; p.R = a->R;
+    p.row_pos = lazy ? a->row_pos : nullptr;
+    p.q = a->q; p.q_hat = a->q_hat; p.o = a->o; p.z = a->z; p.c = a->c;
+    if (lazy) {
+        const WsLayout W = ws_layout(&dm);
+        if (a->K > dm.K) return set_error(FLASHLOOP_ERR_WORKSPACE, "K=%d exceeds dims.K=%d the workspace is sized for", a->K, dm.K);
+        if (!a->workspace || a->workspace_bytes < W.total || reinterpret_cast<uintptr_t>(a->workspace) % kAlign)
+            return set_error(FLASHLOOP_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", W.total);
+        uint8_t *ws = static_cast<uint8_t *>(a->workspace) + W.kv;
+        const size_t one = align_up((size_t)dm.B * dm.H * dm.K * dm.d * 2);
+        uint16_t *kv[4];
+        for (int i = 0; i < 4; ++i) kv[i] = reinterpret_cast<uint16_t *>(ws + i * one);
+        e = launch_reconstruct_keys(make_view(c, a->loop - 1), make_view(c, a->loop), a->key_idx, dm.B, dm.H, a->K,
+                                    dm.N_cap, dm.d, dm.R_cap, kv[0], kv[1], kv[2], kv[3], stream);
+        if (e != cudaSuccess) return cuda_fail(e, "reconstruct_keys");
+        p.K = a->K;
+        p.key_idx = a->key_idx;
+        p.k_old = kv[0]; p.v_old = kv[1]; p.k_new = kv[2]; p.v_new = kv[3];
+        p.kv_rows = a->K;
+    } else {
+        p.K = a->n_keys;
+        p.k_new = c->k_dense[a->loop - 1];
+        p.v_new = c->v_dense[a->loop - 1];
+        if (a->loop > 1) {
+            p.k_old = c->k_dense[a->loop - 2];
+            p.v_old = c->v_dense[a->loop - 2];
+        }
+        p.kv_rows = dm.N_cap;
+    }
+    e = launch_tc_attention(p, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "tc_attention");
+    return FLASHLOOP_OK;
+}
+
+flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop_stream_t stream) {
+    if (!a) return set_error(FLASHLOOP_ERR_INVALID_ARG, "args is NULL");
+    flashloop_status_t st = check_cache(a->cache);
+    if (st != FLASHLOOP_OK) return st;
+    flashloop_kv_cache_t *c = a->cache;
+    const flashloop_dims_t &dm = c->dims;
+    const int l = a->loop;
+    if (l < 1 || l > dm.T) return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad loop %d", l);
+    const bool dense = l <= dm.T_dense;
+    const WsLayout W = ws_layout(&dm);
+    if (!a->workspace || a->workspace_bytes < W.total || reinterpret_cast<uintptr_t>(a->workspace) % kAlign)
+        return set_error(FLASHLOOP_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", W.total);
+    uint8_t *ws = static_cast<uint8_t *>(a->workspace);
+    const int n = c->n_tokens;
+    if (n < 1 || n > dm.N_cap) return set_error(FLASHLOOP_ERR_INVALID_ARG, "cache n_tokens=%d", n);
+
+    flashloop_attn_args_t at;
+    memset(&at, 0, sizeof at);
+    at.loop = l;
+    at.n_keys = n;
+    at.q = a->q; at.q_hat = a->q_hat; at.o = a->o; at.z = a->z; at.c = a->c;
+    at.cache = c;
+    at.workspace = a->workspace;
+    at.workspace_bytes = a->workspace_bytes;
+    at.mode = l == 1 ? FLASHLOOP_ATTN_FIRST_DENSE : dense ? FLASHLOOP_ATTN_DENSE : FLASHLOOP_ATTN_LAZY;
+
+    if (a->decode) {
+        // one new token per sequence at key position n - 1; its state has one row
+        const int pos = n - 1;
+        int32_t *rows = reinterpret_cast<int32_t *>(ws + W.rows);
+        int32_t *slots = reinterpret_cast<int32_t *>(ws + W.slots);
+        fill_rows_kernel<<<ceil_div(dm.B, 128), 128, 0, stream>>>(rows, slots, dm.B, pos);
+        note_launch();
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "fill_rows");
+        if (dense) {
+            if ((st = flashloop_kv_dense_store(c, l, a->k, a->v, pos, 1, stream)) != FLASHLOOP_OK) return st;
+        } else {
+            const int m = l - dm.T_dense - 1;
+            if ((st = flashloop_kv_delta_append(c, l, a->k, a->v, 0, rows, 1, c->count[m], stream)) != FLASHLOOP_OK)
+                return st;
+            if (!a->key_idx) return set_error(FLASHLOOP_ERR_INVALID_ARG, "key_idx is NULL");
+            const int K = dm.K < n ? dm.K : n;
+            if ((st = flashloop_select_keys(a->c, dm.B, dm.H, n, K, a->key_idx, nullptr, 0, stream)) != FLASHLOOP_OK)
+                return st;
+            at.K = K;
+            at.key_idx = a->key_idx;
+        }
+        at.n_state = 1;
+        at.R = 1;
+        at.row_pos = rows;
+        at.row_slot = slots;
+        return flashloop_lazy_attention(&at, stream);
+    }
+
+    // prefill: every token of the sequence is a row
+    at.n_state = n;
+    if (dense) {
+        if ((st = flashloop_kv_dense_store(c, l, a->k, a->v, 0, n, stream)) != FLASHLOOP_OK) return st;
+        at.R = n;
+        return flashloop_lazy_attention(&at, stream);
+    }
+    if (!a->h_prev || !a->h_cur || !a->active_idx || !a->key_idx)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "lazy loop needs h_prev, h_cur, active_idx and key_idx");
+    float *scores = a->scores ? a->scores : reinterpret_cast<float *>(ws + W.scores);
+    if ((st = flashloop_select_tokens(a->h_prev, a->h_cur, dm.B, n, dm.H * dm.d, dm.R, a->active_idx, scores,
+                                      nullptr, 0, stream)) != FLASHLOOP_OK)
+        return st;
+    if ((st = flashloop_kv_delta_append(c, l, a->k, a->v, 1, a->active_idx, dm.R, 0, stream)) != FLASHLOOP_OK)
+        return st;
+    if ((st = flashloop_select_keys(a->c, dm.B, dm.H, n, dm.K, a->key_idx, nullptr, 0, stream)) != FLASHLOOP_OK)
+        return st;
+    at.R = dm.R;
+    at.row_pos = a->active_idx;
+    at.K = dm.K;
+    at.key_idx = a->key_idx;
+    return flashloop_lazy_attention(&at, stream);
+}
+
+flashloop_status_t flashloop_device_status(int32_t *word) {
+    if (!word) return set_error(FLASHLOOP_ERR_INVALID_ARG, "word is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    *word = tc_attention_read_error(true);
+    return *word ? FLASHLOOP_ERR_DEVICE : FLASHLOOP_OK;
+}
+
+}  // extern "C"

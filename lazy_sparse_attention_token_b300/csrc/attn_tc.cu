@@ -1,0 +1,539 @@
+// attn_tc.cu -- lazy (and dense) attention on the tcgen05 tensor cores.
+//
+// rit.work page "FlashLoop: Fast and Memory-Efficient Looped Transformers via
+// Lazy Updates", section "FlashLoop combines three kinds of saving": in a lazy
+// loop only active rows are recomputed, keys are chosen from the previous
+// loop's statistics, and the chosen group keeps its total probability mass
+// (dropping the other keys and renormalising would give the survivors too
+// much weight); early loops run in full.
+//
+// For one (sequence b, head h, tile of 128 rows) a CTA computes, per row i
+// with S_i = {j in S : j <= i}, scale s = 1/sqrt(d):
+//   p_j = exp(qhat_i.k_j^(l-1) s - Z_i),  m = sum p_j,  u = sum p_j v_j^(l-1)
+//   lam = logsumexp(q_i.k_j^(l) s),       Z' = lam - ln m
+//   acc = -u + sum exp(q_i.k_j^(l) s - Z') v_j^(l)        (= -u + m w)
+//   O_i += acc,  Z_i = Z',  qhat_i = q_i,
+//   c_j += sum_i exp(q_i.k_j^(l) s - Z'_i) - p_ij         (column mass)
+// in three passes over the key tiles, all with a known normaliser so no
+// accumulator rescaling is ever needed:
+//   pass OLD: QK_old -> p -> m, acc -= P V_old, colsum -= P
+//   pass LSE: QK_new -> online max/sum -> lam
+//   pass NEW: QK_new -> P' = exp(. - Z') -> acc += P' V_new, colsum += P'
+// The first dense loop skips pass OLD (m = 1, u = 0).
+//
+// Roles (192 threads): warp 0 issues TMA loads of K/V tiles into a 2-stage
+// ring; warp 1 (one thread) issues tcgen05.mma into TMEM; warps 2..5 own one
+// TMEM lane (= one row) each, read S, do the softmax arithmetic, write P as
+// bf16 into shared memory for the PV and column-sum MMAs, and run the
+// epilogue. Column sums are an MMA of P^T (the same shared tile read
+// MN-major) with a ones matrix, so no cross-thread reduction is needed.
+// TMEM columns: S double buffer [0,256), accumulator [256,256+d), column
+// sums [384,400).
+//
+// Every mbarrier wait is bounded (about one second); on timeout the CTA
+// records an error code, stops issuing work, waits (bounded) for its own
+// copies and MMAs, frees TMEM and exits.
+#include <cudaTypedefs.h>
+#include <float.h>
+#include <mutex>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace fl {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int kThreads = 192;
+constexpr int kAtom = 128 * 128;  // bytes of a 128-row x 64-element bf16 tile, 128-byte swizzled
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColAcc = 256, kColCS = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ int g_tc_error;
+
+enum : int { PH_OLD = 0, PH_LSE = 1, PH_NEW = 2 };
+enum : int { BAR_KV_FULL = 0, BAR_KV_EMPTY = 2, BAR_S_FULL = 4, BAR_S_EMPTY = 6, BAR_P_FULL = 8,
+             BAR_P_EMPTY = 9, BAR_ACC = 10, BAR_DRAIN = 11, N_BARS = 12 };
+enum : int { ERR_KV_EMPTY = 1, ERR_KV_FULL = 2, ERR_S_EMPTY = 3, ERR_S_FULL = 4, ERR_P_FULL = 5,
+             ERR_P_EMPTY = 6, ERR_ACC = 7 };
+
+template <int D>
+struct Cfg {
+    static constexpr int NA = (D + 63) / 64;        // 64-element atoms along d
+    static constexpr int TB = NA * kAtom;           // one 128-row tile of Q, K or V
+    static constexpr int OFF_QH = 0;
+    static constexpr int OFF_Q = TB;
+    static constexpr int OFF_KV = 2 * TB;           // stage s: K at +2*TB*s, V at +2*TB*s + TB
+    static constexpr int OFF_P = OFF_KV + 4 * TB;
+    static constexpr int OFF_ONES = OFF_P + 2 * kAtom;
+    static constexpr int OFF_BAR = OFF_ONES + 512;
+    static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int SMEM = BYTES + 1024;       // room to align the base to 1024 bytes
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct KParams {
+    int mode, H, n_keys, n_state, R, K, n_row_tiles;
+    const int32_t *row_pos;
+    const int32_t *key_idx;
+    const uint16_t *q;
+    uint16_t *q_hat;
+    float *o, *z, *c;
+    float sl2;   // log2(e) / sqrt(d)
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Bounded wait: false on timeout or when another role has aborted.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if ((it & 63u) == 0 && globaltimer_ns() - t0 > 1000000000ull) {
+            *abort_flag = 1;
+            atomicCAS(&g_tc_error, 0, code);
+            return false;
+        }
+    }
+}
+
+// Byte offset of 16-byte chunk `ch` (8 bf16) of row r in a 128-row tile laid
+// out as 64-element atoms with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz_off(int r, int ch) {
+    return (uint32_t)((ch >> 3) * kAtom + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tm_k_old,
+                    const __grid_constant__ CUtensorMap tm_v_old, const __grid_constant__ CUtensorMap tm_k_new,
+                    const __grid_constant__ CUtensorMap tm_v_new) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + C::OFF_BAR;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int rt = p.n_row_tiles - 1 - (int)blockIdx.x;   // heavier (later) row tiles first
+    const bool dense = p.mode != FLASHLOOP_ATTN_LAZY;
+    const bool first = p.mode == FLASHLOOP_ATTN_FIRST_DENSE;
+    const int row0 = rt * BM;
+    const int rows = min(BM, p.R - row0);
+    const long long bh = (long long)b * p.H + h;
+    const int32_t *S = dense ? nullptr : p.key_idx + bh * p.K;
+    const int32_t *A = dense ? nullptr : p.row_pos + (long long)b * p.R + row0;
+    const int min_pos = dense ? row0 : __ldg(A);
+    const int max_pos = dense ? row0 + rows - 1 : __ldg(A + rows - 1);
+    int cnt;   // keys (of the list) at or before the last row
+    if (dense) {
+        cnt = min(max_pos + 1, p.n_keys);
+    } else {
+        int lo = 0, hi = p.K;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(S + mid) <= max_pos) lo = mid + 1; else hi = mid;
+        }
+        cnt = lo;
+    }
+    const int n_tiles = (cnt + BN - 1) / BN;
+    if (n_tiles == 0) return;   // every row has an empty key set: state unchanged
+    const int ph0 = first ? PH_LSE : PH_OLD;
+    const int total = (3 - ph0) * n_tiles;
+    const int kcols = dense ? p.n_keys : p.K;
+
+    // ---------------- set-up ----------------
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < N_BARS; ++i) {
+            const bool many = (i == BAR_S_EMPTY || i == BAR_S_EMPTY + 1 || i == BAR_P_FULL);
+            mbar_init(bar(i), many ? 128u : 1u);
+        }
+        misc[1] = 0;
+        mbar_fence_init();
+    }
+    __syncwarp();
+    if (warp == 0) {
+        tmem_alloc(sbase + C::OFF_MISC, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 1) {   // 16x16 bf16 ones (B operand of the column-sum MMA)
+        uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        reinterpret_cast<uint4 *>(smem + C::OFF_ONES)[lane] = one4;
+        fence_proxy_async_smem();
+    }
+    const int r = (warp & 3) * 32 + lane;    // softmax warps: tile row == TMEM lane
+    const bool is_sm = warp >= 2;
+    const bool row_ok = is_sm && r < rows;
+    const int pos = row_ok ? (dense ? row0 + r : __ldg(A + r)) : -1;
+    if (is_sm) {   // gather this row's queries into the swizzled Q tiles
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+        const long long qoff = (((long long)b * p.n_state + max(pos, 0)) * p.H + h) * D;
+        const uint4 *qn = reinterpret_cast<const uint4 *>(p.q + qoff);
+        const uint4 *qo = reinterpret_cast<const uint4 *>(p.q_hat + qoff);
+#pragma unroll
+        for (int ch = 0; ch < D / 8; ++ch) {
+            *reinterpret_cast<uint4 *>(smem + C::OFF_Q + swz_off(r, ch)) = row_ok ? ldg_nc_v4(qn + ch) : zero;
+            if (!first)
+                *reinterpret_cast<uint4 *>(smem + C::OFF_QH + swz_off(r, ch)) = row_ok ? qo[ch] : zero;
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    auto phase_of = [&](int g) { return ph0 + g / n_tiles; };
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tm_k_old); prefetch_tmap(&tm_v_old);
+            prefetch_tmap(&tm_k_new); prefetch_tmap(&tm_v_new);
+            int issued = 0;
+            for (int g = 0; g < total; ++g) {
+                const int s = g & 1, use = g >> 1;
+                if (!wait_bar(bar(BAR_KV_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_KV_EMPTY)) break;
+                const int ph = phase_of(g), t = g % n_tiles;
+                const bool with_v = ph != PH_LSE;
+                const CUtensorMap *mk = ph == PH_OLD ? &tm_k_old : &tm_k_new;
+                const CUtensorMap *mv = ph == PH_OLD ? &tm_v_old : &tm_v_new;
+                const uint32_t kdst = sbase + C::OFF_KV + 2 * C::TB * s;
+                mbar_arrive_expect_tx(bar(BAR_KV_FULL + s), (with_v ? 2 : 1) * C::TB);
+                for (int a = 0; a < C::NA; ++a) {
+                    if (dense) tma_load_4d(kdst + a * kAtom, mk, bar(BAR_KV_FULL + s), a * 64, h, t * BN, b);
+                    else tma_load_4d(kdst + a * kAtom, mk, bar(BAR_KV_FULL + s), a * 64, t * BN, h, b);
+                }
+                if (with_v) {
+                    for (int a = 0; a < C::NA; ++a) {
+                        if (dense) tma_load_4d(kdst + C::TB + a * kAtom, mv, bar(BAR_KV_FULL + s), a * 64, h, t * BN, b);
+                        else tma_load_4d(kdst + C::TB + a * kAtom, mv, bar(BAR_KV_FULL + s), a * 64, t * BN, h, b);
+                    }
+                }
+                issued = g + 1;
+            }
+            if (*abort_flag) {   // let copies already in flight land before the CTA exits
+                for (int g = max(0, issued - 2); g < issued; ++g) {
+                    volatile int never = 0;
+                    wait_bar(bar(BAR_KV_FULL + (g & 1)), (g >> 1) & 1, &never, ERR_KV_FULL);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false, false);
+            constexpr uint32_t id_pv_old = idesc_bf16(128, D, false, true, true);
+            constexpr uint32_t id_pv_new = idesc_bf16(128, D, false, true, false);
+            constexpr uint32_t id_cs_old = idesc_bf16(128, 16, true, false, true);
+            constexpr uint32_t id_cs_new = idesc_bf16(128, 16, true, false, false);
+            const uint64_t ones = smem_desc(sbase + C::OFF_ONES, 128, 256, 0);
+            auto issue_qk = [&](int g) -> bool {
+                const int s = g & 1, use = g >> 1;
+                if (!wait_bar(bar(BAR_KV_FULL + s), use & 1, abort_flag, ERR_KV_FULL)) return false;
+                if (!wait_bar(bar(BAR_S_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_S_EMPTY)) return false;
+                tc_fence_after();
+                const uint32_t qa = sbase + (phase_of(g) == PH_OLD ? C::OFF_QH : C::OFF_Q);
+                const uint32_t ka = sbase + C::OFF_KV + 2 * C::TB * s;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + kColS + 128 * s, smem_desc(qa + off, 16, 1024, 2),
+                                smem_desc(ka + off, 16, 1024, 2), id_qk, kk > 0);
+                }
+                mma_commit(bar(BAR_S_FULL + s));
+                return true;
+            };
+            bool ok = issue_qk(0);
+            int pv = 0;
+            for (int g = 0; ok && g < total; ++g) {
+                if (g + 1 < total && !issue_qk(g + 1)) { ok = false; break; }
+                const int ph = phase_of(g), s = g & 1;
+                if (ph != PH_LSE) {
+                    if (!wait_bar(bar(BAR_P_FULL), pv & 1, abort_flag, ERR_P_FULL)) { ok = false; break; }
+                    tc_fence_after();
+                    const bool neg = ph == PH_OLD;
+                    const uint32_t pa = sbase + C::OFF_P;
+                    const uint32_t va = sbase + C::OFF_KV + 2 * C::TB * s + C::TB;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {   // acc += P[:, 16kk..] * V[16kk.., :]
+                        mma_bf16_ss(tmem + kColAcc,
+                                    smem_desc(pa + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024, 2),
+                                    smem_desc(va + kk * 2048, kAtom, 1024, 2), neg ? id_pv_old : id_pv_new,
+                                    (pv > 0 || kk > 0) ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk) {   // colsum = P^T[:, 16kk..] * ones
+                        mma_bf16_ss(tmem + kColCS, smem_desc(pa + kk * 2048, kAtom, 1024, 2), ones,
+                                    neg ? id_cs_old : id_cs_new, kk > 0);
+                    }
+                    mma_commit(bar(BAR_P_EMPTY));
+                    ++pv;
+                }
+                mma_commit(bar(BAR_KV_EMPTY + s));
+            }
+            if (ok) {
+                mma_commit(bar(BAR_ACC));
+            } else {   // drain whatever was issued before giving up
+                mma_commit(bar(BAR_DRAIN));
+                volatile int never = 0;
+                wait_bar(bar(BAR_DRAIN), 0, &never, ERR_ACC);
+            }
+        }
+    } else {
+        // ---------------- softmax / epilogue warps ----------------
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const float zo2 = (!first && row_ok) ? __ldg(p.z + bh * p.n_state + pos) * kLog2e : 0.f;
+        float m = 0.f, M = -INFINITY, L = 0.f, zn2 = INFINITY;
+        int pv = 0, prev_col = INT_MAX;
+        bool ok = true;
+        float *cb = p.c + bh * p.n_keys;
+        uint32_t pk[BN / 2];   // this row's P for one tile, bf16x2
+        for (int g = 0; g < total && ok; ++g) {
+            const int ph = phase_of(g), t = g % n_tiles, s = g & 1, use = g >> 1;
+            if (ph == PH_NEW && t == 0) {
+                if (first) zn2 = (M > -INFINITY) ? M + __log2f(L) : INFINITY;
+                else zn2 = (M > -INFINITY && m >= FLT_MIN) ? M + __log2f(L) - __log2f(m) : INFINITY;
+            }
+            // column indices of this tile: lane holds entries lane, lane+32, lane+64, lane+96
+            int jreg[4];
+            const int c0 = t * BN;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int cc = c0 + u * 32 + lane;
+                jreg[u] = cc < kcols ? (dense ? cc : __ldg(S + cc)) : INT_MAX;
+            }
+            const int jlast = __shfl_sync(0xffffffffu, jreg[3], 31);
+            const bool no_mask = (c0 + BN <= kcols) && jlast <= min_pos;
+            if (!wait_bar(bar(BAR_S_FULL + s), use & 1, abort_flag, ERR_S_FULL)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t sc = tmem + lane_base + kColS + 128 * s;
+            const float sub = ph == PH_OLD ? zo2 : zn2;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float sv[32];
+                tmem_ld_32x32b_x32(sc + 32 * u, sv);
+                tmem_wait_ld();
+                if (ph == PH_LSE) {
+                    float cmax = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int j = no_mask ? 0 : __shfl_sync(0xffffffffu, jreg[u], e);
+                        sv[e] = (row_ok && (no_mask || j <= pos)) ? sv[e] * p.sl2 : -INFINITY;
+                        cmax = fmaxf(cmax, sv[e]);
+                    }
+                    if (cmax > M) {
+                        L *= ex2(M - cmax);
+                        M = cmax;
+                    }
+                    float acc = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc += ex2(sv[e] - M);
+                    if (M > -INFINITY) L += acc;
+                } else {
+                    float msum = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float pr[2];
+#pragma unroll
+                        for (int f = 0; f < 2; ++f) {
+                            const int j = no_mask ? 0 : __shfl_sync(0xffffffffu, jreg[u], e + f);
+                            const float x = ex2(fmaf(sv[e + f], p.sl2, -sub));
+                            pr[f] = (row_ok && (no_mask || j <= pos)) ? x : 0.f;
+                            msum += pr[f];
+                        }
+                        pk[u * 16 + e / 2] = pack_bf16x2_rn(pr[0], pr[1]);
+                    }
+                    if (ph == PH_OLD) m += msum;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(BAR_S_EMPTY + s));
+            if (ph != PH_LSE) {
+                if (!wait_bar(bar(BAR_P_EMPTY), (pv & 1) ^ 1, abort_flag, ERR_P_EMPTY)) { ok = false; break; }
+                tc_fence_after();
+                if (pv > 0) {   // column sums of the previous P tile
+                    const float cs = tmem_ld_32x32b_x1(tmem + lane_base + kColCS);
+                    tmem_wait_ld();
+                    if (prev_col != INT_MAX && cs != 0.f) atomicAdd(cb + prev_col, cs);
+                }
+                uint8_t *pt = smem + C::OFF_P;
+#pragma unroll
+                for (int ch = 0; ch < BN / 8; ++ch)
+                    *reinterpret_cast<uint4 *>(pt + swz_off(r, ch)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(BAR_P_FULL));
+                // this thread's TMEM lane r is tile column r of the column-sum MMA;
+                // column r = (r/32)*32 + lane is held in jreg[r/32] of this lane
+                const int q4 = warp & 3;
+                prev_col = q4 == 0 ? jreg[0] : q4 == 1 ? jreg[1] : q4 == 2 ? jreg[2] : jreg[3];
+                ++pv;
+            }
+        }
+        if (ok && pv > 0) {
+            if (wait_bar(bar(BAR_P_EMPTY), (pv & 1) ^ 1, abort_flag, ERR_P_EMPTY)) {
+                tc_fence_after();
+                const float cs = tmem_ld_32x32b_x1(tmem + lane_base + kColCS);
+                tmem_wait_ld();
+                if (prev_col != INT_MAX && cs != 0.f) atomicAdd(cb + prev_col, cs);
+            } else {
+                ok = false;
+            }
+        }
+        if (ok && wait_bar(bar(BAR_ACC), 0, abort_flag, ERR_ACC)) {
+            tc_fence_after();
+            const bool update = row_ok && zn2 < INFINITY;
+            const long long srow = ((long long)b * p.n_state + max(pos, 0)) * p.H + h;
+            float4 *orow = reinterpret_cast<float4 *>(p.o + srow * D);
+#pragma unroll
+            for (int u = 0; u < D / 32; ++u) {
+                float av[32];
+                tmem_ld_32x32b_x32(tmem + lane_base + kColAcc + 32 * u, av);
+                tmem_wait_ld();
+                if (update) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        float4 v = first ? make_float4(0.f, 0.f, 0.f, 0.f) : orow[u * 8 + e];
+                        v.x += av[4 * e];
+                        v.y += av[4 * e + 1];
+                        v.z += av[4 * e + 2];
+                        v.w += av[4 * e + 3];
+                        orow[u * 8 + e] = v;
+                    }
+                }
+            }
+            if (update) {
+                p.z[bh * p.n_state + pos] = zn2 * kLn2;
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.q + srow * D);
+                uint4 *dst = reinterpret_cast<uint4 *>(p.q_hat + srow * D);
+#pragma unroll
+                for (int ch = 0; ch < D / 8; ++ch) dst[ch] = ldg_nc_v4(src + ch);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *ptr = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 4-D bf16 tensor map with a (64, box1, box2, 1) box and the 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *base, const cuuint64_t dims[4], const cuuint64_t strides_bytes[3],
+              cuuint32_t box1, cuuint32_t box2) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const cuuint32_t box[4] = {64, box1, box2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides_bytes, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
+    using Cf = Cfg<D>;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaFuncSetAttribute(tc_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    });
+    const bool dense = p.mode != FLASHLOOP_ATTN_LAZY;
+    CUtensorMap maps[4];
+    const uint16_t *src[4] = {p.k_old ? p.k_old : p.k_new, p.v_old ? p.v_old : p.v_new, p.k_new, p.v_new};
+    for (int i = 0; i < 4; ++i) {
+        bool ok;
+        if (dense) {   // cache layer [B, N_cap, H, d]; only the first n_keys positions are read
+            const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)p.H, (cuuint64_t)p.n_keys, (cuuint64_t)p.B};
+            const cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)p.H * D * 2,
+                                       (cuuint64_t)p.kv_rows * p.H * D * 2};
+            ok = make_map(&maps[i], src[i], dims, str, 1, BN);
+        } else {       // dense selected keys [B, H, K, d]
+            const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)p.K, (cuuint64_t)p.H, (cuuint64_t)p.B};
+            const cuuint64_t str[3] = {(cuuint64_t)D * 2, (cuuint64_t)p.K * D * 2, (cuuint64_t)p.H * p.K * D * 2};
+            ok = make_map(&maps[i], src[i], dims, str, BN, 1);
+        }
+        if (!ok) return cudaErrorInvalidValue;
+    }
+    KParams kp;
+    kp.mode = p.mode;
+    kp.H = p.H;
+    kp.n_keys = p.n_keys;
+    kp.n_state = p.n_state;
+    kp.R = p.R;
+    kp.K = dense ? p.n_keys : p.K;
+    kp.n_row_tiles = ceil_div(p.R, BM);
+    kp.row_pos = p.row_pos;
+    kp.key_idx = p.key_idx;
+    kp.q = p.q;
+    kp.q_hat = p.q_hat;
+    kp.o = p.o;
+    kp.z = p.z;
+    kp.c = p.c;
+    kp.sl2 = kLog2e / sqrtf((float)D);
+    dim3 grid(kp.n_row_tiles, p.H, p.B);
+    tc_attention_kernel<D><<<grid, kThreads, Cf::SMEM, s>>>(kp, maps[0], maps[1], maps[2], maps[3]);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_attention(const TcAttnParams &p, cudaStream_t s) {
+    if (p.R == 0) return cudaSuccess;
+    switch (p.d) {
+        case 64: return launch_d<64>(p, s);
+        case 96: return launch_d<96>(p, s);
+        case 128: return launch_d<128>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int32_t tc_attention_read_error(bool clear) {
+    int v = 0;
+    cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(int));
+    if (clear && v) {
+        int zero = 0;
+        cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(int));
+    }
+    return v;
+}
+
+}  // namespace fl

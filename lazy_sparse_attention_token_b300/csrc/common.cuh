@@ -1,0 +1,153 @@
+// common.cuh -- helpers shared by the FlashLoop CUDA sources (sm_103a only).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "flashloop.h"
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ != 1030)
+#error "this library is written for sm_103a only"
+#endif
+
+namespace fl {
+
+// ---- host bookkeeping (api.cu) -------------------------------------------
+void note_launch(int n = 1);
+flashloop_status_t set_error(flashloop_status_t st, const char *fmt, ...);
+flashloop_status_t check_launch(const char *what);
+
+constexpr int kMaxLoops = FLASHLOOP_MAX_LOOPS;
+
+// Device view of the delta layers needed to reconstruct one loop.
+struct DeltaView {
+    const uint16_t *k_base;            // [B, N_cap, H, d] bf16
+    const uint16_t *v_base;
+    int n_layers;                      // delta layers applied, ascending
+    const int32_t *slot[kMaxLoops];    // [B, N_cap]
+    const uint8_t *k_codes[kMaxLoops]; // [B, R_cap, H, d/2]
+    const uint16_t *k_scales[kMaxLoops];
+    const uint8_t *v_codes[kMaxLoops];
+    const uint16_t *v_scales[kMaxLoops];
+};
+
+// ---- launchers (one per kernel family) -----------------------------------
+// select.cu
+cudaError_t launch_token_scores(const uint16_t *h_prev, const uint16_t *h_cur, int B, int N, int D,
+                                float *scores, cudaStream_t s);
+cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t *out, cudaStream_t s);
+// kvcache.cu
+cudaError_t launch_gather_rows(const void *src, int B, int N, int row_bytes, const int32_t *idx, int R,
+                               void *dst, cudaStream_t s);
+cudaError_t launch_store_rows(const uint16_t *src, int B, int n_rows, int row_elems, uint16_t *dst,
+                              int dst_rows, int pos0, cudaStream_t s);
+cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, const uint16_t *v_l,
+                                int rows_are_tokens, int src_rows, const int32_t *active, int R, int at,
+                                int B, int N_cap, int H, int d, int R_cap, int32_t *out_idx,
+                                int32_t *out_slot, uint8_t *k_codes, uint16_t *k_scales, uint8_t *v_codes,
+                                uint16_t *v_scales, cudaStream_t s);
+cudaError_t launch_reconstruct_keys(const DeltaView &old_view, const DeltaView &new_view,
+                                    const int32_t *key_idx, int B, int H, int K, int N_cap, int d,
+                                    int R_cap, uint16_t *k_old, uint16_t *v_old, uint16_t *k_new,
+                                    uint16_t *v_new, cudaStream_t s);
+// attn_tc.cu (tensor-core prefill / dense attention)
+struct TcAttnParams {
+    int mode;            // flashloop_attn_mode_t
+    int B, H, d;
+    int n_keys;          // key positions
+    int n_state;         // state rows per sequence
+    int R;               // rows per sequence
+    const int32_t *row_pos;   // [B,R] or NULL (dense: row = key position)
+    int K;               // key columns per (b,h) (dense: n_keys)
+    const int32_t *key_idx;   // [B,H,K] or NULL (dense)
+    const uint16_t *q;
+    uint16_t *q_hat;
+    float *o, *z, *c;
+    // key/value sources: lazy = dense [B,H,K,d] buffers; dense = cache layers [B,N_cap,H,d]
+    const uint16_t *k_old, *v_old, *k_new, *v_new;
+    int kv_rows;         // rows of the source arrays per (b[,h]) (K or N_cap)
+};
+cudaError_t launch_tc_attention(const TcAttnParams &p, cudaStream_t s);
+int32_t tc_attention_read_error(bool clear);
+// attn_decode.cu (few-row attention reading the cache directly)
+struct DecodeAttnParams {
+    int mode;
+    int B, H, d;
+    int n_keys, n_state, R;
+    const int32_t *row_pos, *row_slot;
+    int K;
+    const int32_t *key_idx;   // NULL for dense modes (all keys)
+    const uint16_t *q;
+    uint16_t *q_hat;
+    float *o, *z, *c;
+    DeltaView old_view, new_view;   // reconstructions at loop-1 and loop
+    int N_cap, R_cap;
+    float *scratch;           // [B, H, R, K] x 2 logits
+};
+cudaError_t launch_decode_attention(const DecodeAttnParams &p, cudaStream_t s);
+
+// ---- device helpers -------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float *f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&t);
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Order-preserving map of a finite fp32 to uint32 (larger float -> larger
+// key); -0 is folded onto +0 so equal values compare equal.
+__device__ __forceinline__ uint32_t f32_order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Adds scale*code of every delta layer of `view` that holds token i to the
+// 8 fp32 values of chunk c8 (elements 8*c8 .. 8*c8+7) of head h.
+__device__ __forceinline__ void apply_deltas(const DeltaView &view, bool is_v, int m0, int m1, long long b,
+                                             int i, int h, int c8, int H, int d, int N_cap, int R_cap,
+                                             float rec[8]) {
+    for (int m = m0; m < m1; ++m) {
+        const int e = __ldg(view.slot[m] + b * N_cap + i);
+        if (e < 0) continue;
+        const long long ent = (b * R_cap + e) * H + h;
+        const uint8_t *codes = is_v ? view.v_codes[m] : view.k_codes[m];
+        const uint16_t *scales = is_v ? view.v_scales[m] : view.k_scales[m];
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(codes + ent * (d / 2)) + c8);
+        const float s = __half2float(__ushort_as_half(__ldg(scales + ent * (d / 32) + c8 / 4)));
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int q = ((int)(w << (28 - 4 * t))) >> 28;   // sign-extended nibble t
+            rec[t] = __fadd_rn(rec[t], __fmul_rn(s, (float)q));
+        }
+    }
+}
+
+__device__ __forceinline__ void load_base8(const uint16_t *base, long long b, int i, int h, int c8, int H,
+                                           int d, int N_cap, float rec[8]) {
+    const uint4 v = ldg_nc_v4(base + ((b * N_cap + i) * H + h) * (long long)d + c8 * 8);
+    unpack_bf16x8(v, rec);
+}
+
+inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+}  // namespace fl

@@ -1,0 +1,198 @@
+// kvcache.cu -- dense gathers and the base + int4-delta KV cache.
+//
+// rit.work page "FlashLoop: Fast and Memory-Efficient Looped Transformers via
+// Lazy Updates":
+//   section "Later loops change only part of the state": neighbouring KV sets
+//   differ less than whole states, so store a base plus small deltas;
+//   section "FlashLoop combines three kinds of saving": the cache is a
+//   compressed base plus a sequence of compressed deltas, a low-bit delta is
+//   written for active tokens and none for inactive ones (4-bit in the main
+//   experiments), and selected data is gathered into dense buffers.
+//
+// Arithmetic that must agree bit for bit with any other implementation of
+// the same definition is written with explicit IEEE intrinsics: fp32
+// reconstruction adds scale*code layer by layer in ascending order, the
+// delta is one fp32 subtraction, scale = fp16_rne(amax / 7) with an IEEE
+// divide, and code = rint_even(delta / scale) clamped to [-7, 7].
+#include "common.cuh"
+
+namespace fl {
+namespace {
+
+constexpr int kCopyWarps = 8;
+
+// dst[b, r, :] = src[b, idx[b, r], :]; one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(kCopyWarps * 32)
+gather_rows_kernel(const uint4 *__restrict__ src, int N, int vecs, const int32_t *__restrict__ idx,
+                   int R, long long rows, uint4 *__restrict__ dst) {
+    const long long row = (long long)blockIdx.x * kCopyWarps + threadIdx.x / 32;
+    if (row >= rows) return;
+    const long long b = row / R;
+    const int i = __ldg(idx + row);
+    const uint4 *s = src + (b * N + i) * (long long)vecs;
+    uint4 *d = dst + row * (long long)vecs;
+    for (int v = threadIdx.x & 31; v < vecs; v += 32) d[v] = ldg_nc_v4(s + v);
+}
+
+// dst[b, pos0 + r, :] = src[b, r, :] for r < n_rows.
+__global__ void __launch_bounds__(kCopyWarps * 32)
+store_rows_kernel(const uint4 *__restrict__ src, int n_rows, int vecs, uint4 *__restrict__ dst,
+                  int dst_rows, int pos0, long long rows) {
+    const long long row = (long long)blockIdx.x * kCopyWarps + threadIdx.x / 32;
+    if (row >= rows) return;
+    const long long b = row / n_rows, r = row % n_rows;
+    const uint4 *s = src + row * (long long)vecs;
+    uint4 *d = dst + (b * dst_rows + pos0 + r) * (long long)vecs;
+    for (int v = threadIdx.x & 31; v < vecs; v += 32) d[v] = ldg_nc_v4(s + v);
+}
+
+// One thread per (sequence, entry, head, 8-element chunk); four neighbouring
+// lanes cover one 32-element quantisation group. blockIdx.y: 0 = K, 1 = V.
+__global__ void __launch_bounds__(256)
+delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint16_t *__restrict__ v_l,
+                    int rows_are_tokens, int src_rows, const int32_t *__restrict__ active, int R, int at,
+                    int H, int d, int N_cap, int R_cap, long long total, int32_t *__restrict__ out_idx,
+                    int32_t *__restrict__ out_slot, uint8_t *__restrict__ k_codes,
+                    uint16_t *__restrict__ k_scales, uint8_t *__restrict__ v_codes,
+                    uint16_t *__restrict__ v_scales) {
+    const long long t_raw = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool in_range = t_raw < total;
+    // Lanes past the end redo the last element (no stores) so that every lane
+    // of the warp takes part in the group-max shuffles below.
+    const long long t = in_range ? t_raw : total - 1;
+    const bool is_v = blockIdx.y == 1;
+    const int chunks = d / 8;
+    const int c8 = (int)(t % chunks);
+    const long long rest = t / chunks;
+    const int h = (int)(rest % H);
+    const long long be = rest / H;   // b * R + e
+    const long long b = be / R;
+    const int e = (int)(be % R);
+    const int i = __ldg(active + be);
+    const long long src_row = rows_are_tokens ? (long long)i : (long long)e;
+
+    const uint16_t *x_l = is_v ? v_l : k_l;
+    float x[8], rec[8];
+    unpack_bf16x8(ldg_nc_v4(x_l + ((b * src_rows + src_row) * H + h) * (long long)d + c8 * 8), x);
+    load_base8(is_v ? view.v_base : view.k_base, b, i, h, c8, H, d, N_cap, rec);
+    apply_deltas(view, is_v, 0, view.n_layers, b, i, h, c8, H, d, N_cap, R_cap, rec);
+
+    float dl[8], amax = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        dl[u] = __fsub_rn(x[u], rec[u]);
+        amax = fmaxf(amax, fabsf(dl[u]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const __half sh = __float2half_rn(__fdiv_rn(amax, 7.0f));
+    const float s = __half2float(sh);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        int q = 0;
+        if (s > 0.f) {
+            const float r = rintf(__fdiv_rn(dl[u], s));
+            q = (int)fminf(7.f, fmaxf(-7.f, r));
+        }
+        packed |= (uint32_t)(q & 0xF) << (4 * u);
+    }
+    if (!in_range) return;
+    const long long ent = (b * R_cap + at + e) * H + h;
+    uint8_t *codes = is_v ? v_codes : k_codes;
+    uint16_t *scales = is_v ? v_scales : k_scales;
+    reinterpret_cast<uint32_t *>(codes + ent * (d / 2))[c8] = packed;
+    if ((c8 & 3) == 0) scales[ent * (d / 32) + c8 / 4] = __half_as_ushort(sh);
+    if (!is_v && h == 0 && c8 == 0) {
+        out_idx[b * R_cap + at + e] = i;
+        out_slot[b * N_cap + i] = at + e;
+    }
+}
+
+// For each selected key j = key_idx[b,h,r]: reconstruction at the old loop
+// (old_layers deltas) and at the new loop (new_layers deltas), bf16 RNE,
+// written densely as [B, H, K, d]. blockIdx.y: 0 = K, 1 = V.
+__global__ void __launch_bounds__(256)
+reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const int32_t *__restrict__ key_idx,
+                        int H, int K, int d, int N_cap, int R_cap, long long total,
+                        uint16_t *__restrict__ k_old, uint16_t *__restrict__ v_old,
+                        uint16_t *__restrict__ k_new, uint16_t *__restrict__ v_new) {
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= total) return;
+    const bool is_v = blockIdx.y == 1;
+    const int chunks = d / 8;
+    const int c8 = (int)(t % chunks);
+    const long long bhr = t / chunks;          // (b * H + h) * K + r
+    const long long bh = bhr / K;
+    const int h = (int)(bh % H);
+    const long long b = bh / H;
+    const int j = __ldg(key_idx + bhr);
+    float rec[8];
+    load_base8(is_v ? view.v_base : view.k_base, b, j, h, c8, H, d, N_cap, rec);
+    apply_deltas(view, is_v, 0, old_layers, b, j, h, c8, H, d, N_cap, R_cap, rec);
+    uint4 o;
+    o.x = pack_bf16x2_rn(rec[0], rec[1]);
+    o.y = pack_bf16x2_rn(rec[2], rec[3]);
+    o.z = pack_bf16x2_rn(rec[4], rec[5]);
+    o.w = pack_bf16x2_rn(rec[6], rec[7]);
+    reinterpret_cast<uint4 *>((is_v ? v_old : k_old) + bhr * d)[c8] = o;
+    apply_deltas(view, is_v, old_layers, new_layers, b, j, h, c8, H, d, N_cap, R_cap, rec);
+    o.x = pack_bf16x2_rn(rec[0], rec[1]);
+    o.y = pack_bf16x2_rn(rec[2], rec[3]);
+    o.z = pack_bf16x2_rn(rec[4], rec[5]);
+    o.w = pack_bf16x2_rn(rec[6], rec[7]);
+    reinterpret_cast<uint4 *>((is_v ? v_new : k_new) + bhr * d)[c8] = o;
+}
+
+}  // namespace
+
+cudaError_t launch_gather_rows(const void *src, int B, int N, int row_bytes, const int32_t *idx, int R,
+                               void *dst, cudaStream_t s) {
+    const long long rows = (long long)B * R;
+    if (rows == 0) return cudaSuccess;
+    gather_rows_kernel<<<ceil_div(rows, kCopyWarps), kCopyWarps * 32, 0, s>>>(
+        static_cast<const uint4 *>(src), N, row_bytes / 16, idx, R, rows, static_cast<uint4 *>(dst));
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_store_rows(const uint16_t *src, int B, int n_rows, int row_elems, uint16_t *dst,
+                              int dst_rows, int pos0, cudaStream_t s) {
+    const long long rows = (long long)B * n_rows;
+    if (rows == 0) return cudaSuccess;
+    store_rows_kernel<<<ceil_div(rows, kCopyWarps), kCopyWarps * 32, 0, s>>>(
+        reinterpret_cast<const uint4 *>(src), n_rows, row_elems / 8, reinterpret_cast<uint4 *>(dst), dst_rows,
+        pos0, rows);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, const uint16_t *v_l,
+                                int rows_are_tokens, int src_rows, const int32_t *active, int R, int at,
+                                int B, int N_cap, int H, int d, int R_cap, int32_t *out_idx,
+                                int32_t *out_slot, uint8_t *k_codes, uint16_t *k_scales, uint8_t *v_codes,
+                                uint16_t *v_scales, cudaStream_t s) {
+    const long long total = (long long)B * R * H * (d / 8);
+    if (total == 0) return cudaSuccess;
+    dim3 grid(ceil_div(total, 256), 2);
+    delta_append_kernel<<<grid, 256, 0, s>>>(view, k_l, v_l, rows_are_tokens, src_rows, active, R, at, H, d,
+                                             N_cap, R_cap, total, out_idx, out_slot, k_codes, k_scales,
+                                             v_codes, v_scales);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reconstruct_keys(const DeltaView &old_view, const DeltaView &new_view,
+                                    const int32_t *key_idx, int B, int H, int K, int N_cap, int d,
+                                    int R_cap, uint16_t *k_old, uint16_t *v_old, uint16_t *k_new,
+                                    uint16_t *v_new, cudaStream_t s) {
+    const long long total = (long long)B * H * K * (d / 8);
+    if (total == 0) return cudaSuccess;
+    dim3 grid(ceil_div(total, 256), 2);
+    reconstruct_keys_kernel<<<grid, 256, 0, s>>>(new_view, old_view.n_layers, new_view.n_layers, key_idx, H, K,
+                                                 d, N_cap, R_cap, total, k_old, v_old, k_new, v_new);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace fl

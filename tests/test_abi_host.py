@@ -1,0 +1,138 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every entry
+point the header declares, and rejects bad arguments on the host before
+touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import lazy_sparse_attention_token_b300 as fl
+from lazy_sparse_attention_token_b300 import build as flbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flashloop.h")
+
+OK, INVALID, UNSUPPORTED, CAPACITY, CUDA, WORKSPACE = 0, -1, -2, -3, -4, -5
+
+
+@pytest.fixture(scope="module")
+def L():
+    flbuild.build()
+    return fl.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flashloop_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) <= set(fl.flashloop.EXPORTS) | set(names)
+
+
+def test_binding_covers_every_entry_point():
+    for n in declared_functions():
+        assert n in fl.flashloop.EXPORTS, n
+
+
+def dims(**kw):
+    base = dict(B=1, N_cap=1024, H=4, d=64, R=256, K=103, T=4, T_dense=1, R_cap=256)
+    base.update(kw)
+    return fl.Dims(**base)
+
+
+def test_sizes(L):
+    dm = dims()
+    ws = fl.flashloop_workspace_bytes(dm)
+    assert ws >= 1024 * 4 + 4 * 1 * 4 * 103 * 64 * 2
+    cb = fl.flashloop_kv_cache_bytes(dm)
+    dense = 1 * 1024 * 4 * 64 * 2
+    per_delta_min = 256 * 4 + 1024 * 4 + 2 * 256 * 4 * (64 // 2 + 2 * 64 // 32)
+    assert cb >= 2 * dense + 3 * per_delta_min
+    assert cb <= 2 * dense + 3 * (per_delta_min + 6 * 256)
+    for bad in (dict(d=80), dict(R=0), dict(K=2000), dict(T_dense=5), dict(R_cap=10), dict(T=40)):
+        assert fl.flashloop_workspace_bytes(dims(**bad)) == 0
+        assert fl.flashloop_kv_cache_bytes(dims(**bad)) == 0
+
+
+def test_status_strings(L):
+    for s in (OK, INVALID, UNSUPPORTED, CAPACITY, CUDA, WORKSPACE, -6):
+        assert L.flashloop_status_string(s)
+    assert L.flashloop_status_string(123) == b"unknown status"
+
+
+P = ctypes.c_void_p
+
+
+def test_select_tokens_rejects_bad_args(L):
+    a, b, out = P(0x1000), P(0x2000), P(0x3000)
+    assert L.flashloop_select_tokens(None, b, 1, 8, 16, 2, out, None, None, 0, None) == INVALID
+    assert L.flashloop_select_tokens(P(0x1001), b, 1, 8, 16, 2, out, None, None, 0, None) == INVALID
+    assert L.flashloop_select_tokens(a, b, 1, 8, 12, 2, out, None, None, 0, None) == INVALID   # D % 8
+    assert L.flashloop_select_tokens(a, b, 1, 8, 16, 9, out, None, None, 0, None) == INVALID   # R > N
+    assert L.flashloop_select_tokens(a, b, 1, 8, 16, 0, out, None, None, 0, None) == INVALID
+    assert L.flashloop_select_tokens(a, b, 1, 8, 16, 2, out, None, None, 0, None) == WORKSPACE  # no scores buffer
+    assert b"workspace" in L.flashloop_last_error()
+
+
+def test_gather_and_keys_reject_bad_args(L):
+    assert L.flashloop_gather(P(0x1000), 1, 8, 24, P(0x2000), 2, P(0x3000), None) == INVALID      # row_bytes % 16
+    assert L.flashloop_gather(P(0x1008), 1, 8, 32, P(0x2000), 2, P(0x3000), None) == INVALID      # misaligned
+    assert L.flashloop_select_keys(P(0x1000), 1, 4, 8, 9, P(0x2000), None, 0, None) == INVALID    # K > N
+    assert L.flashloop_select_keys(None, 1, 4, 8, 2, P(0x2000), None, 0, None) == INVALID
+
+
+def test_cache_init_rejects_bad_args(L):
+    c = fl.KVCache()
+    dm = dims()
+    need = fl.flashloop_kv_cache_bytes(dm)
+    assert L.flashloop_kv_cache_init(ctypes.byref(c), P(0x10000), need - 1, ctypes.byref(dm), None) == CAPACITY
+    assert L.flashloop_kv_cache_init(ctypes.byref(c), P(0x10010), need, ctypes.byref(dm), None) == INVALID
+    bad = dims(d=80)
+    assert L.flashloop_kv_cache_init(ctypes.byref(c), P(0x10000), need, ctypes.byref(bad), None) == UNSUPPORTED
+
+
+def fake_cache(dm):
+    """A descriptor with fake (never dereferenced) pointers for host-side checks."""
+    c = fl.KVCache()
+    c.dims = dm
+    c.n_tokens = dm.N_cap
+    for t in range(dm.T_dense):
+        c.k_dense[t] = 0x100000 * (t + 1)
+        c.v_dense[t] = 0x100000 * (t + 1) + 0x80000
+    return c
+
+
+def test_append_and_attention_reject_bad_args(L):
+    dm = dims()
+    c = fake_cache(dm)
+    k, v, act = P(0x200000), P(0x300000), P(0x400000)
+    # loop 1 is dense: no delta layer
+    assert L.flashloop_kv_delta_append(ctypes.byref(c), 1, k, v, 1, act, 4, 0, None) == INVALID
+    # appending past the layer's capacity
+    assert L.flashloop_kv_delta_append(ctypes.byref(c), 2, k, v, 1, act, 300, 0, None) == CAPACITY
+    # appending at an offset that is neither 0 nor the current count
+    assert L.flashloop_kv_delta_append(ctypes.byref(c), 2, k, v, 1, act, 4, 7, None) == INVALID
+    # dense store of a lazy loop
+    assert L.flashloop_kv_dense_store(ctypes.byref(c), 2, k, v, 0, 4, None) == INVALID
+    assert L.flashloop_kv_dense_store(ctypes.byref(c), 1, k, v, 1020, 8, None) == CAPACITY
+    a = fl.AttnArgs()
+    a.mode, a.loop, a.n_keys, a.n_state, a.R = fl.LAZY, 2, 1024, 1024, 4
+    a.q = a.q_hat = a.o = 0x500000
+    a.z = a.c = 0x600000
+    a.cache = ctypes.pointer(c)
+    assert L.flashloop_lazy_attention(ctypes.byref(a), None) == INVALID       # no key_idx
+    a.mode = fl.DENSE
+    assert L.flashloop_lazy_attention(ctypes.byref(a), None) == INVALID       # loop 2 is lazy
+    a.mode, a.loop = fl.FIRST_DENSE, 2
+    assert L.flashloop_lazy_attention(ctypes.byref(a), None) == INVALID
+    s = fl.StepArgs()
+    s.loop = 2
+    s.cache = ctypes.pointer(c)
+    assert L.flashloop_loop_step(ctypes.byref(s), None) == WORKSPACE
