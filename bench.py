@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Benchmark of the FlashLoop lazy loop step on B300.
+
+One step = one lazy loop of the looped model through flashloop_loop_step:
+token change scores and top-r selection, int4 K/V delta append, top-k key
+columns from the previous loop's column mass, reconstruct-gather of the
+selected keys, and mass-preserving tensor-core attention over them.
+The workload is the 32K prefill (B=1, N=32768, H=16, d=128, T=4 loops with
+loop 1 dense, r=15%, k=10%); steps cycle through lazy loops 2..T of seeded
+synthetic inputs resident in HBM (two 134 MB hidden-state tensors per step,
+so every step reads more than the 126 MB L2).
+
+Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle on
+the host cores instead (a bounded sample of the same workload per step).
+Multi-GPU (torchrun): every rank runs its own replica (no collective on
+the data path), value = all ranks' tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "lazy loop-step tokens/s at 32K prefill; % of tensor/HBM roofline on 1 B300"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0}
+
+
+# --------------------------------------------------------------------------
+# process layout
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            uuid = str(device_index)
+        self.target = uuid
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50", "-i", self.target],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None, "samples": len(rows), "reasons": reasons}
+
+
+# --------------------------------------------------------------------------
+# algorithmic work per step (what the method must move or compute)
+
+def pair_count(A: torch.Tensor, S: torch.Tensor) -> int:
+    """sum over (b, h, active row i) of |{j in S[b,h] : j <= i}|."""
+    B, H, K = S.shape
+    tot = 0
+    for b in range(B):
+        cnt = torch.searchsorted(S[b].contiguous(), A[b].expand(H, -1).contiguous(), right=True)
+        tot += int(cnt.sum().item())
+    return tot
+
+
+def hbm_bytes(w, R, K):
+    """Algorithmic HBM bytes per launch of the streaming kernels (bf16 = 2 B)."""
+    B, N, H, d = w.B, w.N, w.H, w.d
+    D = H * d
+    delta_entry = H * (d // 2 + 2 * (d // 32))           # one token's int4 codes + fp16 scales
+    return {
+        "token_scores": 2 * B * N * D * 2 + B * N * 4,
+        "topk": None,   # two launches of different sizes (tokens, keys); reported by time only
+        # K and V: loop-l rows + base rows read, codes and scales written (earlier delta layers not counted)
+        "delta_append": 2 * (B * R * D * 2 + B * R * D * 2 + B * R * delta_entry) + B * R * 8,
+        # K and V base rows of the selected keys read, old and new bf16 copies written
+        "reconstruct_keys": 2 * (B * H * K * d * 2 + 2 * B * H * K * d * 2) + B * H * K * 4,
+    }
+
+
+# --------------------------------------------------------------------------
+# the CUDA path
+
+def native(args, world, rank, local):
+    import lazy_sparse_attention_token_b300 as fl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload]
+    R, K = synth.active_count(w), synth.key_count(w)
+    dims = fl.make_dims(w.B, w.N, w.H, w.d, R, K, w.T, w.T_dense, R_cap=R)
+    cache = fl.Cache(dims, device=dev)
+    cache.n_tokens = w.N
+    ws = fl.workspace_for(dims, device=dev)
+    loops = [x for x in synth.prefill_loops(w, device=dev)]
+    q_hat = torch.zeros(w.B, w.N, w.H, w.d, dtype=torch.bfloat16, device=dev)
+    o = torch.zeros(w.B, w.N, w.H, w.d, dtype=torch.float32, device=dev)
+    z = torch.zeros(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    c = torch.zeros(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    lazy = list(range(w.T_dense + 1, w.T + 1))
+    act = {l: torch.empty(w.B, R, dtype=torch.int32, device=dev) for l in lazy}
+    keys = {l: torch.empty(w.B, w.H, K, dtype=torch.int32, device=dev) for l in lazy}
+    scores = torch.empty(w.B, w.N, dtype=torch.float32, device=dev)
+
+    def step_loop(l):
+        x = loops[l - 1]
+        if l <= w.T_dense:
+            fl.flashloop_loop_step(cache, l, x["Q"], x["K"], x["V"], q_hat, o, z, c, ws)
+        else:
+            fl.flashloop_loop_step(cache, l, x["Q"], x["K"], x["V"], q_hat, o, z, c, ws,
+                                   h_prev=loops[l - 2]["H"], h_cur=x["H"], active_idx=act[l], key_idx=keys[l],
+                                   scores=scores)
+
+    for l in range(1, w.T_dense + 1):
+        step_loop(l)
+    torch.cuda.synchronize()
+    state1 = (q_hat.clone(), o.clone(), z.clone(), c.clone()) if (rank == 0 and not args.no_cpu_baseline) else None
+    for i in range(args.warmup):
+        step_loop(lazy[i % len(lazy)])
+    torch.cuda.synchronize()
+    assert fl.flashloop_device_status() == 0
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    fl.flashloop_timing_read()          # drop anything recorded so far
+    fl.flashloop_timing_enable(True)
+    n0 = fl.flashloop_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0.record()
+    for i in range(args.steps):
+        step_loop(lazy[(args.warmup + i) % len(lazy)])
+    ev1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    fl.flashloop_timing_enable(False)
+    launches = fl.flashloop_launch_count() - n0
+    per_kernel = fl.flashloop_timing_read()
+    assert fl.flashloop_device_status() == 0
+    secs = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    tokens = w.B * w.N * args.steps * world
+    value = tokens / secs
+
+    # roofline of the kernels, from the sets the timed steps actually used
+    occ = {l: sum(1 for i in range(args.steps) if lazy[(args.warmup + i) % len(lazy)] == l) for l in lazy}
+    pairs = {l: pair_count(act[l], keys[l]) for l in lazy}
+    mean_pairs = sum(pairs[l] * occ[l] for l in lazy) / max(1, args.steps)
+    flops_attn = 4 * 2 * w.d * mean_pairs          # QK old, QK new, PV old, PV new
+    peaks, peak_kind = load_peaks()
+    kernels = {}
+    hb = hbm_bytes(w, R, K)
+    for name, (ms, n) in per_kernel.items():
+        ent = {"launches": n, "ms_per_launch": ms / max(1, n), "share": None}
+        if name == "tc_attention":
+            ent.update(bound="tensor", unit="TFLOP/s", flop_per_launch=flops_attn,
+                       achieved=flops_attn / (ms / n / 1e3) / 1e12)
+            ent["frac"] = ent["achieved"] / peaks["bf16_tflops"]
+        elif hb.get(name):
+            ent.update(bound="hbm", unit="GB/s", bytes_per_launch=hb[name],
+                       achieved=hb[name] / (ms / n / 1e3) / 1e9)
+            ent["frac"] = ent["achieved"] / peaks["hbm_gbs"]
+        kernels[name] = ent
+    tot = sum(ms for ms, _ in per_kernel.values())
+    for name, (ms, n) in per_kernel.items():
+        kernels[name]["share"] = ms / tot if tot else None
+    top = max(kernels, key=lambda k: kernels[k]["share"] or 0)
+    tk = kernels[top]
+    roofline = {"kernel": top, "bound": tk.get("bound"), "achieved": tk.get("achieved"),
+                "peak": peaks["bf16_tflops"] if tk.get("bound") == "tensor" else peaks["hbm_gbs"],
+                "unit": tk.get("unit"), "frac": tk.get("frac"), "traffic": None,
+                "peak_source": f"{peak_kind} ({'bf16 burst' if tk.get('bound') == 'tensor' else 'copy'})",
+                "units_per_launch": (f"{mean_pairs:.0f} (row, key) pairs x 4 contractions x 2 d flop"
+                                     if top == "tc_attention" else None)}
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        tr = json.load(open(prof)).get(top)
+        if tr and tr.get("workload") == args.workload:
+            roofline["traffic"] = tr.get("bytes_per_launch")
+
+    e2e = None if args.no_e2e else e2e_leg(args, w, fl, cache, ws, loops, q_hat, o, z, c, act, keys, scores, lazy,
+                                           dev, world)
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload} prefill lazy loop: B={w.B}, N={w.N}, H={w.H}, d={w.d}, "
+                               f"T={w.T} (loop 1 dense), r={float(w.r):.2f} (R={R}), k={float(w.k):.2f} (K={K})",
+                   "global_batch": w.B * world, "seq_len": w.N, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: each step reads two 134 MB hidden-state tensors",
+                   "active_tokens_per_s": w.B * R * args.steps * world / secs},
+        "roofline": roofline, "kernels": kernels, "gpu_launches": launches,
+        "clocks": clk, "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, R, K, state1, budget_s=args.cpu_budget)
+    return out
+
+
+def e2e_leg(args, w, fl, cache, ws, loops, q_hat, o, z, c, act, keys, scores, lazy, dev, world):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory and reads the active rows' outputs back."""
+    host = {l: {n: loops[l - 1][n].cpu().pin_memory() for n in ("H", "Q", "K", "V")} for l in lazy}
+    R = act[lazy[0]].shape[1]
+    out_dev = torch.empty(w.B, R, w.H, w.d, dtype=torch.float32, device=dev)
+    out_host = torch.empty(w.B, R, w.H, w.d, dtype=torch.float32).pin_memory()
+    idx_host = torch.empty(w.B, R, dtype=torch.int32).pin_memory()
+    steps = min(args.steps, args.e2e_steps)
+
+    def one(i):
+        l = lazy[i % len(lazy)]
+        x = loops[l - 1]
+        for n in ("H", "Q", "K", "V"):
+            x[n].copy_(host[l][n], non_blocking=True)
+        fl.flashloop_loop_step(cache, l, x["Q"], x["K"], x["V"], q_hat, o, z, c, ws,
+                               h_prev=loops[l - 2]["H"], h_cur=x["H"], active_idx=act[l], key_idx=keys[l],
+                               scores=scores)
+        fl.flashloop_gather(o, act[l], out_dev)
+        out_host.copy_(out_dev, non_blocking=True)
+        idx_host.copy_(act[l], non_blocking=True)
+
+    for i in range(2):
+        one(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for i in range(steps):
+        one(i)
+    ev1.record()
+    torch.cuda.synchronize()
+    secs = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    h2d = sum(host[lazy[0]][n].numel() * host[lazy[0]][n].element_size() for n in ("H", "Q", "K", "V"))
+    d2h = out_host.numel() * 4 + idx_host.numel() * 4
+    return {"value": w.B * w.N * steps * world / secs, "unit": "tokens/s", "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle (reported baseline; also the reference arm)
+
+def _oracle_inputs(w, n_heads, device):
+    """Host copies (bf16 bits) of the loop-1 and loop-2 tensors the oracle
+    steps over: hidden states and K/V of every head, queries and loop-1 K/V
+    of the first `n_heads` heads."""
+    import oracle
+    it = synth.prefill_loops(w, device=device, last=2)
+    x1, x2 = next(it), next(it)
+    bits = oracle.bits
+    heads = list(range(n_heads))
+    sl = lambda t: bits(t[:, :, heads].contiguous())
+    return {"H1": bits(x1["H"]), "H2": bits(x2["H"]), "K1": bits(x1["K"]), "V1": bits(x1["V"]),
+            "K2": bits(x2["K"]), "V2": bits(x2["V"]),
+            "k1": sl(x1["K"]), "v1": sl(x1["V"]), "q1": sl(x1["Q"]), "q2": sl(x2["Q"])}
+
+
+def _oracle_loop1(w, inp, n_heads):
+    """The oracle's own dense loop 1 on the sampled heads (seeds the state)."""
+    from oracle import loop as oloop
+    st = oloop.dense_loop(1, inp["q1"], inp["k1"], inp["v1"], oloop.Cache(),
+                          oloop.empty_state(w.B, w.N, n_heads, w.d))
+    inp.update(qh1=st.qhat, o1=st.o, z1=st.z, c1=st.c)
+
+
+def _oracle_step(w, R, K, inp, n_heads, rows_frac=1.0):
+    """One oracle lazy step (loop 2) on a sample: token scores, top-r and the
+    K/V delta append over every token and head; key selection,
+    reconstruction and lazy attention on `n_heads` heads and a `rows_frac`
+    share of the active rows. Returns (seconds scaled to the whole step,
+    seconds measured)."""
+    import oracle
+    t0 = time.perf_counter()
+    sc = oracle.token_scores(inp["H1"], inp["H2"])
+    A = oracle.topk(sc, R)
+    lk = oracle.kv_delta_append(inp["K2"], inp["K1"], [], A)
+    lv = oracle.kv_delta_append(inp["V2"], inp["V1"], [], A)
+    t1 = time.perf_counter()
+    heads = list(range(n_heads))
+    S = oracle.topk(inp["c1"].astype(np.float64), K)
+    sub = lambda lay: oracle.DeltaLayer(lay.idx, lay.codes[:, :, heads], lay.scales[:, :, heads])
+    k_new = oracle.reconstruct(inp["k1"], [sub(lk)], want_f32=False)[1]
+    v_new = oracle.reconstruct(inp["v1"], [sub(lv)], want_f32=False)[1]
+    n_rows = max(1, int(round(R * rows_frac)))
+    rows = A if n_rows >= R else A[:, np.linspace(0, R - 1, n_rows).astype(np.int64)]
+    oracle.attention(False, rows, rows, inp["q2"], inp["qh1"], inp["o1"], inp["z1"], inp["c1"], S,
+                     inp["k1"], inp["v1"], k_new, v_new)
+    t2 = time.perf_counter()
+    return (t1 - t0) + (t2 - t1) * (w.H / n_heads) * (R / n_rows), t2 - t0
+
+
+def _rows_frac_for(w, R, K, inp, n_heads, budget_s):
+    """Share of the active rows that keeps one sampled step near `budget_s`."""
+    _, took = _oracle_step(w, R, K, inp, n_heads, rows_frac=0.02)
+    return float(min(1.0, max(0.02, 0.02 * budget_s / max(took, 1e-3))))
+
+
+def _omp_threads():
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def cpu_baseline(w, R, K, gpu_state, budget_s=20.0):
+    """The oracle as it stands, on the host cores, over a bounded sample of
+    the same lazy step; it starts from the GPU's loop-1 state (sampled heads)."""
+    import oracle
+    oracle.build()
+    n_heads = 1
+    inp = _oracle_inputs(w, n_heads, "cuda")
+    qh, o, z, c = gpu_state
+    inp.update(qh1=oracle.bits(qh[:, :, :n_heads].contiguous()), o1=o[:, :, :n_heads].cpu().numpy(),
+               z1=z[:, :n_heads].cpu().numpy(), c1=c[:, :n_heads].cpu().numpy())
+    frac = _rows_frac_for(w, R, K, inp, n_heads, budget_s)
+    est, took = _oracle_step(w, R, K, inp, n_heads, frac)
+    return {"value": w.B * w.N / est, "unit": "tokens/s", "cores": _omp_threads(), "kind": "oracle",
+            "sample": (f"one lazy step of the {w.name} workload: token scores, top-r and K/V delta append over all "
+                       f"{w.N} tokens; key selection, reconstruction and lazy attention on {n_heads} of {w.H} heads "
+                       f"and {frac:.1%} of the {R} active rows, scaled to the whole step ({took:.1f} s measured)")}
+
+
+def reference(args, world, rank):
+    """`--impl reference`: the CPU oracle as it stands, timed on the host cores."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    w = synth.WORKLOADS[args.workload]
+    R, K = synth.active_count(w), synth.key_count(w)
+    n_heads = 1
+    inp = _oracle_inputs(w, n_heads, "cpu")
+    _oracle_loop1(w, inp, n_heads)
+    per_step = max(0.5, args.ref_budget / max(1, args.steps + args.warmup))
+    frac = _rows_frac_for(w, R, K, inp, n_heads, per_step)
+    for _ in range(args.warmup):
+        _oracle_step(w, R, K, inp, n_heads, frac)
+    ests, took = [], 0.0
+    for _ in range(args.steps):
+        e, t = _oracle_step(w, R, K, inp, n_heads, frac)
+        ests.append(e)
+        took += t
+    secs = sum(ests)
+    value = w.B * w.N * args.steps / secs
+    cores = _omp_threads()
+    sample = (f"per step: token scores, top-r and K/V delta append over all {w.N} tokens; key selection, "
+              f"reconstruction and lazy attention on {n_heads} of {w.H} heads and {frac:.1%} of the {R} active "
+              f"rows, scaled to the full step ({took:.1f} s measured over {args.steps} steps)")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload} prefill lazy loop: B={w.B}, N={w.N}, H={w.H}, d={w.d}, "
+                                   f"T={w.T} (loop 1 dense), r={float(w.r):.2f} (R={R}), k={float(w.k):.2f} (K={K})"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=30)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="32k", choices=["tiny", "8k", "32k"])
+    ap.add_argument("--e2e-steps", type=int, default=60)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_info()
+    if args.impl == "reference":
+        out = reference(args, world, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    dist_init(world, "nccl")
+    out = native(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -263,6 +263,19 @@ flashloop_status_t flashloop_device_status(int32_t *word);
  * process (a counter for benchmarks). */
 int64_t flashloop_launch_count(void);
 
+/* Per-kernel timing for benchmarks. While enabled, every kernel launch of
+ * this library is bracketed by two CUDA events recorded on the launch's own
+ * stream. */
+flashloop_status_t flashloop_timing_enable(int32_t on);
+
+/* SYNCHRONISES the current device, then reports, per kernel family, its
+ * name (written to names + k*name_len, NUL-terminated), the summed event
+ * time in ms and the number of launches since the previous read, and
+ * clears the records. Returns the number of families written (at most
+ * max_kinds), or -1 if the synchronisation failed. */
+int32_t flashloop_timing_read(char *names, int32_t name_len, double *total_ms, int64_t *launches,
+                              int32_t max_kinds);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,6 +13,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "common.cuh"
 
@@ -36,6 +37,45 @@ __global__ void fill_rows_kernel(int32_t *pos, int32_t *slot, int B, int value) 
 }  // namespace
 
 void note_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// ---- optional per-kernel timing ---------------------------------------------
+namespace {
+struct TimingRec {
+    std::string name;
+    cudaEvent_t ev0, ev1;
+};
+std::mutex g_timing_mu;
+std::atomic<bool> g_timing_on{false};
+std::vector<TimingRec> g_timing;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pooled_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+}  // namespace
+
+KernelTimer::KernelTimer(const char *name, cudaStream_t s) : rec_(-1), s_(s) {
+    note_launch();
+    if (!g_timing_on.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    TimingRec r{name, pooled_event(), pooled_event()};
+    cudaEventRecord(r.ev0, s);
+    g_timing.push_back(r);
+    rec_ = (int)g_timing.size() - 1;
+}
+
+KernelTimer::~KernelTimer() {
+    if (rec_ < 0) return;
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    if (rec_ < (int)g_timing.size()) cudaEventRecord(g_timing[rec_].ev1, s_);
+}
 
 flashloop_status_t set_error(flashloop_status_t st, const char *fmt, ...) {
     char buf[512];
@@ -174,6 +214,46 @@ const char *flashloop_status_string(flashloop_status_t s) {
 const char *flashloop_last_error(void) { return g_last_error.c_str(); }
 
 int64_t flashloop_launch_count(void) { return g_launches.load(); }
+
+flashloop_status_t flashloop_timing_enable(int32_t on) {
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    g_timing_on.store(on != 0);
+    return FLASHLOOP_OK;
+}
+
+int32_t flashloop_timing_read(char *names, int32_t name_len, double *total_ms, int64_t *launches, int32_t max_kinds) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    std::vector<std::string> kinds;
+    std::vector<double> ms;
+    std::vector<int64_t> cnt;
+    for (const TimingRec &r : g_timing) {
+        float t = 0.f;
+        cudaEventElapsedTime(&t, r.ev0, r.ev1);
+        size_t k = 0;
+        while (k < kinds.size() && kinds[k] != r.name) ++k;
+        if (k == kinds.size()) {
+            kinds.push_back(r.name);
+            ms.push_back(0.0);
+            cnt.push_back(0);
+        }
+        ms[k] += t;
+        cnt[k] += 1;
+        g_event_pool.push_back(r.ev0);
+        g_event_pool.push_back(r.ev1);
+    }
+    g_timing.clear();
+    const int n = (int)kinds.size() < max_kinds ? (int)kinds.size() : max_kinds;
+    for (int k = 0; k < n; ++k) {
+        if (names && name_len > 0) {
+            strncpy(names + (size_t)k * name_len, kinds[k].c_str(), (size_t)name_len - 1);
+            names[(size_t)k * name_len + name_len - 1] = 0;
+        }
+        if (total_ms) total_ms[k] = ms[k];
+        if (launches) launches[k] = cnt[k];
+    }
+    return n;
+}
 
 size_t flashloop_workspace_bytes(const flashloop_dims_t *dims) {
     if (check_dims(dims) != FLASHLOOP_OK) return 0;
@@ -460,8 +540,10 @@ flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop
         const int pos = n - 1;
         int32_t *rows = reinterpret_cast<int32_t *>(ws + W.rows);
         int32_t *slots = reinterpret_cast<int32_t *>(ws + W.slots);
-        fill_rows_kernel<<<ceil_div(dm.B, 128), 128, 0, stream>>>(rows, slots, dm.B, pos);
-        note_launch();
+        {
+            KernelTimer kt("fill_rows", stream);
+            fill_rows_kernel<<<ceil_div(dm.B, 128), 128, 0, stream>>>(rows, slots, dm.B, pos);
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "fill_rows");
         if (dense) {

@@ -106,9 +106,14 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
     unpack_bf16x8(ldg_nc_v4(p.q + srow + c8 * 8), qn);
     if (!first) unpack_bf16x8(ldg_nc_v4(p.q_hat + srow + c8 * 8), qo);
 
-    // pass 1: logits of every key in the list
-    for (int t = grp; t < nk; t += kGroups) {
-        const int j = dense ? t : __ldg(S + t);
+    // pass 1: logits of every key in the list. Both 16-lane groups of a warp
+    // run the same number of iterations (a group past the end recomputes
+    // key 0 and stores nothing) because the sums below shuffle across the
+    // whole warp.
+    for (int t0 = 0; t0 < nk; t0 += kGroups) {
+        const int t = t0 + grp;
+        const bool tv = t < nk;
+        const int j = dense ? (tv ? t : 0) : __ldg(S + (tv ? t : 0));
         float kn[8], ko[8];
         float so = 0.f, sn = 0.f;
         if (p.shared_base) {
@@ -132,7 +137,7 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
         if (!has_chunk) sn = so = 0.f;
         sn = group16_sum(sn);
         so = group16_sum(so);
-        if (gl == 0) {
+        if (tv && gl == 0) {
             tau[t] = sn * p.scale;
             sig[t] = so * p.scale;
         }
@@ -235,8 +240,10 @@ cudaError_t launch_d(const DecodeAttnParams &q, cudaStream_t s) {
     p.shared_base = q.mode == FLASHLOOP_ATTN_LAZY;
     p.scale = 1.0f / sqrtf((float)D);
     const long long grid = (long long)q.B * q.H * q.R;
-    decode_attention_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(p);
-    note_launch();
+    {
+        KernelTimer kt("decode_attention", s);
+        decode_attention_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(p);
+    }
     return cudaGetLastError();
 }
 

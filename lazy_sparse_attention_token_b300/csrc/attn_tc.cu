@@ -509,8 +509,10 @@ cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
     kp.c = p.c;
     kp.sl2 = kLog2e / sqrtf((float)D);
     dim3 grid(kp.n_row_tiles, p.H, p.B);
-    tc_attention_kernel<D><<<grid, kThreads, Cf::SMEM, s>>>(kp, maps[0], maps[1], maps[2], maps[3]);
-    note_launch();
+    {
+        KernelTimer kt("tc_attention", s);
+        tc_attention_kernel<D><<<grid, kThreads, Cf::SMEM, s>>>(kp, maps[0], maps[1], maps[2], maps[3]);
+    }
     return cudaGetLastError();
 }
 

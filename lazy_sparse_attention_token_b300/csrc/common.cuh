@@ -16,6 +16,17 @@ namespace fl {
 
 // ---- host bookkeeping (api.cu) -------------------------------------------
 void note_launch(int n = 1);
+
+// Brackets one kernel launch with CUDA events on its stream while timing is
+// enabled (flashloop_timing_enable); counts the launch either way.
+class KernelTimer {
+  public:
+    KernelTimer(const char *name, cudaStream_t s);
+    ~KernelTimer();
+  private:
+    int rec_;
+    cudaStream_t s_;
+};
 flashloop_status_t set_error(flashloop_status_t st, const char *fmt, ...);
 flashloop_status_t check_launch(const char *what);
 

@@ -150,9 +150,11 @@ cudaError_t launch_gather_rows(const void *src, int B, int N, int row_bytes, con
                                void *dst, cudaStream_t s) {
     const long long rows = (long long)B * R;
     if (rows == 0) return cudaSuccess;
-    gather_rows_kernel<<<ceil_div(rows, kCopyWarps), kCopyWarps * 32, 0, s>>>(
+    {
+        KernelTimer kt("gather", s);
+        gather_rows_kernel<<<ceil_div(rows, kCopyWarps), kCopyWarps * 32, 0, s>>>(
         static_cast<const uint4 *>(src), N, row_bytes / 16, idx, R, rows, static_cast<uint4 *>(dst));
-    note_launch();
+    }
     return cudaGetLastError();
 }
 
@@ -160,10 +162,12 @@ cudaError_t launch_store_rows(const uint16_t *src, int B, int n_rows, int row_el
                               int dst_rows, int pos0, cudaStream_t s) {
     const long long rows = (long long)B * n_rows;
     if (rows == 0) return cudaSuccess;
-    store_rows_kernel<<<ceil_div(rows, kCopyWarps), kCopyWarps * 32, 0, s>>>(
+    {
+        KernelTimer kt("store_rows", s);
+        store_rows_kernel<<<ceil_div(rows, kCopyWarps), kCopyWarps * 32, 0, s>>>(
         reinterpret_cast<const uint4 *>(src), n_rows, row_elems / 8, reinterpret_cast<uint4 *>(dst), dst_rows,
         pos0, rows);
-    note_launch();
+    }
     return cudaGetLastError();
 }
 
@@ -175,10 +179,12 @@ cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, cons
     const long long total = (long long)B * R * H * (d / 8);
     if (total == 0) return cudaSuccess;
     dim3 grid(ceil_div(total, 256), 2);
-    delta_append_kernel<<<grid, 256, 0, s>>>(view, k_l, v_l, rows_are_tokens, src_rows, active, R, at, H, d,
+    {
+        KernelTimer kt("delta_append", s);
+        delta_append_kernel<<<grid, 256, 0, s>>>(view, k_l, v_l, rows_are_tokens, src_rows, active, R, at, H, d,
                                              N_cap, R_cap, total, out_idx, out_slot, k_codes, k_scales,
                                              v_codes, v_scales);
-    note_launch();
+    }
     return cudaGetLastError();
 }
 
@@ -189,9 +195,11 @@ cudaError_t launch_reconstruct_keys(const DeltaView &old_view, const DeltaView &
     const long long total = (long long)B * H * K * (d / 8);
     if (total == 0) return cudaSuccess;
     dim3 grid(ceil_div(total, 256), 2);
-    reconstruct_keys_kernel<<<grid, 256, 0, s>>>(new_view, old_view.n_layers, new_view.n_layers, key_idx, H, K,
+    {
+        KernelTimer kt("reconstruct_keys", s);
+        reconstruct_keys_kernel<<<grid, 256, 0, s>>>(new_view, old_view.n_layers, new_view.n_layers, key_idx, H, K,
                                                  d, N_cap, R_cap, total, k_old, v_old, k_new, v_new);
-    note_launch();
+    }
     return cudaGetLastError();
 }
 

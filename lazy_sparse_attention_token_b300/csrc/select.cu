@@ -174,8 +174,10 @@ topk_rows_kernel(const float *__restrict__ vals, int n, int k, int32_t *__restri
 cudaError_t launch_token_scores(const uint16_t *h_prev, const uint16_t *h_cur, int B, int N, int D,
                                 float *scores, cudaStream_t s) {
     const long long rows = (long long)B * N;
-    token_scores_kernel<<<ceil_div(rows, kScoreWarps), kScoreWarps * 32, 0, s>>>(h_prev, h_cur, rows, D, scores);
-    note_launch();
+    {
+        KernelTimer kt("token_scores", s);
+        token_scores_kernel<<<ceil_div(rows, kScoreWarps), kScoreWarps * 32, 0, s>>>(h_prev, h_cur, rows, D, scores);
+    }
     return cudaGetLastError();
 }
 
@@ -189,11 +191,16 @@ cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t 
                                  kTopkSmemMaxN * 4);
             attr_set = true;
         }
-        topk_rows_kernel<true><<<rows, kTopkThreads, smem, s>>>(vals, n, k, out);
+        {
+            KernelTimer kt("topk", s);
+            topk_rows_kernel<true><<<rows, kTopkThreads, smem, s>>>(vals, n, k, out);
+        }
     } else {
-        topk_rows_kernel<false><<<rows, kTopkThreads, 0, s>>>(vals, n, k, out);
+        {
+            KernelTimer kt("topk", s);
+            topk_rows_kernel<false><<<rows, kTopkThreads, 0, s>>>(vals, n, k, out);
+        }
     }
-    note_launch();
     return cudaGetLastError();
 }
 

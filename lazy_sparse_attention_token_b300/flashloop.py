@@ -63,6 +63,7 @@ EXPORTS = [
     "flashloop_select_tokens", "flashloop_gather", "flashloop_kv_delta_append", "flashloop_kv_dense_store",
     "flashloop_select_keys", "flashloop_reconstruct_keys", "flashloop_lazy_attention", "flashloop_loop_step",
     "flashloop_status_string", "flashloop_last_error", "flashloop_device_status", "flashloop_launch_count",
+    "flashloop_timing_enable", "flashloop_timing_read",
 ]
 
 
@@ -91,9 +92,13 @@ def lib() -> ctypes.CDLL:
         L.flashloop_last_error.restype = ctypes.c_char_p
         L.flashloop_device_status.argtypes = [ctypes.POINTER(I32)]
         L.flashloop_launch_count.restype = ctypes.c_int64
+        L.flashloop_timing_enable.argtypes = [I32]
+        L.flashloop_timing_read.restype = I32
+        L.flashloop_timing_read.argtypes = [ctypes.c_char_p, I32, ctypes.POINTER(ctypes.c_double),
+                                            ctypes.POINTER(ctypes.c_int64), I32]
         for name in EXPORTS:
             if name not in ("flashloop_workspace_bytes", "flashloop_kv_cache_bytes", "flashloop_status_string",
-                            "flashloop_last_error", "flashloop_launch_count"):
+                            "flashloop_last_error", "flashloop_launch_count", "flashloop_timing_read"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -278,6 +283,22 @@ def flashloop_device_status() -> int:
 
 def flashloop_launch_count() -> int:
     return int(lib().flashloop_launch_count())
+
+
+def flashloop_timing_enable(on: bool = True):
+    _check(lib().flashloop_timing_enable(int(on)), "flashloop_timing_enable")
+
+
+def flashloop_timing_read(max_kinds: int = 32):
+    """{kernel family: (total ms, launches)} since the previous read (synchronises)."""
+    name_len = 64
+    names = ctypes.create_string_buffer(name_len * max_kinds)
+    ms = (ctypes.c_double * max_kinds)()
+    cnt = (ctypes.c_int64 * max_kinds)()
+    n = lib().flashloop_timing_read(names, name_len, ms, cnt, max_kinds)
+    if n < 0:
+        raise FlashLoopError(-4, "flashloop_timing_read")
+    return {names.raw[k * name_len:(k + 1) * name_len].split(b"\0")[0].decode(): (ms[k], cnt[k]) for k in range(n)}
 
 
 def workspace_for(dims: Dims, device="cuda") -> torch.Tensor:

@@ -46,6 +46,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <omp.h>
+
 /* ------------------------------------------------------------------ */
 /* number formats (IEEE 754 binary16 and bfloat16, round to nearest even) */
 
@@ -302,11 +304,96 @@ void orc_reconstruct(const uint16_t *base, int nl, const int32_t *const *idx,
  * so the selected keys keep the old total mass m instead of being
  * renormalised to one. `first` is the first dense loop: no previous state,
  * m := 1, u := 0, p := 0, and c is overwritten rather than updated.
- * Rows are processed per (b, h) independently; `bh_mask` (may be NULL)
- * restricts the work to a subset of (b, h) pairs.
+ * Rows are independent; the column-mass changes of all rows are summed in
+ * double and added to c once per (b, h). `bh_mask` (may be NULL) restricts
+ * the work to a subset of (b, h) pairs.
  * Shapes: q, qhat [B,Ns,H,d] bf16; o [B,Ns,H,d] f32; z [B,H,Ns] f32;
  * c [B,H,Nk] f32; S [B,H,K] i32; k/v old/new [B,Nk,H,d] bf16;
  * pos, slot [B,R] i32; m_out [B,H,R] double (may be NULL; NaN when skipped). */
+typedef struct {
+    int first;
+    int64_t B, H, d, Nk, Ns, R, K;
+    const int32_t *pos, *slot;
+    const uint16_t *q;
+    uint16_t *qhat;
+    float *o, *z;
+    const int32_t *S;
+    const uint16_t *k_old, *v_old, *k_new, *v_new;
+    double *m_out;
+} orc_attn_args;
+
+/* One row: updates its own state row and adds its column-mass changes to
+ * dc[0..K) (indexed like S). Scratch p, tau hold K doubles, u, w hold d. */
+static void orc_attention_row(const orc_attn_args *a, int64_t b, int64_t h, int64_t r, double *dc,
+                              double *p, double *tau, double *u, double *w) {
+    const int64_t d = a->d, H = a->H, Nk = a->Nk, Ns = a->Ns, K = a->K;
+    const double inv_sqrt_d = 1.0 / sqrt((double)d);
+    const int32_t *Sb = a->S + (b * H + h) * K;
+    int64_t i = a->pos[b * a->R + r], s = a->slot[b * a->R + r];
+    if (a->m_out) a->m_out[(b * H + h) * a->R + r] = NAN;
+    int64_t ns = 0;                     /* |S_i|: S is ascending */
+    while (ns < K && Sb[ns] <= i) ++ns;
+    if (ns == 0) return;
+    const uint16_t *qs = a->q + ((b * Ns + s) * H + h) * d;
+    uint16_t *qh = a->qhat + ((b * Ns + s) * H + h) * d;
+    float *os = a->o + ((b * Ns + s) * H + h) * d;
+    float *zs = a->z + (b * H + h) * Ns + s;
+    double m = 0.0;
+    for (int64_t x = 0; x < d; ++x) u[x] = 0.0;
+    if (a->first) {
+        m = 1.0;
+        for (int64_t t = 0; t < ns; ++t) p[t] = 0.0;
+    } else {
+        for (int64_t t = 0; t < ns; ++t) {
+            int64_t j = Sb[t];
+            const uint16_t *kj = a->k_old + ((b * Nk + j) * H + h) * d;
+            const uint16_t *vj = a->v_old + ((b * Nk + j) * H + h) * d;
+            double dot = 0.0;
+            for (int64_t x = 0; x < d; ++x)
+                dot += (double)orc_bf16_to_f32(qh[x]) * (double)orc_bf16_to_f32(kj[x]);
+            p[t] = exp(dot * inv_sqrt_d - (double)*zs);
+            m += p[t];
+            for (int64_t x = 0; x < d; ++x) u[x] += p[t] * (double)orc_bf16_to_f32(vj[x]);
+        }
+        if (!(m >= (double)FLT_MIN)) return;     /* R3: old mass underflowed */
+    }
+    double mx = -INFINITY;
+    for (int64_t t = 0; t < ns; ++t) {
+        int64_t j = Sb[t];
+        const uint16_t *kj = a->k_new + ((b * Nk + j) * H + h) * d;
+        double dot = 0.0;
+        for (int64_t x = 0; x < d; ++x)
+            dot += (double)orc_bf16_to_f32(qs[x]) * (double)orc_bf16_to_f32(kj[x]);
+        tau[t] = dot * inv_sqrt_d;
+        if (tau[t] > mx) mx = tau[t];
+    }
+    double sum = 0.0;
+    for (int64_t t = 0; t < ns; ++t) sum += exp(tau[t] - mx);
+    double lam = mx + log(sum);
+    for (int64_t x = 0; x < d; ++x) w[x] = 0.0;
+    for (int64_t t = 0; t < ns; ++t) {
+        int64_t j = Sb[t];
+        const uint16_t *vj = a->v_new + ((b * Nk + j) * H + h) * d;
+        double e = exp(tau[t] - lam);
+        for (int64_t x = 0; x < d; ++x) w[x] += e * (double)orc_bf16_to_f32(vj[x]);
+        dc[t] += m * e - p[t];
+    }
+    for (int64_t x = 0; x < d; ++x) {
+        double prev = a->first ? 0.0 : (double)os[x];
+        os[x] = (float)(prev - u[x] + m * w[x]);
+    }
+    *zs = (float)(lam - log(m));
+    for (int64_t x = 0; x < d; ++x) qh[x] = qs[x];
+    if (a->m_out) a->m_out[(b * H + h) * a->R + r] = m;
+}
+
+static void orc_apply_dc(const orc_attn_args *a, int64_t b, int64_t h, float *c, const double *dc) {
+    const int32_t *Sb = a->S + (b * a->H + h) * a->K;
+    float *cb = c + (b * a->H + h) * a->Nk;
+    if (a->first) for (int64_t j = 0; j < a->Nk; ++j) cb[j] = 0.0f;
+    for (int64_t t = 0; t < a->K; ++t) cb[Sb[t]] = (float)((double)cb[Sb[t]] + dc[t]);
+}
+
 void orc_attention(int first, int64_t B, int64_t H, int64_t d, int64_t Nk, int64_t Ns,
                    int64_t R, const int32_t *pos, const int32_t *slot,
                    const uint16_t *q, uint16_t *qhat, float *o, float *z, float *c,
@@ -314,82 +401,51 @@ void orc_attention(int first, int64_t B, int64_t H, int64_t d, int64_t Nk, int64
                    const uint16_t *k_old, const uint16_t *v_old,
                    const uint16_t *k_new, const uint16_t *v_new,
                    const uint8_t *bh_mask, double *m_out) {
-    const double inv_sqrt_d = 1.0 / sqrt((double)d);
-#pragma omp parallel for collapse(2) schedule(dynamic, 1)
-    for (int64_t b = 0; b < B; ++b) {
-        for (int64_t h = 0; h < H; ++h) {
-            if (bh_mask && !bh_mask[b * H + h]) continue;
-            const int32_t *Sb = S + (b * H + h) * K;
+    orc_attn_args a = {first, B, H, d, Nk, Ns, R, K, pos, slot, q, qhat, o, z, S,
+                       k_old, v_old, k_new, v_new, m_out};
+    int nthreads = omp_get_max_threads();
+    int64_t n_bh = 0;
+    for (int64_t bh = 0; bh < B * H; ++bh) n_bh += (!bh_mask || bh_mask[bh]);
+    if (n_bh >= nthreads) {
+        /* enough (b, h) pairs to keep every thread busy: one pair per task */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t bh = 0; bh < B * H; ++bh) {
+            if (bh_mask && !bh_mask[bh]) continue;
             double *dc = (double *)calloc((size_t)K, sizeof(double));
-            double *p = (double *)malloc(sizeof(double) * (size_t)K);
-            double *tau = (double *)malloc(sizeof(double) * (size_t)K);
+            double *p = (double *)malloc(sizeof(double) * (size_t)(K + 1));
+            double *tau = (double *)malloc(sizeof(double) * (size_t)(K + 1));
             double *u = (double *)malloc(sizeof(double) * (size_t)d);
             double *w = (double *)malloc(sizeof(double) * (size_t)d);
-            for (int64_t r = 0; r < R; ++r) {
-                int64_t i = pos[b * R + r], s = slot[b * R + r];
-                if (m_out) m_out[(b * H + h) * R + r] = NAN;
-                int64_t ns = 0;                     /* |S_i|: S is ascending */
-                while (ns < K && Sb[ns] <= i) ++ns;
-                if (ns == 0) continue;
-                const uint16_t *qs = q + ((b * Ns + s) * H + h) * d;
-                const uint16_t *qh = qhat + ((b * Ns + s) * H + h) * d;
-                float *os = o + ((b * Ns + s) * H + h) * d;
-                float *zs = z + (b * H + h) * Ns + s;
-                double m = 0.0;
-                for (int64_t x = 0; x < d; ++x) u[x] = 0.0;
-                if (first) {
-                    m = 1.0;
-                    for (int64_t t = 0; t < ns; ++t) p[t] = 0.0;
-                } else {
-                    for (int64_t t = 0; t < ns; ++t) {
-                        int64_t j = Sb[t];
-                        const uint16_t *kj = k_old + ((b * Nk + j) * H + h) * d;
-                        const uint16_t *vj = v_old + ((b * Nk + j) * H + h) * d;
-                        double dot = 0.0;
-                        for (int64_t x = 0; x < d; ++x)
-                            dot += (double)orc_bf16_to_f32(qh[x]) * (double)orc_bf16_to_f32(kj[x]);
-                        p[t] = exp(dot * inv_sqrt_d - (double)*zs);
-                        m += p[t];
-                        for (int64_t x = 0; x < d; ++x) u[x] += p[t] * (double)orc_bf16_to_f32(vj[x]);
-                    }
-                    if (!(m >= (double)FLT_MIN)) continue;     /* R3: old mass underflowed */
-                }
-                double mx = -INFINITY;
-                for (int64_t t = 0; t < ns; ++t) {
-                    int64_t j = Sb[t];
-                    const uint16_t *kj = k_new + ((b * Nk + j) * H + h) * d;
-                    double dot = 0.0;
-                    for (int64_t x = 0; x < d; ++x)
-                        dot += (double)orc_bf16_to_f32(qs[x]) * (double)orc_bf16_to_f32(kj[x]);
-                    tau[t] = dot * inv_sqrt_d;
-                    if (tau[t] > mx) mx = tau[t];
-                }
-                double sum = 0.0;
-                for (int64_t t = 0; t < ns; ++t) sum += exp(tau[t] - mx);
-                double lam = mx + log(sum);
-                for (int64_t x = 0; x < d; ++x) w[x] = 0.0;
-                for (int64_t t = 0; t < ns; ++t) {
-                    int64_t j = Sb[t];
-                    const uint16_t *vj = v_new + ((b * Nk + j) * H + h) * d;
-                    double a = exp(tau[t] - lam);
-                    for (int64_t x = 0; x < d; ++x) w[x] += a * (double)orc_bf16_to_f32(vj[x]);
-                    dc[t] += m * a - p[t];
-                }
-                for (int64_t x = 0; x < d; ++x) {
-                    double prev = first ? 0.0 : (double)os[x];
-                    os[x] = (float)(prev - u[x] + m * w[x]);
-                }
-                *zs = (float)(lam - log(m));
-                uint16_t *qw = qhat + ((b * Ns + s) * H + h) * d;
-                for (int64_t x = 0; x < d; ++x) qw[x] = qs[x];
-                if (m_out) m_out[(b * H + h) * R + r] = m;
-            }
-            float *cb = c + (b * H + h) * Nk;
-            if (first) for (int64_t j = 0; j < Nk; ++j) cb[j] = 0.0f;
-            for (int64_t t = 0; t < K; ++t) cb[Sb[t]] = (float)((double)cb[Sb[t]] + dc[t]);
+            for (int64_t r = 0; r < R; ++r) orc_attention_row(&a, bh / H, bh % H, r, dc, p, tau, u, w);
+            orc_apply_dc(&a, bh / H, bh % H, c, dc);
             free(dc); free(p); free(tau); free(u); free(w);
         }
+        return;
     }
+    /* few (b, h) pairs: split the rows of each pair across threads; each
+     * thread sums its rows' column-mass changes, and the per-thread sums are
+     * added in thread order */
+    double *dc_all = (double *)calloc((size_t)nthreads * (size_t)K, sizeof(double));
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        if (bh_mask && !bh_mask[bh]) continue;
+        memset(dc_all, 0, sizeof(double) * (size_t)nthreads * (size_t)K);
+#pragma omp parallel num_threads(nthreads)
+        {
+            int t = omp_get_thread_num();
+            double *dc = dc_all + (size_t)t * (size_t)K;
+            double *p = (double *)malloc(sizeof(double) * (size_t)(K + 1));
+            double *tau = (double *)malloc(sizeof(double) * (size_t)(K + 1));
+            double *u = (double *)malloc(sizeof(double) * (size_t)d);
+            double *w = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(static, 16)
+            for (int64_t r = 0; r < R; ++r) orc_attention_row(&a, bh / H, bh % H, r, dc, p, tau, u, w);
+            free(p); free(tau); free(u); free(w);
+        }
+        for (int t = 1; t < nthreads; ++t)
+            for (int64_t k = 0; k < K; ++k) dc_all[k] += dc_all[(size_t)t * (size_t)K + k];
+        orc_apply_dc(&a, bh / H, bh % H, c, dc_all);
+    }
+    free(dc_all);
 }
 
 /* Textbook causal softmax attention in double (used to pin the lazy
