@@ -21,18 +21,21 @@
 //   pass NEW: QK_new -> P' = exp(. - Z') -> acc += P' V_new, colsum += P'
 // The first dense loop skips pass OLD (m = 1, u = 0).
 //
-// Roles (192 threads): warp 0 issues TMA loads of K/V tiles into a 2-stage
-// ring; warp 1 (one thread) issues tcgen05.mma into TMEM; warps 2..5 own one
-// TMEM lane (= one row) each, read S, do the softmax arithmetic, write P as
-// bf16 into shared memory for the PV and column-sum MMAs, and run the
-// epilogue. Column sums are an MMA of P^T (the same shared tile read
+// Roles (320 threads): warp 0 issues TMA loads into a K ring and a V ring
+// (2 stages each; a K slot is released as soon as its QK product is done);
+// warp 1 (one thread) issues tcgen05.mma into TMEM; warps 2..9 are two
+// softmax warpgroups that each own one TMEM lane (= one row) and one half
+// of the tile's 128 columns: they read S, do the softmax arithmetic, write
+// P as bf16 into shared memory for the PV and column-sum MMAs, merge their
+// row statistics once (after pass LSE), and split the epilogue. Column sums are an MMA of P^T (the same shared tile read
 // MN-major) with a ones matrix, so no cross-thread reduction is needed.
 // TMEM columns: S double buffer [0,256), accumulator [256,256+d), column
 // sums [384,400).
 //
-// Every mbarrier wait is bounded (about one second); on timeout the CTA
-// records an error code, stops issuing work, waits (bounded) for its own
-// copies and MMAs, frees TMEM and exits.
+// Waiting threads sleep in a hinted try_wait instead of spinning. Every
+// mbarrier wait is bounded (about one second); on timeout the CTA records an
+// error code, stops issuing work, waits (bounded) for its own copies and
+// MMAs, frees TMEM and exits.
 #include <cudaTypedefs.h>
 #include <float.h>
 #include <mutex>
@@ -47,7 +50,8 @@ using namespace ptx;
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2..5 and 6..9 softmax (column halves)
+constexpr int kSoftmax = 256;
 constexpr int kAtom = 128 * 128;  // bytes of a 128-row x 64-element bf16 tile, 128-byte swizzled
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColAcc = 256, kColCS = 384;
@@ -57,25 +61,28 @@ constexpr float kLn2 = 0.6931471805599453f;
 __device__ int g_tc_error;
 
 enum : int { PH_OLD = 0, PH_LSE = 1, PH_NEW = 2 };
-enum : int { BAR_KV_FULL = 0, BAR_KV_EMPTY = 2, BAR_S_FULL = 4, BAR_S_EMPTY = 6, BAR_P_FULL = 8,
-             BAR_P_EMPTY = 9, BAR_ACC = 10, BAR_DRAIN = 11, N_BARS = 12 };
-enum : int { ERR_KV_EMPTY = 1, ERR_KV_FULL = 2, ERR_S_EMPTY = 3, ERR_S_FULL = 4, ERR_P_FULL = 5,
-             ERR_P_EMPTY = 6, ERR_ACC = 7 };
+enum : int { BAR_K_FULL = 0, BAR_K_EMPTY = 2, BAR_V_FULL = 4, BAR_V_EMPTY = 6, BAR_S_FULL = 8,
+             BAR_S_EMPTY = 10, BAR_P_FULL = 12, BAR_P_EMPTY = 13, BAR_ACC = 14, BAR_STATS = 15,
+             BAR_DRAIN = 16, N_BARS = 17 };
+enum : int { ERR_K_EMPTY = 1, ERR_K_FULL = 2, ERR_V_EMPTY = 3, ERR_V_FULL = 4, ERR_S_EMPTY = 5, ERR_S_FULL = 6,
+             ERR_P_FULL = 7, ERR_P_EMPTY = 8, ERR_ACC = 9, ERR_STATS = 10 };
 
 template <int D>
 struct Cfg {
     static constexpr int NA = (D + 63) / 64;        // 64-element atoms along d
     static constexpr int TB = NA * kAtom;           // one 128-row tile of Q, K or V
-    static constexpr int OFF_QH = 0;
+    static constexpr int OFF_QH = 0;                // also the row-statistics exchange after pass OLD
     static constexpr int OFF_Q = TB;
-    static constexpr int OFF_KV = 2 * TB;           // stage s: K at +2*TB*s, V at +2*TB*s + TB
-    static constexpr int OFF_P = OFF_KV + 4 * TB;
+    static constexpr int OFF_K = 2 * TB;            // K ring: 2 stages
+    static constexpr int OFF_V = 4 * TB;            // V ring: 2 stages
+    static constexpr int OFF_P = 6 * TB;
     static constexpr int OFF_ONES = OFF_P + 2 * kAtom;
     static constexpr int OFF_BAR = OFF_ONES + 512;
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM = BYTES + 1024;       // room to align the base to 1024 bytes
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(2 * kSoftmax / 2 * 3 * 4 <= TB, "statistics exchange fits the Q-hat tile");
 };
 
 struct KParams {
@@ -94,14 +101,16 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Bounded wait: false on timeout or when another role has aborted.
+// Bounded wait. The thread sleeps inside try_wait (hinted) rather than
+// spinning; it gives up after about one second, or as soon as another role
+// has given up, recording the first failure code.
 __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort_flag) return false;
-        if ((it & 63u) == 0 && globaltimer_ns() - t0 > 1000000000ull) {
+        if (globaltimer_ns() - t0 > 1000000000ull) {
             *abort_flag = 1;
             atomicCAS(&g_tc_error, 0, code);
             return false;
@@ -157,12 +166,15 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const int ph0 = first ? PH_LSE : PH_OLD;
     const int total = (3 - ph0) * n_tiles;
     const int kcols = dense ? p.n_keys : p.K;
+    auto phase_of = [&](int g) { return ph0 + g / n_tiles; };
+    auto col_index = [&](int cc) { return cc < kcols ? (dense ? cc : __ldg(S + cc)) : INT_MAX; };
 
     // ---------------- set-up ----------------
     if (threadIdx.x == 0) {
         for (int i = 0; i < N_BARS; ++i) {
-            const bool many = (i == BAR_S_EMPTY || i == BAR_S_EMPTY + 1 || i == BAR_P_FULL);
-            mbar_init(bar(i), many ? 128u : 1u);
+            uint32_t count = 1;
+            if (i == BAR_S_EMPTY || i == BAR_S_EMPTY + 1 || i == BAR_P_FULL || i == BAR_STATS) count = kSoftmax;
+            mbar_init(bar(i), count);
         }
         misc[1] = 0;
         mbar_fence_init();
@@ -177,17 +189,17 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         reinterpret_cast<uint4 *>(smem + C::OFF_ONES)[lane] = one4;
         fence_proxy_async_smem();
     }
-    const int r = (warp & 3) * 32 + lane;    // softmax warps: tile row == TMEM lane
     const bool is_sm = warp >= 2;
+    const int wg = is_sm ? (warp - 2) >> 2 : 0;   // column half of the softmax warps
+    const int r = (warp & 3) * 32 + lane;          // tile row == TMEM lane
     const bool row_ok = is_sm && r < rows;
     const int pos = row_ok ? (dense ? row0 + r : __ldg(A + r)) : -1;
-    if (is_sm) {   // gather this row's queries into the swizzled Q tiles
+    if (is_sm) {   // gather this row's queries into the swizzled Q tiles; each half loads half the chunks
         const uint4 zero = make_uint4(0, 0, 0, 0);
         const long long qoff = (((long long)b * p.n_state + max(pos, 0)) * p.H + h) * D;
         const uint4 *qn = reinterpret_cast<const uint4 *>(p.q + qoff);
         const uint4 *qo = reinterpret_cast<const uint4 *>(p.q_hat + qoff);
-#pragma unroll
-        for (int ch = 0; ch < D / 8; ++ch) {
+        for (int ch = wg; ch < D / 8; ch += 2) {
             *reinterpret_cast<uint4 *>(smem + C::OFF_Q + swz_off(r, ch)) = row_ok ? ldg_nc_v4(qn + ch) : zero;
             if (!first)
                 *reinterpret_cast<uint4 *>(smem + C::OFF_QH + swz_off(r, ch)) = row_ok ? qo[ch] : zero;
@@ -199,40 +211,47 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    auto phase_of = [&](int g) { return ph0 + g / n_tiles; };
-
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
+        // ---------------- TMA producer: K ring and V ring ----------------
         if (lane == 0) {
             prefetch_tmap(&tm_k_old); prefetch_tmap(&tm_v_old);
             prefetch_tmap(&tm_k_new); prefetch_tmap(&tm_v_new);
-            int issued = 0;
-            for (int g = 0; g < total; ++g) {
-                const int s = g & 1, use = g >> 1;
-                if (!wait_bar(bar(BAR_KV_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_KV_EMPTY)) break;
+            int k_issued = 0, v_issued = 0;
+            bool ok = true;
+            for (int g = 0; g < total && ok; ++g) {
                 const int ph = phase_of(g), t = g % n_tiles;
-                const bool with_v = ph != PH_LSE;
-                const CUtensorMap *mk = ph == PH_OLD ? &tm_k_old : &tm_k_new;
-                const CUtensorMap *mv = ph == PH_OLD ? &tm_v_old : &tm_v_new;
-                const uint32_t kdst = sbase + C::OFF_KV + 2 * C::TB * s;
-                mbar_arrive_expect_tx(bar(BAR_KV_FULL + s), (with_v ? 2 : 1) * C::TB);
-                for (int a = 0; a < C::NA; ++a) {
-                    if (dense) tma_load_4d(kdst + a * kAtom, mk, bar(BAR_KV_FULL + s), a * 64, h, t * BN, b);
-                    else tma_load_4d(kdst + a * kAtom, mk, bar(BAR_KV_FULL + s), a * 64, t * BN, h, b);
-                }
-                if (with_v) {
+                const int key0 = t * BN;
+                {
+                    const int s = g & 1, use = g >> 1;
+                    if (!wait_bar(bar(BAR_K_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_K_EMPTY)) { ok = false; break; }
+                    const CUtensorMap *mk = ph == PH_OLD ? &tm_k_old : &tm_k_new;
+                    const uint32_t dst = sbase + C::OFF_K + C::TB * s;
+                    mbar_arrive_expect_tx(bar(BAR_K_FULL + s), C::TB);
                     for (int a = 0; a < C::NA; ++a) {
-                        if (dense) tma_load_4d(kdst + C::TB + a * kAtom, mv, bar(BAR_KV_FULL + s), a * 64, h, t * BN, b);
-                        else tma_load_4d(kdst + C::TB + a * kAtom, mv, bar(BAR_KV_FULL + s), a * 64, t * BN, h, b);
+                        if (dense) tma_load_4d(dst + a * kAtom, mk, bar(BAR_K_FULL + s), a * 64, h, key0, b);
+                        else tma_load_4d(dst + a * kAtom, mk, bar(BAR_K_FULL + s), a * 64, key0, h, b);
                     }
+                    k_issued = g + 1;
                 }
-                issued = g + 1;
+                if (ph != PH_LSE) {
+                    const int vi = v_issued, s = vi & 1, use = vi >> 1;
+                    if (!wait_bar(bar(BAR_V_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_V_EMPTY)) { ok = false; break; }
+                    const CUtensorMap *mv = ph == PH_OLD ? &tm_v_old : &tm_v_new;
+                    const uint32_t dst = sbase + C::OFF_V + C::TB * s;
+                    mbar_arrive_expect_tx(bar(BAR_V_FULL + s), C::TB);
+                    for (int a = 0; a < C::NA; ++a) {
+                        if (dense) tma_load_4d(dst + a * kAtom, mv, bar(BAR_V_FULL + s), a * 64, h, key0, b);
+                        else tma_load_4d(dst + a * kAtom, mv, bar(BAR_V_FULL + s), a * 64, key0, h, b);
+                    }
+                    v_issued = vi + 1;
+                }
             }
-            if (*abort_flag) {   // let copies already in flight land before the CTA exits
-                for (int g = max(0, issued - 2); g < issued; ++g) {
-                    volatile int never = 0;
-                    wait_bar(bar(BAR_KV_FULL + (g & 1)), (g >> 1) & 1, &never, ERR_KV_FULL);
-                }
+            if (!ok) {   // let copies already in flight land before the CTA exits
+                volatile int never = 0;
+                for (int g = max(0, k_issued - 2); g < k_issued; ++g)
+                    wait_bar(bar(BAR_K_FULL + (g & 1)), (g >> 1) & 1, &never, ERR_K_FULL);
+                for (int v = max(0, v_issued - 2); v < v_issued; ++v)
+                    wait_bar(bar(BAR_V_FULL + (v & 1)), (v >> 1) & 1, &never, ERR_V_FULL);
             }
         }
     } else if (warp == 1) {
@@ -246,11 +265,11 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             const uint64_t ones = smem_desc(sbase + C::OFF_ONES, 128, 256, 0);
             auto issue_qk = [&](int g) -> bool {
                 const int s = g & 1, use = g >> 1;
-                if (!wait_bar(bar(BAR_KV_FULL + s), use & 1, abort_flag, ERR_KV_FULL)) return false;
+                if (!wait_bar(bar(BAR_K_FULL + s), use & 1, abort_flag, ERR_K_FULL)) return false;
                 if (!wait_bar(bar(BAR_S_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_S_EMPTY)) return false;
                 tc_fence_after();
                 const uint32_t qa = sbase + (phase_of(g) == PH_OLD ? C::OFF_QH : C::OFF_Q);
-                const uint32_t ka = sbase + C::OFF_KV + 2 * C::TB * s;
+                const uint32_t ka = sbase + C::OFF_K + C::TB * s;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
@@ -258,35 +277,36 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                                 smem_desc(ka + off, 16, 1024, 2), id_qk, kk > 0);
                 }
                 mma_commit(bar(BAR_S_FULL + s));
+                mma_commit(bar(BAR_K_EMPTY + s));
                 return true;
             };
             bool ok = issue_qk(0);
             int pv = 0;
             for (int g = 0; ok && g < total; ++g) {
                 if (g + 1 < total && !issue_qk(g + 1)) { ok = false; break; }
-                const int ph = phase_of(g), s = g & 1;
-                if (ph != PH_LSE) {
-                    if (!wait_bar(bar(BAR_P_FULL), pv & 1, abort_flag, ERR_P_FULL)) { ok = false; break; }
-                    tc_fence_after();
-                    const bool neg = ph == PH_OLD;
-                    const uint32_t pa = sbase + C::OFF_P;
-                    const uint32_t va = sbase + C::OFF_KV + 2 * C::TB * s + C::TB;
+                const int ph = phase_of(g);
+                if (ph == PH_LSE) continue;
+                const int s = pv & 1, use = pv >> 1;
+                if (!wait_bar(bar(BAR_V_FULL + s), use & 1, abort_flag, ERR_V_FULL)) { ok = false; break; }
+                if (!wait_bar(bar(BAR_P_FULL), pv & 1, abort_flag, ERR_P_FULL)) { ok = false; break; }
+                tc_fence_after();
+                const bool neg = ph == PH_OLD;
+                const uint32_t pa = sbase + C::OFF_P;
+                const uint32_t va = sbase + C::OFF_V + C::TB * s;
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {   // acc += P[:, 16kk..] * V[16kk.., :]
-                        mma_bf16_ss(tmem + kColAcc,
-                                    smem_desc(pa + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024, 2),
-                                    smem_desc(va + kk * 2048, kAtom, 1024, 2), neg ? id_pv_old : id_pv_new,
-                                    (pv > 0 || kk > 0) ? 1u : 0u);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk) {   // colsum = P^T[:, 16kk..] * ones
-                        mma_bf16_ss(tmem + kColCS, smem_desc(pa + kk * 2048, kAtom, 1024, 2), ones,
-                                    neg ? id_cs_old : id_cs_new, kk > 0);
-                    }
-                    mma_commit(bar(BAR_P_EMPTY));
-                    ++pv;
+                for (int kk = 0; kk < BN / 16; ++kk) {   // acc += P[:, 16kk..] * V[16kk.., :]
+                    mma_bf16_ss(tmem + kColAcc, smem_desc(pa + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024, 2),
+                                smem_desc(va + kk * 2048, kAtom, 1024, 2), neg ? id_pv_old : id_pv_new,
+                                (pv > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(BAR_KV_EMPTY + s));
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk) {   // colsum = P^T[:, 16kk..] * ones
+                    mma_bf16_ss(tmem + kColCS, smem_desc(pa + kk * 2048, kAtom, 1024, 2), ones,
+                                neg ? id_cs_old : id_cs_new, kk > 0);
+                }
+                mma_commit(bar(BAR_P_EMPTY));
+                mma_commit(bar(BAR_V_EMPTY + s));
+                ++pv;
             }
             if (ok) {
                 mma_commit(bar(BAR_ACC));
@@ -297,98 +317,100 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             }
         }
     } else {
-        // ---------------- softmax / epilogue warps ----------------
+        // ---------------- softmax / epilogue: two warpgroups, one column half each ----------------
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int half = wg * 64;
         const float zo2 = (!first && row_ok) ? __ldg(p.z + bh * p.n_state + pos) * kLog2e : 0.f;
         float m = 0.f, M = -INFINITY, L = 0.f, zn2 = INFINITY;
         int pv = 0, prev_col = INT_MAX;
         bool ok = true;
         float *cb = p.c + bh * p.n_keys;
-        uint32_t pk[BN / 2];   // this row's P for one tile, bf16x2
+        uint32_t pk[32];   // this row's P over the half's 64 columns, bf16x2
         for (int g = 0; g < total && ok; ++g) {
             const int ph = phase_of(g), t = g % n_tiles, s = g & 1, use = g >> 1;
             if (ph == PH_NEW && t == 0) {
-                if (first) zn2 = (M > -INFINITY) ? M + __log2f(L) : INFINITY;
-                else zn2 = (M > -INFINITY && m >= FLT_MIN) ? M + __log2f(L) - __log2f(m) : INFINITY;
+                // merge the two halves' row statistics (exchange through the Q-hat tile,
+                // whose last reader, pass OLD's QK, has completed)
+                float *ex = reinterpret_cast<float *>(smem + C::OFF_QH);
+                ex[(wg * 128 + r) * 3 + 0] = m;
+                ex[(wg * 128 + r) * 3 + 1] = M;
+                ex[(wg * 128 + r) * 3 + 2] = L;
+                mbar_arrive(bar(BAR_STATS));
+                if (!wait_bar(bar(BAR_STATS), 0, abort_flag, ERR_STATS)) { ok = false; break; }
+                const float mo = ex[((1 - wg) * 128 + r) * 3 + 0];
+                const float Mo = ex[((1 - wg) * 128 + r) * 3 + 1];
+                const float Lo = ex[((1 - wg) * 128 + r) * 3 + 2];
+                const float Mx = fmaxf(M, Mo);
+                const float Lx = (Mx > -INFINITY) ? L * ex2(M - Mx) + Lo * ex2(Mo - Mx) : 0.f;
+                const float mx = first ? 1.f : m + mo;
+                zn2 = (Mx > -INFINITY && mx >= FLT_MIN) ? Mx + __log2f(Lx) - __log2f(mx) : INFINITY;
             }
-            // column indices of this tile: lane holds entries lane, lane+32, lane+64, lane+96
-            int jreg[4];
             const int c0 = t * BN;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int cc = c0 + u * 32 + lane;
-                jreg[u] = cc < kcols ? (dense ? cc : __ldg(S + cc)) : INT_MAX;
-            }
-            const int jlast = __shfl_sync(0xffffffffu, jreg[3], 31);
+            const int j0 = col_index(c0 + half + lane), j1 = col_index(c0 + half + 32 + lane);
+            const int jr = col_index(c0 + r);   // this lane's column of the column-sum MMA
+            const int jlast = col_index(min(c0 + BN, kcols) - 1);
             const bool no_mask = (c0 + BN <= kcols) && jlast <= min_pos;
             if (!wait_bar(bar(BAR_S_FULL + s), use & 1, abort_flag, ERR_S_FULL)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sc = tmem + lane_base + kColS + 128 * s;
-            const float sub = ph == PH_OLD ? zo2 : zn2;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float sv[32];
-                tmem_ld_32x32b_x32(sc + 32 * u, sv);
-                tmem_wait_ld();
-                if (ph == PH_LSE) {
-                    float cmax = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int j = no_mask ? 0 : __shfl_sync(0xffffffffu, jreg[u], e);
-                        sv[e] = (row_ok && (no_mask || j <= pos)) ? sv[e] * p.sl2 : -INFINITY;
-                        cmax = fmaxf(cmax, sv[e]);
-                    }
-                    if (cmax > M) {
-                        L *= ex2(M - cmax);
-                        M = cmax;
-                    }
-                    float acc = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) acc += ex2(sv[e] - M);
-                    if (M > -INFINITY) L += acc;
-                } else {
-                    float msum = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float pr[2];
-#pragma unroll
-                        for (int f = 0; f < 2; ++f) {
-                            const int j = no_mask ? 0 : __shfl_sync(0xffffffffu, jreg[u], e + f);
-                            const float x = ex2(fmaf(sv[e + f], p.sl2, -sub));
-                            pr[f] = (row_ok && (no_mask || j <= pos)) ? x : 0.f;
-                            msum += pr[f];
-                        }
-                        pk[u * 16 + e / 2] = pack_bf16x2_rn(pr[0], pr[1]);
-                    }
-                    if (ph == PH_OLD) m += msum;
-                }
-            }
+            float sv[64];
+            const uint32_t sc = tmem + lane_base + kColS + 128 * s + half;
+            tmem_ld_32x32b_x32(sc, sv);
+            tmem_ld_32x32b_x32(sc + 32, sv + 32);
+            tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(BAR_S_EMPTY + s));
-            if (ph != PH_LSE) {
-                if (!wait_bar(bar(BAR_P_EMPTY), (pv & 1) ^ 1, abort_flag, ERR_P_EMPTY)) { ok = false; break; }
-                tc_fence_after();
-                if (pv > 0) {   // column sums of the previous P tile
-                    const float cs = tmem_ld_32x32b_x1(tmem + lane_base + kColCS);
-                    tmem_wait_ld();
-                    if (prev_col != INT_MAX && cs != 0.f) atomicAdd(cb + prev_col, cs);
-                }
-                uint8_t *pt = smem + C::OFF_P;
+            if (ph == PH_LSE) {
+                float cmax = -INFINITY;
 #pragma unroll
-                for (int ch = 0; ch < BN / 8; ++ch)
-                    *reinterpret_cast<uint4 *>(pt + swz_off(r, ch)) =
-                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(bar(BAR_P_FULL));
-                // this thread's TMEM lane r is tile column r of the column-sum MMA;
-                // column r = (r/32)*32 + lane is held in jreg[r/32] of this lane
-                const int q4 = warp & 3;
-                prev_col = q4 == 0 ? jreg[0] : q4 == 1 ? jreg[1] : q4 == 2 ? jreg[2] : jreg[3];
-                ++pv;
+                for (int e = 0; e < 64; ++e) {
+                    const int j = no_mask ? 0 : __shfl_sync(0xffffffffu, e < 32 ? j0 : j1, e & 31);
+                    sv[e] = (row_ok && (no_mask || j <= pos)) ? sv[e] * p.sl2 : -INFINITY;
+                    cmax = fmaxf(cmax, sv[e]);
+                }
+                if (cmax > M) {
+                    L *= ex2(M - cmax);
+                    M = cmax;
+                }
+                float acc = 0.f;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) acc += ex2(sv[e] - M);
+                if (M > -INFINITY) L += acc;
+                continue;
             }
+            const float sub = ph == PH_OLD ? zo2 : zn2;
+            float msum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+                float pr[2];
+#pragma unroll
+                for (int f = 0; f < 2; ++f) {
+                    const int j = no_mask ? 0 : __shfl_sync(0xffffffffu, e < 32 ? j0 : j1, (e + f) & 31);
+                    const float x = ex2(fmaf(sv[e + f], p.sl2, -sub));
+                    pr[f] = (row_ok && (no_mask || j <= pos)) ? x : 0.f;
+                    msum += pr[f];
+                }
+                pk[e / 2] = pack_bf16x2_rn(pr[0], pr[1]);
+            }
+            if (ph == PH_OLD) m += msum;
+            if (!wait_bar(bar(BAR_P_EMPTY), (pv & 1) ^ 1, abort_flag, ERR_P_EMPTY)) { ok = false; break; }
+            tc_fence_after();
+            if (wg == 0 && pv > 0) {   // column sums of the previous P tile
+                const float cs = tmem_ld_32x32b_x1(tmem + lane_base + kColCS);
+                tmem_wait_ld();
+                if (prev_col != INT_MAX && cs != 0.f) atomicAdd(cb + prev_col, cs);
+            }
+            uint8_t *pt = smem + C::OFF_P;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4 *>(pt + swz_off(r, wg * 8 + q)) =
+                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(BAR_P_FULL));
+            prev_col = jr;
+            ++pv;
         }
-        if (ok && pv > 0) {
+        if (ok && pv > 0 && wg == 0) {
             if (wait_bar(bar(BAR_P_EMPTY), (pv & 1) ^ 1, abort_flag, ERR_P_EMPTY)) {
                 tc_fence_after();
                 const float cs = tmem_ld_32x32b_x1(tmem + lane_base + kColCS);
@@ -403,24 +425,26 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             const bool update = row_ok && zn2 < INFINITY;
             const long long srow = ((long long)b * p.n_state + max(pos, 0)) * p.H + h;
             float4 *orow = reinterpret_cast<float4 *>(p.o + srow * D);
+            constexpr int HALF_D = D / 2;   // accumulator columns per warpgroup
 #pragma unroll
-            for (int u = 0; u < D / 32; ++u) {
-                float av[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + kColAcc + 32 * u, av);
+            for (int u = 0; u < HALF_D / 16; ++u) {
+                float av[16];
+                const int col = wg * HALF_D + 16 * u;
+                tmem_ld_32x32b_x16(tmem + lane_base + kColAcc + col, av);
                 tmem_wait_ld();
                 if (update) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        float4 v = first ? make_float4(0.f, 0.f, 0.f, 0.f) : orow[u * 8 + e];
+                    for (int e = 0; e < 4; ++e) {
+                        float4 v = first ? make_float4(0.f, 0.f, 0.f, 0.f) : orow[col / 4 + e];
                         v.x += av[4 * e];
                         v.y += av[4 * e + 1];
                         v.z += av[4 * e + 2];
                         v.w += av[4 * e + 3];
-                        orow[u * 8 + e] = v;
+                        orow[col / 4 + e] = v;
                     }
                 }
             }
-            if (update) {
+            if (update && wg == 0) {
                 p.z[bh * p.n_state + pos] = zn2 * kLn2;
                 const uint4 *src = reinterpret_cast<const uint4 *>(p.q + srow * D);
                 uint4 *dst = reinterpret_cast<uint4 *>(p.q_hat + srow * D);
