@@ -104,7 +104,7 @@ __device__ __forceinline__ float ex2(float x) {
 // Bounded wait. The thread sleeps inside try_wait (hinted) rather than
 // spinning; it gives up after about one second, or as soon as another role
 // has given up, recording the first failure code.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code) {
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
@@ -116,6 +116,21 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile in
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code) {
+    if (mbar_test_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, abort_flag, code);
+}
+
+// Number of entries of the ascending list S[0, n) that are <= x.
+__device__ __forceinline__ int count_le(const int32_t *S, int n, int x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(S + mid) <= x) lo = mid + 1; else hi = mid;
+    }
+    return lo;
 }
 
 // Byte offset of 16-byte chunk `ch` (8 bf16) of row r in a 128-row tile laid
@@ -150,17 +165,10 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const int32_t *A = dense ? nullptr : p.row_pos + (long long)b * p.R + row0;
     const int min_pos = dense ? row0 : __ldg(A);
     const int max_pos = dense ? row0 + rows - 1 : __ldg(A + rows - 1);
-    int cnt;   // keys (of the list) at or before the last row
-    if (dense) {
-        cnt = min(max_pos + 1, p.n_keys);
-    } else {
-        int lo = 0, hi = p.K;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (__ldg(S + mid) <= max_pos) lo = mid + 1; else hi = mid;
-        }
-        cnt = lo;
-    }
+    // Rows and keys are both ascending, so the keys a row may see are a
+    // prefix of the list: row i sees the first count_le(S, i) of them.
+    const int cnt = dense ? min(max_pos + 1, p.n_keys) : count_le(S, p.K, max_pos);      // last row
+    const int cnt_min = dense ? min(min_pos + 1, p.n_keys) : count_le(S, p.K, min_pos);  // first row
     const int n_tiles = (cnt + BN - 1) / BN;
     if (n_tiles == 0) return;   // every row has an empty key set: state unchanged
     const int ph0 = first ? PH_LSE : PH_OLD;
@@ -321,13 +329,16 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const int half = wg * 64;
         const float zo2 = (!first && row_ok) ? __ldg(p.z + bh * p.n_state + pos) * kLog2e : 0.f;
+        const int cnt_i = !row_ok ? 0 : dense ? min(pos + 1, p.n_keys) : count_le(S, p.K, pos);
         float m = 0.f, M = -INFINITY, L = 0.f, zn2 = INFINITY;
         int pv = 0, prev_col = INT_MAX;
         bool ok = true;
         float *cb = p.c + bh * p.n_keys;
         uint32_t pk[32];   // this row's P over the half's 64 columns, bf16x2
-        for (int g = 0; g < total && ok; ++g) {
-            const int ph = phase_of(g), t = g % n_tiles, s = g & 1, use = g >> 1;
+        int ph = ph0, t = 0;
+        for (int g = 0; g < total && ok; ++g, ++t) {
+            if (t == n_tiles) { t = 0; ++ph; }
+            const int s = g & 1, use = g >> 1;
             if (ph == PH_NEW && t == 0) {
                 // merge the two halves' row statistics (exchange through the Q-hat tile,
                 // whose last reader, pass OLD's QK, has completed)
@@ -346,10 +357,12 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 zn2 = (Mx > -INFINITY && mx >= FLT_MIN) ? Mx + __log2f(Lx) - __log2f(mx) : INFINITY;
             }
             const int c0 = t * BN;
-            const int j0 = col_index(c0 + half + lane), j1 = col_index(c0 + half + 32 + lane);
-            const int jr = col_index(c0 + r);   // this lane's column of the column-sum MMA
-            const int jlast = col_index(min(c0 + BN, kcols) - 1);
-            const bool no_mask = (c0 + BN <= kcols) && jlast <= min_pos;
+            const bool with_v = ph != PH_LSE;
+            // this lane's column of the column-sum MMA (only the first half reads it back)
+            const int jr = (with_v && wg == 0) ? col_index(c0 + r) : INT_MAX;
+            // every row of the tile sees all 128 columns (uniform), else mask by the prefix count
+            const bool full = c0 + BN <= cnt_min;
+            const int nv = min(64, max(0, cnt_i - c0 - half));
             if (!wait_bar(bar(BAR_S_FULL + s), use & 1, abort_flag, ERR_S_FULL)) { ok = false; break; }
             tc_fence_after();
             float sv[64];
@@ -359,39 +372,51 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(BAR_S_EMPTY + s));
-            if (ph == PH_LSE) {
-                float cmax = -INFINITY;
+            if (!with_v) {
+                // online logsumexp of this tile's new logits (log2 units)
+                if (full) {
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const int j = no_mask ? 0 : __shfl_sync(0xffffffffu, e < 32 ? j0 : j1, e & 31);
-                    sv[e] = (row_ok && (no_mask || j <= pos)) ? sv[e] * p.sl2 : -INFINITY;
-                    cmax = fmaxf(cmax, sv[e]);
+                    for (int e = 0; e < 64; ++e) sv[e] *= p.sl2;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) sv[e] = e < nv ? sv[e] * p.sl2 : -INFINITY;
                 }
+                float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int e = 0; e < 64; ++e) c4[e & 3] = fmaxf(c4[e & 3], sv[e]);
+                const float cmax = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
                 if (cmax > M) {
                     L *= ex2(M - cmax);
                     M = cmax;
                 }
-                float acc = 0.f;
+                float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int e = 0; e < 64; ++e) acc += ex2(sv[e] - M);
-                if (M > -INFINITY) L += acc;
+                for (int e = 0; e < 64; ++e) a4[e & 3] += ex2(sv[e] - M);
+                if (M > -INFINITY) L += (a4[0] + a4[1]) + (a4[2] + a4[3]);
                 continue;
             }
-            const float sub = ph == PH_OLD ? zo2 : zn2;
-            float msum = 0.f;
+            // probabilities with a known normaliser: exp(logit - Z) (rows outside the
+            // tile or the sequence get zero through an infinite normaliser)
+            const float sub = !row_ok ? INFINITY : ph == PH_OLD ? zo2 : zn2;
+            float m4[4] = {0.f, 0.f, 0.f, 0.f};
+            if (full) {
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-                float pr[2];
-#pragma unroll
-                for (int f = 0; f < 2; ++f) {
-                    const int j = no_mask ? 0 : __shfl_sync(0xffffffffu, e < 32 ? j0 : j1, (e + f) & 31);
-                    const float x = ex2(fmaf(sv[e + f], p.sl2, -sub));
-                    pr[f] = (row_ok && (no_mask || j <= pos)) ? x : 0.f;
-                    msum += pr[f];
+                for (int e = 0; e < 64; e += 2) {
+                    const float x0 = ex2(fmaf(sv[e], p.sl2, -sub));
+                    const float x1 = ex2(fmaf(sv[e + 1], p.sl2, -sub));
+                    m4[(e >> 1) & 3] += x0 + x1;
+                    pk[e / 2] = pack_bf16x2_rn(x0, x1);
                 }
-                pk[e / 2] = pack_bf16x2_rn(pr[0], pr[1]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 64; e += 2) {
+                    const float x0 = e < nv ? ex2(fmaf(sv[e], p.sl2, -sub)) : 0.f;
+                    const float x1 = e + 1 < nv ? ex2(fmaf(sv[e + 1], p.sl2, -sub)) : 0.f;
+                    m4[(e >> 1) & 3] += x0 + x1;
+                    pk[e / 2] = pack_bf16x2_rn(x0, x1);
+                }
             }
-            if (ph == PH_OLD) m += msum;
+            if (ph == PH_OLD) m += (m4[0] + m4[1]) + (m4[2] + m4[3]);
             if (!wait_bar(bar(BAR_P_EMPTY), (pv & 1) ^ 1, abort_flag, ERR_P_EMPTY)) { ok = false; break; }
             tc_fence_after();
             if (wg == 0 && pv > 0) {   // column sums of the previous P tile
