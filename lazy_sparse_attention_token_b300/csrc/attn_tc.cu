@@ -26,11 +26,13 @@
 // warp 1 (one thread) issues tcgen05.mma into TMEM; warps 2..9 are two
 // softmax warpgroups that each own one TMEM lane (= one row) and one half
 // of the tile's 128 columns: they read S, do the softmax arithmetic, write
-// P as bf16 into shared memory for the PV and column-sum MMAs, merge their
-// row statistics once (after pass LSE), and split the epilogue. Column sums are an MMA of P^T (the same shared tile read
+// P as bf16 into one of two shared buffers for the PV and column-sum MMAs
+// (so the next tile's P never waits for the current PV), merge their row
+// statistics once through TMEM, and split the epilogue. One query tile
+// holds qhat for pass OLD and is reloaded with q before pass LSE. Column sums are an MMA of P^T (the same shared tile read
 // MN-major) with a ones matrix, so no cross-thread reduction is needed.
 // TMEM columns: S double buffer [0,256), accumulator [256,256+d), column
-// sums [384,400).
+// sums double buffer [384,416), row-statistics exchange [448,456).
 //
 // Waiting threads sleep in a hinted try_wait instead of spinning. Every
 // mbarrier wait is bounded (about one second); on timeout the CTA records an
@@ -54,7 +56,8 @@ constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2..5 and 6..9
 constexpr int kSoftmax = 256;
 constexpr int kAtom = 128 * 128;  // bytes of a 128-row x 64-element bf16 tile, 128-byte swizzled
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColAcc = 256, kColCS = 384;
+// TMEM columns: S double buffer, accumulator, column sums (double buffer), row-statistics exchange
+constexpr uint32_t kColS = 0, kColAcc = 256, kColCS = 384, kColX = 448;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -62,27 +65,25 @@ __device__ int g_tc_error;
 
 enum : int { PH_OLD = 0, PH_LSE = 1, PH_NEW = 2 };
 enum : int { BAR_K_FULL = 0, BAR_K_EMPTY = 2, BAR_V_FULL = 4, BAR_V_EMPTY = 6, BAR_S_FULL = 8,
-             BAR_S_EMPTY = 10, BAR_P_FULL = 12, BAR_P_EMPTY = 13, BAR_ACC = 14, BAR_STATS = 15,
-             BAR_DRAIN = 16, N_BARS = 17 };
+             BAR_S_EMPTY = 10, BAR_P_FULL = 12, BAR_P_EMPTY = 14, BAR_ACC = 16, BAR_STATS = 17,
+             BAR_Q_READY = 18, BAR_DRAIN = 19, N_BARS = 20 };
 enum : int { ERR_K_EMPTY = 1, ERR_K_FULL = 2, ERR_V_EMPTY = 3, ERR_V_FULL = 4, ERR_S_EMPTY = 5, ERR_S_FULL = 6,
-             ERR_P_FULL = 7, ERR_P_EMPTY = 8, ERR_ACC = 9, ERR_STATS = 10 };
+             ERR_P_FULL = 7, ERR_P_EMPTY = 8, ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11 };
 
 template <int D>
 struct Cfg {
     static constexpr int NA = (D + 63) / 64;        // 64-element atoms along d
     static constexpr int TB = NA * kAtom;           // one 128-row tile of Q, K or V
-    static constexpr int OFF_QH = 0;                // also the row-statistics exchange after pass OLD
-    static constexpr int OFF_Q = TB;
-    static constexpr int OFF_K = 2 * TB;            // K ring: 2 stages
-    static constexpr int OFF_V = 4 * TB;            // V ring: 2 stages
-    static constexpr int OFF_P = 6 * TB;
-    static constexpr int OFF_ONES = OFF_P + 2 * kAtom;
+    static constexpr int OFF_Q = 0;                 // queries: qhat for pass OLD, then q
+    static constexpr int OFF_K = TB;                // K ring: 2 stages
+    static constexpr int OFF_V = 3 * TB;            // V ring: 2 stages
+    static constexpr int OFF_P = 5 * TB;            // P: 2 buffers of 128 x 128 bf16
+    static constexpr int OFF_ONES = OFF_P + 4 * kAtom;
     static constexpr int OFF_BAR = OFF_ONES + 512;
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM = BYTES + 1024;       // room to align the base to 1024 bytes
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert(2 * kSoftmax / 2 * 3 * 4 <= TB, "statistics exchange fits the Q-hat tile");
 };
 
 struct KParams {
@@ -139,6 +140,17 @@ __device__ __forceinline__ uint32_t swz_off(int r, int ch) {
     return (uint32_t)((ch >> 3) * kAtom + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
+// Gathers row r's query (qhat or q) into the swizzled query tile; the two
+// softmax halves each write every other 16-byte chunk.
+template <int D>
+__device__ __forceinline__ void load_query_row(uint8_t *tile, const uint16_t *src_row, bool row_ok, int r, int wg) {
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    const uint4 *src = reinterpret_cast<const uint4 *>(src_row);
+#pragma unroll
+    for (int ch = wg; ch < D / 8; ch += 2)
+        *reinterpret_cast<uint4 *>(tile + swz_off(r, ch)) = row_ok ? src[ch] : zero;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tm_k_old,
@@ -174,14 +186,15 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const int ph0 = first ? PH_LSE : PH_OLD;
     const int total = (3 - ph0) * n_tiles;
     const int kcols = dense ? p.n_keys : p.K;
-    auto phase_of = [&](int g) { return ph0 + g / n_tiles; };
     auto col_index = [&](int cc) { return cc < kcols ? (dense ? cc : __ldg(S + cc)) : INT_MAX; };
 
     // ---------------- set-up ----------------
     if (threadIdx.x == 0) {
         for (int i = 0; i < N_BARS; ++i) {
             uint32_t count = 1;
-            if (i == BAR_S_EMPTY || i == BAR_S_EMPTY + 1 || i == BAR_P_FULL || i == BAR_STATS) count = kSoftmax;
+            if (i == BAR_S_EMPTY || i == BAR_S_EMPTY + 1 || i == BAR_P_FULL || i == BAR_P_FULL + 1 ||
+                i == BAR_STATS || i == BAR_Q_READY)
+                count = kSoftmax;
             mbar_init(bar(i), count);
         }
         misc[1] = 0;
@@ -202,16 +215,9 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const int r = (warp & 3) * 32 + lane;          // tile row == TMEM lane
     const bool row_ok = is_sm && r < rows;
     const int pos = row_ok ? (dense ? row0 + r : __ldg(A + r)) : -1;
-    if (is_sm) {   // gather this row's queries into the swizzled Q tiles; each half loads half the chunks
-        const uint4 zero = make_uint4(0, 0, 0, 0);
-        const long long qoff = (((long long)b * p.n_state + max(pos, 0)) * p.H + h) * D;
-        const uint4 *qn = reinterpret_cast<const uint4 *>(p.q + qoff);
-        const uint4 *qo = reinterpret_cast<const uint4 *>(p.q_hat + qoff);
-        for (int ch = wg; ch < D / 8; ch += 2) {
-            *reinterpret_cast<uint4 *>(smem + C::OFF_Q + swz_off(r, ch)) = row_ok ? ldg_nc_v4(qn + ch) : zero;
-            if (!first)
-                *reinterpret_cast<uint4 *>(smem + C::OFF_QH + swz_off(r, ch)) = row_ok ? qo[ch] : zero;
-        }
+    const long long qoff = (((long long)b * p.n_state + max(pos, 0)) * p.H + h) * D;
+    if (is_sm) {   // pass OLD reads qhat; the first dense loop starts with q
+        load_query_row<D>(smem + C::OFF_Q, first ? p.q + qoff : p.q_hat + qoff, row_ok, r, wg);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -225,13 +231,13 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             prefetch_tmap(&tm_k_old); prefetch_tmap(&tm_v_old);
             prefetch_tmap(&tm_k_new); prefetch_tmap(&tm_v_new);
             int k_issued = 0, v_issued = 0;
-            bool ok = true;
-            for (int g = 0; g < total && ok; ++g) {
-                const int ph = phase_of(g), t = g % n_tiles;
+            int ph = ph0, t = 0;
+            for (int g = 0; g < total; ++g, ++t) {
+                if (t == n_tiles) { t = 0; ++ph; }
                 const int key0 = t * BN;
                 {
                     const int s = g & 1, use = g >> 1;
-                    if (!wait_bar(bar(BAR_K_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_K_EMPTY)) { ok = false; break; }
+                    if (!wait_bar(bar(BAR_K_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_K_EMPTY)) break;
                     const CUtensorMap *mk = ph == PH_OLD ? &tm_k_old : &tm_k_new;
                     const uint32_t dst = sbase + C::OFF_K + C::TB * s;
                     mbar_arrive_expect_tx(bar(BAR_K_FULL + s), C::TB);
@@ -243,7 +249,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
                 if (ph != PH_LSE) {
                     const int vi = v_issued, s = vi & 1, use = vi >> 1;
-                    if (!wait_bar(bar(BAR_V_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_V_EMPTY)) { ok = false; break; }
+                    if (!wait_bar(bar(BAR_V_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_V_EMPTY)) break;
                     const CUtensorMap *mv = ph == PH_OLD ? &tm_v_old : &tm_v_new;
                     const uint32_t dst = sbase + C::OFF_V + C::TB * s;
                     mbar_arrive_expect_tx(bar(BAR_V_FULL + s), C::TB);
@@ -254,7 +260,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                     v_issued = vi + 1;
                 }
             }
-            if (!ok) {   // let copies already in flight land before the CTA exits
+            if (*abort_flag) {   // let copies already in flight land before the CTA exits
                 volatile int never = 0;
                 for (int g = max(0, k_issued - 2); g < k_issued; ++g)
                     wait_bar(bar(BAR_K_FULL + (g & 1)), (g >> 1) & 1, &never, ERR_K_FULL);
@@ -270,49 +276,55 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             constexpr uint32_t id_pv_new = idesc_bf16(128, D, false, true, false);
             constexpr uint32_t id_cs_old = idesc_bf16(128, 16, true, false, true);
             constexpr uint32_t id_cs_new = idesc_bf16(128, 16, true, false, false);
+            // descriptors are built once; per k-step only the start address moves
+            const uint64_t d_q = smem_desc(sbase + C::OFF_Q, 16, 1024, 2);
+            const uint64_t d_k = smem_desc(sbase + C::OFF_K, 16, 1024, 2);
+            const uint64_t d_v = smem_desc(sbase + C::OFF_V, kAtom, 1024, 2);
+            const uint64_t d_p = smem_desc(sbase + C::OFF_P, 16, 1024, 2);
+            const uint64_t d_pt = smem_desc(sbase + C::OFF_P, kAtom, 1024, 2);
             const uint64_t ones = smem_desc(sbase + C::OFF_ONES, 128, 256, 0);
+            constexpr uint64_t TB16 = C::TB >> 4, ATOM16 = kAtom >> 4;
+            int ph_next = ph0, t_next = 0;   // phase of tile g + 1 while issuing it
             auto issue_qk = [&](int g) -> bool {
                 const int s = g & 1, use = g >> 1;
+                const int ph = ph_next;
+                if (++t_next == n_tiles) { t_next = 0; ++ph_next; }
                 if (!wait_bar(bar(BAR_K_FULL + s), use & 1, abort_flag, ERR_K_FULL)) return false;
                 if (!wait_bar(bar(BAR_S_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_S_EMPTY)) return false;
+                if (ph == PH_LSE && g == (PH_LSE - ph0) * n_tiles && !first) {   // queries reloaded after pass OLD
+                    if (!wait_bar(bar(BAR_Q_READY), 0, abort_flag, ERR_Q_READY)) return false;
+                }
                 tc_fence_after();
-                const uint32_t qa = sbase + (phase_of(g) == PH_OLD ? C::OFF_QH : C::OFF_Q);
-                const uint32_t ka = sbase + C::OFF_K + C::TB * s;
+                const uint64_t dk = d_k + TB16 * s;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + kColS + 128 * s, smem_desc(qa + off, 16, 1024, 2),
-                                smem_desc(ka + off, 16, 1024, 2), id_qk, kk > 0);
+                    const uint64_t off = (kk >> 2) * ATOM16 + (kk & 3) * 2;
+                    mma_bf16_ss(tmem + kColS + 128 * s, d_q + off, dk + off, id_qk, kk > 0);
                 }
                 mma_commit(bar(BAR_S_FULL + s));
                 mma_commit(bar(BAR_K_EMPTY + s));
                 return true;
             };
             bool ok = issue_qk(0);
-            int pv = 0;
-            for (int g = 0; ok && g < total; ++g) {
+            int pv = 0, ph = ph0, t = 0;
+            for (int g = 0; ok && g < total; ++g, ++t) {
+                if (t == n_tiles) { t = 0; ++ph; }
                 if (g + 1 < total && !issue_qk(g + 1)) { ok = false; break; }
-                const int ph = phase_of(g);
                 if (ph == PH_LSE) continue;
-                const int s = pv & 1, use = pv >> 1;
+                const int s = pv & 1, use = pv >> 1;   // V ring slot and P buffer share the with-V count
                 if (!wait_bar(bar(BAR_V_FULL + s), use & 1, abort_flag, ERR_V_FULL)) { ok = false; break; }
-                if (!wait_bar(bar(BAR_P_FULL), pv & 1, abort_flag, ERR_P_FULL)) { ok = false; break; }
+                if (!wait_bar(bar(BAR_P_FULL + s), use & 1, abort_flag, ERR_P_FULL)) { ok = false; break; }
                 tc_fence_after();
                 const bool neg = ph == PH_OLD;
-                const uint32_t pa = sbase + C::OFF_P;
-                const uint32_t va = sbase + C::OFF_V + C::TB * s;
+                const uint64_t dp = d_p + 2 * ATOM16 * s, dpt = d_pt + 2 * ATOM16 * s, dv = d_v + TB16 * s;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {   // acc += P[:, 16kk..] * V[16kk.., :]
-                    mma_bf16_ss(tmem + kColAcc, smem_desc(pa + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024, 2),
-                                smem_desc(va + kk * 2048, kAtom, 1024, 2), neg ? id_pv_old : id_pv_new,
-                                (pv > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)   // acc += P[:, 16kk..] * V[16kk.., :]
+                    mma_bf16_ss(tmem + kColAcc, dp + (kk >> 2) * ATOM16 + (kk & 3) * 2, dv + kk * 128,
+                                neg ? id_pv_old : id_pv_new, (pv > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk) {   // colsum = P^T[:, 16kk..] * ones
-                    mma_bf16_ss(tmem + kColCS, smem_desc(pa + kk * 2048, kAtom, 1024, 2), ones,
-                                neg ? id_cs_old : id_cs_new, kk > 0);
-                }
-                mma_commit(bar(BAR_P_EMPTY));
+                for (int kk = 0; kk < BM / 16; ++kk)   // colsum = P^T[:, 16kk..] * ones
+                    mma_bf16_ss(tmem + kColCS + 16 * s, dpt + kk * 128, ones, neg ? id_cs_old : id_cs_new, kk > 0);
+                mma_commit(bar(BAR_P_EMPTY + s));
                 mma_commit(bar(BAR_V_EMPTY + s));
                 ++pv;
             }
@@ -331,34 +343,48 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         const float zo2 = (!first && row_ok) ? __ldg(p.z + bh * p.n_state + pos) * kLog2e : 0.f;
         const int cnt_i = !row_ok ? 0 : dense ? min(pos + 1, p.n_keys) : count_le(S, p.K, pos);
         float m = 0.f, M = -INFINITY, L = 0.f, zn2 = INFINITY;
-        int pv = 0, prev_col = INT_MAX;
+        int pv = 0;
+        int col_hist[2] = {INT_MAX, INT_MAX};   // this lane's column of the last two P tiles
         bool ok = true;
         float *cb = p.c + bh * p.n_keys;
         uint32_t pk[32];   // this row's P over the half's 64 columns, bf16x2
+        // column sums of P tile `idx` (done once its PV/colsum MMAs completed)
+        auto flush_colsum = [&](int idx) {
+            const float cs = tmem_ld_32x32b_x1(tmem + lane_base + kColCS + 16 * (idx & 1));
+            tmem_wait_ld();
+            const int col = col_hist[idx & 1];
+            if (col != INT_MAX && cs != 0.f) atomicAdd(cb + col, cs);
+        };
         int ph = ph0, t = 0;
         for (int g = 0; g < total && ok; ++g, ++t) {
             if (t == n_tiles) { t = 0; ++ph; }
             const int s = g & 1, use = g >> 1;
+            if (ph == PH_LSE && t == 0 && !first) {
+                // pass OLD's products are all done (their S tiles were consumed):
+                // reload the query tile with this loop's q
+                load_query_row<D>(smem + C::OFF_Q, p.q + qoff, row_ok, r, wg);
+                fence_proxy_async_smem();
+                mbar_arrive(bar(BAR_Q_READY));
+            }
             if (ph == PH_NEW && t == 0) {
-                // merge the two halves' row statistics (exchange through the Q-hat tile,
-                // whose last reader, pass OLD's QK, has completed)
-                float *ex = reinterpret_cast<float *>(smem + C::OFF_QH);
-                ex[(wg * 128 + r) * 3 + 0] = m;
-                ex[(wg * 128 + r) * 3 + 1] = M;
-                ex[(wg * 128 + r) * 3 + 2] = L;
+                // merge the two halves' row statistics through TMEM (same lane, own columns)
+                tmem_st_32x32b_x4(tmem + lane_base + kColX + 4 * wg, m, M, L, 0.f);
+                tmem_wait_st();
+                tc_fence_before();
                 mbar_arrive(bar(BAR_STATS));
                 if (!wait_bar(bar(BAR_STATS), 0, abort_flag, ERR_STATS)) { ok = false; break; }
-                const float mo = ex[((1 - wg) * 128 + r) * 3 + 0];
-                const float Mo = ex[((1 - wg) * 128 + r) * 3 + 1];
-                const float Lo = ex[((1 - wg) * 128 + r) * 3 + 2];
-                const float Mx = fmaxf(M, Mo);
-                const float Lx = (Mx > -INFINITY) ? L * ex2(M - Mx) + Lo * ex2(Mo - Mx) : 0.f;
-                const float mx = first ? 1.f : m + mo;
+                tc_fence_after();
+                float o4[4];
+                tmem_ld_32x32b_x4(tmem + lane_base + kColX + 4 * (1 - wg), o4);
+                tmem_wait_ld();
+                const float Mx = fmaxf(M, o4[1]);
+                const float Lx = (Mx > -INFINITY) ? L * ex2(M - Mx) + o4[2] * ex2(o4[1] - Mx) : 0.f;
+                const float mx = first ? 1.f : m + o4[0];
                 zn2 = (Mx > -INFINITY && mx >= FLT_MIN) ? Mx + __log2f(Lx) - __log2f(mx) : INFINITY;
             }
             const int c0 = t * BN;
             const bool with_v = ph != PH_LSE;
-            // this lane's column of the column-sum MMA (only the first half reads it back)
+            // this lane's column of the column-sum MMA (only the first half reads sums back)
             const int jr = (with_v && wg == 0) ? col_index(c0 + r) : INT_MAX;
             // every row of the tile sees all 128 columns (uniform), else mask by the prefix count
             const bool full = c0 + BN <= cnt_min;
@@ -417,32 +443,27 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
             }
             if (ph == PH_OLD) m += (m4[0] + m4[1]) + (m4[2] + m4[3]);
-            if (!wait_bar(bar(BAR_P_EMPTY), (pv & 1) ^ 1, abort_flag, ERR_P_EMPTY)) { ok = false; break; }
+            // P buffer pb was last read by the MMAs of P tile pv - 2
+            const int pb = pv & 1, puse = pv >> 1;
+            if (!wait_bar(bar(BAR_P_EMPTY + pb), (puse & 1) ^ 1, abort_flag, ERR_P_EMPTY)) { ok = false; break; }
             tc_fence_after();
-            if (wg == 0 && pv > 0) {   // column sums of the previous P tile
-                const float cs = tmem_ld_32x32b_x1(tmem + lane_base + kColCS);
-                tmem_wait_ld();
-                if (prev_col != INT_MAX && cs != 0.f) atomicAdd(cb + prev_col, cs);
-            }
-            uint8_t *pt = smem + C::OFF_P;
+            if (wg == 0 && pv >= 2) flush_colsum(pv - 2);
+            uint8_t *pt = smem + C::OFF_P + 2 * kAtom * pb;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 *reinterpret_cast<uint4 *>(pt + swz_off(r, wg * 8 + q)) =
                     make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar(BAR_P_FULL));
-            prev_col = jr;
+            mbar_arrive(bar(BAR_P_FULL + pb));
+            col_hist[pb] = jr;
             ++pv;
         }
-        if (ok && pv > 0 && wg == 0) {
-            if (wait_bar(bar(BAR_P_EMPTY), (pv & 1) ^ 1, abort_flag, ERR_P_EMPTY)) {
+        if (ok && wg == 0) {   // column sums of the last (up to) two P tiles
+            for (int idx = max(0, pv - 2); idx < pv && ok; ++idx) {
+                if (!wait_bar(bar(BAR_P_EMPTY + (idx & 1)), (idx >> 1) & 1, abort_flag, ERR_P_EMPTY)) { ok = false; break; }
                 tc_fence_after();
-                const float cs = tmem_ld_32x32b_x1(tmem + lane_base + kColCS);
-                tmem_wait_ld();
-                if (prev_col != INT_MAX && cs != 0.f) atomicAdd(cb + prev_col, cs);
-            } else {
-                ok = false;
+                flush_colsum(idx);
             }
         }
         if (ok && wait_bar(bar(BAR_ACC), 0, abort_flag, ERR_ACC)) {
