@@ -195,6 +195,23 @@ flashloop_status_t flashloop_select_tokens(const uint16_t *h_prev, const uint16_
                                            void *workspace, size_t workspace_bytes,
                                            flashloop_stream_t stream);
 
+/* Token selection that allocates nothing (no counterpart in the paper; an
+ * interface for callers that may not allocate device memory: code running
+ * inside a memory arena it does not own, such as a serving engine's fixed
+ * budget or a plugin host, or on a path where an allocation could stall or
+ * fail at the wrong moment). Same operation and result as
+ * flashloop_select_tokens, but the B*N change scores live in a fixed array
+ * of this library (at most 1,048,576 scores, 4 MiB, held on every device
+ * that loads the library until the process exits) instead of a caller
+ * workspace; larger B*N returns FLASHLOOP_ERR_CAPACITY. The first call on
+ * each device looks up the array's device address (no allocation), so make
+ * that first call before any stream capture. All calls share the array:
+ * calls whose work may overlap on the device (different streams, or
+ * different host threads) race and must be serialised by the caller. */
+flashloop_status_t flashloop_select_tokens_noalloc(const uint16_t *h_prev, const uint16_t *h_cur,
+                                                   int32_t B, int32_t N, int32_t D, int32_t R,
+                                                   int32_t *active_idx, flashloop_stream_t stream);
+
 /* Gather of selected rows into a dense buffer ("the selected data is
  * gathered into dense buffers"): dst[b, r, :] = src[b, idx[b, r], :].
  * src [B, N, row_bytes], idx [B, R] in [0, N), dst [B, R, row_bytes];

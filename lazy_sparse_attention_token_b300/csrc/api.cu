@@ -87,12 +87,12 @@ flashloop_status_t set_error(flashloop_status_t st, const char *fmt, ...) {
     return st;
 }
 
-static flashloop_status_t cuda_fail(cudaError_t e, const char *what) {
+flashloop_status_t cuda_fail(cudaError_t e, const char *what) {
     return set_error(FLASHLOOP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
 // Every compute entry point runs only on an sm_103 device.
-static flashloop_status_t check_device() {
+flashloop_status_t check_device() {
     static std::mutex mu;
     static int cached_dev = -1;
     static bool cached_ok = false;

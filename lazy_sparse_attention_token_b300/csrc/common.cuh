@@ -29,6 +29,8 @@ class KernelTimer {
 };
 flashloop_status_t set_error(flashloop_status_t st, const char *fmt, ...);
 flashloop_status_t check_launch(const char *what);
+flashloop_status_t check_device();
+flashloop_status_t cuda_fail(cudaError_t e, const char *what);
 
 constexpr int kMaxLoops = FLASHLOOP_MAX_LOOPS;
 

@@ -5,6 +5,8 @@
 // loops rank tokens by how much their hidden states changed and recompute
 // only the active ones; keys are chosen from the previous loop's statistics.
 // Both rankings keep the top-k with ties to the lower index, ascending.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace fl {
@@ -205,3 +207,63 @@ cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t 
 }
 
 }  // namespace fl
+
+// ---------------------------------------------------------------------------
+// Token selection without allocation.
+//
+// For callers that may not allocate device memory at all: code that runs
+// inside a memory arena it does not own (a serving engine's fixed budget, a
+// plugin host), or on a path where an allocation could stall or fail at the
+// wrong moment. The change scores, the only scratch this step needs, live in
+// a fixed array of this library instead of a caller workspace. Every device
+// that loads the library holds the array until the process exits.
+namespace fl {
+namespace {
+constexpr long long kNoAllocMaxScores = 1ll << 20;   // B * N limit: 1,048,576 fp32 scores (4 MiB)
+constexpr int kNoAllocMaxDevices = 64;
+static __device__ __align__(256) float g_noalloc_scores[kNoAllocMaxScores];
+std::mutex g_noalloc_mu;
+float *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+}  // namespace
+
+}  // namespace fl
+
+using namespace fl;
+
+extern "C" flashloop_status_t flashloop_select_tokens_noalloc(const uint16_t *h_prev, const uint16_t *h_cur,
+                                                              int32_t B, int32_t N, int32_t D, int32_t R,
+                                                              int32_t *active_idx, flashloop_stream_t stream) {
+    if (!h_prev || !h_cur || !active_idx) return set_error(FLASHLOOP_ERR_INVALID_ARG, "NULL pointer");
+    if ((reinterpret_cast<uintptr_t>(h_prev) | reinterpret_cast<uintptr_t>(h_cur)) & 15u)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "inputs must be 16-byte aligned");
+    if (B < 1 || N < 1 || D < 8 || D % 8 || R < 1 || R > N)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad sizes (B=%d N=%d D=%d R=%d)", B, N, D, R);
+    if ((long long)B * N > kNoAllocMaxScores)
+        return set_error(FLASHLOOP_ERR_CAPACITY, "B*N = %lld exceeds the fixed scratch of %lld scores",
+                         (long long)B * N, kNoAllocMaxScores);
+    flashloop_status_t st = check_device();
+    if (st != FLASHLOOP_OK) return st;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return set_error(FLASHLOOP_ERR_UNSUPPORTED, "device index %d", dev);
+    float *scores = nullptr;
+    {
+        // once per device, with that device current: the device address of the array
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            e = cudaGetSymbolAddress(reinterpret_cast<void **>(&g_noalloc_ptr[dev]), g_noalloc_scores);
+            if (e != cudaSuccess) {
+                g_noalloc_ptr[dev] = nullptr;
+                return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+            }
+        }
+        scores = g_noalloc_ptr[dev];
+    }
+    // every score is written before it is read: nothing needs clearing
+    e = launch_token_scores(h_prev, h_cur, B, N, D, scores, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "token_scores");
+    e = launch_topk_rows(scores, B, N, R, active_idx, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "topk(tokens)");
+    return FLASHLOOP_OK;
+}

@@ -63,7 +63,7 @@ EXPORTS = [
     "flashloop_select_tokens", "flashloop_gather", "flashloop_kv_delta_append", "flashloop_kv_dense_store",
     "flashloop_select_keys", "flashloop_reconstruct_keys", "flashloop_lazy_attention", "flashloop_loop_step",
     "flashloop_status_string", "flashloop_last_error", "flashloop_device_status", "flashloop_launch_count",
-    "flashloop_timing_enable", "flashloop_timing_read",
+    "flashloop_timing_enable", "flashloop_timing_read", "flashloop_select_tokens_noalloc",
 ]
 
 
@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
         L.flashloop_kv_cache_bytes.argtypes = [ctypes.POINTER(Dims)]
         L.flashloop_kv_cache_init.argtypes = [ctypes.POINTER(KVCache), P, SZ, ctypes.POINTER(Dims), P]
         L.flashloop_select_tokens.argtypes = [P, P, I32, I32, I32, I32, P, P, P, SZ, P]
+        L.flashloop_select_tokens_noalloc.argtypes = [P, P, I32, I32, I32, I32, P, P]
         L.flashloop_gather.argtypes = [P, I32, I32, I32, P, I32, P, P]
         L.flashloop_kv_delta_append.argtypes = [ctypes.POINTER(KVCache), I32, P, P, I32, P, I32, I32, P]
         L.flashloop_kv_dense_store.argtypes = [ctypes.POINTER(KVCache), I32, P, P, I32, I32, P]
@@ -199,6 +200,16 @@ def flashloop_select_tokens(h_prev, h_cur, R: int, active_idx=None, scores=None,
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().flashloop_select_tokens(_ptr(h_prev), _ptr(h_cur), B, N, D, R, _ptr(active_idx), _ptr(scores),
                                          _ptr(workspace), ws_bytes, _stream(stream)), "flashloop_select_tokens")
+    return active_idx
+
+
+def flashloop_select_tokens_noalloc(h_prev, h_cur, R: int, active_idx=None, stream=None):
+    """flashloop_select_tokens with the library's fixed scratch (no workspace, no allocation)."""
+    B, N, D = h_prev.shape
+    if active_idx is None:
+        active_idx = torch.empty(B, R, dtype=torch.int32, device=h_prev.device)
+    _check(lib().flashloop_select_tokens_noalloc(_ptr(h_prev), _ptr(h_cur), B, N, D, R, _ptr(active_idx),
+                                                 _stream(stream)), "flashloop_select_tokens_noalloc")
     return active_idx
 
 
