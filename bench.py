@@ -161,6 +161,26 @@ def hbm_bytes(w, R, K):
     }
 
 
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu record (profiles/traffic.txt),
+    or None when there is none or the kernel's source changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) != 5 or line.startswith("#") or parts[0] != kernel or parts[1] != workload:
+            continue
+        src = os.path.join(ROOT, "lazy_sparse_attention_token_b300", "csrc", parts[3])
+        if not os.path.exists(src):
+            return None
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != parts[4]:
+            return None
+        return int(parts[2])
+    return None
+
+
 # --------------------------------------------------------------------------
 # the CUDA path
 
@@ -257,11 +277,9 @@ def native(args, world, rank, local):
                 "peak_source": f"{peak_kind} ({'bf16 burst' if tk.get('bound') == 'tensor' else 'copy'})",
                 "units_per_launch": (f"{mean_pairs:.0f} (row, key) pairs x 4 contractions x 2 d flop"
                                      if top == "tc_attention" else None)}
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        tr = json.load(open(prof)).get(top)
-        if tr and tr.get("workload") == args.workload:
-            roofline["traffic"] = tr.get("bytes_per_launch")
+    roofline["traffic"] = recorded_traffic(top, args.workload)
+    for name, ent in kernels.items():
+        ent["traffic"] = recorded_traffic(name, args.workload)
 
     e2e = None if args.no_e2e else e2e_leg(args, w, fl, cache, ws, loops, q_hat, o, z, c, act, keys, scores, lazy,
                                            dev, world)
