@@ -16,23 +16,26 @@
 //   c_j += sum_i exp(q_i.k_j^(l) s - Z'_i) - p_ij         (column mass)
 // in three passes over the key tiles, all with a known normaliser so no
 // accumulator rescaling is ever needed:
-//   pass OLD: QK_old -> p -> m, acc -= P V_old, colsum -= P
+//   pass OLD: QK_old -> -p -> m, acc += (-P) V_old, column sums of -P
 //   pass LSE: QK_new -> online max/sum -> lam
-//   pass NEW: QK_new -> P' = exp(. - Z') -> acc += P' V_new, colsum += P'
+//   pass NEW: QK_new -> P' = exp(. - Z') -> acc += P' V_new, column sums of P'
 // The first dense loop skips pass OLD (m = 1, u = 0).
 //
-// Roles (320 threads): warp 0 issues TMA loads into a K ring and a V ring
-// (2 stages each; a K slot is released as soon as its QK product is done);
-// warp 1 (one thread) issues tcgen05.mma into TMEM; warps 2..9 are two
-// softmax warpgroups that each own one TMEM lane (= one row) and one half
-// of the tile's 128 columns: they read S, do the softmax arithmetic, write
-// P as bf16 into one of two shared buffers for the PV and column-sum MMAs
-// (so the next tile's P never waits for the current PV), merge their row
-// statistics once through TMEM, and split the epilogue. One query tile
-// holds qhat for pass OLD and is reloaded with q before pass LSE. Column sums are an MMA of P^T (the same shared tile read
-// MN-major) with a ones matrix, so no cross-thread reduction is needed.
-// TMEM columns: S double buffer [0,256), accumulator [256,256+d), column
-// sums double buffer [384,416), row-statistics exchange [448,456).
+// Roles (576 threads): warp 0 issues TMA loads into a K ring (3 stages) and
+// a V ring (2 stages); warp 1 (one thread) issues tcgen05.mma; warps 2..17
+// are four softmax groups of four warps. A warp owns 32 TMEM lanes (= rows)
+// and its group owns 32 of the tile's 128 columns. A tile's logits land in
+// one of three 128-column TMEM buffers; the softmax writes the bf16
+// probabilities back over the first half of the columns it has read, and the
+// PV product takes them straight from TMEM (A operand in tensor memory), so P
+// never touches shared memory. The probabilities are handed over before the
+// column masses are formed: those are summed after the hand-off by integer
+// warp reductions of a fixed-point encoding and added to c with one atomic
+// per column and warp. A buffer is reused once the softmax has read it and,
+// for tiles with a PV product, once that product completed. The query tile
+// holds qhat for pass OLD and is reloaded with q before pass LSE; the four
+// groups merge row statistics once, through shared memory.
+// TMEM columns: S/P buffers [0,384), accumulator [384,384+d).
 //
 // Waiting threads sleep in a hinted try_wait instead of spinning. Every
 // mbarrier wait is bounded (about one second); on timeout the CTA records an
@@ -52,34 +55,44 @@ using namespace ptx;
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int kThreads = 320;     // warp 0 TMA, warp 1 MMA, warps 2..5 and 6..9 softmax (column halves)
-constexpr int kSoftmax = 256;
+constexpr int BN_ = BN;
+constexpr int kThreads = 576;     // warp 0 TMA, warp 1 MMA, warps 2..17 softmax (4 groups x 4 warps)
+constexpr int kGroups = 4;        // softmax warpgroups, each owns 32 of a tile's 128 columns
+constexpr int kGroupCols = BN_ / kGroups;
+constexpr int kSoftmaxWarps = 4 * kGroups;   // softmax-side barriers take one elected arrival per warp
 constexpr int kAtom = 128 * 128;  // bytes of a 128-row x 64-element bf16 tile, 128-byte swizzled
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S double buffer, accumulator, column sums (double buffer), row-statistics exchange
-constexpr uint32_t kColS = 0, kColAcc = 256, kColCS = 384, kColX = 448;
+constexpr int kSBufs = 3;         // S/P buffers in TMEM, 128 columns each
+constexpr uint32_t kColAcc = 384; // accumulator columns [384, 384 + d)
+constexpr int kKStages = 3, kVStages = 2;
+static_assert(kKStages == kSBufs, "a tile's K slot and S/P buffer share one index");
+static_assert(kVStages == 2, "the MMA issuer indexes the V ring with a parity bit");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// Column sums are taken on integers: x*2^20 rounded into the mantissa of
+// x*2^20 + 1.5*2^23 (exact while |x| < 4), so a warp reduction is exact and
+// the sum of 32 lanes' offsets is removed afterwards.
+constexpr float kFixScale = 1048576.0f, kFixMagic = 12582912.0f;
+constexpr uint32_t kFixBits = 0x4B400000u;
 
 __device__ int g_tc_error;
 
 enum : int { PH_OLD = 0, PH_LSE = 1, PH_NEW = 2 };
-enum : int { BAR_K_FULL = 0, BAR_K_EMPTY = 2, BAR_V_FULL = 4, BAR_V_EMPTY = 6, BAR_S_FULL = 8,
-             BAR_S_EMPTY = 10, BAR_P_FULL = 12, BAR_P_EMPTY = 14, BAR_ACC = 16, BAR_STATS = 17,
-             BAR_Q_READY = 18, BAR_DRAIN = 19, N_BARS = 20 };
-enum : int { ERR_K_EMPTY = 1, ERR_K_FULL = 2, ERR_V_EMPTY = 3, ERR_V_FULL = 4, ERR_S_EMPTY = 5, ERR_S_FULL = 6,
-             ERR_P_FULL = 7, ERR_P_EMPTY = 8, ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11 };
+enum : int { BAR_K_FULL = 0, BAR_K_EMPTY = 3, BAR_V_FULL = 6, BAR_V_EMPTY = 8, BAR_S_FULL = 10, BAR_S_READ = 13,
+             BAR_P_FULL = 16, BAR_PV_DONE = 19, BAR_ACC = 22, BAR_STATS = 23, BAR_Q_READY = 24, BAR_DRAIN = 25,
+             N_BARS = 26 };
+enum : int { ERR_K_EMPTY = 1, ERR_K_FULL = 2, ERR_V_EMPTY = 3, ERR_V_FULL = 4, ERR_S_READ = 5, ERR_S_FULL = 6,
+             ERR_P_FULL = 7, ERR_PV_DONE = 8, ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11 };
 
 template <int D>
 struct Cfg {
     static constexpr int NA = (D + 63) / 64;        // 64-element atoms along d
     static constexpr int TB = NA * kAtom;           // one 128-row tile of Q, K or V
     static constexpr int OFF_Q = 0;                 // queries: qhat for pass OLD, then q
-    static constexpr int OFF_K = TB;                // K ring: 2 stages
-    static constexpr int OFF_V = 3 * TB;            // V ring: 2 stages
-    static constexpr int OFF_P = 5 * TB;            // P: 2 buffers of 128 x 128 bf16
-    static constexpr int OFF_ONES = OFF_P + 4 * kAtom;
-    static constexpr int OFF_BAR = OFF_ONES + 512;
+    static constexpr int OFF_K = TB;                // K ring
+    static constexpr int OFF_V = OFF_K + kKStages * TB;   // V ring
+    static constexpr int OFF_X = OFF_V + kVStages * TB;   // row-statistics exchange: [groups][128][3] fp32
+    static constexpr int OFF_BAR = OFF_X + kGroups * 128 * 3 * 4;
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM = BYTES + 1024;       // room to align the base to 1024 bytes
@@ -140,16 +153,29 @@ __device__ __forceinline__ uint32_t swz_off(int r, int ch) {
     return (uint32_t)((ch >> 3) * kAtom + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
-// Gathers row r's query (qhat or q) into the swizzled query tile; the two
-// softmax halves each write every other 16-byte chunk.
+// Gathers row r's query (qhat or q) into the swizzled query tile; each
+// softmax group writes every kGroups-th 16-byte chunk.
 template <int D>
 __device__ __forceinline__ void load_query_row(uint8_t *tile, const uint16_t *src_row, bool row_ok, int r, int wg) {
     const uint4 zero = make_uint4(0, 0, 0, 0);
     const uint4 *src = reinterpret_cast<const uint4 *>(src_row);
 #pragma unroll
-    for (int ch = wg; ch < D / 8; ch += 2)
+    for (int ch = wg; ch < D / 8; ch += kGroups)
         *reinterpret_cast<uint4 *>(tile + swz_off(r, ch)) = row_ok ? src[ch] : zero;
 }
+
+// One arrival per warp: every lane's earlier shared-memory and tensor-memory
+// work is ordered before lane 0 arrives.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+}
+
+// TMEM column of the P values for keys [16 kk, 16 kk + 16) of an S/P buffer:
+// each softmax group writes bf16 pairs over the first 16 of the 32 S columns
+// it read itself (keys 32 g .. 32 g + 31 -> columns 32 g .. 32 g + 15).
+__device__ __forceinline__ uint32_t p_col(int kk) { return 32u * (kk >> 1) + 8u * (kk & 1); }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -166,8 +192,11 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.z, h = blockIdx.y;
-    const int rt = p.n_row_tiles - 1 - (int)blockIdx.x;   // heavier (later) row tiles first
+    // Work grows with a row tile's last position (later rows see more keys), so the
+    // linear CTA order runs every head's heaviest row tiles first and leaves the
+    // lightest ones for the last, partial wave.
+    const int b = blockIdx.z, h = (int)(blockIdx.x % p.H);
+    const int rt = p.n_row_tiles - 1 - (int)(blockIdx.x / p.H);
     const bool dense = p.mode != FLASHLOOP_ATTN_LAZY;
     const bool first = p.mode == FLASHLOOP_ATTN_FIRST_DENSE;
     const int row0 = rt * BM;
@@ -191,11 +220,9 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     // ---------------- set-up ----------------
     if (threadIdx.x == 0) {
         for (int i = 0; i < N_BARS; ++i) {
-            uint32_t count = 1;
-            if (i == BAR_S_EMPTY || i == BAR_S_EMPTY + 1 || i == BAR_P_FULL || i == BAR_P_FULL + 1 ||
-                i == BAR_STATS || i == BAR_Q_READY)
-                count = kSoftmax;
-            mbar_init(bar(i), count);
+            const bool many = (i >= BAR_S_READ && i < BAR_S_READ + kSBufs) || (i >= BAR_P_FULL && i < BAR_P_FULL + kSBufs) ||
+                              i == BAR_STATS || i == BAR_Q_READY;
+            mbar_init(bar(i), many ? (uint32_t)kSoftmaxWarps : 1u);
         }
         misc[1] = 0;
         mbar_fence_init();
@@ -205,13 +232,8 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         tmem_alloc(sbase + C::OFF_MISC, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 1) {   // 16x16 bf16 ones (B operand of the column-sum MMA)
-        uint4 one4 = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-        reinterpret_cast<uint4 *>(smem + C::OFF_ONES)[lane] = one4;
-        fence_proxy_async_smem();
-    }
     const bool is_sm = warp >= 2;
-    const int wg = is_sm ? (warp - 2) >> 2 : 0;   // column half of the softmax warps
+    const int wg = is_sm ? (warp - 2) >> 2 : 0;   // softmax group: columns [32 wg, 32 wg + 32) of a tile
     const int r = (warp & 3) * 32 + lane;          // tile row == TMEM lane
     const bool row_ok = is_sm && r < rows;
     const int pos = row_ok ? (dense ? row0 + r : __ldg(A + r)) : -1;
@@ -226,7 +248,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const uint32_t tmem = misc[0];
 
     if (warp == 0) {
-        // ---------------- TMA producer: K ring and V ring ----------------
+        // ---------------- TMA producer: K ring (3 stages) and V ring (2 stages) ----------------
         if (lane == 0) {
             prefetch_tmap(&tm_k_old); prefetch_tmap(&tm_v_old);
             prefetch_tmap(&tm_k_new); prefetch_tmap(&tm_v_new);
@@ -236,7 +258,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 if (t == n_tiles) { t = 0; ++ph; }
                 const int key0 = t * BN;
                 {
-                    const int s = g & 1, use = g >> 1;
+                    const int s = g % kKStages, use = g / kKStages;
                     if (!wait_bar(bar(BAR_K_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_K_EMPTY)) break;
                     const CUtensorMap *mk = ph == PH_OLD ? &tm_k_old : &tm_k_new;
                     const uint32_t dst = sbase + C::OFF_K + C::TB * s;
@@ -248,7 +270,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                     k_issued = g + 1;
                 }
                 if (ph != PH_LSE) {
-                    const int vi = v_issued, s = vi & 1, use = vi >> 1;
+                    const int vi = v_issued, s = vi % kVStages, use = vi / kVStages;
                     if (!wait_bar(bar(BAR_V_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_V_EMPTY)) break;
                     const CUtensorMap *mv = ph == PH_OLD ? &tm_v_old : &tm_v_new;
                     const uint32_t dst = sbase + C::OFF_V + C::TB * s;
@@ -262,70 +284,79 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             }
             if (*abort_flag) {   // let copies already in flight land before the CTA exits
                 volatile int never = 0;
-                for (int g = max(0, k_issued - 2); g < k_issued; ++g)
-                    wait_bar(bar(BAR_K_FULL + (g & 1)), (g >> 1) & 1, &never, ERR_K_FULL);
-                for (int v = max(0, v_issued - 2); v < v_issued; ++v)
-                    wait_bar(bar(BAR_V_FULL + (v & 1)), (v >> 1) & 1, &never, ERR_V_FULL);
+                for (int g = max(0, k_issued - kKStages); g < k_issued; ++g)
+                    wait_bar(bar(BAR_K_FULL + g % kKStages), (g / kKStages) & 1, &never, ERR_K_FULL);
+                for (int v = max(0, v_issued - kVStages); v < v_issued; ++v)
+                    wait_bar(bar(BAR_V_FULL + v % kVStages), (v / kVStages) & 1, &never, ERR_V_FULL);
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false, false);
-            constexpr uint32_t id_pv_old = idesc_bf16(128, D, false, true, true);
-            constexpr uint32_t id_pv_new = idesc_bf16(128, D, false, true, false);
-            constexpr uint32_t id_cs_old = idesc_bf16(128, 16, true, false, true);
-            constexpr uint32_t id_cs_new = idesc_bf16(128, 16, true, false, false);
+            constexpr uint32_t id_pv = idesc_bf16(128, D, false, true, false);   // A = P from TMEM
             // descriptors are built once; per k-step only the start address moves
             const uint64_t d_q = smem_desc(sbase + C::OFF_Q, 16, 1024, 2);
             const uint64_t d_k = smem_desc(sbase + C::OFF_K, 16, 1024, 2);
             const uint64_t d_v = smem_desc(sbase + C::OFF_V, kAtom, 1024, 2);
-            const uint64_t d_p = smem_desc(sbase + C::OFF_P, 16, 1024, 2);
-            const uint64_t d_pt = smem_desc(sbase + C::OFF_P, kAtom, 1024, 2);
-            const uint64_t ones = smem_desc(sbase + C::OFF_ONES, 128, 256, 0);
             constexpr uint64_t TB16 = C::TB >> 4, ATOM16 = kAtom >> 4;
-            int ph_next = ph0, t_next = 0;   // phase of tile g + 1 while issuing it
+            // Bookkeeping stays in registers: the tensor core buffers only about two
+            // MMAs, so any scalar latency between MMA groups is idle tensor time.
+            // Per S/P buffer (= K slot) b, bit b of: used (ever written), upar (parity
+            // of its uses so far), hadv (its last tile had a PV product), pfpar (parity
+            // of P-ready waits), pdpar (parity of PV-done commits).
+            uint32_t used = 0, upar = 0, hadv = 0, pfpar = 0, pdpar = 0;
+            int qb = 0;                      // S/P buffer and K slot of the next QK
+            int ph_next = ph0, t_next = 0;   // phase and tile of the next QK
             auto issue_qk = [&](int g) -> bool {
-                const int s = g & 1, use = g >> 1;
                 const int ph = ph_next;
                 if (++t_next == n_tiles) { t_next = 0; ++ph_next; }
-                if (!wait_bar(bar(BAR_K_FULL + s), use & 1, abort_flag, ERR_K_FULL)) return false;
-                if (!wait_bar(bar(BAR_S_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_S_EMPTY)) return false;
-                if (ph == PH_LSE && g == (PH_LSE - ph0) * n_tiles && !first) {   // queries reloaded after pass OLD
+                const uint32_t bit = 1u << qb, par = (upar >> qb) & 1u;
+                if (!wait_bar(bar(BAR_K_FULL + qb), par, abort_flag, ERR_K_FULL)) return false;
+                if (used & bit) {   // the buffer's last S was read, and its last P consumed by PV
+                    if (!wait_bar(bar(BAR_S_READ + qb), par ^ 1u, abort_flag, ERR_S_READ)) return false;
+                    if ((hadv & bit) && !wait_bar(bar(BAR_PV_DONE + qb), ((pdpar >> qb) & 1u) ^ 1u, abort_flag, ERR_PV_DONE))
+                        return false;
+                }
+                if (ph == PH_LSE && g == n_tiles && !first) {   // queries reloaded after pass OLD
                     if (!wait_bar(bar(BAR_Q_READY), 0, abort_flag, ERR_Q_READY)) return false;
                 }
                 tc_fence_after();
-                const uint64_t dk = d_k + TB16 * s;
+                const uint64_t dk = d_k + TB16 * (uint32_t)qb;
+                const uint32_t dst = tmem + 128u * (uint32_t)qb;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (kk >> 2) * ATOM16 + (kk & 3) * 2;
-                    mma_bf16_ss(tmem + kColS + 128 * s, d_q + off, dk + off, id_qk, kk > 0);
+                    mma_bf16_ss(dst, d_q + off, dk + off, id_qk, kk > 0);
                 }
-                mma_commit(bar(BAR_S_FULL + s));
-                mma_commit(bar(BAR_K_EMPTY + s));
+                mma_commit(bar(BAR_S_FULL + qb));
+                mma_commit(bar(BAR_K_EMPTY + qb));
+                used |= bit;
+                upar ^= bit;
+                hadv = ph != PH_LSE ? (hadv | bit) : (hadv & ~bit);
+                qb = qb == kSBufs - 1 ? 0 : qb + 1;
                 return true;
             };
             bool ok = issue_qk(0);
-            int pv = 0, ph = ph0, t = 0;
-            for (int g = 0; ok && g < total; ++g, ++t) {
+            int pv = 0, ph = ph0, t = 0, pb = 0;   // pb: S/P buffer of tile g
+            for (int g = 0; ok && g < total; ++g, ++t, pb = pb == kSBufs - 1 ? 0 : pb + 1) {
                 if (t == n_tiles) { t = 0; ++ph; }
                 if (g + 1 < total && !issue_qk(g + 1)) { ok = false; break; }
                 if (ph == PH_LSE) continue;
-                const int s = pv & 1, use = pv >> 1;   // V ring slot and P buffer share the with-V count
-                if (!wait_bar(bar(BAR_V_FULL + s), use & 1, abort_flag, ERR_V_FULL)) { ok = false; break; }
-                if (!wait_bar(bar(BAR_P_FULL + s), use & 1, abort_flag, ERR_P_FULL)) { ok = false; break; }
+                const int vs = pv & 1;
+                const uint32_t bit = 1u << pb;
+                if (!wait_bar(bar(BAR_V_FULL + vs), (pv >> 1) & 1, abort_flag, ERR_V_FULL)) { ok = false; break; }
+                if (!wait_bar(bar(BAR_P_FULL + pb), (pfpar >> pb) & 1u, abort_flag, ERR_P_FULL)) { ok = false; break; }
+                pfpar ^= bit;
                 tc_fence_after();
-                const bool neg = ph == PH_OLD;
-                const uint64_t dp = d_p + 2 * ATOM16 * s, dpt = d_pt + 2 * ATOM16 * s, dv = d_v + TB16 * s;
+                const uint64_t dv = d_v + TB16 * (uint32_t)vs;
+                const uint32_t pa = tmem + 128u * (uint32_t)pb;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)   // acc += P[:, 16kk..] * V[16kk.., :]
-                    mma_bf16_ss(tmem + kColAcc, dp + (kk >> 2) * ATOM16 + (kk & 3) * 2, dv + kk * 128,
-                                neg ? id_pv_old : id_pv_new, (pv > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)   // colsum = P^T[:, 16kk..] * ones
-                    mma_bf16_ss(tmem + kColCS + 16 * s, dpt + kk * 128, ones, neg ? id_cs_old : id_cs_new, kk > 0);
-                mma_commit(bar(BAR_P_EMPTY + s));
-                mma_commit(bar(BAR_V_EMPTY + s));
+                for (int kk = 0; kk < BN / 16; ++kk)   // acc += P[:, 16kk..] * V[16kk.., :]  (P is signed)
+                    mma_bf16_ts(tmem + kColAcc, pa + p_col(kk), dv + kk * 128, id_pv, (pv > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(BAR_PV_DONE + pb));
+                pdpar ^= bit;
+                mma_commit(bar(BAR_V_EMPTY + vs));
                 ++pv;
             }
             if (ok) {
@@ -337,79 +368,73 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             }
         }
     } else {
-        // ---------------- softmax / epilogue: two warpgroups, one column half each ----------------
+        // ---------------- softmax / epilogue: four groups, 32 columns each ----------------
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const int half = wg * 64;
+        const int cbase = wg * kGroupCols;
         const float zo2 = (!first && row_ok) ? __ldg(p.z + bh * p.n_state + pos) * kLog2e : 0.f;
-        const int cnt_i = !row_ok ? 0 : dense ? min(pos + 1, p.n_keys) : count_le(S, p.K, pos);
+        // every row of the tile sees the same keys when the first and last rows do
+        const int cnt_i = !row_ok ? 0 : cnt_min == cnt ? cnt : dense ? min(pos + 1, p.n_keys) : count_le(S, p.K, pos);
         float m = 0.f, M = -INFINITY, L = 0.f, zn2 = INFINITY;
-        int pv = 0;
-        int col_hist[2] = {INT_MAX, INT_MAX};   // this lane's column of the last two P tiles
         bool ok = true;
         float *cb = p.c + bh * p.n_keys;
-        uint32_t pk[32];   // this row's P over the half's 64 columns, bf16x2
-        // column sums of P tile `idx` (done once its PV/colsum MMAs completed)
-        auto flush_colsum = [&](int idx) {
-            const float cs = tmem_ld_32x32b_x1(tmem + lane_base + kColCS + 16 * (idx & 1));
-            tmem_wait_ld();
-            const int col = col_hist[idx & 1];
-            if (col != INT_MAX && cs != 0.f) atomicAdd(cb + col, cs);
-        };
         int ph = ph0, t = 0;
         for (int g = 0; g < total && ok; ++g, ++t) {
             if (t == n_tiles) { t = 0; ++ph; }
-            const int s = g & 1, use = g >> 1;
+            const int sb = g % kSBufs, suse = g / kSBufs;
             if (ph == PH_LSE && t == 0 && !first) {
                 // pass OLD's products are all done (their S tiles were consumed):
                 // reload the query tile with this loop's q
                 load_query_row<D>(smem + C::OFF_Q, p.q + qoff, row_ok, r, wg);
                 fence_proxy_async_smem();
-                mbar_arrive(bar(BAR_Q_READY));
+                warp_arrive(bar(BAR_Q_READY), lane);
             }
             if (ph == PH_NEW && t == 0) {
-                // merge the two halves' row statistics through TMEM (same lane, own columns)
-                tmem_st_32x32b_x4(tmem + lane_base + kColX + 4 * wg, m, M, L, 0.f);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(bar(BAR_STATS));
+                // merge the groups' row statistics
+                float *ex = reinterpret_cast<float *>(smem + C::OFF_X);
+                ex[(wg * 128 + r) * 3 + 0] = m;
+                ex[(wg * 128 + r) * 3 + 1] = M;
+                ex[(wg * 128 + r) * 3 + 2] = L;
+                warp_arrive(bar(BAR_STATS), lane);
                 if (!wait_bar(bar(BAR_STATS), 0, abort_flag, ERR_STATS)) { ok = false; break; }
-                tc_fence_after();
-                float o4[4];
-                tmem_ld_32x32b_x4(tmem + lane_base + kColX + 4 * (1 - wg), o4);
-                tmem_wait_ld();
-                const float Mx = fmaxf(M, o4[1]);
-                const float Lx = (Mx > -INFINITY) ? L * ex2(M - Mx) + o4[2] * ex2(o4[1] - Mx) : 0.f;
-                const float mx = first ? 1.f : m + o4[0];
+                float mx = 0.f, Mx = -INFINITY, Lx = 0.f;
+#pragma unroll
+                for (int k = 0; k < kGroups; ++k) {
+                    mx += ex[(k * 128 + r) * 3 + 0];
+                    Mx = fmaxf(Mx, ex[(k * 128 + r) * 3 + 1]);
+                }
+                if (Mx > -INFINITY) {
+#pragma unroll
+                    for (int k = 0; k < kGroups; ++k)
+                        Lx += ex[(k * 128 + r) * 3 + 2] * ex2(ex[(k * 128 + r) * 3 + 1] - Mx);
+                }
+                if (first) mx = 1.f;
                 zn2 = (Mx > -INFINITY && mx >= FLT_MIN) ? Mx + __log2f(Lx) - __log2f(mx) : INFINITY;
             }
             const int c0 = t * BN;
             const bool with_v = ph != PH_LSE;
-            // this lane's column of the column-sum MMA (only the first half reads sums back)
-            const int jr = (with_v && wg == 0) ? col_index(c0 + r) : INT_MAX;
+            // key position of this lane's column (for the column-mass atomics)
+            const int jcol = with_v ? col_index(c0 + cbase + lane) : INT_MAX;
             // every row of the tile sees all 128 columns (uniform), else mask by the prefix count
             const bool full = c0 + BN <= cnt_min;
-            const int nv = min(64, max(0, cnt_i - c0 - half));
-            if (!wait_bar(bar(BAR_S_FULL + s), use & 1, abort_flag, ERR_S_FULL)) { ok = false; break; }
+            const int nv = min(kGroupCols, max(0, cnt_i - c0 - cbase));
+            if (!wait_bar(bar(BAR_S_FULL + sb), suse & 1, abort_flag, ERR_S_FULL)) { ok = false; break; }
             tc_fence_after();
-            float sv[64];
-            const uint32_t sc = tmem + lane_base + kColS + 128 * s + half;
-            tmem_ld_32x32b_x32(sc, sv);
-            tmem_ld_32x32b_x32(sc + 32, sv + 32);
+            float sv[kGroupCols];
+            tmem_ld_32x32b_x32(tmem + lane_base + 128u * sb + cbase, sv);
             tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar(BAR_S_EMPTY + s));
+            warp_arrive(bar(BAR_S_READ + sb), lane);
             if (!with_v) {
                 // online logsumexp of this tile's new logits (log2 units)
                 if (full) {
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) sv[e] *= p.sl2;
+                    for (int e = 0; e < kGroupCols; ++e) sv[e] *= p.sl2;
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) sv[e] = e < nv ? sv[e] * p.sl2 : -INFINITY;
+                    for (int e = 0; e < kGroupCols; ++e) sv[e] = e < nv ? sv[e] * p.sl2 : -INFINITY;
                 }
                 float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int e = 0; e < 64; ++e) c4[e & 3] = fmaxf(c4[e & 3], sv[e]);
+                for (int e = 0; e < kGroupCols; ++e) c4[e & 3] = fmaxf(c4[e & 3], sv[e]);
                 const float cmax = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
                 if (cmax > M) {
                     L *= ex2(M - cmax);
@@ -417,85 +442,74 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
                 float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int e = 0; e < 64; ++e) a4[e & 3] += ex2(sv[e] - M);
+                for (int e = 0; e < kGroupCols; ++e) a4[e & 3] += ex2(sv[e] - M);
                 if (M > -INFINITY) L += (a4[0] + a4[1]) + (a4[2] + a4[3]);
                 continue;
             }
-            // probabilities with a known normaliser: exp(logit - Z) (rows outside the
-            // tile or the sequence get zero through an infinite normaliser)
+            // probabilities with a known normaliser, signed by pass (OLD subtracts):
+            // sign * exp(logit - Z); rows outside the tile or the sequence get zero
+            // through an infinite normaliser
             const float sub = !row_ok ? INFINITY : ph == PH_OLD ? zo2 : zn2;
-            float m4[4] = {0.f, 0.f, 0.f, 0.f};
+            const float sgn = ph == PH_OLD ? -1.f : 1.f;
             if (full) {
 #pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    const float x0 = ex2(fmaf(sv[e], p.sl2, -sub));
-                    const float x1 = ex2(fmaf(sv[e + 1], p.sl2, -sub));
-                    m4[(e >> 1) & 3] += x0 + x1;
-                    pk[e / 2] = pack_bf16x2_rn(x0, x1);
-                }
+                for (int e = 0; e < kGroupCols; ++e) sv[e] = sgn * ex2(fmaf(sv[e], p.sl2, -sub));
             } else {
 #pragma unroll
-                for (int e = 0; e < 64; e += 2) {
-                    const float x0 = e < nv ? ex2(fmaf(sv[e], p.sl2, -sub)) : 0.f;
-                    const float x1 = e + 1 < nv ? ex2(fmaf(sv[e + 1], p.sl2, -sub)) : 0.f;
-                    m4[(e >> 1) & 3] += x0 + x1;
-                    pk[e / 2] = pack_bf16x2_rn(x0, x1);
-                }
+                for (int e = 0; e < kGroupCols; ++e) sv[e] = e < nv ? sgn * ex2(fmaf(sv[e], p.sl2, -sub)) : 0.f;
             }
-            if (ph == PH_OLD) m += (m4[0] + m4[1]) + (m4[2] + m4[3]);
-            // P buffer pb was last read by the MMAs of P tile pv - 2
-            const int pb = pv & 1, puse = pv >> 1;
-            if (!wait_bar(bar(BAR_P_EMPTY + pb), (puse & 1) ^ 1, abort_flag, ERR_P_EMPTY)) { ok = false; break; }
-            tc_fence_after();
-            if (wg == 0 && pv >= 2) flush_colsum(pv - 2);
-            uint8_t *pt = smem + C::OFF_P + 2 * kAtom * pb;
+            uint32_t pk[kGroupCols / 2];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<uint4 *>(pt + swz_off(r, wg * 8 + q)) =
-                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(BAR_P_FULL + pb));
-            col_hist[pb] = jr;
-            ++pv;
-        }
-        if (ok && wg == 0) {   // column sums of the last (up to) two P tiles
-            for (int idx = max(0, pv - 2); idx < pv && ok; ++idx) {
-                if (!wait_bar(bar(BAR_P_EMPTY + (idx & 1)), (idx >> 1) & 1, abort_flag, ERR_P_EMPTY)) { ok = false; break; }
-                tc_fence_after();
-                flush_colsum(idx);
+            for (int e = 0; e < kGroupCols; e += 2) pk[e / 2] = pack_bf16x2_rn(sv[e], sv[e + 1]);
+            // this tile's P, bf16, over the first half of the S columns this group just read;
+            // handing it over is the PV product's critical path, the sums below are not
+            tmem_st_32x32b_x16(tmem + lane_base + 128u * sb + cbase, pk);
+            tmem_wait_st();
+            warp_arrive(bar(BAR_P_FULL + sb), lane);
+            if (ph == PH_OLD) {
+                float m4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < kGroupCols; ++e) m4[e & 3] += sv[e];
+                m -= (m4[0] + m4[1]) + (m4[2] + m4[3]);
             }
+            // column masses over the warp's 32 rows, exact on fixed-point integers
+            uint32_t csum = 0u;
+#pragma unroll
+            for (int e = 0; e < kGroupCols; ++e) {
+                const uint32_t tot = __reduce_add_sync(0xffffffffu, __float_as_uint(fmaf(sv[e], kFixScale, kFixMagic)));
+                if (e == lane) csum = tot;
+            }
+            const int fixed = (int)(csum - 32u * kFixBits);
+            if (jcol != INT_MAX && fixed != 0) atomicAdd(cb + jcol, (float)fixed * (1.0f / kFixScale));
         }
         if (ok && wait_bar(bar(BAR_ACC), 0, abort_flag, ERR_ACC)) {
             tc_fence_after();
+            constexpr int GD = D / kGroups;   // accumulator columns per group (16, 24 or 32)
+            float av[GD];
+#pragma unroll
+            for (int u = 0; u < GD / 8; ++u) tmem_ld_32x32b_x8(tmem + lane_base + kColAcc + wg * GD + 8 * u, av + 8 * u);
+            tmem_wait_ld();
             const bool update = row_ok && zn2 < INFINITY;
-            const long long srow = ((long long)b * p.n_state + max(pos, 0)) * p.H + h;
-            float4 *orow = reinterpret_cast<float4 *>(p.o + srow * D);
-            constexpr int HALF_D = D / 2;   // accumulator columns per warpgroup
+            if (update) {
+                const long long srow = ((long long)b * p.n_state + pos) * p.H + h;
+                float4 *orow = reinterpret_cast<float4 *>(p.o + srow * D) + wg * (GD / 4);
+                float4 ov[GD / 4];
 #pragma unroll
-            for (int u = 0; u < HALF_D / 16; ++u) {
-                float av[16];
-                const int col = wg * HALF_D + 16 * u;
-                tmem_ld_32x32b_x16(tmem + lane_base + kColAcc + col, av);
-                tmem_wait_ld();
-                if (update) {
+                for (int e = 0; e < GD / 4; ++e) ov[e] = first ? make_float4(0.f, 0.f, 0.f, 0.f) : orow[e];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float4 v = first ? make_float4(0.f, 0.f, 0.f, 0.f) : orow[col / 4 + e];
-                        v.x += av[4 * e];
-                        v.y += av[4 * e + 1];
-                        v.z += av[4 * e + 2];
-                        v.w += av[4 * e + 3];
-                        orow[col / 4 + e] = v;
-                    }
+                for (int e = 0; e < GD / 4; ++e) {
+                    ov[e].x += av[4 * e];
+                    ov[e].y += av[4 * e + 1];
+                    ov[e].z += av[4 * e + 2];
+                    ov[e].w += av[4 * e + 3];
+                    orow[e] = ov[e];
                 }
-            }
-            if (update && wg == 0) {
-                p.z[bh * p.n_state + pos] = zn2 * kLn2;
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.q + srow * D);
+                if (wg == 0) p.z[bh * p.n_state + pos] = zn2 * kLn2;
+                // the query tile holds this loop's q: copy this group's chunks of it to qhat
                 uint4 *dst = reinterpret_cast<uint4 *>(p.q_hat + srow * D);
 #pragma unroll
-                for (int ch = 0; ch < D / 8; ++ch) dst[ch] = ldg_nc_v4(src + ch);
+                for (int ch = wg; ch < D / 8; ch += kGroups)
+                    dst[ch] = *reinterpret_cast<const uint4 *>(smem + C::OFF_Q + swz_off(r, ch));
             }
         }
     }
@@ -578,7 +592,7 @@ cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
     kp.z = p.z;
     kp.c = p.c;
     kp.sl2 = kLog2e / sqrtf((float)D);
-    dim3 grid(kp.n_row_tiles, p.H, p.B);
+    dim3 grid(kp.n_row_tiles * p.H, 1, p.B);
     {
         KernelTimer kt("tc_attention", s);
         tc_attention_kernel<D><<<grid, kThreads, Cf::SMEM, s>>>(kp, maps[0], maps[1], maps[2], maps[3]);
