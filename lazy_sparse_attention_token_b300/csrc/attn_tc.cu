@@ -21,21 +21,25 @@
 //   pass NEW: QK_new -> P' = exp(. - Z') -> acc += P' V_new, column sums of P'
 // The first dense loop skips pass OLD (m = 1, u = 0).
 //
-// Roles (576 threads): warp 0 issues TMA loads into a K ring (3 stages) and
-// a V ring (2 stages); warp 1 (one thread) issues tcgen05.mma; warps 2..17
-// are four softmax groups of four warps. A warp owns 32 TMEM lanes (= rows)
-// and its group owns 32 of the tile's 128 columns. A tile's logits land in
-// one of three 128-column TMEM buffers; the softmax writes the bf16
-// probabilities back over the first half of the columns it has read, and the
-// PV product takes them straight from TMEM (A operand in tensor memory), so P
-// never touches shared memory. The probabilities are handed over before the
-// column masses are formed: those are summed after the hand-off by integer
-// warp reductions of a fixed-point encoding and added to c with one atomic
-// per column and warp. A buffer is reused once the softmax has read it and,
-// for tiles with a PV product, once that product completed. The query tile
-// holds qhat for pass OLD and is reloaded with q before pass LSE; the four
-// groups merge row statistics once, through shared memory.
-// TMEM columns: S/P buffers [0,384), accumulator [384,384+d).
+// Roles (608 threads): warp 0 issues TMA loads into a K ring (3 stages) and
+// a V ring (2 stages), keys two tiles ahead of values; warp 1 issues the QK
+// products and warp 2 the PV products (one thread each): the tensor pipe
+// buffers only about two MMAs, and a second issuing thread covers the
+// barrier tests the first makes between its batches. The QK issuer runs up
+// to two tiles ahead of the softmax. Warps 3..18 are four softmax groups of
+// four warps, a group owning 32 of a tile's 128 columns and a warp owning one
+// 32-lane quadrant (32 rows) of TMEM.
+// A softmax thread holds 4 rows x 8 columns of its group's block (two
+// 16x256b TMEM loads), so row statistics stay per-thread partials that are
+// merged once per pass, and a column mass is an in-thread sum over four rows
+// plus a three-step butterfly over lanes. The bf16 probabilities go back to
+// TMEM (two 16x128b stores) in the packed key order the PV product reads as
+// its A operand, so P never touches shared memory; pass OLD's subtraction is
+// the instruction descriptor's negate-A bit. Column masses are formed after
+// P has been handed over and added to c with one atomic per column and warp.
+// The query tile holds qhat for pass OLD and is reloaded with q before pass
+// LSE. TMEM columns: S buffers [0,256), P buffers [256,384), accumulator
+// [384,384+d).
 //
 // Waiting threads sleep in a hinted try_wait instead of spinning. Every
 // mbarrier wait is bounded (about one second); on timeout the CTA records an
@@ -56,33 +60,33 @@ using namespace ptx;
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int BN_ = BN;
-constexpr int kThreads = 576;     // warp 0 TMA, warp 1 MMA, warps 2..17 softmax (4 groups x 4 warps)
-constexpr int kGroups = 4;        // softmax warpgroups, each owns 32 of a tile's 128 columns
+constexpr int kThreads = 608;     // warp 0 TMA, warp 1 QK MMAs, warp 2 PV MMAs, warps 3..18 softmax (4 x 4)
+constexpr int kFirstSoftmaxWarp = 3;
+constexpr int kGroups = 4;        // softmax groups, each owns 32 of a tile's 128 columns
 constexpr int kGroupCols = BN_ / kGroups;
 constexpr int kSoftmaxWarps = 4 * kGroups;   // softmax-side barriers take one elected arrival per warp
 constexpr int kAtom = 128 * 128;  // bytes of a 128-row x 64-element bf16 tile, 128-byte swizzled
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSBufs = 3;         // S/P buffers in TMEM, 128 columns each
+constexpr int kSBufs = 2;         // logits S: two buffers of 128 fp32 columns, [0, 256)
+constexpr uint32_t kColP = 256;   // probabilities P: two buffers of 64 columns (128 bf16), [256, 384)
 constexpr uint32_t kColAcc = 384; // accumulator columns [384, 384 + d)
 constexpr int kKStages = 3, kVStages = 2;
-static_assert(kKStages == kSBufs, "a tile's K slot and S/P buffer share one index");
-static_assert(kVStages == 2, "the MMA issuer indexes the V ring with a parity bit");
+constexpr int kAhead = 2;         // K tiles loaded ahead of the V tile being loaded
+static_assert(kSBufs == 2 && kVStages == 2, "S, P and V buffers are indexed with a parity bit");
+static_assert(kKStages > kAhead, "the K ring holds every tile issued ahead");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// Column sums are taken on integers: x*2^20 rounded into the mantissa of
-// x*2^20 + 1.5*2^23 (exact while |x| < 4), so a warp reduction is exact and
-// the sum of 32 lanes' offsets is removed afterwards.
-constexpr float kFixScale = 1048576.0f, kFixMagic = 12582912.0f;
-constexpr uint32_t kFixBits = 0x4B400000u;
 
 __device__ int g_tc_error;
 
 enum : int { PH_OLD = 0, PH_LSE = 1, PH_NEW = 2 };
-enum : int { BAR_K_FULL = 0, BAR_K_EMPTY = 3, BAR_V_FULL = 6, BAR_V_EMPTY = 8, BAR_S_FULL = 10, BAR_S_READ = 13,
-             BAR_P_FULL = 16, BAR_PV_DONE = 19, BAR_ACC = 22, BAR_STATS = 23, BAR_Q_READY = 24, BAR_DRAIN = 25,
-             N_BARS = 26 };
+// PV_DONE[b] completes when the PV product of the tile in P buffer / V slot b is
+// done: it releases both the P buffer (softmax) and the V slot (producer).
+enum : int { BAR_K_FULL = 0, BAR_K_EMPTY = 3, BAR_V_FULL = 6, BAR_S_FULL = 8, BAR_S_READ = 10, BAR_P_FULL = 12,
+             BAR_PV_DONE = 14, BAR_ACC = 16, BAR_STATS = 17, BAR_Q_READY = 18, BAR_DRAIN = 19 /* QK, PV */,
+             BAR_ZN = 21, N_BARS = 22 };
 enum : int { ERR_K_EMPTY = 1, ERR_K_FULL = 2, ERR_V_EMPTY = 3, ERR_V_FULL = 4, ERR_S_READ = 5, ERR_S_FULL = 6,
-             ERR_P_FULL = 7, ERR_PV_DONE = 8, ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11 };
+             ERR_P_FULL = 7, ERR_PV_DONE = 8, ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11, ERR_ZN = 12 };
 
 template <int D>
 struct Cfg {
@@ -92,7 +96,8 @@ struct Cfg {
     static constexpr int OFF_K = TB;                // K ring
     static constexpr int OFF_V = OFF_K + kKStages * TB;   // V ring
     static constexpr int OFF_X = OFF_V + kVStages * TB;   // row-statistics exchange: [groups][128][3] fp32
-    static constexpr int OFF_BAR = OFF_X + kGroups * 128 * 3 * 4;
+    static constexpr int OFF_ROW = OFF_X + kGroups * 128 * 3 * 4;   // per row: key count, old and new normaliser
+    static constexpr int OFF_BAR = OFF_ROW + 128 * 12;
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM = BYTES + 1024;       // room to align the base to 1024 bytes
@@ -172,10 +177,34 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
     if (lane == 0) mbar_arrive(bar);
 }
 
-// TMEM column of the P values for keys [16 kk, 16 kk + 16) of an S/P buffer:
-// each softmax group writes bf16 pairs over the first 16 of the 32 S columns
-// it read itself (keys 32 g .. 32 g + 31 -> columns 32 g .. 32 g + 15).
-__device__ __forceinline__ uint32_t p_col(int kk) { return 32u * (kk >> 1) + 8u * (kk & 1); }
+// Softmax fragment layout. Each softmax thread holds, per tile, rows
+// rq + lane/4 + 8k (k = 0..3) of its warp's 32-lane quadrant rq and columns
+// cbase + 8j + 2(lane%4) + e (j = 0..3, e = 0..1) of its group's 32 columns:
+// two 16x256b loads. Index of (k, j, e) among the 32 registers:
+__device__ __forceinline__ constexpr int frag(int k, int j, int e) { return 16 * (k >> 1) + 4 * j + 2 * (k & 1) + e; }
+
+// Column sums of a fragment over the warp's 32 rows: in-thread over the four
+// rows, then a transposing butterfly over the eight lanes with the same lane%4.
+// Lane l ends with the sum of column 8(J/2) + 2(l%4) + J%2, J = l/4.
+__device__ __forceinline__ float column_sum(const float *v, int lane) {
+    float cs[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+            cs[2 * j + e] = (v[frag(0, j, e)] + v[frag(1, j, e)]) + (v[frag(2, j, e)] + v[frag(3, j, e)]);
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1) {
+        const bool up = lane & (w << 2);
+#pragma unroll
+        for (int e = 0; e < w; ++e) {
+            const float send = up ? cs[e] : cs[e + w];
+            const float keep = up ? cs[e + w] : cs[e];
+            cs[e] = keep + __shfl_xor_sync(0xffffffffu, send, w << 2);
+        }
+    }
+    return cs[0];
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -190,6 +219,9 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    int *row_cnt = reinterpret_cast<int *>(smem + C::OFF_ROW);
+    float *row_zo = reinterpret_cast<float *>(smem + C::OFF_ROW + 128 * 4);
+    float *row_zn = reinterpret_cast<float *>(smem + C::OFF_ROW + 128 * 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Work grows with a row tile's last position (later rows see more keys), so the
@@ -220,8 +252,8 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     // ---------------- set-up ----------------
     if (threadIdx.x == 0) {
         for (int i = 0; i < N_BARS; ++i) {
-            const bool many = (i >= BAR_S_READ && i < BAR_S_READ + kSBufs) || (i >= BAR_P_FULL && i < BAR_P_FULL + kSBufs) ||
-                              i == BAR_STATS || i == BAR_Q_READY;
+            const bool many = (i >= BAR_S_READ && i < BAR_S_READ + kSBufs) || (i >= BAR_P_FULL && i < BAR_P_FULL + 2) ||
+                              i == BAR_STATS || i == BAR_Q_READY || i == BAR_ZN;
             mbar_init(bar(i), many ? (uint32_t)kSoftmaxWarps : 1u);
         }
         misc[1] = 0;
@@ -232,15 +264,20 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         tmem_alloc(sbase + C::OFF_MISC, kTmemCols);
         tmem_relinquish();
     }
-    const bool is_sm = warp >= 2;
-    const int wg = is_sm ? (warp - 2) >> 2 : 0;   // softmax group: columns [32 wg, 32 wg + 32) of a tile
-    const int r = (warp & 3) * 32 + lane;          // tile row == TMEM lane
+    const bool is_sm = warp >= kFirstSoftmaxWarp;
+    // softmax group: columns [32 wg, 32 wg + 32) of a tile; its four warps cover the four lane quadrants
+    const int wg = is_sm ? (warp - kFirstSoftmaxWarp) >> 2 : 0;
+    const int r = (warp & 3) * 32 + lane;          // the row this thread loads and writes back
     const bool row_ok = is_sm && r < rows;
     const int pos = row_ok ? (dense ? row0 + r : __ldg(A + r)) : -1;
     const long long qoff = (((long long)b * p.n_state + max(pos, 0)) * p.H + h) * D;
     if (is_sm) {   // pass OLD reads qhat; the first dense loop starts with q
         load_query_row<D>(smem + C::OFF_Q, first ? p.q + qoff : p.q_hat + qoff, row_ok, r, wg);
         fence_proxy_async_smem();
+        if (wg == 0) {   // per row, shared by the four groups: key count and old normaliser (log2 units)
+            row_cnt[r] = !row_ok ? 0 : cnt_min == cnt ? cnt : dense ? min(pos + 1, p.n_keys) : count_le(S, p.K, pos);
+            row_zo[r] = !row_ok ? INFINITY : first ? 0.f : __ldg(p.z + bh * p.n_state + pos) * kLog2e;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -252,135 +289,148 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         if (lane == 0) {
             prefetch_tmap(&tm_k_old); prefetch_tmap(&tm_v_old);
             prefetch_tmap(&tm_k_new); prefetch_tmap(&tm_v_new);
-            int k_issued = 0, v_issued = 0;
+            int kg = 0, kph = ph0, kt = 0;   // next K tile: index, pass, tile within the pass
+            int vi = 0;                       // V tiles issued
+            bool ok = true;
             int ph = ph0, t = 0;
-            for (int g = 0; g < total; ++g, ++t) {
+            for (int g = 0; ok && g < total; ++g, ++t) {
                 if (t == n_tiles) { t = 0; ++ph; }
-                const int key0 = t * BN;
-                {
-                    const int s = g % kKStages, use = g / kKStages;
-                    if (!wait_bar(bar(BAR_K_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_K_EMPTY)) break;
-                    const CUtensorMap *mk = ph == PH_OLD ? &tm_k_old : &tm_k_new;
+                // keys run kAhead tiles ahead of values, the order the issuers consume them
+                for (; kg < total && kg <= g + kAhead; ++kg, ++kt) {
+                    if (kt == n_tiles) { kt = 0; ++kph; }
+                    const int s = kg % kKStages, use = kg / kKStages;
+                    if (!wait_bar(bar(BAR_K_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_K_EMPTY)) { ok = false; break; }
+                    const CUtensorMap *mk = kph == PH_OLD ? &tm_k_old : &tm_k_new;
                     const uint32_t dst = sbase + C::OFF_K + C::TB * s;
                     mbar_arrive_expect_tx(bar(BAR_K_FULL + s), C::TB);
                     for (int a = 0; a < C::NA; ++a) {
-                        if (dense) tma_load_4d(dst + a * kAtom, mk, bar(BAR_K_FULL + s), a * 64, h, key0, b);
-                        else tma_load_4d(dst + a * kAtom, mk, bar(BAR_K_FULL + s), a * 64, key0, h, b);
+                        if (dense) tma_load_4d(dst + a * kAtom, mk, bar(BAR_K_FULL + s), a * 64, h, kt * BN, b);
+                        else tma_load_4d(dst + a * kAtom, mk, bar(BAR_K_FULL + s), a * 64, kt * BN, h, b);
                     }
-                    k_issued = g + 1;
                 }
+                if (!ok) break;
                 if (ph != PH_LSE) {
-                    const int vi = v_issued, s = vi % kVStages, use = vi / kVStages;
-                    if (!wait_bar(bar(BAR_V_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_V_EMPTY)) break;
+                    const int s = vi & 1, use = vi >> 1;
+                    if (!wait_bar(bar(BAR_PV_DONE + s), (use & 1) ^ 1, abort_flag, ERR_V_EMPTY)) break;
                     const CUtensorMap *mv = ph == PH_OLD ? &tm_v_old : &tm_v_new;
                     const uint32_t dst = sbase + C::OFF_V + C::TB * s;
                     mbar_arrive_expect_tx(bar(BAR_V_FULL + s), C::TB);
                     for (int a = 0; a < C::NA; ++a) {
-                        if (dense) tma_load_4d(dst + a * kAtom, mv, bar(BAR_V_FULL + s), a * 64, h, key0, b);
-                        else tma_load_4d(dst + a * kAtom, mv, bar(BAR_V_FULL + s), a * 64, key0, h, b);
+                        if (dense) tma_load_4d(dst + a * kAtom, mv, bar(BAR_V_FULL + s), a * 64, h, t * BN, b);
+                        else tma_load_4d(dst + a * kAtom, mv, bar(BAR_V_FULL + s), a * 64, t * BN, h, b);
                     }
-                    v_issued = vi + 1;
+                    ++vi;
                 }
             }
             if (*abort_flag) {   // let copies already in flight land before the CTA exits
                 volatile int never = 0;
-                for (int g = max(0, k_issued - kKStages); g < k_issued; ++g)
+                for (int g = max(0, kg - kKStages); g < kg; ++g)
                     wait_bar(bar(BAR_K_FULL + g % kKStages), (g / kKStages) & 1, &never, ERR_K_FULL);
-                for (int v = max(0, v_issued - kVStages); v < v_issued; ++v)
-                    wait_bar(bar(BAR_V_FULL + v % kVStages), (v / kVStages) & 1, &never, ERR_V_FULL);
+                for (int v = max(0, vi - kVStages); v < vi; ++v)
+                    wait_bar(bar(BAR_V_FULL + (v & 1)), (v >> 1) & 1, &never, ERR_V_FULL);
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+        // ---------------- QK issuer: S = Q K^T into the S buffer of tile g ----------------
+        // Two issuing threads keep the tensor pipe fed: it buffers only about two MMAs,
+        // and each issuer's barrier tests between batches are covered by the other's MMAs.
         if (lane == 0) {
             constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false, false);
-            constexpr uint32_t id_pv = idesc_bf16(128, D, false, true, false);   // A = P from TMEM
             // descriptors are built once; per k-step only the start address moves
             const uint64_t d_q = smem_desc(sbase + C::OFF_Q, 16, 1024, 2);
             const uint64_t d_k = smem_desc(sbase + C::OFF_K, 16, 1024, 2);
-            const uint64_t d_v = smem_desc(sbase + C::OFF_V, kAtom, 1024, 2);
             constexpr uint64_t TB16 = C::TB >> 4, ATOM16 = kAtom >> 4;
-            // Bookkeeping stays in registers: the tensor core buffers only about two
-            // MMAs, so any scalar latency between MMA groups is idle tensor time.
-            // Per S/P buffer (= K slot) b, bit b of: used (ever written), upar (parity
-            // of its uses so far), hadv (its last tile had a PV product), pfpar (parity
-            // of P-ready waits), pdpar (parity of PV-done commits).
-            uint32_t used = 0, upar = 0, hadv = 0, pfpar = 0, pdpar = 0;
-            int qb = 0;                      // S/P buffer and K slot of the next QK
-            int ph_next = ph0, t_next = 0;   // phase and tile of the next QK
-            auto issue_qk = [&](int g) -> bool {
-                const int ph = ph_next;
-                if (++t_next == n_tiles) { t_next = 0; ++ph_next; }
-                const uint32_t bit = 1u << qb, par = (upar >> qb) & 1u;
-                if (!wait_bar(bar(BAR_K_FULL + qb), par, abort_flag, ERR_K_FULL)) return false;
-                if (used & bit) {   // the buffer's last S was read, and its last P consumed by PV
-                    if (!wait_bar(bar(BAR_S_READ + qb), par ^ 1u, abort_flag, ERR_S_READ)) return false;
-                    if ((hadv & bit) && !wait_bar(bar(BAR_PV_DONE + qb), ((pdpar >> qb) & 1u) ^ 1u, abort_flag, ERR_PV_DONE))
-                        return false;
+            int ks = 0;          // K slot of tile g
+            uint32_t kpar = 0;   // that slot's fill parity
+            bool ok = true;
+            int ph = ph0, t = 0;
+            for (int g = 0; g < total; ++g, ++t) {
+                if (t == n_tiles) { t = 0; ++ph; }
+                if (!wait_bar(bar(BAR_K_FULL + ks), kpar, abort_flag, ERR_K_FULL)) { ok = false; break; }
+                const int sb = g & 1;
+                // the S buffer's previous tile has been read by the softmax
+                if (g >= kSBufs && !wait_bar(bar(BAR_S_READ + sb), ((g >> 1) - 1) & 1, abort_flag, ERR_S_READ)) {
+                    ok = false;
+                    break;
                 }
-                if (ph == PH_LSE && g == n_tiles && !first) {   // queries reloaded after pass OLD
-                    if (!wait_bar(bar(BAR_Q_READY), 0, abort_flag, ERR_Q_READY)) return false;
+                // pass LSE starts once the query tile holds this loop's q
+                if (ph == PH_LSE && t == 0 && !first && !wait_bar(bar(BAR_Q_READY), 0, abort_flag, ERR_Q_READY)) {
+                    ok = false;
+                    break;
                 }
                 tc_fence_after();
-                const uint64_t dk = d_k + TB16 * (uint32_t)qb;
-                const uint32_t dst = tmem + 128u * (uint32_t)qb;
+                const uint64_t dk = d_k + TB16 * (uint32_t)ks;
+                const uint32_t dst = tmem + 128u * (uint32_t)sb;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (kk >> 2) * ATOM16 + (kk & 3) * 2;
                     mma_bf16_ss(dst, d_q + off, dk + off, id_qk, kk > 0);
                 }
-                mma_commit(bar(BAR_S_FULL + qb));
-                mma_commit(bar(BAR_K_EMPTY + qb));
-                used |= bit;
-                upar ^= bit;
-                hadv = ph != PH_LSE ? (hadv | bit) : (hadv & ~bit);
-                qb = qb == kSBufs - 1 ? 0 : qb + 1;
-                return true;
-            };
-            bool ok = issue_qk(0);
-            int pv = 0, ph = ph0, t = 0, pb = 0;   // pb: S/P buffer of tile g
-            for (int g = 0; ok && g < total; ++g, ++t, pb = pb == kSBufs - 1 ? 0 : pb + 1) {
-                if (t == n_tiles) { t = 0; ++ph; }
-                if (g + 1 < total && !issue_qk(g + 1)) { ok = false; break; }
-                if (ph == PH_LSE) continue;
-                const int vs = pv & 1;
-                const uint32_t bit = 1u << pb;
-                if (!wait_bar(bar(BAR_V_FULL + vs), (pv >> 1) & 1, abort_flag, ERR_V_FULL)) { ok = false; break; }
-                if (!wait_bar(bar(BAR_P_FULL + pb), (pfpar >> pb) & 1u, abort_flag, ERR_P_FULL)) { ok = false; break; }
-                pfpar ^= bit;
-                tc_fence_after();
-                const uint64_t dv = d_v + TB16 * (uint32_t)vs;
-                const uint32_t pa = tmem + 128u * (uint32_t)pb;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)   // acc += P[:, 16kk..] * V[16kk.., :]  (P is signed)
-                    mma_bf16_ts(tmem + kColAcc, pa + p_col(kk), dv + kk * 128, id_pv, (pv > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(BAR_PV_DONE + pb));
-                pdpar ^= bit;
-                mma_commit(bar(BAR_V_EMPTY + vs));
-                ++pv;
+                mma_commit(bar(BAR_S_FULL + sb));
+                mma_commit(bar(BAR_K_EMPTY + ks));
+                if (++ks == kKStages) { ks = 0; kpar ^= 1u; }
             }
-            if (ok) {
-                mma_commit(bar(BAR_ACC));
-            } else {   // drain whatever was issued before giving up
+            if (!ok) {   // drain whatever was issued before giving up
                 mma_commit(bar(BAR_DRAIN));
                 volatile int never = 0;
                 wait_bar(bar(BAR_DRAIN), 0, &never, ERR_ACC);
             }
         }
+    } else if (warp == 2) {
+        // ---------------- PV issuer: acc -= P V (pass OLD), acc += P' V (pass NEW) ----------------
+        if (lane == 0) {
+            constexpr uint32_t id_pv = idesc_bf16(128, D, false, true, false);       // A = P from TMEM
+            constexpr uint32_t id_pv_neg = idesc_bf16(128, D, false, true, true);    // pass OLD subtracts
+            const uint64_t d_v = smem_desc(sbase + C::OFF_V, kAtom, 1024, 2);
+            constexpr uint64_t TB16 = C::TB >> 4;
+            const int n_pv = (ph0 == PH_OLD ? 2 : 1) * n_tiles;
+            bool ok = true;
+            for (int pv = 0; pv < n_pv; ++pv) {
+                const int vs = pv & 1;   // V slot and P buffer of this tile
+                const uint32_t vpar = (uint32_t)(pv >> 1) & 1u;
+                if (!wait_bar(bar(BAR_V_FULL + vs), vpar, abort_flag, ERR_V_FULL)) { ok = false; break; }
+                if (!wait_bar(bar(BAR_P_FULL + vs), vpar, abort_flag, ERR_P_FULL)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t dv = d_v + TB16 * (uint32_t)vs;
+                const uint32_t pa = tmem + kColP + 64u * (uint32_t)vs;
+                const uint32_t idp = ph0 == PH_OLD && pv < n_tiles ? id_pv_neg : id_pv;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)   // acc +-= P[:, 16kk..] * V[16kk.., :]
+                    mma_bf16_ts(tmem + kColAcc, pa + 8u * kk, dv + kk * 128, idp, (pv > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(BAR_PV_DONE + vs));
+            }
+            if (ok) {
+                mma_commit(bar(BAR_ACC));
+            } else {
+                mma_commit(bar(BAR_DRAIN + 1));
+                volatile int never = 0;
+                wait_bar(bar(BAR_DRAIN + 1), 0, &never, ERR_ACC);
+            }
+        }
     } else {
         // ---------------- softmax / epilogue: four groups, 32 columns each ----------------
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int rq = (warp & 3) * 32;            // the warp's TMEM lane quadrant
+        const int q4 = lane & 3;
+        const int rlo = rq + (lane >> 2);          // fragment rows rlo + 8k
         const int cbase = wg * kGroupCols;
-        const float zo2 = (!first && row_ok) ? __ldg(p.z + bh * p.n_state + pos) * kLog2e : 0.f;
-        // every row of the tile sees the same keys when the first and last rows do
-        const int cnt_i = !row_ok ? 0 : cnt_min == cnt ? cnt : dense ? min(pos + 1, p.n_keys) : count_le(S, p.K, pos);
-        float m = 0.f, M = -INFINITY, L = 0.f, zn2 = INFINITY;
+        const uint32_t t_lo = tmem + ((uint32_t)rq << 16), t_hi = tmem + ((uint32_t)(rq + 16) << 16);
+        // per fragment row: partial old mass, running maximum of raw logits, sum of
+        // 2^((logit - Mk) sl2); key counts and normalisers are read from shared memory
+        float mk[4], Mk[4], Lk[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            mk[k] = 0.f;
+            Mk[k] = -INFINITY;
+            Lk[k] = 0.f;
+        }
         bool ok = true;
         float *cb = p.c + bh * p.n_keys;
-        int ph = ph0, t = 0;
+        // this lane's column after the butterfly of column_sum()
+        const int Jc = lane >> 2;
+        const int mycol = cbase + 8 * (Jc >> 1) + 2 * q4 + (Jc & 1);
+        int ph = ph0, t = 0, pv = 0;
         for (int g = 0; g < total && ok; ++g, ++t) {
             if (t == n_tiles) { t = 0; ++ph; }
-            const int sb = g % kSBufs, suse = g / kSBufs;
             if (ph == PH_LSE && t == 0 && !first) {
                 // pass OLD's products are all done (their S tiles were consumed):
                 // reload the query tile with this loop's q
@@ -389,122 +439,175 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 warp_arrive(bar(BAR_Q_READY), lane);
             }
             if (ph == PH_NEW && t == 0) {
-                // merge the groups' row statistics
+                // merge row statistics: the four lanes of a row, then the four groups
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                    for (int off = 1; off <= 2; off <<= 1) {
+                        const float mo = __shfl_xor_sync(0xffffffffu, mk[k], off);
+                        const float Mo = __shfl_xor_sync(0xffffffffu, Mk[k], off);
+                        const float Lo = __shfl_xor_sync(0xffffffffu, Lk[k], off);
+                        const float Mx = fmaxf(Mk[k], Mo);
+                        Lk[k] = Mx == -INFINITY ? 0.f : Lk[k] * ex2((Mk[k] - Mx) * p.sl2) + Lo * ex2((Mo - Mx) * p.sl2);
+                        Mk[k] = Mx;
+                        mk[k] += mo;
+                    }
+                }
                 float *ex = reinterpret_cast<float *>(smem + C::OFF_X);
-                ex[(wg * 128 + r) * 3 + 0] = m;
-                ex[(wg * 128 + r) * 3 + 1] = M;
-                ex[(wg * 128 + r) * 3 + 2] = L;
+                if (q4 == 0) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float *e = ex + (wg * 128 + rlo + 8 * k) * 3;
+                        e[0] = mk[k];
+                        e[1] = Mk[k];
+                        e[2] = Lk[k];
+                    }
+                }
                 warp_arrive(bar(BAR_STATS), lane);
                 if (!wait_bar(bar(BAR_STATS), 0, abort_flag, ERR_STATS)) { ok = false; break; }
-                float mx = 0.f, Mx = -INFINITY, Lx = 0.f;
+                // Z' = lam - ln m in log2 units; rows with an empty key set or no old mass keep their state
+                auto merged = [&](int row) -> float {
+                    if (row >= rows) return INFINITY;
+                    float mx = 0.f, Mx = -INFINITY, Lx = 0.f;
 #pragma unroll
-                for (int k = 0; k < kGroups; ++k) {
-                    mx += ex[(k * 128 + r) * 3 + 0];
-                    Mx = fmaxf(Mx, ex[(k * 128 + r) * 3 + 1]);
-                }
-                if (Mx > -INFINITY) {
+                    for (int k = 0; k < kGroups; ++k) {
+                        mx += ex[(k * 128 + row) * 3 + 0];
+                        Mx = fmaxf(Mx, ex[(k * 128 + row) * 3 + 1]);
+                    }
+                    if (Mx == -INFINITY) return INFINITY;
 #pragma unroll
                     for (int k = 0; k < kGroups; ++k)
-                        Lx += ex[(k * 128 + r) * 3 + 2] * ex2(ex[(k * 128 + r) * 3 + 1] - Mx);
-                }
-                if (first) mx = 1.f;
-                zn2 = (Mx > -INFINITY && mx >= FLT_MIN) ? Mx + __log2f(Lx) - __log2f(mx) : INFINITY;
+                        Lx += ex[(k * 128 + row) * 3 + 2] * ex2((ex[(k * 128 + row) * 3 + 1] - Mx) * p.sl2);
+                    if (first) mx = 1.f;
+                    return mx >= FLT_MIN ? Mx * p.sl2 + __log2f(Lx) - __log2f(mx) : INFINITY;
+                };
+                if (wg == 0) row_zn[r] = merged(r);
+                warp_arrive(bar(BAR_ZN), lane);
+                if (!wait_bar(bar(BAR_ZN), 0, abort_flag, ERR_ZN)) { ok = false; break; }
             }
             const int c0 = t * BN;
             const bool with_v = ph != PH_LSE;
-            // key position of this lane's column (for the column-mass atomics)
-            const int jcol = with_v ? col_index(c0 + cbase + lane) : INT_MAX;
+            // key position of this lane's column mass, loaded before the waits below
+            const int jcol = with_v ? col_index(c0 + mycol) : INT_MAX;
             // every row of the tile sees all 128 columns (uniform), else mask by the prefix count
             const bool full = c0 + BN <= cnt_min;
-            const int nv = min(kGroupCols, max(0, cnt_i - c0 - cbase));
-            if (!wait_bar(bar(BAR_S_FULL + sb), suse & 1, abort_flag, ERR_S_FULL)) { ok = false; break; }
+            const int sb = g & 1;
+            if (!wait_bar(bar(BAR_S_FULL + sb), (g >> 1) & 1, abort_flag, ERR_S_FULL)) { ok = false; break; }
             tc_fence_after();
-            float sv[kGroupCols];
-            tmem_ld_32x32b_x32(tmem + lane_base + 128u * sb + cbase, sv);
+            float v[32];
+            tmem_ld_16x256b_x4(t_lo + 128u * sb + cbase, v);
+            tmem_ld_16x256b_x4(t_hi + 128u * sb + cbase, v + 16);
             tmem_wait_ld();
             warp_arrive(bar(BAR_S_READ + sb), lane);
+            if (!full) {   // keys past a row's prefix count are outside its set
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int nv = row_cnt[rlo + 8 * k] - c0 - cbase - 2 * q4;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            if (8 * j + e >= nv) v[frag(k, j, e)] = -INFINITY;
+                }
+            }
             if (!with_v) {
-                // online logsumexp of this tile's new logits (log2 units)
-                if (full) {
+                // online logsumexp of this tile's new logits, per fragment row
 #pragma unroll
-                    for (int e = 0; e < kGroupCols; ++e) sv[e] *= p.sl2;
-                } else {
+                for (int k = 0; k < 4; ++k) {
+                    float c4[4];
 #pragma unroll
-                    for (int e = 0; e < kGroupCols; ++e) sv[e] = e < nv ? sv[e] * p.sl2 : -INFINITY;
+                    for (int j = 0; j < 4; ++j) c4[j] = fmaxf(v[frag(k, j, 0)], v[frag(k, j, 1)]);
+                    const float cm = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
+                    if (cm > Mk[k]) {
+                        Lk[k] *= ex2((Mk[k] - cm) * p.sl2);
+                        Mk[k] = cm;
+                    }
+                    if (Mk[k] > -INFINITY) {
+                        const float nb = -Mk[k] * p.sl2;
+                        float a2[2] = {0.f, 0.f};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) a2[e] += ex2(fmaf(v[frag(k, j, e)], p.sl2, nb));
+                        Lk[k] += a2[0] + a2[1];
+                    }
                 }
-                float c4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int e = 0; e < kGroupCols; ++e) c4[e & 3] = fmaxf(c4[e & 3], sv[e]);
-                const float cmax = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
-                if (cmax > M) {
-                    L *= ex2(M - cmax);
-                    M = cmax;
-                }
-                float a4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int e = 0; e < kGroupCols; ++e) a4[e & 3] += ex2(sv[e] - M);
-                if (M > -INFINITY) L += (a4[0] + a4[1]) + (a4[2] + a4[3]);
                 continue;
             }
-            // probabilities with a known normaliser, signed by pass (OLD subtracts):
-            // sign * exp(logit - Z); rows outside the tile or the sequence get zero
-            // through an infinite normaliser
-            const float sub = !row_ok ? INFINITY : ph == PH_OLD ? zo2 : zn2;
-            const float sgn = ph == PH_OLD ? -1.f : 1.f;
-            if (full) {
+            // probabilities with a known normaliser: exp(logit - Z); rows outside the
+            // tile or the sequence get zero through an infinite normaliser
+            const bool old = ph == PH_OLD;
 #pragma unroll
-                for (int e = 0; e < kGroupCols; ++e) sv[e] = sgn * ex2(fmaf(sv[e], p.sl2, -sub));
-            } else {
+            for (int k = 0; k < 4; ++k) {
+                const float nz = -(old ? row_zo[rlo + 8 * k] : row_zn[rlo + 8 * k]);
 #pragma unroll
-                for (int e = 0; e < kGroupCols; ++e) sv[e] = e < nv ? sgn * ex2(fmaf(sv[e], p.sl2, -sub)) : 0.f;
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) v[frag(k, j, e)] = ex2(fmaf(v[frag(k, j, e)], p.sl2, nz));
             }
-            uint32_t pk[kGroupCols / 2];
+            // P buffer pv & 1 was last read by the PV product of the V tile two before
+            const int pb = pv & 1;
+            if (pv >= 2 && !wait_bar(bar(BAR_PV_DONE + pb), (uint32_t)((pv >> 1) - 1) & 1u, abort_flag, ERR_PV_DONE)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // bf16 pairs of adjacent keys: register pair (2i, 2i + 1) is one packed P column
+            const uint32_t pcol = kColP + 64u * (uint32_t)pb + (uint32_t)(cbase >> 1);
 #pragma unroll
-            for (int e = 0; e < kGroupCols; e += 2) pk[e / 2] = pack_bf16x2_rn(sv[e], sv[e + 1]);
-            // this tile's P, bf16, over the first half of the S columns this group just read;
-            // handing it over is the PV product's critical path, the sums below are not
-            tmem_st_32x32b_x16(tmem + lane_base + 128u * sb + cbase, pk);
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2_rn(v[16 * half + 2 * i], v[16 * half + 2 * i + 1]);
+                tmem_st_16x128b_x4((half ? t_hi : t_lo) + pcol, pk);
+            }
             tmem_wait_st();
-            warp_arrive(bar(BAR_P_FULL + sb), lane);
-            if (ph == PH_OLD) {
-                float m4[4] = {0.f, 0.f, 0.f, 0.f};
+            warp_arrive(bar(BAR_P_FULL + pb), lane);
+            ++pv;
+            // after the hand-off: the old mass m and the column masses
+            if (old) {
 #pragma unroll
-                for (int e = 0; e < kGroupCols; ++e) m4[e & 3] += sv[e];
-                m -= (m4[0] + m4[1]) + (m4[2] + m4[3]);
-            }
-            // column masses over the warp's 32 rows, exact on fixed-point integers
-            uint32_t csum = 0u;
+                for (int k = 0; k < 4; ++k) {
+                    float a2[2] = {0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < kGroupCols; ++e) {
-                const uint32_t tot = __reduce_add_sync(0xffffffffu, __float_as_uint(fmaf(sv[e], kFixScale, kFixMagic)));
-                if (e == lane) csum = tot;
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) a2[e] += v[frag(k, j, e)];
+                    mk[k] += a2[0] + a2[1];
+                }
             }
-            const int fixed = (int)(csum - 32u * kFixBits);
-            if (jcol != INT_MAX && fixed != 0) atomicAdd(cb + jcol, (float)fixed * (1.0f / kFixScale));
+            const float cs = column_sum(v, lane);
+            if (jcol != INT_MAX && cs != 0.f) atomicAdd(cb + jcol, old ? -cs : cs);
         }
         if (ok && wait_bar(bar(BAR_ACC), 0, abort_flag, ERR_ACC)) {
             tc_fence_after();
             constexpr int GD = D / kGroups;   // accumulator columns per group (16, 24 or 32)
-            float av[GD];
+            constexpr int GC = GD % 16 == 0 ? 16 : 8;   // columns per chunk, to bound live registers
+            const uint32_t lane_base = (uint32_t)rq << 16;
+            const float zn_r = row_zn[r];
+            const bool update = row_ok && zn_r < INFINITY;
+            const long long srow = ((long long)b * p.n_state + max(pos, 0)) * p.H + h;
 #pragma unroll
-            for (int u = 0; u < GD / 8; ++u) tmem_ld_32x32b_x8(tmem + lane_base + kColAcc + wg * GD + 8 * u, av + 8 * u);
-            tmem_wait_ld();
-            const bool update = row_ok && zn2 < INFINITY;
-            if (update) {
-                const long long srow = ((long long)b * p.n_state + pos) * p.H + h;
-                float4 *orow = reinterpret_cast<float4 *>(p.o + srow * D) + wg * (GD / 4);
-                float4 ov[GD / 4];
+            for (int u0 = 0; u0 < GD; u0 += GC) {
+                float av[GC];
 #pragma unroll
-                for (int e = 0; e < GD / 4; ++e) ov[e] = first ? make_float4(0.f, 0.f, 0.f, 0.f) : orow[e];
+                for (int u = 0; u < GC; u += 8) tmem_ld_32x32b_x8(tmem + lane_base + kColAcc + wg * GD + u0 + u, av + u);
+                tmem_wait_ld();
+                if (update) {
+                    float4 *orow = reinterpret_cast<float4 *>(p.o + srow * D + wg * GD + u0);
 #pragma unroll
-                for (int e = 0; e < GD / 4; ++e) {
-                    ov[e].x += av[4 * e];
-                    ov[e].y += av[4 * e + 1];
-                    ov[e].z += av[4 * e + 2];
-                    ov[e].w += av[4 * e + 3];
-                    orow[e] = ov[e];
+                    for (int e = 0; e < GC / 4; ++e) {
+                        float4 ov = first ? make_float4(0.f, 0.f, 0.f, 0.f) : orow[e];
+                        ov.x += av[4 * e];
+                        ov.y += av[4 * e + 1];
+                        ov.z += av[4 * e + 2];
+                        ov.w += av[4 * e + 3];
+                        orow[e] = ov;
+                    }
                 }
-                if (wg == 0) p.z[bh * p.n_state + pos] = zn2 * kLn2;
+            }
+            if (update) {
+                if (wg == 0) p.z[bh * p.n_state + pos] = zn_r * kLn2;
                 // the query tile holds this loop's q: copy this group's chunks of it to qhat
                 uint4 *dst = reinterpret_cast<uint4 *>(p.q_hat + srow * D);
 #pragma unroll

@@ -193,6 +193,29 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
         "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
+// TMEM -> registers, 16 lanes x 32 columns in the 16x256b shape repeated four
+// times along the columns: for repeat j, thread t receives
+//   v[4j + 0], v[4j + 1] = lane base + t/4,     columns 8j + 2(t%4) + {0, 1}
+//   v[4j + 2], v[4j + 3] = lane base + t/4 + 8, the same two columns.
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// registers -> TMEM, 16 lanes x 16 columns in the 16x128b shape repeated four
+// times: for repeat j, thread t writes r[2j] to lane base + t/4 and r[2j + 1]
+// to lane base + t/4 + 8, both at column 4j + t%4.
+__device__ __forceinline__ void tmem_st_16x128b_x4(uint32_t taddr, const uint32_t *r) {
+    asm volatile("tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
 // registers -> TMEM: 32 lanes x 4 consecutive fp32 columns (thread t -> lane quadrant*32 + t).
 __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, float a, float b, float c, float d) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
