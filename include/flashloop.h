@@ -117,7 +117,10 @@ typedef enum {
  * m = 1, u = 0, p = 0 and overwrites c with the column sums. DENSE and
  * FIRST_DENSE take every key and every row (row_pos is ignored, R = n_state
  * = n_keys). The dense layer of loop `loop` must already hold K/V.
- * Precision: bf16 operands, fp32 accumulation and softmax. */
+ * Precision: bf16 operands, fp32 accumulation and softmax.
+ * LAZY with more than 8 rows uses `workspace` (flashloop_workspace_bytes of
+ * the cache's dims) for the gathered keys and the per-row key counts, and
+ * needs K <= dims.K and R <= dims.R_cap; otherwise FLASHLOOP_ERR_WORKSPACE. */
 typedef struct {
     int32_t mode;             /* flashloop_attn_mode_t */
     int32_t loop;             /* l, 1-based */

@@ -125,7 +125,7 @@ static flashloop_status_t check_dims(const flashloop_dims_t *dm) {
 }
 
 struct WsLayout {
-    size_t scores, kv, rows, slots, total;
+    size_t scores, kv, rows, slots, counts, total;
 };
 
 static WsLayout ws_layout(const flashloop_dims_t *dm) {
@@ -139,6 +139,8 @@ static WsLayout ws_layout(const flashloop_dims_t *dm) {
     off += align_up((size_t)dm->B * sizeof(int32_t));
     w.slots = off;
     off += align_up((size_t)dm->B * sizeof(int32_t));
+    w.counts = off;   // lazy attention: keys each row sees, [B,H,R_cap]
+    off += align_up((size_t)dm->B * dm->H * dm->R_cap * sizeof(int32_t));
     w.total = off;
     return w;
 }
@@ -481,6 +483,8 @@ flashloop_status_t flashloop_lazy_attention(const flashloop_attn_args_t *a, flas
     if (lazy) {
         const WsLayout W = ws_layout(&dm);
         if (a->K > dm.K) return set_error(FLASHLOOP_ERR_WORKSPACE, "K=%d exceeds dims.K=%d the workspace is sized for", a->K, dm.K);
+        if (a->R > dm.R_cap)
+            return set_error(FLASHLOOP_ERR_WORKSPACE, "R=%d exceeds dims.R_cap=%d the workspace is sized for", a->R, dm.R_cap);
         if (!a->workspace || a->workspace_bytes < W.total || reinterpret_cast<uintptr_t>(a->workspace) % kAlign)
             return set_error(FLASHLOOP_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", W.total);
         uint8_t *ws = static_cast<uint8_t *>(a->workspace) + W.kv;
@@ -494,6 +498,7 @@ flashloop_status_t flashloop_lazy_attention(const flashloop_attn_args_t *a, flas
         p.key_idx = a->key_idx;
         p.k_old = kv[0]; p.v_old = kv[1]; p.k_new = kv[2]; p.v_new = kv[3];
         p.kv_rows = a->K;
+        p.row_cnt = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(a->workspace) + W.counts);
     } else {
         p.K = a->n_keys;
         p.k_new = c->k_dense[a->loop - 1];

@@ -84,9 +84,9 @@ enum : int { PH_OLD = 0, PH_LSE = 1, PH_NEW = 2 };
 // done: it releases both the P buffer (softmax) and the V slot (producer).
 enum : int { BAR_K_FULL = 0, BAR_K_EMPTY = 3, BAR_V_FULL = 6, BAR_S_FULL = 8, BAR_S_READ = 10, BAR_P_FULL = 12,
              BAR_PV_DONE = 14, BAR_ACC = 16, BAR_STATS = 17, BAR_Q_READY = 18, BAR_DRAIN = 19 /* QK, PV */,
-             BAR_ZN = 21, N_BARS = 22 };
+             BAR_ZN = 21, BAR_EPI = 22, N_BARS = 23 };
 enum : int { ERR_K_EMPTY = 1, ERR_K_FULL = 2, ERR_V_EMPTY = 3, ERR_V_FULL = 4, ERR_S_READ = 5, ERR_S_FULL = 6,
-             ERR_P_FULL = 7, ERR_PV_DONE = 8, ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11, ERR_ZN = 12 };
+             ERR_P_FULL = 7, ERR_PV_DONE = 8, ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11, ERR_ZN = 12, ERR_EPI = 13 };
 
 template <int D>
 struct Cfg {
@@ -97,7 +97,10 @@ struct Cfg {
     static constexpr int OFF_V = OFF_K + kKStages * TB;   // V ring
     static constexpr int OFF_X = OFF_V + kVStages * TB;   // row-statistics exchange: [groups][128][3] fp32
     static constexpr int OFF_ROW = OFF_X + kGroups * 128 * 3 * 4;   // per row: key count, old and new normaliser
-    static constexpr int OFF_BAR = OFF_ROW + 128 * 12;
+    static constexpr int OFF_BAR = OFF_ROW + 128 * 16;
+    // epilogue: the finished accumulator rows, parked in the (then idle) K ring
+    static constexpr int XS = D + 4;   // padded row stride in floats
+    static_assert(128 * XS * 4 <= kKStages * TB, "accumulator rows fit the K ring");
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM = BYTES + 1024;       // room to align the base to 1024 bytes
@@ -107,6 +110,7 @@ struct Cfg {
 struct KParams {
     int mode, H, n_keys, n_state, R, K, n_row_tiles;
     const int32_t *row_pos;
+    const int32_t *row_cnt;   // lazy: keys each row sees, [B,H,R]
     const int32_t *key_idx;
     const uint16_t *q;
     uint16_t *q_hat;
@@ -142,31 +146,30 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     return wait_bar_slow(bar, parity, abort_flag, code);
 }
 
-// Number of entries of the ascending list S[0, n) that are <= x.
-__device__ __forceinline__ int count_le(const int32_t *S, int n, int x) {
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(S + mid) <= x) lo = mid + 1; else hi = mid;
-    }
-    return lo;
-}
-
 // Byte offset of 16-byte chunk `ch` (8 bf16) of row r in a 128-row tile laid
 // out as 64-element atoms with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t swz_off(int r, int ch) {
     return (uint32_t)((ch >> 3) * kAtom + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
-// Gathers row r's query (qhat or q) into the swizzled query tile; each
-// softmax group writes every kGroups-th 16-byte chunk.
+// Gathers the tile's query rows (qhat or q, [B, n_state, H, D] bf16) into the
+// swizzled query tile. The softmax threads (index st) take consecutive 16-byte
+// chunks, so a warp reads whole rows; rows past the tile's end are zero.
 template <int D>
-__device__ __forceinline__ void load_query_row(uint8_t *tile, const uint16_t *src_row, bool row_ok, int r, int wg) {
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    const uint4 *src = reinterpret_cast<const uint4 *>(src_row);
-#pragma unroll
-    for (int ch = wg; ch < D / 8; ch += kGroups)
-        *reinterpret_cast<uint4 *>(tile + swz_off(r, ch)) = row_ok ? src[ch] : zero;
+__device__ __forceinline__ void load_query_tile(uint8_t *tile, const uint16_t *src, int st, int b, int h, int H,
+                                                int n_state, int rows, int row0, const int32_t *A) {
+    constexpr int CPR = D / 8;   // 16-byte chunks per row
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+#pragma unroll 4
+    for (int c = st; c < BM * CPR; c += 32 * kSoftmaxWarps) {
+        const int rr = c / CPR, ch = c - rr * CPR;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (rr < rows) {
+            const int pos = A ? __ldg(A + rr) : row0 + rr;
+            val = s4[(((long long)b * n_state + pos) * H + h) * CPR + ch];
+        }
+        *reinterpret_cast<uint4 *>(tile + swz_off(rr, ch)) = val;
+    }
 }
 
 // One arrival per warp: every lane's earlier shared-memory and tensor-memory
@@ -222,6 +225,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     int *row_cnt = reinterpret_cast<int *>(smem + C::OFF_ROW);
     float *row_zo = reinterpret_cast<float *>(smem + C::OFF_ROW + 128 * 4);
     float *row_zn = reinterpret_cast<float *>(smem + C::OFF_ROW + 128 * 8);
+    int *row_pos_s = reinterpret_cast<int *>(smem + C::OFF_ROW + 128 * 12);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Work grows with a row tile's last position (later rows see more keys), so the
@@ -236,12 +240,12 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const long long bh = (long long)b * p.H + h;
     const int32_t *S = dense ? nullptr : p.key_idx + bh * p.K;
     const int32_t *A = dense ? nullptr : p.row_pos + (long long)b * p.R + row0;
-    const int min_pos = dense ? row0 : __ldg(A);
-    const int max_pos = dense ? row0 + rows - 1 : __ldg(A + rows - 1);
     // Rows and keys are both ascending, so the keys a row may see are a
-    // prefix of the list: row i sees the first count_le(S, i) of them.
-    const int cnt = dense ? min(max_pos + 1, p.n_keys) : count_le(S, p.K, max_pos);      // last row
-    const int cnt_min = dense ? min(min_pos + 1, p.n_keys) : count_le(S, p.K, min_pos);  // first row
+    // prefix of the list: row i sees the keys of S that are <= i, counted for
+    // every lazy row by row_key_counts_kernel.
+    const int32_t *RC = dense ? nullptr : p.row_cnt + bh * p.R + row0;
+    const int cnt = dense ? min(row0 + rows, p.n_keys) : __ldg(RC + rows - 1);   // last row
+    const int cnt_min = dense ? min(row0 + 1, p.n_keys) : __ldg(RC);             // first row
     const int n_tiles = (cnt + BN - 1) / BN;
     if (n_tiles == 0) return;   // every row has an empty key set: state unchanged
     const int ph0 = first ? PH_LSE : PH_OLD;
@@ -253,7 +257,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     if (threadIdx.x == 0) {
         for (int i = 0; i < N_BARS; ++i) {
             const bool many = (i >= BAR_S_READ && i < BAR_S_READ + kSBufs) || (i >= BAR_P_FULL && i < BAR_P_FULL + 2) ||
-                              i == BAR_STATS || i == BAR_Q_READY || i == BAR_ZN;
+                              i == BAR_STATS || i == BAR_Q_READY || i == BAR_ZN || i == BAR_EPI;
             mbar_init(bar(i), many ? (uint32_t)kSoftmaxWarps : 1u);
         }
         misc[1] = 0;
@@ -270,13 +274,14 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const int r = (warp & 3) * 32 + lane;          // the row this thread loads and writes back
     const bool row_ok = is_sm && r < rows;
     const int pos = row_ok ? (dense ? row0 + r : __ldg(A + r)) : -1;
-    const long long qoff = (((long long)b * p.n_state + max(pos, 0)) * p.H + h) * D;
+    const int st = (int)threadIdx.x - 32 * kFirstSoftmaxWarp;   // softmax thread index
     if (is_sm) {   // pass OLD reads qhat; the first dense loop starts with q
-        load_query_row<D>(smem + C::OFF_Q, first ? p.q + qoff : p.q_hat + qoff, row_ok, r, wg);
+        load_query_tile<D>(smem + C::OFF_Q, first ? p.q : p.q_hat, st, b, h, p.H, p.n_state, rows, row0, A);
         fence_proxy_async_smem();
         if (wg == 0) {   // per row, shared by the four groups: key count and old normaliser (log2 units)
-            row_cnt[r] = !row_ok ? 0 : cnt_min == cnt ? cnt : dense ? min(pos + 1, p.n_keys) : count_le(S, p.K, pos);
+            row_cnt[r] = !row_ok ? 0 : cnt_min == cnt ? cnt : dense ? min(pos + 1, p.n_keys) : __ldg(RC + r);
             row_zo[r] = !row_ok ? INFINITY : first ? 0.f : __ldg(p.z + bh * p.n_state + pos) * kLog2e;
+            row_pos_s[r] = pos;
         }
     }
     tc_fence_before();
@@ -434,11 +439,16 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             if (ph == PH_LSE && t == 0 && !first) {
                 // pass OLD's products are all done (their S tiles were consumed):
                 // reload the query tile with this loop's q
-                load_query_row<D>(smem + C::OFF_Q, p.q + qoff, row_ok, r, wg);
+                load_query_tile<D>(smem + C::OFF_Q, p.q, st, b, h, p.H, p.n_state, rows, row0, A);
                 fence_proxy_async_smem();
                 warp_arrive(bar(BAR_Q_READY), lane);
             }
             if (ph == PH_NEW && t == 0) {
+                // the epilogue reads this thread's part of its O row: fetch it into L2 now
+                if (row_ok && !first) {
+                    const float *orow = p.o + ((((long long)b * p.n_state + pos) * p.H + h) * D + wg * (D / kGroups));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(orow));
+                }
                 // merge row statistics: the four lanes of a row, then the four groups
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -581,38 +591,55 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         }
         if (ok && wait_bar(bar(BAR_ACC), 0, abort_flag, ERR_ACC)) {
             tc_fence_after();
+            // Epilogue. A thread's accumulator row goes to shared memory (the K ring is idle
+            // now); then each warp walks whole rows so that O, Z and qhat move in full lines.
             constexpr int GD = D / kGroups;   // accumulator columns per group (16, 24 or 32)
-            constexpr int GC = GD % 16 == 0 ? 16 : 8;   // columns per chunk, to bound live registers
+            float *xo = reinterpret_cast<float *>(smem + C::OFF_K);
             const uint32_t lane_base = (uint32_t)rq << 16;
-            const float zn_r = row_zn[r];
-            const bool update = row_ok && zn_r < INFINITY;
-            const long long srow = ((long long)b * p.n_state + max(pos, 0)) * p.H + h;
 #pragma unroll
-            for (int u0 = 0; u0 < GD; u0 += GC) {
-                float av[GC];
-#pragma unroll
-                for (int u = 0; u < GC; u += 8) tmem_ld_32x32b_x8(tmem + lane_base + kColAcc + wg * GD + u0 + u, av + u);
+            for (int u = 0; u < GD; u += 8) {
+                float av[8];
+                tmem_ld_32x32b_x8(tmem + lane_base + kColAcc + wg * GD + u, av);
                 tmem_wait_ld();
-                if (update) {
-                    float4 *orow = reinterpret_cast<float4 *>(p.o + srow * D + wg * GD + u0);
-#pragma unroll
-                    for (int e = 0; e < GC / 4; ++e) {
-                        float4 ov = first ? make_float4(0.f, 0.f, 0.f, 0.f) : orow[e];
-                        ov.x += av[4 * e];
-                        ov.y += av[4 * e + 1];
-                        ov.z += av[4 * e + 2];
-                        ov.w += av[4 * e + 3];
-                        orow[e] = ov;
-                    }
-                }
+                float4 *dst = reinterpret_cast<float4 *>(xo + r * C::XS + wg * GD + u);
+                dst[0] = make_float4(av[0], av[1], av[2], av[3]);
+                dst[1] = make_float4(av[4], av[5], av[6], av[7]);
             }
-            if (update) {
-                if (wg == 0) p.z[bh * p.n_state + pos] = zn_r * kLn2;
-                // the query tile holds this loop's q: copy this group's chunks of it to qhat
-                uint4 *dst = reinterpret_cast<uint4 *>(p.q_hat + srow * D);
+            warp_arrive(bar(BAR_EPI), lane);
+            if (wait_bar(bar(BAR_EPI), 0, abort_flag, ERR_EPI)) {
+                constexpr int RPW = BM / kSoftmaxWarps;   // rows per warp
+                const int sw = warp - kFirstSoftmaxWarp;
+                float4 ov[RPW];
+                long long srow[RPW];
+                bool upd[RPW];
+                // all of this warp's O loads first, then the updates
 #pragma unroll
-                for (int ch = wg; ch < D / 8; ch += kGroups)
-                    dst[ch] = *reinterpret_cast<const uint4 *>(smem + C::OFF_Q + swz_off(r, ch));
+                for (int i = 0; i < RPW; ++i) {
+                    const int rr = sw + kSoftmaxWarps * i;
+                    upd[i] = rr < rows && row_zn[rr] < INFINITY;
+                    srow[i] = upd[i] ? ((long long)b * p.n_state + row_pos_s[rr]) * p.H + h : 0;
+                    ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (upd[i] && !first && lane < D / 4) ov[i] = reinterpret_cast<const float4 *>(p.o + srow[i] * D)[lane];
+                }
+#pragma unroll
+                for (int i = 0; i < RPW; ++i) {
+                    if (!upd[i]) continue;
+                    const int rr = sw + kSoftmaxWarps * i;
+                    if (lane < D / 4) {
+                        const float4 a4 = reinterpret_cast<const float4 *>(xo + rr * C::XS)[lane];
+                        float4 o4 = ov[i];
+                        o4.x += a4.x;
+                        o4.y += a4.y;
+                        o4.z += a4.z;
+                        o4.w += a4.w;
+                        reinterpret_cast<float4 *>(p.o + srow[i] * D)[lane] = o4;
+                    }
+                    // the query tile holds this loop's q: it becomes qhat
+                    if (lane < D / 8)
+                        reinterpret_cast<uint4 *>(p.q_hat + srow[i] * D)[lane] =
+                            *reinterpret_cast<const uint4 *>(smem + C::OFF_Q + swz_off(rr, lane));
+                    if (lane == 0) p.z[bh * p.n_state + row_pos_s[rr]] = row_zn[rr] * kLn2;
+                }
             }
         }
     }
@@ -623,6 +650,32 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Keys each lazy row sees, #{j in S_bh : j <= pos_i} for every (b, h, i), with the
+// head's ascending key list staged in shared memory when it fits.
+constexpr int kCountThreads = 256;
+constexpr int kCountStage = 12288;   // keys staged in shared memory (48 KB)
+__global__ void __launch_bounds__(kCountThreads)
+row_key_counts_kernel(const int32_t *__restrict__ key_idx, const int32_t *__restrict__ row_pos, int H, int K, int R,
+                      int32_t *__restrict__ row_cnt) {
+    extern __shared__ int32_t keys_s[];
+    const int h = blockIdx.y, b = blockIdx.z;
+    const long long bh = (long long)b * H + h;
+    const int32_t *S = key_idx + bh * K;
+    const bool staged = K <= kCountStage;
+    if (staged)
+        for (int j = threadIdx.x; j < K; j += kCountThreads) keys_s[j] = __ldg(S + j);
+    __syncthreads();
+    const int i = blockIdx.x * kCountThreads + threadIdx.x;
+    if (i >= R) return;
+    const int x = __ldg(row_pos + (long long)b * R + i);
+    int lo = 0, hi = K;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((staged ? keys_s[mid] : __ldg(S + mid)) <= x) lo = mid + 1; else hi = mid;
+    }
+    row_cnt[bh * R + i] = lo;
 }
 
 // ---------------------------------------------------------------------------
@@ -688,6 +741,7 @@ cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
     kp.K = dense ? p.n_keys : p.K;
     kp.n_row_tiles = ceil_div(p.R, BM);
     kp.row_pos = p.row_pos;
+    kp.row_cnt = p.row_cnt;
     kp.key_idx = p.key_idx;
     kp.q = p.q;
     kp.q_hat = p.q_hat;
@@ -696,6 +750,13 @@ cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
     kp.c = p.c;
     kp.sl2 = kLog2e / sqrtf((float)D);
     dim3 grid(kp.n_row_tiles * p.H, 1, p.B);
+    if (!dense) {
+        if (!p.row_cnt) return cudaErrorInvalidValue;
+        KernelTimer kt("row_key_counts", s);
+        const int stage = p.K <= kCountStage ? p.K : 0;
+        row_key_counts_kernel<<<dim3(ceil_div(p.R, kCountThreads), p.H, p.B), kCountThreads, stage * 4, s>>>(
+            p.key_idx, p.row_pos, p.H, p.K, p.R, p.row_cnt);
+    }
     {
         KernelTimer kt("tc_attention", s);
         tc_attention_kernel<D><<<grid, kThreads, Cf::SMEM, s>>>(kp, maps[0], maps[1], maps[2], maps[3]);

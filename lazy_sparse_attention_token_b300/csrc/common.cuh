@@ -75,6 +75,7 @@ struct TcAttnParams {
     const int32_t *row_pos;   // [B,R] or NULL (dense: row = key position)
     int K;               // key columns per (b,h) (dense: n_keys)
     const int32_t *key_idx;   // [B,H,K] or NULL (dense)
+    int32_t *row_cnt;         // lazy: workspace [B,H,R] for the keys each row sees
     const uint16_t *q;
     uint16_t *q_hat;
     float *o, *z, *c;
