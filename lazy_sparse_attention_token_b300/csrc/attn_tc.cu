@@ -48,6 +48,7 @@
 #include <cudaTypedefs.h>
 #include <float.h>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -117,6 +118,12 @@ struct KParams {
     float *o, *z, *c;
     float sl2;   // log2(e) / sqrt(d)
 };
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -433,83 +440,20 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         // this lane's column after the butterfly of column_sum()
         const int Jc = lane >> 2;
         const int mycol = cbase + 8 * (Jc >> 1) + 2 * q4 + (Jc & 1);
-        int ph = ph0, t = 0, pv = 0;
-        for (int g = 0; g < total && ok; ++g, ++t) {
-            if (t == n_tiles) { t = 0; ++ph; }
-            if (ph == PH_LSE && t == 0 && !first) {
-                // pass OLD's products are all done (their S tiles were consumed):
-                // reload the query tile with this loop's q
-                load_query_tile<D>(smem + C::OFF_Q, p.q, st, b, h, p.H, p.n_state, rows, row0, A);
-                fence_proxy_async_smem();
-                warp_arrive(bar(BAR_Q_READY), lane);
-            }
-            if (ph == PH_NEW && t == 0) {
-                // the epilogue reads this thread's part of its O row: fetch it into L2 now
-                if (row_ok && !first) {
-                    const float *orow = p.o + ((((long long)b * p.n_state + pos) * p.H + h) * D + wg * (D / kGroups));
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(orow));
-                }
-                // merge row statistics: the four lanes of a row, then the four groups
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-#pragma unroll
-                    for (int off = 1; off <= 2; off <<= 1) {
-                        const float mo = __shfl_xor_sync(0xffffffffu, mk[k], off);
-                        const float Mo = __shfl_xor_sync(0xffffffffu, Mk[k], off);
-                        const float Lo = __shfl_xor_sync(0xffffffffu, Lk[k], off);
-                        const float Mx = fmaxf(Mk[k], Mo);
-                        Lk[k] = Mx == -INFINITY ? 0.f : Lk[k] * ex2((Mk[k] - Mx) * p.sl2) + Lo * ex2((Mo - Mx) * p.sl2);
-                        Mk[k] = Mx;
-                        mk[k] += mo;
-                    }
-                }
-                float *ex = reinterpret_cast<float *>(smem + C::OFF_X);
-                if (q4 == 0) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float *e = ex + (wg * 128 + rlo + 8 * k) * 3;
-                        e[0] = mk[k];
-                        e[1] = Mk[k];
-                        e[2] = Lk[k];
-                    }
-                }
-                warp_arrive(bar(BAR_STATS), lane);
-                if (!wait_bar(bar(BAR_STATS), 0, abort_flag, ERR_STATS)) { ok = false; break; }
-                // Z' = lam - ln m in log2 units; rows with an empty key set or no old mass keep their state
-                auto merged = [&](int row) -> float {
-                    if (row >= rows) return INFINITY;
-                    float mx = 0.f, Mx = -INFINITY, Lx = 0.f;
-#pragma unroll
-                    for (int k = 0; k < kGroups; ++k) {
-                        mx += ex[(k * 128 + row) * 3 + 0];
-                        Mx = fmaxf(Mx, ex[(k * 128 + row) * 3 + 1]);
-                    }
-                    if (Mx == -INFINITY) return INFINITY;
-#pragma unroll
-                    for (int k = 0; k < kGroups; ++k)
-                        Lx += ex[(k * 128 + row) * 3 + 2] * ex2((ex[(k * 128 + row) * 3 + 1] - Mx) * p.sl2);
-                    if (first) mx = 1.f;
-                    return mx >= FLT_MIN ? Mx * p.sl2 + __log2f(Lx) - __log2f(mx) : INFINITY;
-                };
-                if (wg == 0) row_zn[r] = merged(r);
-                warp_arrive(bar(BAR_ZN), lane);
-                if (!wait_bar(bar(BAR_ZN), 0, abort_flag, ERR_ZN)) { ok = false; break; }
-            }
-            const int c0 = t * BN;
-            const bool with_v = ph != PH_LSE;
-            // key position of this lane's column mass, loaded before the waits below
-            const int jcol = with_v ? col_index(c0 + mycol) : INT_MAX;
-            // every row of the tile sees all 128 columns (uniform), else mask by the prefix count
-            const bool full = c0 + BN <= cnt_min;
+        int g = 0, pv = 0;   // tile index over all passes; tiles with a PV product so far
+
+        // Waits for tile g's logits and loads this thread's fragment of them; keys
+        // past a row's prefix count are masked to -inf.
+        auto load_s = [&](int t, float (&v)[32]) -> bool {
             const int sb = g & 1;
-            if (!wait_bar(bar(BAR_S_FULL + sb), (g >> 1) & 1, abort_flag, ERR_S_FULL)) { ok = false; break; }
+            if (!wait_bar(bar(BAR_S_FULL + sb), (g >> 1) & 1, abort_flag, ERR_S_FULL)) return false;
             tc_fence_after();
-            float v[32];
             tmem_ld_16x256b_x4(t_lo + 128u * sb + cbase, v);
             tmem_ld_16x256b_x4(t_hi + 128u * sb + cbase, v + 16);
             tmem_wait_ld();
             warp_arrive(bar(BAR_S_READ + sb), lane);
-            if (!full) {   // keys past a row's prefix count are outside its set
+            const int c0 = t * BN;
+            if (c0 + BN > cnt_min) {   // not every row of the tile sees all 128 columns
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int nv = row_cnt[rlo + 8 * k] - c0 - cbase - 2 * q4;
@@ -520,47 +464,29 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                             if (8 * j + e >= nv) v[frag(k, j, e)] = -INFINITY;
                 }
             }
-            if (!with_v) {
-                // online logsumexp of this tile's new logits, per fragment row
+            return true;
+        };
+
+        // One tile of pass OLD or NEW: probabilities with a known normaliser (nz =
+        // -Z in log2 units; rows outside the tile or the sequence have nz = -inf and
+        // get zero), P to TMEM for the PV product, then the old mass (pass OLD) and
+        // the column masses.
+        auto pv_tile = [&](auto old_c, int t, const float (&nz)[4]) -> bool {
+            constexpr bool OLD = decltype(old_c)::value;
+            // key position of this lane's column mass, loaded before the waits below
+            const int jcol = col_index(t * BN + mycol);
+            float v[32];
+            if (!load_s(t, v)) return false;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float c4[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) c4[j] = fmaxf(v[frag(k, j, 0)], v[frag(k, j, 1)]);
-                    const float cm = fmaxf(fmaxf(c4[0], c4[1]), fmaxf(c4[2], c4[3]));
-                    if (cm > Mk[k]) {
-                        Lk[k] *= ex2((Mk[k] - cm) * p.sl2);
-                        Mk[k] = cm;
-                    }
-                    if (Mk[k] > -INFINITY) {
-                        const float nb = -Mk[k] * p.sl2;
-                        float a2[2] = {0.f, 0.f};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) a2[e] += ex2(fmaf(v[frag(k, j, e)], p.sl2, nb));
-                        Lk[k] += a2[0] + a2[1];
-                    }
-                }
-                continue;
-            }
-            // probabilities with a known normaliser: exp(logit - Z); rows outside the
-            // tile or the sequence get zero through an infinite normaliser
-            const bool old = ph == PH_OLD;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float nz = -(old ? row_zo[rlo + 8 * k] : row_zn[rlo + 8 * k]);
+            for (int k = 0; k < 4; ++k)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) v[frag(k, j, e)] = ex2(fmaf(v[frag(k, j, e)], p.sl2, nz));
-            }
+                    for (int e = 0; e < 2; ++e) v[frag(k, j, e)] = ex2(fmaf(v[frag(k, j, e)], p.sl2, nz[k]));
             // P buffer pv & 1 was last read by the PV product of the V tile two before
             const int pb = pv & 1;
-            if (pv >= 2 && !wait_bar(bar(BAR_PV_DONE + pb), (uint32_t)((pv >> 1) - 1) & 1u, abort_flag, ERR_PV_DONE)) {
-                ok = false;
-                break;
-            }
+            if (pv >= 2 && !wait_bar(bar(BAR_PV_DONE + pb), (uint32_t)((pv >> 1) - 1) & 1u, abort_flag, ERR_PV_DONE))
+                return false;
             tc_fence_after();
             // bf16 pairs of adjacent keys: register pair (2i, 2i + 1) is one packed P column
             const uint32_t pcol = kColP + 64u * (uint32_t)pb + (uint32_t)(cbase >> 1);
@@ -574,8 +500,9 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             tmem_wait_st();
             warp_arrive(bar(BAR_P_FULL + pb), lane);
             ++pv;
+            ++g;
             // after the hand-off: the old mass m and the column masses
-            if (old) {
+            if constexpr (OLD) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     float a2[2] = {0.f, 0.f};
@@ -587,7 +514,110 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
             }
             const float cs = column_sum(v, lane);
-            if (jcol != INT_MAX && cs != 0.f) atomicAdd(cb + jcol, old ? -cs : cs);
+            if (jcol != INT_MAX && cs != 0.f) atomicAdd(cb + jcol, OLD ? -cs : cs);
+            return true;
+        };
+
+        // ---- pass OLD: previous-loop probabilities, subtracted ----
+        if (!first) {
+            float nz[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) nz[k] = -row_zo[rlo + 8 * k];
+            for (int t = 0; ok && t < n_tiles; ++t) ok = pv_tile(std::true_type{}, t, nz);
+            if (ok) {
+                // pass OLD's products are all done (their S tiles were consumed):
+                // reload the query tile with this loop's q
+                load_query_tile<D>(smem + C::OFF_Q, p.q, st, b, h, p.H, p.n_state, rows, row0, A);
+                fence_proxy_async_smem();
+                warp_arrive(bar(BAR_Q_READY), lane);
+            }
+        }
+        // ---- pass LSE: online logsumexp of the new logits, per fragment row ----
+        for (int t = 0; ok && t < n_tiles; ++t) {
+            float v[32];
+            if (!(ok = load_s(t, v))) break;
+            ++g;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float m1 = max3f(v[frag(k, 0, 0)], v[frag(k, 0, 1)], v[frag(k, 1, 0)]);
+                const float m2 = max3f(v[frag(k, 1, 1)], v[frag(k, 2, 0)], v[frag(k, 2, 1)]);
+                const float m3 = max3f(v[frag(k, 3, 0)], v[frag(k, 3, 1)], Mk[k]);
+                const float mnew = max3f(m1, m2, m3);
+                // a row that has seen no key yet keeps M = -inf and L = 0 (every term is 0)
+                const float nb = mnew == -INFINITY ? 0.f : -mnew * p.sl2;
+                float a2[2] = {Lk[k] * ex2(fmaf(Mk[k], p.sl2, nb)), 0.f};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) a2[e] += ex2(fmaf(v[frag(k, j, e)], p.sl2, nb));
+                Lk[k] = a2[0] + a2[1];
+                Mk[k] = mnew;
+            }
+        }
+        // ---- merge the row statistics: Z' = lam - ln m ----
+        if (ok) {
+            // the epilogue reads this thread's part of its O row: fetch it into L2 now
+            if (row_ok && !first) {
+                const float *orow = p.o + ((((long long)b * p.n_state + pos) * p.H + h) * D + wg * (D / kGroups));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(orow));
+            }
+            // the four lanes of a row, then the four groups
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                for (int off = 1; off <= 2; off <<= 1) {
+                    const float mo = __shfl_xor_sync(0xffffffffu, mk[k], off);
+                    const float Mo = __shfl_xor_sync(0xffffffffu, Mk[k], off);
+                    const float Lo = __shfl_xor_sync(0xffffffffu, Lk[k], off);
+                    const float Mx = fmaxf(Mk[k], Mo);
+                    Lk[k] = Mx == -INFINITY ? 0.f : Lk[k] * ex2((Mk[k] - Mx) * p.sl2) + Lo * ex2((Mo - Mx) * p.sl2);
+                    Mk[k] = Mx;
+                    mk[k] += mo;
+                }
+            }
+            float *ex = reinterpret_cast<float *>(smem + C::OFF_X);
+            if (q4 == 0) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float *e = ex + (wg * 128 + rlo + 8 * k) * 3;
+                    e[0] = mk[k];
+                    e[1] = Mk[k];
+                    e[2] = Lk[k];
+                }
+            }
+            warp_arrive(bar(BAR_STATS), lane);
+            ok = wait_bar(bar(BAR_STATS), 0, abort_flag, ERR_STATS);
+            if (ok && wg == 0) {
+                // rows with an empty key set or no old mass keep their state (Z' = inf)
+                float zn = INFINITY;
+                if (r < rows) {
+                    float mx = 0.f, Mx = -INFINITY, Lx = 0.f;
+#pragma unroll
+                    for (int k = 0; k < kGroups; ++k) {
+                        mx += ex[(k * 128 + r) * 3 + 0];
+                        Mx = fmaxf(Mx, ex[(k * 128 + r) * 3 + 1]);
+                    }
+                    if (Mx > -INFINITY) {
+#pragma unroll
+                        for (int k = 0; k < kGroups; ++k)
+                            Lx += ex[(k * 128 + r) * 3 + 2] * ex2((ex[(k * 128 + r) * 3 + 1] - Mx) * p.sl2);
+                        if (first) mx = 1.f;
+                        if (mx >= FLT_MIN) zn = Mx * p.sl2 + __log2f(Lx) - __log2f(mx);
+                    }
+                }
+                row_zn[r] = zn;
+            }
+            if (ok) {
+                warp_arrive(bar(BAR_ZN), lane);
+                ok = wait_bar(bar(BAR_ZN), 0, abort_flag, ERR_ZN);
+            }
+        }
+        // ---- pass NEW: this loop's probabilities with the merged normaliser, added ----
+        if (ok) {
+            float nz[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) nz[k] = -row_zn[rlo + 8 * k];
+            for (int t = 0; ok && t < n_tiles; ++t) ok = pv_tile(std::false_type{}, t, nz);
         }
         if (ok && wait_bar(bar(BAR_ACC), 0, abort_flag, ERR_ACC)) {
             tc_fence_after();
