@@ -342,33 +342,35 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                     wait_bar(bar(BAR_V_FULL + (v & 1)), (v >> 1) & 1, &never, ERR_V_FULL);
             }
         }
-    } else if (warp == 1) {
-        // ---------------- QK issuer: S = Q K^T into the S buffer of tile g ----------------
-        // Two issuing threads keep the tensor pipe fed: it buffers only about two MMAs,
-        // and each issuer's barrier tests between batches are covered by the other's MMAs.
+    } else if (warp == 1 || warp == 2) {
+        // ---------------- MMA issuers (one thread each) ----------------
+        // Warp 1 issues the QK products, warp 2 the PV products, and pass LSE's QK
+        // products (no PV there) are split by tile parity between the two: the tensor
+        // pipe buffers only about two MMAs, and each issuer's barrier tests between
+        // its batches are covered by the other's MMAs. Tile g's logits go to S buffer
+        // g & 1, so each buffer of pass LSE has a single issuer.
         if (lane == 0) {
             constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false, false);
+            constexpr uint32_t id_pv = idesc_bf16(128, D, false, true, false);       // A = P from TMEM
+            constexpr uint32_t id_pv_neg = idesc_bf16(128, D, false, true, true);    // pass OLD subtracts
             // descriptors are built once; per k-step only the start address moves
             const uint64_t d_q = smem_desc(sbase + C::OFF_Q, 16, 1024, 2);
             const uint64_t d_k = smem_desc(sbase + C::OFF_K, 16, 1024, 2);
+            const uint64_t d_v = smem_desc(sbase + C::OFF_V, kAtom, 1024, 2);
             constexpr uint64_t TB16 = C::TB >> 4, ATOM16 = kAtom >> 4;
-            int ks = 0;          // K slot of tile g
-            uint32_t kpar = 0;   // that slot's fill parity
-            bool ok = true;
-            int ph = ph0, t = 0;
-            for (int g = 0; g < total; ++g, ++t) {
-                if (t == n_tiles) { t = 0; ++ph; }
-                if (!wait_bar(bar(BAR_K_FULL + ks), kpar, abort_flag, ERR_K_FULL)) { ok = false; break; }
-                const int sb = g & 1;
+            const int n_old = first ? 0 : n_tiles;   // tiles of pass OLD; pass LSE covers [n_old, n_old + n_tiles)
+            const int lse0 = n_old, new0 = n_old + n_tiles;
+            bool q_seen = first;   // the query tile holds this loop's q (passes LSE and NEW)
+            // S = Q K^T for tile g (K slot g % 3) into S buffer g & 1
+            auto issue_qk = [&](int g) -> bool {
+                const int ks = g % kKStages, sb = g & 1;
+                if (!wait_bar(bar(BAR_K_FULL + ks), (uint32_t)(g / kKStages) & 1u, abort_flag, ERR_K_FULL)) return false;
                 // the S buffer's previous tile has been read by the softmax
-                if (g >= kSBufs && !wait_bar(bar(BAR_S_READ + sb), ((g >> 1) - 1) & 1, abort_flag, ERR_S_READ)) {
-                    ok = false;
-                    break;
-                }
-                // pass LSE starts once the query tile holds this loop's q
-                if (ph == PH_LSE && t == 0 && !first && !wait_bar(bar(BAR_Q_READY), 0, abort_flag, ERR_Q_READY)) {
-                    ok = false;
-                    break;
+                if (g >= kSBufs && !wait_bar(bar(BAR_S_READ + sb), ((g >> 1) - 1) & 1, abort_flag, ERR_S_READ))
+                    return false;
+                if (g >= lse0 && !q_seen) {   // after pass OLD, once the query tile holds this loop's q
+                    if (!wait_bar(bar(BAR_Q_READY), 0, abort_flag, ERR_Q_READY)) return false;
+                    q_seen = true;
                 }
                 tc_fence_after();
                 const uint64_t dk = d_k + TB16 * (uint32_t)ks;
@@ -380,43 +382,41 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
                 mma_commit(bar(BAR_S_FULL + sb));
                 mma_commit(bar(BAR_K_EMPTY + ks));
-                if (++ks == kKStages) { ks = 0; kpar ^= 1u; }
-            }
-            if (!ok) {   // drain whatever was issued before giving up
-                mma_commit(bar(BAR_DRAIN));
-                volatile int never = 0;
-                wait_bar(bar(BAR_DRAIN), 0, &never, ERR_ACC);
-            }
-        }
-    } else if (warp == 2) {
-        // ---------------- PV issuer: acc -= P V (pass OLD), acc += P' V (pass NEW) ----------------
-        if (lane == 0) {
-            constexpr uint32_t id_pv = idesc_bf16(128, D, false, true, false);       // A = P from TMEM
-            constexpr uint32_t id_pv_neg = idesc_bf16(128, D, false, true, true);    // pass OLD subtracts
-            const uint64_t d_v = smem_desc(sbase + C::OFF_V, kAtom, 1024, 2);
-            constexpr uint64_t TB16 = C::TB >> 4;
-            const int n_pv = (ph0 == PH_OLD ? 2 : 1) * n_tiles;
-            bool ok = true;
-            for (int pv = 0; pv < n_pv; ++pv) {
-                const int vs = pv & 1;   // V slot and P buffer of this tile
+                return true;
+            };
+            // acc (+/-)= P V for the tile with PV index pv (P buffer and V slot pv & 1)
+            auto issue_pv = [&](int pv, bool old) -> bool {
+                const int vs = pv & 1;
                 const uint32_t vpar = (uint32_t)(pv >> 1) & 1u;
-                if (!wait_bar(bar(BAR_V_FULL + vs), vpar, abort_flag, ERR_V_FULL)) { ok = false; break; }
-                if (!wait_bar(bar(BAR_P_FULL + vs), vpar, abort_flag, ERR_P_FULL)) { ok = false; break; }
+                if (!wait_bar(bar(BAR_V_FULL + vs), vpar, abort_flag, ERR_V_FULL)) return false;
+                if (!wait_bar(bar(BAR_P_FULL + vs), vpar, abort_flag, ERR_P_FULL)) return false;
                 tc_fence_after();
                 const uint64_t dv = d_v + TB16 * (uint32_t)vs;
                 const uint32_t pa = tmem + kColP + 64u * (uint32_t)vs;
-                const uint32_t idp = ph0 == PH_OLD && pv < n_tiles ? id_pv_neg : id_pv;
+                const uint32_t idp = old ? id_pv_neg : id_pv;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)   // acc +-= P[:, 16kk..] * V[16kk.., :]
                     mma_bf16_ts(tmem + kColAcc, pa + 8u * kk, dv + kk * 128, idp, (pv > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(BAR_PV_DONE + vs));
-            }
-            if (ok) {
-                mma_commit(bar(BAR_ACC));
+                return true;
+            };
+            bool ok = true;
+            if (warp == 1) {
+                for (int g = 0; ok && g < lse0; ++g) ok = issue_qk(g);
+                for (int g = lse0; ok && g < new0; ++g)
+                    if ((g & 1) == 0) ok = issue_qk(g);
+                for (int g = new0; ok && g < total; ++g) ok = issue_qk(g);
             } else {
-                mma_commit(bar(BAR_DRAIN + 1));
+                for (int pv = 0; ok && pv < n_old; ++pv) ok = issue_pv(pv, true);
+                for (int g = lse0; ok && g < new0; ++g)
+                    if ((g & 1) == 1) ok = issue_qk(g);
+                for (int t = 0; ok && t < n_tiles; ++t) ok = issue_pv(n_old + t, false);
+                if (ok) mma_commit(bar(BAR_ACC));
+            }
+            if (!ok) {   // drain whatever this thread issued before giving up
+                mma_commit(bar(BAR_DRAIN + (warp - 1)));
                 volatile int never = 0;
-                wait_bar(bar(BAR_DRAIN + 1), 0, &never, ERR_ACC);
+                wait_bar(bar(BAR_DRAIN + (warp - 1)), 0, &never, ERR_ACC);
             }
         }
     } else {
