@@ -135,10 +135,11 @@ __device__ __forceinline__ float ex2(float x) {
 // spinning; it gives up after about one second, or as soon as another role
 // has given up, recording the first failure code.
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i)
+            if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > 1000000000ull) {
             *abort_flag = 1;
@@ -182,9 +183,10 @@ __device__ __forceinline__ void load_query_tile(uint8_t *tile, const uint16_t *s
 // One arrival per warp: every lane's earlier shared-memory and tensor-memory
 // work is ordered before lane 0 arrives.
 __device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+    (void)lane;
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar);
+    mbar_arrive_elected(bar);
 }
 
 // Softmax fragment layout. Each softmax thread holds, per tile, rows
@@ -514,7 +516,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
             }
             const float cs = column_sum(v, lane);
-            if (jcol != INT_MAX && cs != 0.f) atomicAdd(cb + jcol, OLD ? -cs : cs);
+            red_add_f32_if(cb + (jcol != INT_MAX ? jcol : 0), OLD ? -cs : cs, jcol != INT_MAX && cs != 0.f);
             return true;
         };
 
