@@ -225,7 +225,6 @@ def native(args, world, rank, local):
 
     clocks = ClockSampler(local) if rank == 0 else None
     fl.flashloop_timing_read()          # drop anything recorded so far
-    fl.flashloop_timing_enable(True)
     n0 = fl.flashloop_launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if clocks:
@@ -239,11 +238,19 @@ def native(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop() if clocks else None
-    fl.flashloop_timing_enable(False)
     launches = fl.flashloop_launch_count() - n0
+    secs = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    # Per-kernel durations: the same steps once more, every launch bracketed by a
+    # CUDA event pair on its stream (the pairs add about 5% to a step, so the
+    # pass above, which gives the step time, runs without them).
+    fl.flashloop_timing_enable(True)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        step_loop(lazy[(args.warmup + i) % len(lazy)])
+    torch.cuda.synchronize()
+    fl.flashloop_timing_enable(False)
     per_kernel = fl.flashloop_timing_read()
     assert fl.flashloop_device_status() == 0
-    secs = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
     tokens = w.B * w.N * args.steps * world
     value = tokens / secs
 
@@ -291,6 +298,8 @@ def native(args, world, rank, local):
                                f"T={w.T} (loop 1 dense), r={float(w.r):.2f} (R={R}), k={float(w.k):.2f} (K={K})",
                    "global_batch": w.B * world, "seq_len": w.N, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: each step reads two 134 MB hidden-state tensors",
+                   "kernel_timing": "per-kernel durations from a second timed pass of the same steps with a CUDA "
+                                    "event pair around every launch",
                    "active_tokens_per_s": w.B * R * args.steps * world / secs},
         "roofline": roofline, "kernels": kernels, "gpu_launches": launches,
         "clocks": clk, "e2e": e2e,

@@ -85,16 +85,17 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const __half sh = __float2half_rn(__fdiv_rn(amax, 7.0f));
+    const __half sh = __float2half_rn(__fdiv_rn(amax, 7.0f));   // the scale is exact: fp16(fp32(amax / 7))
     const float s = __half2float(sh);
+    // code = rint(delta / scale): the quotient is taken as delta * (1 / scale), within
+    // about one ulp of the divided one, so a code can only differ where the quotient
+    // lies within ~1e-6 of a rounding boundary (n + 1/2)
+    const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
     uint32_t packed = 0;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-        int q = 0;
-        if (s > 0.f) {
-            const float r = rintf(__fdiv_rn(dl[u], s));
-            q = (int)fminf(7.f, fmaxf(-7.f, r));
-        }
+        const float r = rintf(dl[u] * inv);
+        const int q = (int)fminf(7.f, fmaxf(-7.f, r));
         packed |= (uint32_t)(q & 0xF) << (4 * u);
     }
     if (!in_range) return;
