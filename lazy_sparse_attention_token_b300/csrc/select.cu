@@ -62,48 +62,100 @@ token_scores_kernel(const uint16_t *__restrict__ h_prev, const uint16_t *__restr
     if (lane == 0) score[row] = acc;
 }
 
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkSmemMaxN = 48 * 1024;   // rows up to this length are staged in shared memory
 
-// Exact top-k of one row of fp32 values per CTA. The k-th largest key is
-// found by four 8-bit radix passes (most significant digit first) over
-// order-preserving uint32 keys; then elements above it, and the first
-// (lowest-index) ones equal to it, are written in ascending index order.
+// ---- top-k over a cluster of CTAs --------------------------------------------
+// Exact top-k of each row of fp32 values: the k-th largest order-preserving
+// uint32 key is found by four 8-bit radix passes (most significant digit
+// first); then the keys above it, and the first (lowest-index) ones equal to
+// it, are written in ascending index order. A row is split over a cluster of
+// kTopkCluster CTAs (one row alone would otherwise run on a single SM): each
+// CTA histograms its own contiguous segment and adds the histogram into a
+// fresh one on cluster rank 0 (distributed shared memory); after one cluster
+// barrier every rank reads the merged histogram and takes the same digit. The
+// output order is rank order, then warp segments, so indices stay ascending.
+constexpr int kTopkCluster = 8;
+constexpr int kTopkClThreads = 512;
+constexpr int kTopkClWarps = kTopkClThreads / 32;
+constexpr int kTopkClStageMax = 24 * 1024;   // keys per CTA staged in shared memory (96 KB)
+
+__device__ __forceinline__ uint32_t cl_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cl_red_add(uint32_t addr, uint32_t v) {
+    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t cl_ld(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void cl_st(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Every thread of every CTA of the cluster passes each of these.
+__device__ __forceinline__ void cl_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 template <bool kStaged>
-__global__ void __launch_bounds__(kTopkThreads)
-topk_rows_kernel(const float *__restrict__ vals, int n, int k, int32_t *__restrict__ out) {
+__global__ void __launch_bounds__(kTopkClThreads)
+topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__restrict__ out) {
     extern __shared__ uint32_t staged[];
-    __shared__ uint32_t hist[256];
+    __shared__ uint32_t whist[kTopkClWarps][256];   // one histogram per warp: keys of similar
+                                                    // magnitude share a digit, so a single
+                                                    // histogram would serialise on one bin
+    __shared__ uint32_t g_hist[4][256];        // merged histograms, used on rank 0
+    __shared__ uint32_t cta_cnt[kTopkCluster][2];   // per-rank (greater, equal) counts, used on rank 0
     __shared__ uint32_t s_prefix;
     __shared__ int s_kleft;
-    __shared__ unsigned long long warp_tot[kTopkWarps];
+    __shared__ unsigned long long warp_tot[kTopkClWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float *row = vals + (size_t)blockIdx.x * n;
-    int32_t *orow = out + (size_t)blockIdx.x * k;
+    const uint32_t rank = cl_rank();
+    const int row_id = blockIdx.x / kTopkCluster;
+    const float *row = vals + (size_t)row_id * n;
+    int32_t *orow = out + (size_t)row_id * k;
+    // this CTA's segment of the row, a multiple of 32 keys
+    const int seg = ((n + kTopkCluster - 1) / kTopkCluster + 31) & ~31;
+    const int lo = min(n, (int)rank * seg), hi = min(n, lo + seg), len = hi - lo;
 
-    if (kStaged) {
-        for (int i = tid; i < n; i += kTopkThreads) staged[i] = f32_order_key(__ldg(row + i));
-    }
-    auto key_at = [&](int i) -> uint32_t { return kStaged ? staged[i] : f32_order_key(__ldg(row + i)); };
+    if (rank == 0)
+        for (int i = tid; i < 4 * 256; i += kTopkClThreads) (&g_hist[0][0])[i] = 0u;
+    if (kStaged)
+        for (int i = tid; i < len; i += kTopkClThreads) staged[i] = f32_order_key(__ldg(row + lo + i));
+    auto key_at = [&](int i) -> uint32_t { return kStaged ? staged[i] : f32_order_key(__ldg(row + lo + i)); };
+    cl_sync();   // rank 0's merged histograms are zero; every CTA of the cluster runs
 
     uint32_t prefix = 0, mask = 0;
     int kleft = k;
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        if (tid < 256) hist[tid] = 0;
+        for (int i = tid; i < kTopkClWarps * 256; i += kTopkClThreads) (&whist[0][0])[i] = 0u;
         __syncthreads();
-        for (int i = tid; i < n; i += kTopkThreads) {
+        for (int i = tid; i < len; i += kTopkClThreads) {
             const uint32_t key = key_at(i);
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            if ((key & mask) == prefix) atomicAdd(&whist[warp][(key >> shift) & 255u], 1u);
         }
         __syncthreads();
+        if (tid < 256) {
+            uint32_t tot = 0;
+#pragma unroll
+            for (int w = 0; w < kTopkClWarps; ++w) tot += whist[w][tid];
+            if (tot != 0u) cl_red_add(cl_map(&g_hist[pass][tid], 0), tot);
+        }
+        cl_sync();
         if (warp == 0) {
             uint32_t c[8], local = 0;
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                c[t] = hist[255 - 8 * lane - t];
+                c[t] = cl_ld(cl_map(&g_hist[pass][255 - 8 * lane - t], 0));
                 local += c[t];
             }
             uint32_t incl = local;
@@ -134,41 +186,55 @@ topk_rows_kernel(const float *__restrict__ vals, int n, int k, int32_t *__restri
         mask |= 255u << shift;
     }
     const uint32_t thr = prefix;   // the k-th largest key
-    const int need_eq = kleft;     // how many elements equal to it are kept
+    const int need_eq = kleft;     // how many keys equal to it are kept
 
-    // Each warp owns one contiguous segment; lanes walk it 32 at a time so
-    // the loads stay coalesced and ballots keep index order.
-    const int seg = ((n + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
-    const int lo = warp * seg, hi = min(n, lo + seg);
+    // counts in this CTA's segment, warp by warp (each warp owns a contiguous part)
+    const int wseg = ((len + kTopkClWarps - 1) / kTopkClWarps + 31) & ~31;
+    const int wlo = min(len, warp * wseg), whi = min(len, wlo + wseg);
     const unsigned lt = (1u << lane) - 1u;
     uint32_t gt_cnt = 0, eq_cnt = 0;
-    for (int base = lo; base < hi; base += 32) {
+    for (int base = wlo; base < whi; base += 32) {
         const int i = base + lane;
-        const uint32_t key = i < hi ? key_at(i) : 0u;
-        gt_cnt += __popc(__ballot_sync(0xffffffffu, i < hi && key > thr));
-        eq_cnt += __popc(__ballot_sync(0xffffffffu, i < hi && key == thr));
+        const uint32_t key = i < whi ? key_at(i) : 0u;
+        gt_cnt += __popc(__ballot_sync(0xffffffffu, i < whi && key > thr));
+        eq_cnt += __popc(__ballot_sync(0xffffffffu, i < whi && key == thr));
     }
     if (lane == 0) warp_tot[warp] = ((unsigned long long)gt_cnt << 32) | eq_cnt;
     __syncthreads();
-    unsigned long long before = 0;
-    for (int w = 0; w < warp; ++w) before += warp_tot[w];
-    uint32_t gt_run = (uint32_t)(before >> 32), eq_run = (uint32_t)(before & 0xffffffffu);
-    for (int base = lo; base < hi; base += 32) {
+    if (tid == 0) {
+        unsigned long long tot = 0;
+        for (int w = 0; w < kTopkClWarps; ++w) tot += warp_tot[w];
+        cl_st(cl_map(&cta_cnt[rank][0], 0), (uint32_t)(tot >> 32));
+        cl_st(cl_map(&cta_cnt[rank][1], 0), (uint32_t)(tot & 0xffffffffu));
+    }
+    cl_sync();
+    // keys before this CTA's segment (lower ranks), then before this warp's part
+    uint32_t gt_run = 0, eq_run = 0;
+    for (uint32_t q = 0; q < rank; ++q) {
+        gt_run += cl_ld(cl_map(&cta_cnt[q][0], 0));
+        eq_run += cl_ld(cl_map(&cta_cnt[q][1], 0));
+    }
+    for (int w = 0; w < warp; ++w) {
+        gt_run += (uint32_t)(warp_tot[w] >> 32);
+        eq_run += (uint32_t)(warp_tot[w] & 0xffffffffu);
+    }
+    for (int base = wlo; base < whi; base += 32) {
         const int i = base + lane;
-        const uint32_t key = i < hi ? key_at(i) : 0u;
-        const uint32_t gb = __ballot_sync(0xffffffffu, i < hi && key > thr);
-        const uint32_t eb = __ballot_sync(0xffffffffu, i < hi && key == thr);
+        const uint32_t key = i < whi ? key_at(i) : 0u;
+        const uint32_t gb = __ballot_sync(0xffffffffu, i < whi && key > thr);
+        const uint32_t eb = __ballot_sync(0xffffffffu, i < whi && key == thr);
         const int eq_left = max(0, need_eq - (int)eq_run);
         const int eq_take = min(eq_left, __popc(eb));
         const int out_base = (int)gt_run + min((int)eq_run, need_eq);
         if (gb & (1u << lane)) {
-            orow[out_base + __popc(gb & lt) + min(__popc(eb & lt), eq_take)] = i;
+            orow[out_base + __popc(gb & lt) + min(__popc(eb & lt), eq_take)] = lo + i;
         } else if ((eb & (1u << lane)) && __popc(eb & lt) < eq_take) {
-            orow[out_base + __popc(gb & lt) + __popc(eb & lt)] = i;
+            orow[out_base + __popc(gb & lt) + __popc(eb & lt)] = lo + i;
         }
         gt_run += __popc(gb);
         eq_run += __popc(eb);
     }
+    cl_sync();   // rank 0's counts stay readable until every rank is done with them
 }
 
 }  // namespace
@@ -185,25 +251,32 @@ cudaError_t launch_token_scores(const uint16_t *h_prev, const uint16_t *h_cur, i
 
 cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t *out, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    if (n <= kTopkSmemMaxN) {
-        const size_t smem = (size_t)n * 4;
-        static bool attr_set = false;
-        if (!attr_set) {
-            cudaFuncSetAttribute(topk_rows_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kTopkSmemMaxN * 4);
-            attr_set = true;
-        }
-        {
-            KernelTimer kt("topk", s);
-            topk_rows_kernel<true><<<rows, kTopkThreads, smem, s>>>(vals, n, k, out);
-        }
-    } else {
-        {
-            KernelTimer kt("topk", s);
-            topk_rows_kernel<false><<<rows, kTopkThreads, 0, s>>>(vals, n, k, out);
-        }
+    const int seg = ((n + kTopkCluster - 1) / kTopkCluster + 31) & ~31;
+    const bool staged = seg <= kTopkClStageMax;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaFuncSetAttribute(topk_cluster_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTopkClStageMax * 4);
+    });
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows * kTopkCluster));
+    cfg.blockDim = dim3(kTopkClThreads);
+    cfg.dynamicSmemBytes = staged ? (size_t)seg * 4 : 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kTopkCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    {
+        KernelTimer kt("topk", s);
+        e = staged ? cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, vals, n, k, out)
+                   : cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, vals, n, k, out);
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace fl
