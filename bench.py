@@ -223,6 +223,27 @@ def native(args, world, rank, local):
     torch.cuda.synchronize()
     assert fl.flashloop_device_status() == 0
 
+    # One CUDA graph per lazy loop index, captured once and replayed by the timed
+    # pass (the step's 7 launches and its memset without per-launch host work).
+    graphs, launch_mode = {}, "direct launches"
+    if not args.no_graph:
+        try:
+            n_cap = fl.flashloop_launch_count()
+            for l in lazy:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    step_loop(l)
+                graphs[l] = g
+            launches_per_step = (fl.flashloop_launch_count() - n_cap) / len(lazy)
+            for l in lazy:
+                graphs[l].replay()
+            torch.cuda.synchronize()
+            assert fl.flashloop_device_status() == 0
+            launch_mode = "CUDA graph per lazy loop, replayed"
+        except Exception as exc:   # capture unsupported here: time direct launches
+            graphs, launch_mode = {}, f"direct launches (graph capture failed: {str(exc)[:80]})"
+            torch.cuda.synchronize()
+
     clocks = ClockSampler(local) if rank == 0 else None
     fl.flashloop_timing_read()          # drop anything recorded so far
     n0 = fl.flashloop_launch_count()
@@ -233,12 +254,17 @@ def native(args, world, rank, local):
     torch.cuda.synchronize()
     ev0.record()
     for i in range(args.steps):
-        step_loop(lazy[(args.warmup + i) % len(lazy)])
+        l = lazy[(args.warmup + i) % len(lazy)]
+        if graphs:
+            graphs[l].replay()
+        else:
+            step_loop(l)
     ev1.record()
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop() if clocks else None
-    launches = fl.flashloop_launch_count() - n0
+    # launches inside the timed pass (a replayed graph holds the captured step's launches)
+    launches = int(round(launches_per_step * args.steps)) if graphs else fl.flashloop_launch_count() - n0
     secs = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
     # Per-kernel durations: the same steps once more, every launch bracketed by a
     # CUDA event pair on its stream (the pairs add about 5% to a step, so the
@@ -285,6 +311,14 @@ def native(args, world, rank, local):
                 "units_per_launch": (f"{mean_pairs:.0f} (row, key) pairs x 4 contractions x 2 d flop"
                                      if top == "tc_attention" else None)}
     roofline["traffic"] = recorded_traffic(top, args.workload)
+    # Step-level roofline: the whole step's algorithmic bytes at the copy peak plus its
+    # contraction FLOP at the bf16 peak, against the measured step time.
+    state_bytes = w.B * R * w.H * w.d * (2 + 2 + 2 + 8) + w.B * R * w.H * 8 + w.B * w.H * w.N * 8
+    step_bytes = sum(v for v in hb.values() if v) + state_bytes
+    ideal_s = step_bytes / (peaks["hbm_gbs"] * 1e9) + flops_attn / (peaks["bf16_tflops"] * 1e12)
+    step_roofline = {"algorithmic_bytes": step_bytes, "algorithmic_flop": flops_attn,
+                     "ideal_us": ideal_s * 1e6, "measured_us": secs / args.steps * 1e6,
+                     "frac": ideal_s / (secs / args.steps)}
     for name, ent in kernels.items():
         ent["traffic"] = recorded_traffic(name, args.workload)
 
@@ -300,8 +334,9 @@ def native(args, world, rank, local):
                    "l2": "inputs larger than L2: each step reads two 134 MB hidden-state tensors",
                    "kernel_timing": "per-kernel durations from a second timed pass of the same steps with a CUDA "
                                     "event pair around every launch",
+                   "launch": launch_mode,
                    "active_tokens_per_s": w.B * R * args.steps * world / secs},
-        "roofline": roofline, "kernels": kernels, "gpu_launches": launches,
+        "roofline": roofline, "step_roofline": step_roofline, "kernels": kernels, "gpu_launches": launches,
         "clocks": clk, "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -473,6 +508,7 @@ def main():
     ap.add_argument("--workload", default="32k", choices=["tiny", "8k", "32k"])
     ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of replayed CUDA graphs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
