@@ -36,6 +36,21 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "lazy loop-step tokens/s at 32K prefill; % of tensor/HBM roofline on 1 B300"
+
+
+def metric_for(workload):
+    """The headline metric names the 32K prefill; other workloads say which they are."""
+    if workload == "32k":
+        return METRIC
+    if workload == "decode":
+        return "decode tokens/s (one new token per sequence through every loop); % of HBM roofline on 1 B300"
+    return f"lazy loop-step tokens/s at the {workload} workload; % of tensor/HBM roofline on 1 B300"
+
+
+def workload_text(w, R, K):
+    dense = "loop 1 dense" if w.T_dense == 1 else f"loops 1-{w.T_dense} dense"
+    return (f"{w.name} prefill lazy loop: B={w.B}, N={w.N}, H={w.H}, d={w.d}, T={w.T} ({dense}), "
+            f"r={float(w.r):.2f} (R={R}), k={float(w.k):.2f} (K={K})")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0}
 
 
@@ -325,11 +340,10 @@ def native(args, world, rank, local):
     e2e = None if args.no_e2e else e2e_leg(args, w, fl, cache, ws, loops, q_hat, o, z, c, act, keys, scores, lazy,
                                            dev, world)
     out = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric_for(args.workload), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{args.workload} prefill lazy loop: B={w.B}, N={w.N}, H={w.H}, d={w.d}, "
-                               f"T={w.T} (loop 1 dense), r={float(w.r):.2f} (R={R}), k={float(w.k):.2f} (K={K})",
+        "config": {"workload": workload_text(w, R, K),
                    "global_batch": w.B * world, "seq_len": w.N, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2: each step reads two 134 MB hidden-state tensors",
                    "kernel_timing": "per-kernel durations from a second timed pass of the same steps with a CUDA "
@@ -342,6 +356,131 @@ def native(args, world, rank, local):
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, R, K, state1, budget_s=args.cpu_budget)
     return out
+
+
+def native_decode(args, world, rank, local):
+    """Decode: a 16K-token context cache (bf16 base + one int4 delta layer per lazy
+    loop over a nested 25% of the tokens, written by the library's own append), then
+    one new token per sequence through every loop per step (loop 1 dense over all
+    keys, later loops lazy over the top-k columns). Steps reuse the same new-token
+    position; the loops' delta entries for it are rewritten in place."""
+    import lazy_sparse_attention_token_b300 as fl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synth.WORKLOADS["decode"]
+    ctx = synth.decode_context(w, device=dev)
+    R_ctx = ctx["loops"][2]["active"].shape[1]
+    Nk = w.N + 1
+    K = synth.key_count(w, Nk)
+    dims = fl.make_dims(w.B, Nk, w.H, w.d, R_ctx, K, w.T, w.T_dense, R_cap=R_ctx + 1)
+    cache = fl.Cache(dims, device=dev)
+    cache.n_tokens = w.N
+    ws = fl.workspace_for(dims, device=dev)
+    fl.flashloop_kv_dense_store(cache, 1, ctx["K1"], ctx["V1"])
+    for l in range(2, w.T + 1):
+        L = ctx["loops"][l]
+        fl.flashloop_kv_delta_append(cache, l, L["K"], L["V"], L["active"])
+    del ctx
+    cache.n_tokens = Nk
+    counts = [cache.c.count[m] for m in range(w.T - w.T_dense)]
+    toks = list(synth.decode_token_loops(w, device=dev))
+    q_hat = torch.zeros(w.B, 1, w.H, w.d, dtype=torch.bfloat16, device=dev)
+    o = torch.zeros(w.B, 1, w.H, w.d, dtype=torch.float32, device=dev)
+    z = torch.zeros(w.B, w.H, 1, dtype=torch.float32, device=dev)
+    c = torch.zeros(w.B, w.H, Nk, dtype=torch.float32, device=dev)
+    keys = torch.empty(w.B, w.H, K, dtype=torch.int32, device=dev)
+
+    def token_step():
+        for t in toks:
+            fl.flashloop_loop_step(cache, t["loop"], t["q"], t["k"], t["v"], q_hat, o, z, c, ws, key_idx=keys,
+                                   decode=True)
+        for m, n in enumerate(counts):   # the new token's entries go to the same slots next step
+            cache.c.count[m] = n
+
+    for _ in range(args.warmup):
+        token_step()
+    torch.cuda.synchronize()
+    assert fl.flashloop_device_status() == 0
+    graph, launch_mode = None, "direct launches"
+    if not args.no_graph:
+        try:
+            n_cap = fl.flashloop_launch_count()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                token_step()
+            launches_per_step = fl.flashloop_launch_count() - n_cap
+            graph.replay()
+            torch.cuda.synchronize()
+            assert fl.flashloop_device_status() == 0
+            launch_mode = "CUDA graph of one token step, replayed"
+        except Exception as exc:
+            graph, launch_mode = None, f"direct launches (graph capture failed: {str(exc)[:80]})"
+            torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    fl.flashloop_timing_read()
+    n0 = fl.flashloop_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0.record()
+    for _ in range(args.steps):
+        if graph is not None:
+            graph.replay()
+        else:
+            token_step()
+    ev1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    launches = launches_per_step * args.steps if graph is not None else fl.flashloop_launch_count() - n0
+    secs = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    fl.flashloop_timing_enable(True)
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        token_step()
+    torch.cuda.synchronize()
+    fl.flashloop_timing_enable(False)
+    per_kernel = fl.flashloop_timing_read()
+    assert fl.flashloop_device_status() == 0
+
+    peaks, peak_kind = load_peaks()
+    # decode attention reads, per (sequence, head), the K and V base rows of the keys it
+    # sees: all Nk in the dense loop, K in each lazy loop (delta entries not counted)
+    dense_bytes = w.B * w.H * Nk * w.d * 2 * 2
+    lazy_bytes = w.B * w.H * K * w.d * 2 * 2
+    kernels = {}
+    tot = sum(ms for ms, _ in per_kernel.values())
+    for name, (ms, n) in per_kernel.items():
+        ent = {"launches": n, "ms_per_launch": ms / max(1, n), "share": ms / tot if tot else None}
+        if name == "decode_attention":
+            per_launch = (w.T_dense * dense_bytes + (w.T - w.T_dense) * lazy_bytes) / w.T
+            ent.update(bound="hbm", unit="GB/s", bytes_per_launch=per_launch,
+                       achieved=per_launch / (ms / n / 1e3) / 1e9)
+            ent["frac"] = ent["achieved"] / peaks["hbm_gbs"]
+        kernels[name] = ent
+    top = max(kernels, key=lambda k: kernels[k]["share"] or 0)
+    tk = kernels[top]
+    roofline = {"kernel": top, "bound": tk.get("bound"), "achieved": tk.get("achieved"), "peak": peaks["hbm_gbs"],
+                "unit": tk.get("unit"), "frac": tk.get("frac"), "traffic": None,
+                "peak_source": f"{peak_kind} (copy)",
+                "units_per_launch": "base K/V rows of the keys each (sequence, head) attends to"}
+    value = w.B * args.steps * world / secs
+    return {
+        "metric": metric_for("decode"), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"decode: B={w.B}, {w.N}-token context + 1 new token, H={w.H}, d={w.d}, T={w.T} "
+                               f"(loop 1 dense), base + {w.T - w.T_dense} int4 delta layers over {R_ctx} tokens, "
+                               f"k={float(w.k):.2f} (K={K})",
+                   "global_batch": w.B * world, "seq_len": Nk, "parallelism": f"replicas x{world}",
+                   "step": "one new token per sequence through loops 1..T", "launch": launch_mode,
+                   "kernel_timing": "per-kernel durations from a second timed pass with a CUDA event pair "
+                                    "around every launch"},
+        "roofline": roofline, "kernels": kernels, "gpu_launches": launches, "clocks": clk, "e2e": None,
+    }
 
 
 def e2e_leg(args, w, fl, cache, ws, loops, q_hat, o, z, c, act, keys, scores, lazy, dev, world):
@@ -467,6 +606,9 @@ def reference(args, world, rank):
     """`--impl reference`: the CPU oracle as it stands, timed on the host cores."""
     if rank != 0:
         return None
+    if args.workload == "decode":
+        return {"impl": "reference", "unavailable": "the oracle's timed sample covers prefill lazy steps; "
+                                                   "decode is checked against the oracle for parity only"}
     import oracle
     oracle.build()
     w = synth.WORKLOADS[args.workload]
@@ -489,12 +631,11 @@ def reference(args, world, rank):
     sample = (f"per step: token scores, top-r and K/V delta append over all {w.N} tokens; key selection, "
               f"reconstruction and lazy attention on {n_heads} of {w.H} heads and {frac:.1%} of the {R} active "
               f"rows, scaled to the full step ({took:.1f} s measured over {args.steps} steps)")
-    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+    return {"impl": "reference", "metric": metric_for(args.workload), "value": value, "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{args.workload} prefill lazy loop: B={w.B}, N={w.N}, H={w.H}, d={w.d}, "
-                                   f"T={w.T} (loop 1 dense), r={float(w.r):.2f} (R={R}), k={float(w.k):.2f} (K={K})"},
+            "config": {"workload": workload_text(w, R, K)},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -505,7 +646,7 @@ def main():
     ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=30)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="32k", choices=["tiny", "8k", "32k"])
+    ap.add_argument("--workload", default="32k", choices=["tiny", "8k", "32k", "deep", "decode"])
     ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of replayed CUDA graphs")
@@ -522,7 +663,7 @@ def main():
             print(json.dumps(out), flush=True)
         return
     dist_init(world, "nccl")
-    out = native(args, world, rank, local)
+    out = native_decode(args, world, rank, local) if args.workload == "decode" else native(args, world, rank, local)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
