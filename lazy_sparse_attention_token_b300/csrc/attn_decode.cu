@@ -10,10 +10,16 @@
 // reconstructed (base + dequantised deltas, fp32, rounded to bf16) on the fly
 // instead of being materialised first.
 //
-// One CTA per (sequence, head, row). 16 groups of 16 lanes walk the key list;
-// a lane owns an 8-element chunk of d. Pass 1 stores the old and new logits
-// of every key in shared memory, the row statistics (m, lam) come from
-// block reductions, pass 2 accumulates u and w and updates the column mass.
+// One thread-block cluster per (sequence, head, row); its CTAs split the row's
+// key list into contiguous chunks, so a long list is streamed by several SMs.
+// In a CTA, 16 groups of 16 lanes walk the chunk, kU keys per group at a time:
+// all their base rows, then layer by layer all their slot lookups and then all
+// their delta codes are loaded together, so a key's chain of dependent loads
+// is shared by kU keys. Pass 1 keeps the chunk's old and new logits in shared
+// memory; the row statistics (old mass m, logsumexp lam) are merged across the
+// cluster through distributed shared memory; pass 2 accumulates u and w and
+// updates the column mass; the u and w partials are summed on cluster rank 0,
+// which updates the row's state.
 #include <float.h>
 #include <mutex>
 
@@ -24,6 +30,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kGroups = kThreads / 16;
+constexpr int kU = 4;              // keys per group per step
+constexpr int kMaxCluster = 8;
+constexpr int kKeysPerCta = 1024;  // a CTA per this many keys, up to kMaxCluster
 
 __device__ __forceinline__ float group16_sum(float v) {
     v += __shfl_xor_sync(0xffffffffu, v, 8);
@@ -55,8 +64,36 @@ __device__ float block_reduce(float v, float *red) {
     return v;
 }
 
+// ---- cluster helpers (distributed shared memory) --------------------------------
+__device__ __forceinline__ uint32_t cl_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cl_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cl_st_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cl_red_add_f32(uint32_t addr, float v) {
+    asm volatile("red.shared::cluster.add.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Every thread of every CTA of the cluster passes each of these.
+__device__ __forceinline__ void cl_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 struct DecKParams {
     int mode, H, n_keys, n_state, R, K, N_cap, R_cap;
+    int chunk;   // keys per CTA (shared-memory sizing)
     const int32_t *row_pos, *row_slot, *key_idx;
     const uint16_t *q;
     uint16_t *q_hat;
@@ -66,13 +103,70 @@ struct DecKParams {
     float scale;
 };
 
+// Reconstructions of kU cache rows (8-element chunk c8 of head h): `o` at the
+// old view (base + its delta layers), `n` at the new view (o + the new view's
+// further layers); deltas are added in ascending loop order in fp32. Loads
+// are issued in rounds shared by the kU rows: base rows, then per layer the
+// slot lookups and then the codes and scales.
+template <int D>
+__device__ __forceinline__ void load_rec(const DeltaView &ov, const DeltaView &nv, bool is_v, long long b,
+                                         const int (&j)[kU], int h, int c8, int H, int N_cap, int R_cap,
+                                         float (&o)[kU][8], float (&n)[kU][8]) {
+    const uint16_t *base = is_v ? ov.v_base : ov.k_base;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) load_base8(base, b, j[u], h, c8, H, D, N_cap, o[u]);
+    for (int m = 0; m < nv.n_layers; ++m) {
+        if (m == ov.n_layers) {
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) n[u][e] = o[u][e];
+        }
+        int ent[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) ent[u] = __ldg(nv.slot[m] + b * N_cap + j[u]);
+        const uint8_t *codes = is_v ? nv.v_codes[m] : nv.k_codes[m];
+        const uint16_t *scales = is_v ? nv.v_scales[m] : nv.k_scales[m];
+        uint32_t w[kU];
+        float s[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            w[u] = 0u;
+            s[u] = 0.f;
+            if (ent[u] >= 0) {
+                const long long e = (b * R_cap + ent[u]) * H + h;
+                w[u] = __ldg(reinterpret_cast<const uint32_t *>(codes + e * (D / 2)) + c8);
+                s[u] = __half2float(__ushort_as_half(__ldg(scales + e * (D / 32) + c8 / 4)));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (ent[u] < 0) continue;
+            float *r = m < ov.n_layers ? o[u] : n[u];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int qv = ((int)(w[u] << (28 - 4 * t))) >> 28;   // sign-extended nibble t
+                r[t] = __fadd_rn(r[t], __fmul_rn(s[u], (float)qv));
+            }
+        }
+    }
+    if (nv.n_layers <= ov.n_layers) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) n[u][e] = o[u][e];
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads)
 decode_attention_kernel(const __grid_constant__ DecKParams p) {
     extern __shared__ float sm[];
     constexpr int CH = D / 8;
-    const int row = blockIdx.x % p.R;
-    const long long bh = blockIdx.x / p.R;
+    const uint32_t ncta = cl_size(), rank = cl_rank();
+    const long long item = blockIdx.x / ncta;   // (sequence, head, row)
+    const int row = (int)(item % p.R);
+    const long long bh = item / p.R;
     const int h = (int)(bh % p.H);
     const long long b = bh / p.H;
     const bool dense = p.mode != FLASHLOOP_ATTN_LAZY;
@@ -80,9 +174,11 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
     const int pos = __ldg(p.row_pos + b * p.R + row);
     const int slot = p.row_slot ? __ldg(p.row_slot + b * p.R + row) : pos;
     const int32_t *S = dense ? nullptr : p.key_idx + bh * p.K;
-    int nk;
+    int nk;   // keys at or before the row: a prefix of the ascending list
     if (dense) {
         nk = min(pos + 1, p.n_keys);
+    } else if (__ldg(S + p.K - 1) <= pos) {
+        nk = p.K;
     } else {
         int lo = 0, hi = p.K;
         while (lo < hi) {
@@ -91,12 +187,19 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
         }
         nk = lo;
     }
-    if (nk == 0) return;   // no key at or before the row: state unchanged
+    if (nk == 0) return;   // no key at or before the row: state unchanged (the whole cluster)
 
-    float *sig = sm;                   // [nk] old logits (scaled)
-    float *tau = sm + nk;              // [nk] new logits (scaled)
-    float *red = sm + 2 * nk;          // [kThreads/32]
-    float *acc = red + kThreads / 32;  // [2][kGroups][D]
+    // this CTA's chunk of the key list
+    const int chunk = (nk + (int)ncta - 1) / (int)ncta;
+    const int k0 = min(nk, (int)rank * chunk), cn = min(nk, k0 + chunk) - k0;
+
+    int *idx = reinterpret_cast<int *>(sm);                  // [p.chunk] key positions (lazy)
+    float *sig = sm + p.chunk;                                // [p.chunk] old logits (scaled)
+    float *tau = sig + p.chunk;                               // [p.chunk] new logits (scaled)
+    float *red = tau + p.chunk;                               // [kThreads/32]
+    float *acc = red + kThreads / 32;                         // [2][kGroups][D]
+    float *stats = acc + 2 * kGroups * D;                     // [kMaxCluster][3] (mx, ls, ms) of every rank
+    float *uw = stats + kMaxCluster * 3;                      // [2][D] cluster sums of u, w (rank 0)
 
     const int grp = threadIdx.x >> 4, gl = threadIdx.x & 15;
     const bool has_chunk = gl < CH;
@@ -105,105 +208,157 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
     float qn[8], qo[8];
     unpack_bf16x8(ldg_nc_v4(p.q + srow + c8 * 8), qn);
     if (!first) unpack_bf16x8(ldg_nc_v4(p.q_hat + srow + c8 * 8), qo);
+    if (!dense)
+        for (int t = threadIdx.x; t < cn; t += kThreads) idx[t] = __ldg(S + k0 + t);
+    if (rank == 0)
+        for (int x = threadIdx.x; x < 2 * D; x += kThreads) uw[x] = 0.f;
+    __syncthreads();
+    auto key_at = [&](int t) { return dense ? k0 + t : idx[t]; };
 
-    // pass 1: logits of every key in the list. Both 16-lane groups of a warp
-    // run the same number of iterations (a group past the end recomputes
-    // key 0 and stores nothing) because the sums below shuffle across the
-    // whole warp.
-    for (int t0 = 0; t0 < nk; t0 += kGroups) {
-        const int t = t0 + grp;
-        const bool tv = t < nk;
-        const int j = dense ? (tv ? t : 0) : __ldg(S + (tv ? t : 0));
-        float kn[8], ko[8];
-        float so = 0.f, sn = 0.f;
+    // pass 1: logits of the chunk's keys. Both 16-lane groups of a warp run the
+    // same number of steps (keys past the end recompute the chunk's first key and
+    // store nothing) because the sums below shuffle across the whole warp.
+    for (int t0 = 0; t0 < cn; t0 += kGroups * kU) {
+        int jj[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int t = t0 + u * kGroups + grp;
+            jj[u] = key_at(t < cn ? t : 0);
+        }
+        float kn[kU][8], ko[kU][8];
         if (p.shared_base) {
-            load_base8(p.old_view.k_base, b, j, h, c8, p.H, D, p.N_cap, ko);
-            apply_deltas(p.old_view, false, 0, p.old_view.n_layers, b, j, h, c8, p.H, D, p.N_cap, p.R_cap, ko);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) kn[e] = ko[e];
-            apply_deltas(p.new_view, false, p.old_view.n_layers, p.new_view.n_layers, b, j, h, c8, p.H, D, p.N_cap,
-                         p.R_cap, kn);
+            load_rec<D>(p.old_view, p.new_view, false, b, jj, h, c8, p.H, p.N_cap, p.R_cap, ko, kn);
         } else {
-            load_base8(p.new_view.k_base, b, j, h, c8, p.H, D, p.N_cap, kn);
-            if (!first) load_base8(p.old_view.k_base, b, j, h, c8, p.H, D, p.N_cap, ko);
-        }
-        round_bf16x8(kn);
-        if (!first) round_bf16x8(ko);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            sn = fmaf(qn[e], kn[e], sn);
-            if (!first) so = fmaf(qo[e], ko[e], so);
+            for (int u = 0; u < kU; ++u) {
+                load_base8(p.new_view.k_base, b, jj[u], h, c8, p.H, D, p.N_cap, kn[u]);
+                if (!first) load_base8(p.old_view.k_base, b, jj[u], h, c8, p.H, D, p.N_cap, ko[u]);
+            }
         }
-        if (!has_chunk) sn = so = 0.f;
-        sn = group16_sum(sn);
-        so = group16_sum(so);
-        if (tv && gl == 0) {
-            tau[t] = sn * p.scale;
-            sig[t] = so * p.scale;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            round_bf16x8(kn[u]);
+            if (!first) round_bf16x8(ko[u]);
+            float so = 0.f, sn = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                sn = fmaf(qn[e], kn[u][e], sn);
+                if (!first) so = fmaf(qo[e], ko[u][e], so);
+            }
+            if (!has_chunk) sn = so = 0.f;
+            sn = group16_sum(sn);
+            so = group16_sum(so);
+            const int t = t0 + u * kGroups + grp;
+            if (t < cn && gl == 0) {
+                tau[t] = sn * p.scale;
+                sig[t] = so * p.scale;
+            }
         }
     }
     __syncthreads();
 
-    // row statistics
+    // row statistics of the chunk, then of the row (merged over the cluster)
     const float zo = first ? 0.f : __ldg(p.z + bh * p.n_state + slot);
-    float mx = -INFINITY, ms = 0.f;
-    for (int t = threadIdx.x; t < nk; t += kThreads) {
-        mx = fmaxf(mx, tau[t]);
+    float mx = -INFINITY;
+    for (int t = threadIdx.x; t < cn; t += kThreads) mx = fmaxf(mx, tau[t]);
+    mx = block_reduce<true>(mx, red);
+    float ls = 0.f, ms = 0.f;
+    for (int t = threadIdx.x; t < cn; t += kThreads) {
+        ls += mx > -INFINITY ? expf(tau[t] - mx) : 0.f;
         if (!first) ms += expf(sig[t] - zo);
     }
-    mx = block_reduce<true>(mx, red);
-    const float m = first ? 1.f : block_reduce<false>(ms, red);
-    float ls = 0.f;
-    for (int t = threadIdx.x; t < nk; t += kThreads) ls += expf(tau[t] - mx);
     ls = block_reduce<false>(ls, red);
-    const float lam = mx + logf(ls);
-    if (!first && !(m >= FLT_MIN)) return;   // old mass underflowed: keep the row's state
+    ms = first ? 0.f : block_reduce<false>(ms, red);
+    if (ncta > 1) {
+        if (threadIdx.x < ncta) {
+            cl_st_f32(cl_map(&stats[rank * 3 + 0], threadIdx.x), mx);
+            cl_st_f32(cl_map(&stats[rank * 3 + 1], threadIdx.x), ls);
+            cl_st_f32(cl_map(&stats[rank * 3 + 2], threadIdx.x), ms);
+        }
+        cl_sync();
+    } else {
+        if (threadIdx.x == 0) {
+            stats[0] = mx;
+            stats[1] = ls;
+            stats[2] = ms;
+        }
+        __syncthreads();
+    }
+    float gmx = -INFINITY, gls = 0.f, m = 0.f;
+    for (uint32_t r = 0; r < ncta; ++r) gmx = fmaxf(gmx, stats[r * 3]);
+    for (uint32_t r = 0; r < ncta; ++r) {
+        if (stats[r * 3] > -INFINITY) gls += stats[r * 3 + 1] * expf(stats[r * 3] - gmx);
+        m += stats[r * 3 + 2];
+    }
+    if (first) m = 1.f;
+    const float lam = gmx + logf(gls);
+    if (!first && !(m >= FLT_MIN)) return;   // old mass underflowed: keep the row's state (the whole cluster)
 
-    // pass 2: u = sum p v_old, w = sum a v_new, column mass
-    float u[8] = {0, 0, 0, 0, 0, 0, 0, 0}, w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    // pass 2: u = sum p v_old, w = sum a v_new over the chunk, column mass
+    float u_[8] = {0, 0, 0, 0, 0, 0, 0, 0}, w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float *cb = p.c + bh * p.n_keys;
-    for (int t = grp; t < nk; t += kGroups) {
-        const int j = dense ? t : __ldg(S + t);
-        const float a = expf(tau[t] - lam);
-        const float pj = first ? 0.f : expf(sig[t] - zo);
-        float vn[8], vo[8];
+    for (int t0 = 0; t0 < cn; t0 += kGroups * kU) {
+        int jj[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int t = t0 + u * kGroups + grp;
+            jj[u] = key_at(t < cn ? t : 0);
+        }
+        float vn[kU][8], vo[kU][8];
         if (p.shared_base) {
-            load_base8(p.old_view.v_base, b, j, h, c8, p.H, D, p.N_cap, vo);
-            apply_deltas(p.old_view, true, 0, p.old_view.n_layers, b, j, h, c8, p.H, D, p.N_cap, p.R_cap, vo);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) vn[e] = vo[e];
-            apply_deltas(p.new_view, true, p.old_view.n_layers, p.new_view.n_layers, b, j, h, c8, p.H, D, p.N_cap,
-                         p.R_cap, vn);
+            load_rec<D>(p.old_view, p.new_view, true, b, jj, h, c8, p.H, p.N_cap, p.R_cap, vo, vn);
         } else {
-            load_base8(p.new_view.v_base, b, j, h, c8, p.H, D, p.N_cap, vn);
-            if (!first) load_base8(p.old_view.v_base, b, j, h, c8, p.H, D, p.N_cap, vo);
-        }
-        round_bf16x8(vn);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = fmaf(a, vn[e], w[e]);
-        if (!first) {
-            round_bf16x8(vo);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) u[e] = fmaf(pj, vo[e], u[e]);
+            for (int u = 0; u < kU; ++u) {
+                load_base8(p.new_view.v_base, b, jj[u], h, c8, p.H, D, p.N_cap, vn[u]);
+                if (!first) load_base8(p.old_view.v_base, b, jj[u], h, c8, p.H, D, p.N_cap, vo[u]);
+            }
         }
-        if (gl == 0) atomicAdd(cb + j, m * a - pj);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int t = t0 + u * kGroups + grp;
+            if (t >= cn) continue;
+            const float a = expf(tau[t] - lam);
+            const float pj = first ? 0.f : expf(sig[t] - zo);
+            round_bf16x8(vn[u]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = fmaf(a, vn[u][e], w[e]);
+            if (!first) {
+                round_bf16x8(vo[u]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) u_[e] = fmaf(pj, vo[u][e], u_[e]);
+            }
+            if (gl == 0) atomicAdd(cb + jj[u], m * a - pj);
+        }
     }
     if (has_chunk) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            acc[grp * D + c8 * 8 + e] = u[e];
+            acc[grp * D + c8 * 8 + e] = u_[e];
             acc[(kGroups + grp) * D + c8 * 8 + e] = w[e];
         }
     }
     __syncthreads();
+    // the chunk's u and w, summed over the groups, into rank 0's cluster sums
     for (int x = threadIdx.x; x < D; x += kThreads) {
         float us = 0.f, ws = 0.f;
         for (int g = 0; g < kGroups; ++g) {
             us += acc[g * D + x];
             ws += acc[(kGroups + g) * D + x];
         }
+        if (ncta > 1) {
+            cl_red_add_f32(cl_map(&uw[x], 0), us);
+            cl_red_add_f32(cl_map(&uw[D + x], 0), ws);
+        } else {
+            uw[x] = us;
+            uw[D + x] = ws;
+        }
+    }
+    if (ncta > 1) cl_sync(); else __syncthreads();
+    if (rank != 0) return;
+    for (int x = threadIdx.x; x < D; x += kThreads) {
         const float prev = first ? 0.f : p.o[srow + x];
-        p.o[srow + x] = prev - us + m * ws;
+        p.o[srow + x] = prev - uw[x] + m * uw[D + x];
         p.q_hat[srow + x] = p.q[srow + x];
     }
     if (threadIdx.x == 0) p.z[bh * p.n_state + slot] = lam - logf(m);
@@ -211,8 +366,10 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
 
 template <int D>
 cudaError_t launch_d(const DecodeAttnParams &q, cudaStream_t s) {
-    int nk_max = q.mode == FLASHLOOP_ATTN_LAZY ? q.K : q.n_keys;
-    const size_t smem = (size_t)(2 * nk_max + kThreads / 32 + 2 * kGroups * D) * sizeof(float);
+    const int nk_max = q.mode == FLASHLOOP_ATTN_LAZY ? q.K : q.n_keys;
+    const int ncta = max(1, min(kMaxCluster, (nk_max + kKeysPerCta - 1) / kKeysPerCta));
+    const int chunk = (nk_max + ncta - 1) / ncta;
+    const size_t smem = (size_t)(3 * chunk + kThreads / 32 + 2 * kGroups * D + kMaxCluster * 3 + 2 * D) * sizeof(float);
     if (smem > 220 * 1024) return cudaErrorInvalidValue;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -227,6 +384,7 @@ cudaError_t launch_d(const DecodeAttnParams &q, cudaStream_t s) {
     p.K = q.K;
     p.N_cap = q.N_cap;
     p.R_cap = q.R_cap;
+    p.chunk = chunk;
     p.row_pos = q.row_pos;
     p.row_slot = q.row_slot;
     p.key_idx = q.key_idx;
@@ -239,12 +397,25 @@ cudaError_t launch_d(const DecodeAttnParams &q, cudaStream_t s) {
     p.new_view = q.new_view;
     p.shared_base = q.mode == FLASHLOOP_ATTN_LAZY;
     p.scale = 1.0f / sqrtf((float)D);
-    const long long grid = (long long)q.B * q.H * q.R;
+    const long long grid = (long long)q.B * q.H * q.R * ncta;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ncta;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
     {
         KernelTimer kt("decode_attention", s);
-        decode_attention_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(p);
+        e = cudaLaunchKernelEx(&cfg, decode_attention_kernel<D>, p);
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -68,7 +68,8 @@ token_scores_kernel(const uint16_t *__restrict__ h_prev, const uint16_t *__restr
 // uint32 key is found by four 8-bit radix passes (most significant digit
 // first); then the keys above it, and the first (lowest-index) ones equal to
 // it, are written in ascending index order. A row is split over a cluster of
-// kTopkCluster CTAs (one row alone would otherwise run on a single SM): each
+// up to kTopkCluster CTAs (one row alone would otherwise run on a single SM;
+// with many rows, one CTA per row already fills the GPU): each
 // CTA histograms its own contiguous segment and adds the histogram into a
 // fresh one on cluster rank 0 (distributed shared memory); after one cluster
 // barrier every rank reads the merged histogram and takes the same digit. The
@@ -76,11 +77,17 @@ token_scores_kernel(const uint16_t *__restrict__ h_prev, const uint16_t *__restr
 constexpr int kTopkCluster = 8;
 constexpr int kTopkClThreads = 512;
 constexpr int kTopkClWarps = kTopkClThreads / 32;
-constexpr int kTopkClStageMax = 24 * 1024;   // keys per CTA staged in shared memory (96 KB)
+constexpr int kTopkClStageMax = 48 * 1024;   // keys per CTA staged in shared memory (192 KB)
+constexpr int kTopkRowsForSingle = 128;      // with this many rows, one CTA per row fills the GPU
 
 __device__ __forceinline__ uint32_t cl_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cl_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
     return r;
 }
 __device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank) {
@@ -118,12 +125,12 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
     __shared__ unsigned long long warp_tot[kTopkClWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t rank = cl_rank();
-    const int row_id = blockIdx.x / kTopkCluster;
+    const uint32_t rank = cl_rank(), ncta = cl_size();
+    const int row_id = blockIdx.x / ncta;
     const float *row = vals + (size_t)row_id * n;
     int32_t *orow = out + (size_t)row_id * k;
     // this CTA's segment of the row, a multiple of 32 keys
-    const int seg = ((n + kTopkCluster - 1) / kTopkCluster + 31) & ~31;
+    const int seg = ((n + (int)ncta - 1) / (int)ncta + 31) & ~31;
     const int lo = min(n, (int)rank * seg), hi = min(n, lo + seg), len = hi - lo;
 
     if (rank == 0)
@@ -251,7 +258,8 @@ cudaError_t launch_token_scores(const uint16_t *h_prev, const uint16_t *h_cur, i
 
 cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t *out, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    const int seg = ((n + kTopkCluster - 1) / kTopkCluster + 31) & ~31;
+    const int ncta = rows >= kTopkRowsForSingle ? 1 : kTopkCluster;
+    const int seg = ((n + ncta - 1) / ncta + 31) & ~31;
     const bool staged = seg <= kTopkClStageMax;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -259,13 +267,13 @@ cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t 
                              kTopkClStageMax * 4);
     });
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(rows * kTopkCluster));
+    cfg.gridDim = dim3((unsigned)(rows * ncta));
     cfg.blockDim = dim3(kTopkClThreads);
     cfg.dynamicSmemBytes = staged ? (size_t)seg * 4 : 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kTopkCluster;
+    attr[0].val.clusterDim.x = (unsigned)ncta;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
