@@ -147,7 +147,11 @@ typedef struct {
  * active tokens, select_keys on c, and lazy attention. `decode` = 1 runs the
  * same loop for ONE new token per sequence at key position cache->n_tokens-1
  * (the caller counts it in n_tokens before loop 1): state arrays then have
- * one row, the token is always active, and h_prev/h_cur are unused. */
+ * one row, the token is always active, and h_prev/h_cur are unused.
+ * In a lazy prefill loop the key selection runs on a library-owned stream
+ * forked from `stream` with an event and joined back to it before the
+ * attention, so every piece of the loop is ordered on `stream` as usual (and
+ * the call can be captured into a CUDA graph from `stream`). */
 typedef struct {
     int32_t loop;
     int32_t decode;

@@ -111,6 +111,32 @@ flashloop_status_t check_device() {
     return FLASHLOOP_OK;
 }
 
+// A second stream per device for work of one loop that may overlap the
+// caller's stream (the key selection of a lazy prefill loop), forked from and
+// joined back to that stream with two events. The mutex is held while one
+// call enqueues its fork and join; the stream and events live until exit.
+struct SideStream {
+    std::mutex mu;
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool ok = false;
+};
+constexpr int kMaxSideDevices = 64;
+
+static SideStream *side_stream() {
+    static SideStream side[kMaxSideDevices];
+    static std::once_flag once[kMaxSideDevices];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return nullptr;
+    SideStream &ss = side[dev];
+    std::call_once(once[dev], [&ss] {
+        ss.ok = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) == cudaSuccess &&
+                cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) == cudaSuccess &&
+                cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) == cudaSuccess;
+    });
+    return ss.ok ? &ss : nullptr;
+}
+
 static bool head_dim_ok(int d) { return d == 64 || d == 96 || d == 128; }
 
 static flashloop_status_t check_dims(const flashloop_dims_t *dm) {
@@ -581,13 +607,31 @@ flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop
     if (!a->h_prev || !a->h_cur || !a->active_idx || !a->key_idx)
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "lazy loop needs h_prev, h_cur, active_idx and key_idx");
     float *scores = a->scores ? a->scores : reinterpret_cast<float *>(ws + W.scores);
-    if ((st = flashloop_select_tokens(a->h_prev, a->h_cur, dm.B, n, dm.H * dm.d, dm.R, a->active_idx, scores,
-                                      nullptr, 0, stream)) != FLASHLOOP_OK)
-        return st;
-    if ((st = flashloop_kv_delta_append(c, l, a->k, a->v, 1, a->active_idx, dm.R, 0, stream)) != FLASHLOOP_OK)
-        return st;
-    if ((st = flashloop_select_keys(a->c, dm.B, dm.H, n, dm.K, a->key_idx, nullptr, 0, stream)) != FLASHLOOP_OK)
-        return st;
+    // The key columns depend only on the previous loop's column mass, so their
+    // selection runs on a side stream while the token selection and the K/V
+    // delta append run on the caller's; the attention waits for both.
+    SideStream *ss = side_stream();
+    std::unique_lock<std::mutex> side_lock;
+    flashloop_stream_t key_stream = stream;
+    if (ss) {
+        side_lock = std::unique_lock<std::mutex>(ss->mu);
+        cudaError_t e = cudaEventRecord(ss->fork, static_cast<cudaStream_t>(stream));
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "fork of the key selection");
+        key_stream = ss->s;
+    }
+    st = flashloop_select_keys(a->c, dm.B, dm.H, n, dm.K, a->key_idx, nullptr, 0, key_stream);
+    if (st == FLASHLOOP_OK)
+        st = flashloop_select_tokens(a->h_prev, a->h_cur, dm.B, n, dm.H * dm.d, dm.R, a->active_idx, scores,
+                                     nullptr, 0, stream);
+    if (st == FLASHLOOP_OK) st = flashloop_kv_delta_append(c, l, a->k, a->v, 1, a->active_idx, dm.R, 0, stream);
+    if (ss) {   // join (also on failure, so that the caller's stream is never left forked)
+        cudaError_t e = cudaEventRecord(ss->join, ss->s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), ss->join, 0);
+        side_lock.unlock();
+        if (e != cudaSuccess && st == FLASHLOOP_OK) return cuda_fail(e, "join of the key selection");
+    }
+    if (st != FLASHLOOP_OK) return st;
     at.R = dm.R;
     at.row_pos = a->active_idx;
     at.K = dm.K;
