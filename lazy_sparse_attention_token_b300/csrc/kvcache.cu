@@ -46,8 +46,11 @@ store_rows_kernel(const uint4 *__restrict__ src, int n_rows, int vecs, uint4 *__
     for (int v = threadIdx.x & 31; v < vecs; v += 32) d[v] = ldg_nc_v4(s + v);
 }
 
-// One thread per (sequence, entry, head, 8-element chunk); four neighbouring
-// lanes cover one 32-element quantisation group. blockIdx.y: 0 = K, 1 = V.
+// One thread per (sequence, entry, head, 32-element quantisation group): the
+// group's four 8-element chunks of the loop-l row and of the base row are
+// loaded together, each earlier delta layer costs one slot lookup, one
+// 16-byte codes load and one scale load for the whole group, and the group's
+// 32 codes (16 bytes) go out in one store. blockIdx.y: 0 = K, 1 = V.
 __global__ void __launch_bounds__(256)
 delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint16_t *__restrict__ v_l,
                     int rows_are_tokens, int src_rows, const int32_t *__restrict__ active, int R, int at,
@@ -55,15 +58,12 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
                     int32_t *__restrict__ out_slot, uint8_t *__restrict__ k_codes,
                     uint16_t *__restrict__ k_scales, uint8_t *__restrict__ v_codes,
                     uint16_t *__restrict__ v_scales) {
-    const long long t_raw = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const bool in_range = t_raw < total;
-    // Lanes past the end redo the last element (no stores) so that every lane
-    // of the warp takes part in the group-max shuffles below.
-    const long long t = in_range ? t_raw : total - 1;
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= total) return;
     const bool is_v = blockIdx.y == 1;
-    const int chunks = d / 8;
-    const int c8 = (int)(t % chunks);
-    const long long rest = t / chunks;
+    const int gpr = d / 32;   // quantisation groups per (row, head)
+    const int g = (int)(t % gpr);
+    const long long rest = t / gpr;
     const int h = (int)(rest % H);
     const long long be = rest / H;   // b * R + e
     const long long b = be / R;
@@ -71,40 +71,67 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
     const int i = __ldg(active + be);
     const long long src_row = rows_are_tokens ? (long long)i : (long long)e;
 
-    const uint16_t *x_l = is_v ? v_l : k_l;
-    float x[8], rec[8];
-    unpack_bf16x8(ldg_nc_v4(x_l + ((b * src_rows + src_row) * H + h) * (long long)d + c8 * 8), x);
-    load_base8(is_v ? view.v_base : view.k_base, b, i, h, c8, H, d, N_cap, rec);
-    apply_deltas(view, is_v, 0, view.n_layers, b, i, h, c8, H, d, N_cap, R_cap, rec);
-
-    float dl[8], amax = 0.f;
+    const uint16_t *x_l = (is_v ? v_l : k_l) + ((b * src_rows + src_row) * H + h) * (long long)d + g * 32;
+    const uint16_t *base = (is_v ? view.v_base : view.k_base) + ((b * N_cap + i) * H + h) * (long long)d + g * 32;
+    uint4 xv[4], bv[4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        dl[u] = __fsub_rn(x[u], rec[u]);
-        amax = fmaxf(amax, fabsf(dl[u]));
+    for (int c = 0; c < 4; ++c) xv[c] = ldg_nc_v4(x_l + c * 8);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bv[c] = ldg_nc_v4(base + c * 8);
+    float x[32], rec[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        unpack_bf16x8(xv[c], x + 8 * c);
+        unpack_bf16x8(bv[c], rec + 8 * c);
     }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    // the previous loop's reconstruction: base plus each earlier layer's deltas, in order
+    for (int m = 0; m < view.n_layers; ++m) {
+        const int en = __ldg(view.slot[m] + b * N_cap + i);
+        if (en < 0) continue;
+        const long long ent = (b * R_cap + en) * H + h;
+        const uint8_t *codes = is_v ? view.v_codes[m] : view.k_codes[m];
+        const uint16_t *scales = is_v ? view.v_scales[m] : view.k_scales[m];
+        const uint4 w4 = __ldg(reinterpret_cast<const uint4 *>(codes + ent * (d / 2) + g * 16));
+        const float sc = __half2float(__ushort_as_half(__ldg(scales + ent * (d / 32) + g)));
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int qv = ((int)(w[c] << (28 - 4 * k))) >> 28;   // sign-extended nibble k
+                rec[8 * c + k] = __fadd_rn(rec[8 * c + k], __fmul_rn(sc, (float)qv));
+            }
+    }
+
+    float amax = 0.f;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+        x[u] = __fsub_rn(x[u], rec[u]);   // the delta
+        amax = fmaxf(amax, fabsf(x[u]));
+    }
     const __half sh = __float2half_rn(__fdiv_rn(amax, 7.0f));   // the scale is exact: fp16(fp32(amax / 7))
     const float s = __half2float(sh);
     // code = rint(delta / scale): the quotient is taken as delta * (1 / scale), within
     // about one ulp of the divided one, so a code can only differ where the quotient
     // lies within ~1e-6 of a rounding boundary (n + 1/2)
     const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
-    uint32_t packed = 0;
+    uint32_t packed[4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const float r = rintf(dl[u] * inv);
-        const int q = (int)fminf(7.f, fmaxf(-7.f, r));
-        packed |= (uint32_t)(q & 0xF) << (4 * u);
+    for (int c = 0; c < 4; ++c) {
+        packed[c] = 0u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float r = rintf(x[8 * c + k] * inv);
+            const int q = (int)fminf(7.f, fmaxf(-7.f, r));
+            packed[c] |= (uint32_t)(q & 0xF) << (4 * k);
+        }
     }
-    if (!in_range) return;
     const long long ent = (b * R_cap + at + e) * H + h;
     uint8_t *codes = is_v ? v_codes : k_codes;
     uint16_t *scales = is_v ? v_scales : k_scales;
-    reinterpret_cast<uint32_t *>(codes + ent * (d / 2))[c8] = packed;
-    if ((c8 & 3) == 0) scales[ent * (d / 32) + c8 / 4] = __half_as_ushort(sh);
-    if (!is_v && h == 0 && c8 == 0) {
+    *reinterpret_cast<uint4 *>(codes + ent * (d / 2) + g * 16) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    scales[ent * (d / 32) + g] = __half_as_ushort(sh);
+    if (!is_v && h == 0 && g == 0) {
         out_idx[b * R_cap + at + e] = i;
         out_slot[b * N_cap + i] = at + e;
     }
@@ -177,7 +204,7 @@ cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, cons
                                 int B, int N_cap, int H, int d, int R_cap, int32_t *out_idx,
                                 int32_t *out_slot, uint8_t *k_codes, uint16_t *k_scales, uint8_t *v_codes,
                                 uint16_t *v_scales, cudaStream_t s) {
-    const long long total = (long long)B * R * H * (d / 8);
+    const long long total = (long long)B * R * H * (d / 32);
     if (total == 0) return cudaSuccess;
     dim3 grid(ceil_div(total, 256), 2);
     {
