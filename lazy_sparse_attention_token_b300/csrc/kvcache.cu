@@ -137,9 +137,21 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
     }
 }
 
+// 32 fp32 values as bf16 (RNE), four 16-byte stores.
+__device__ __forceinline__ void store_group_bf16(const float (&rec)[32], uint16_t *dst) {
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        d4[c] = make_uint4(pack_bf16x2_rn(rec[8 * c + 0], rec[8 * c + 1]), pack_bf16x2_rn(rec[8 * c + 2], rec[8 * c + 3]),
+                           pack_bf16x2_rn(rec[8 * c + 4], rec[8 * c + 5]), pack_bf16x2_rn(rec[8 * c + 6], rec[8 * c + 7]));
+}
+
 // For each selected key j = key_idx[b,h,r]: reconstruction at the old loop
 // (old_layers deltas) and at the new loop (new_layers deltas), bf16 RNE,
-// written densely as [B, H, K, d]. blockIdx.y: 0 = K, 1 = V.
+// written densely as [B, H, K, d]. One thread per 32-element group of a
+// selected row: its four base chunks load together and each delta layer is
+// one slot lookup, one 16-byte codes load and one scale load for the group.
+// blockIdx.y: 0 = K, 1 = V.
 __global__ void __launch_bounds__(256)
 reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const int32_t *__restrict__ key_idx,
                         int H, int K, int d, int N_cap, int R_cap, long long total,
@@ -148,28 +160,40 @@ reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const in
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= total) return;
     const bool is_v = blockIdx.y == 1;
-    const int chunks = d / 8;
-    const int c8 = (int)(t % chunks);
-    const long long bhr = t / chunks;          // (b * H + h) * K + r
+    const int gpr = d / 32;
+    const int g = (int)(t % gpr);
+    const long long bhr = t / gpr;          // (b * H + h) * K + r
     const long long bh = bhr / K;
     const int h = (int)(bh % H);
     const long long b = bh / H;
     const int j = __ldg(key_idx + bhr);
-    float rec[8];
-    load_base8(is_v ? view.v_base : view.k_base, b, j, h, c8, H, d, N_cap, rec);
-    apply_deltas(view, is_v, 0, old_layers, b, j, h, c8, H, d, N_cap, R_cap, rec);
-    uint4 o;
-    o.x = pack_bf16x2_rn(rec[0], rec[1]);
-    o.y = pack_bf16x2_rn(rec[2], rec[3]);
-    o.z = pack_bf16x2_rn(rec[4], rec[5]);
-    o.w = pack_bf16x2_rn(rec[6], rec[7]);
-    reinterpret_cast<uint4 *>((is_v ? v_old : k_old) + bhr * d)[c8] = o;
-    apply_deltas(view, is_v, old_layers, new_layers, b, j, h, c8, H, d, N_cap, R_cap, rec);
-    o.x = pack_bf16x2_rn(rec[0], rec[1]);
-    o.y = pack_bf16x2_rn(rec[2], rec[3]);
-    o.z = pack_bf16x2_rn(rec[4], rec[5]);
-    o.w = pack_bf16x2_rn(rec[6], rec[7]);
-    reinterpret_cast<uint4 *>((is_v ? v_new : k_new) + bhr * d)[c8] = o;
+    const uint16_t *base = (is_v ? view.v_base : view.k_base) + ((b * N_cap + j) * H + h) * (long long)d + g * 32;
+    uint4 bv[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bv[c] = ldg_nc_v4(base + c * 8);
+    float rec[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) unpack_bf16x8(bv[c], rec + 8 * c);
+    for (int m = 0; m < new_layers; ++m) {
+        if (m == old_layers) store_group_bf16(rec, (is_v ? v_old : k_old) + bhr * d + g * 32);
+        const int en = __ldg(view.slot[m] + b * N_cap + j);
+        if (en < 0) continue;
+        const long long ent = (b * R_cap + en) * H + h;
+        const uint8_t *codes = is_v ? view.v_codes[m] : view.k_codes[m];
+        const uint16_t *scales = is_v ? view.v_scales[m] : view.k_scales[m];
+        const uint4 w4 = __ldg(reinterpret_cast<const uint4 *>(codes + ent * (d / 2) + g * 16));
+        const float sc = __half2float(__ushort_as_half(__ldg(scales + ent * (d / 32) + g)));
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int qv = ((int)(w[c] << (28 - 4 * k))) >> 28;   // sign-extended nibble k
+                rec[8 * c + k] = __fadd_rn(rec[8 * c + k], __fmul_rn(sc, (float)qv));
+            }
+    }
+    if (new_layers <= old_layers) store_group_bf16(rec, (is_v ? v_old : k_old) + bhr * d + g * 32);
+    store_group_bf16(rec, (is_v ? v_new : k_new) + bhr * d + g * 32);
 }
 
 }  // namespace
@@ -220,7 +244,7 @@ cudaError_t launch_reconstruct_keys(const DeltaView &old_view, const DeltaView &
                                     const int32_t *key_idx, int B, int H, int K, int N_cap, int d,
                                     int R_cap, uint16_t *k_old, uint16_t *v_old, uint16_t *k_new,
                                     uint16_t *v_new, cudaStream_t s) {
-    const long long total = (long long)B * H * K * (d / 8);
+    const long long total = (long long)B * H * K * (d / 32);
     if (total == 0) return cudaSuccess;
     dim3 grid(ceil_div(total, 256), 2);
     {
