@@ -145,8 +145,7 @@ __device__ __forceinline__ void load_rec(const DeltaView &ov, const DeltaView &n
             float *r = m < ov.n_layers ? o[u] : n[u];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                const int qv = ((int)(w[u] << (28 - 4 * t))) >> 28;   // sign-extended nibble t
-                r[t] = __fadd_rn(r[t], __fmul_rn(s[u], (float)qv));
+                r[t] = __fadd_rn(r[t], __fmul_rn(s[u], code_f32(w[u], t)));
             }
         }
     }

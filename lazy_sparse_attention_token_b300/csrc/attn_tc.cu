@@ -63,6 +63,7 @@ constexpr int BN = 128;
 constexpr int BN_ = BN;
 constexpr int kThreads = 608;     // warp 0 TMA, warp 1 QK MMAs, warp 2 PV MMAs, warps 3..18 softmax (4 x 4)
 constexpr int kFirstSoftmaxWarp = 3;
+constexpr int kSetupBar = 1;      // named barrier of the set-up (0 is __syncthreads)
 constexpr int kGroups = 4;        // softmax groups, each owns 32 of a tile's 128 columns
 constexpr int kGroupCols = BN_ / kGroups;
 constexpr int kSoftmaxWarps = 4 * kGroups;   // softmax-side barriers take one elected arrival per warp
@@ -284,19 +285,27 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const bool row_ok = is_sm && r < rows;
     const int pos = row_ok ? (dense ? row0 + r : __ldg(A + r)) : -1;
     const int st = (int)threadIdx.x - 32 * kFirstSoftmaxWarp;   // softmax thread index
-    if (is_sm) {   // pass OLD reads qhat; the first dense loop starts with q
-        load_query_tile<D>(smem + C::OFF_Q, first ? p.q : p.q_hat, st, b, h, p.H, p.n_state, rows, row0, A);
-        fence_proxy_async_smem();
-        if (wg == 0) {   // per row, shared by the four groups: key count and old normaliser (log2 units)
-            row_cnt[r] = !row_ok ? 0 : cnt_min == cnt ? cnt : dense ? min(pos + 1, p.n_keys) : __ldg(RC + r);
-            row_zo[r] = !row_ok ? INFINITY : first ? 0.f : __ldg(p.z + bh * p.n_state + pos) * kLog2e;
-            row_pos_s[r] = pos;
+    // The producer needs only the barriers, so it arrives on the set-up barrier
+    // without waiting and starts the K/V copies while the other warps wait for
+    // the query tile and the per-row values.
+    if (warp == 0) {
+        tc_fence_before();
+        named_bar_arrive(kSetupBar, kThreads);
+    } else {
+        if (is_sm) {   // pass OLD reads qhat; the first dense loop starts with q
+            load_query_tile<D>(smem + C::OFF_Q, first ? p.q : p.q_hat, st, b, h, p.H, p.n_state, rows, row0, A);
+            fence_proxy_async_smem();
+            if (wg == 0) {   // per row, shared by the four groups: key count and old normaliser (log2 units)
+                row_cnt[r] = !row_ok ? 0 : cnt_min == cnt ? cnt : dense ? min(pos + 1, p.n_keys) : __ldg(RC + r);
+                row_zo[r] = !row_ok ? INFINITY : first ? 0.f : __ldg(p.z + bh * p.n_state + pos) * kLog2e;
+                row_pos_s[r] = pos;
+            }
         }
+        tc_fence_before();
+        named_bar_sync(kSetupBar, kThreads);
+        tc_fence_after();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = misc[0];
+    const uint32_t tmem = misc[0];   // read by warp 0 only after the closing barrier
 
     if (warp == 0) {
         // ---------------- TMA producer: K ring (3 stages) and V ring (2 stages) ----------------
@@ -680,7 +689,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(misc[0], kTmemCols);
     }
 }
 

@@ -135,6 +135,16 @@ __device__ __forceinline__ uint32_t f32_order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Code t (bits [4t, 4t + 4) of w, two's complement in [-8, 7]) as an exact fp32.
+// Offset by 8 the code is a nibble in [0, 15]; written into the low mantissa
+// bits of 2^23 it gives the float 2^23 + 8 + code, and subtracting 2^23 + 8
+// (exact: both are integers below 2^24) leaves the code. This keeps the
+// conversion on the integer and fp32 pipes rather than the slower
+// integer-to-float conversion unit.
+__device__ __forceinline__ float code_f32(uint32_t w, int t) {
+    return __fsub_rn(__uint_as_float(((w >> (4 * t)) & 0xFu) ^ 0x4B000008u), 8388616.0f);
+}
+
 // Adds scale*code of every delta layer of `view` that holds token i to the
 // 8 fp32 values of chunk c8 (elements 8*c8 .. 8*c8+7) of head h.
 __device__ __forceinline__ void apply_deltas(const DeltaView &view, bool is_v, int m0, int m1, long long b,
@@ -150,8 +160,7 @@ __device__ __forceinline__ void apply_deltas(const DeltaView &view, bool is_v, i
         const float s = __half2float(__ushort_as_half(__ldg(scales + ent * (d / 32) + c8 / 4)));
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            const int q = ((int)(w << (28 - 4 * t))) >> 28;   // sign-extended nibble t
-            rec[t] = __fadd_rn(rec[t], __fmul_rn(s, (float)q));
+            rec[t] = __fadd_rn(rec[t], __fmul_rn(s, code_f32(w, t)));
         }
     }
 }

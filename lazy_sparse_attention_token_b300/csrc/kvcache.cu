@@ -13,7 +13,9 @@
 // the same definition is written with explicit IEEE intrinsics: fp32
 // reconstruction adds scale*code layer by layer in ascending order, the
 // delta is one fp32 subtraction, scale = fp16_rne(amax / 7) with an IEEE
-// divide, and code = rint_even(delta / scale) clamped to [-7, 7].
+// divide, and code = rint_even(delta / scale) clamped to [-7, 7]. Codes
+// become floats, and quotients codes, through exact fp32 bit tricks rather
+// than the conversion unit.
 #include "common.cuh"
 
 namespace fl {
@@ -98,8 +100,7 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
         for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const int qv = ((int)(w[c] << (28 - 4 * k))) >> 28;   // sign-extended nibble k
-                rec[8 * c + k] = __fadd_rn(rec[8 * c + k], __fmul_rn(sc, (float)qv));
+                rec[8 * c + k] = __fadd_rn(rec[8 * c + k], __fmul_rn(sc, code_f32(w[c], k)));
             }
     }
 
@@ -121,9 +122,12 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
         packed[c] = 0u;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const float r = rintf(x[8 * c + k] * inv);
-            const int q = (int)fminf(7.f, fmaxf(-7.f, r));
-            packed[c] |= (uint32_t)(q & 0xF) << (4 * k);
+            // rint is monotone and fixes +-7, so clamping before rounding gives the
+            // same integer; adding 1.5 * 2^23 rounds the clamped quotient to an
+            // integer (ties to even) in the low mantissa bits, whose low nibble is
+            // then the code in two's complement
+            const float r = fminf(7.f, fmaxf(-7.f, __fmul_rn(x[8 * c + k], inv)));
+            packed[c] |= (__float_as_uint(__fadd_rn(r, 12582912.0f)) & 0xFu) << (4 * k);
         }
     }
     const long long ent = (b * R_cap + at + e) * H + h;
@@ -188,8 +192,7 @@ reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const in
         for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const int qv = ((int)(w[c] << (28 - 4 * k))) >> 28;   // sign-extended nibble k
-                rec[8 * c + k] = __fadd_rn(rec[8 * c + k], __fmul_rn(sc, (float)qv));
+                rec[8 * c + k] = __fadd_rn(rec[8 * c + k], __fmul_rn(sc, code_f32(w[c], k)));
             }
     }
     if (new_layers <= old_layers) store_group_bf16(rec, (is_v ? v_old : k_old) + bhr * d + g * 32);
