@@ -21,8 +21,10 @@
 //   pass NEW: QK_new -> P' = exp(. - Z') -> acc += P' V_new, column sums of P'
 // The first dense loop skips pass OLD (m = 1, u = 0).
 //
-// Roles (608 threads): warp 0 issues TMA loads into a K ring (3 stages) and
-// a V ring (2 stages), keys two tiles ahead of values; warp 1 issues the QK
+// Roles (608 threads): warp 0 issues TMA loads into one ring of five K/V
+// tile slots, in the order the products consume them (a pass with PV products
+// loads K(0), then K(t+1) before V(t); pass LSE loads keys only and so keeps
+// five key tiles in flight); warp 1 issues the QK
 // products and warp 2 the PV products (one thread each): the tensor pipe
 // buffers only about two MMAs, and a second issuing thread covers the
 // barrier tests the first makes between its batches. The QK issuer runs up
@@ -72,37 +74,42 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 2;         // logits S: two buffers of 128 fp32 columns, [0, 256)
 constexpr uint32_t kColP = 256;   // probabilities P: two buffers of 64 columns (128 bf16), [256, 384)
 constexpr uint32_t kColAcc = 384; // accumulator columns [384, 384 + d)
-constexpr int kKStages = 3, kVStages = 2;
-constexpr int kAhead = 2;         // K tiles loaded ahead of the V tile being loaded
-static_assert(kSBufs == 2 && kVStages == 2, "S, P and V buffers are indexed with a parity bit");
-static_assert(kKStages > kAhead, "the K ring holds every tile issued ahead");
+constexpr int kStages = 5;        // K/V tile slots of the load ring
+static_assert(kSBufs == 2, "S and P buffers are indexed with a parity bit");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ int g_tc_error;
 
 enum : int { PH_OLD = 0, PH_LSE = 1, PH_NEW = 2 };
-// PV_DONE[b] completes when the PV product of the tile in P buffer / V slot b is
-// done: it releases both the P buffer (softmax) and the V slot (producer).
-enum : int { BAR_K_FULL = 0, BAR_K_EMPTY = 3, BAR_V_FULL = 6, BAR_S_FULL = 8, BAR_S_READ = 10, BAR_P_FULL = 12,
-             BAR_PV_DONE = 14, BAR_ACC = 16, BAR_STATS = 17, BAR_Q_READY = 18, BAR_DRAIN = 19 /* QK, PV */,
-             BAR_ZN = 21, BAR_EPI = 22, N_BARS = 23 };
-enum : int { ERR_K_EMPTY = 1, ERR_K_FULL = 2, ERR_V_EMPTY = 3, ERR_V_FULL = 4, ERR_S_READ = 5, ERR_S_FULL = 6,
-             ERR_P_FULL = 7, ERR_PV_DONE = 8, ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11, ERR_ZN = 12, ERR_EPI = 13 };
+// PV_DONE[b] completes when the PV product that read P buffer b is done (the
+// softmax may then overwrite it); the product also releases its V tile's slot.
+// FULL[s] / EMPTY[s]: ring slot s holds a landed tile / is free again.
+enum : int { BAR_FULL = 0, BAR_EMPTY = 5, BAR_S_FULL = 10, BAR_S_READ = 12, BAR_P_FULL = 14, BAR_PV_DONE = 16,
+             BAR_ACC = 18, BAR_STATS = 19, BAR_Q_READY = 20, BAR_DRAIN = 21 /* QK, PV */, BAR_ZN = 23, BAR_EPI = 24,
+             N_BARS = 25 };
+static_assert(BAR_EMPTY == BAR_FULL + kStages && BAR_S_FULL == BAR_EMPTY + kStages, "barrier layout");
+enum : int { ERR_EMPTY = 1, ERR_FULL = 2, ERR_S_READ = 5, ERR_S_FULL = 6, ERR_P_FULL = 7, ERR_PV_DONE = 8,
+             ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11, ERR_ZN = 12, ERR_EPI = 13 };
+
+// Ring position of a pass's loads. A pass with PV products loads K(0), then
+// K(t+1) before V(t) for every t, and V(n-1) last (2n loads); pass LSE loads
+// K(t) in order (n loads).
+__device__ __forceinline__ int kv_pos_k(int t) { return t == 0 ? 0 : 2 * t - 1; }
+__device__ __forceinline__ int kv_pos_v(int t, int n) { return t + 1 < n ? 2 * t + 2 : 2 * t + 1; }
 
 template <int D>
 struct Cfg {
     static constexpr int NA = (D + 63) / 64;        // 64-element atoms along d
     static constexpr int TB = NA * kAtom;           // one 128-row tile of Q, K or V
     static constexpr int OFF_Q = 0;                 // queries: qhat for pass OLD, then q
-    static constexpr int OFF_K = TB;                // K ring
-    static constexpr int OFF_V = OFF_K + kKStages * TB;   // V ring
-    static constexpr int OFF_X = OFF_V + kVStages * TB;   // row-statistics exchange: [groups][128][3] fp32
+    static constexpr int OFF_KV = TB;               // K/V ring
+    static constexpr int OFF_X = OFF_KV + kStages * TB;   // row-statistics exchange: [groups][128][3] fp32
     static constexpr int OFF_ROW = OFF_X + kGroups * 128 * 3 * 4;   // per row: key count, old and new normaliser
     static constexpr int OFF_BAR = OFF_ROW + 128 * 16;
-    // epilogue: the finished accumulator rows, parked in the (then idle) K ring
+    // epilogue: the finished accumulator rows, parked in the (then idle) ring
     static constexpr int XS = D + 4;   // padded row stride in floats
-    static_assert(128 * XS * 4 <= kKStages * TB, "accumulator rows fit the K ring");
+    static_assert(128 * XS * 4 <= kStages * TB, "accumulator rows fit the ring");
     static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM = BYTES + 1024;       // room to align the base to 1024 bytes
@@ -124,6 +131,27 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
+}
+
+// Packed two-lane fp32 arithmetic (one instruction for both lanes, each lane
+// rounded exactly as its scalar counterpart): a * b + c and a + b.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -169,13 +197,14 @@ __device__ __forceinline__ void load_query_tile(uint8_t *tile, const uint16_t *s
                                                 int n_state, int rows, int row0, const int32_t *A) {
     constexpr int CPR = D / 8;   // 16-byte chunks per row
     const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    const uint64_t stream = l2_policy_evict_first();   // each query row is read by one row tile
 #pragma unroll 4
     for (int c = st; c < BM * CPR; c += 32 * kSoftmaxWarps) {
         const int rr = c / CPR, ch = c - rr * CPR;
         uint4 val = make_uint4(0, 0, 0, 0);
         if (rr < rows) {
             const int pos = A ? __ldg(A + rr) : row0 + rr;
-            val = s4[(((long long)b * n_state + pos) * H + h) * CPR + ch];
+            val = ld_global_v4_hint(s4 + (((long long)b * n_state + pos) * H + h) * CPR + ch, stream);
         }
         *reinterpret_cast<uint4 *>(tile + swz_off(rr, ch)) = val;
     }
@@ -201,11 +230,13 @@ __device__ __forceinline__ constexpr int frag(int k, int j, int e) { return 16 *
 // Lane l ends with the sum of column 8(J/2) + 2(l%4) + J%2, J = l/4.
 __device__ __forceinline__ float column_sum(const float *v, int lane) {
     float cs[8];
+    auto pr = [&](int k, int j) { return make_float2(v[frag(k, j, 0)], v[frag(k, j, 1)]); };
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-            cs[2 * j + e] = (v[frag(0, j, e)] + v[frag(1, j, e)]) + (v[frag(2, j, e)] + v[frag(3, j, e)]);
+    for (int j = 0; j < 4; ++j) {   // the two columns of a pair together
+        const float2 t = add2(add2(pr(0, j), pr(1, j)), add2(pr(2, j), pr(3, j)));
+        cs[2 * j] = t.x;
+        cs[2 * j + 1] = t.y;
+    }
 #pragma unroll
     for (int w = 4; w >= 1; w >>= 1) {
         const bool up = lane & (w << 2);
@@ -308,49 +339,44 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const uint32_t tmem = misc[0];   // read by warp 0 only after the closing barrier
 
     if (warp == 0) {
-        // ---------------- TMA producer: K ring (3 stages) and V ring (2 stages) ----------------
+        // ---------------- TMA producer: one ring of K/V tile slots ----------------
         if (lane == 0) {
             prefetch_tmap(&tm_k_old); prefetch_tmap(&tm_v_old);
             prefetch_tmap(&tm_k_new); prefetch_tmap(&tm_v_new);
-            int kg = 0, kph = ph0, kt = 0;   // next K tile: index, pass, tile within the pass
-            int vi = 0;                       // V tiles issued
-            bool ok = true;
-            int ph = ph0, t = 0;
-            for (int g = 0; ok && g < total; ++g, ++t) {
-                if (t == n_tiles) { t = 0; ++ph; }
-                // keys run kAhead tiles ahead of values, the order the issuers consume them
-                for (; kg < total && kg <= g + kAhead; ++kg, ++kt) {
-                    if (kt == n_tiles) { kt = 0; ++kph; }
-                    const int s = kg % kKStages, use = kg / kKStages;
-                    if (!wait_bar(bar(BAR_K_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_K_EMPTY)) { ok = false; break; }
-                    const CUtensorMap *mk = kph == PH_OLD ? &tm_k_old : &tm_k_new;
-                    const uint32_t dst = sbase + C::OFF_K + C::TB * s;
-                    mbar_arrive_expect_tx(bar(BAR_K_FULL + s), C::TB);
-                    for (int a = 0; a < C::NA; ++a) {
-                        if (dense) tma_load_4d(dst + a * kAtom, mk, bar(BAR_K_FULL + s), a * 64, h, kt * BN, b);
-                        else tma_load_4d(dst + a * kAtom, mk, bar(BAR_K_FULL + s), a * 64, kt * BN, h, b);
-                    }
+            int pos = 0;   // loads issued
+            // the K/V tiles are read once per pass by every row tile of the head: keep them in
+            // L2 ahead of the streamed query, output and normaliser traffic
+            const uint64_t keep = l2_policy_evict_last();
+            // K or V tile t of pass ph into the next slot, once its previous tile is consumed
+            auto load = [&](bool is_v, int ph, int t) -> bool {
+                const int s = pos % kStages, use = pos / kStages;
+                if (!wait_bar(bar(BAR_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_EMPTY)) return false;
+                const CUtensorMap *m = is_v ? (ph == PH_OLD ? &tm_v_old : &tm_v_new) : (ph == PH_OLD ? &tm_k_old : &tm_k_new);
+                const uint32_t dst = sbase + C::OFF_KV + C::TB * s;
+                mbar_arrive_expect_tx(bar(BAR_FULL + s), C::TB);
+                for (int a = 0; a < C::NA; ++a) {
+                    if (dense) tma_load_4d_hint(dst + a * kAtom, m, bar(BAR_FULL + s), a * 64, h, t * BN, b, keep);
+                    else tma_load_4d_hint(dst + a * kAtom, m, bar(BAR_FULL + s), a * 64, t * BN, h, b, keep);
                 }
-                if (!ok) break;
-                if (ph != PH_LSE) {
-                    const int s = vi & 1, use = vi >> 1;
-                    if (!wait_bar(bar(BAR_PV_DONE + s), (use & 1) ^ 1, abort_flag, ERR_V_EMPTY)) break;
-                    const CUtensorMap *mv = ph == PH_OLD ? &tm_v_old : &tm_v_new;
-                    const uint32_t dst = sbase + C::OFF_V + C::TB * s;
-                    mbar_arrive_expect_tx(bar(BAR_V_FULL + s), C::TB);
-                    for (int a = 0; a < C::NA; ++a) {
-                        if (dense) tma_load_4d(dst + a * kAtom, mv, bar(BAR_V_FULL + s), a * 64, h, t * BN, b);
-                        else tma_load_4d(dst + a * kAtom, mv, bar(BAR_V_FULL + s), a * 64, t * BN, h, b);
+                ++pos;
+                return true;
+            };
+            bool ok = true;
+            for (int ph = ph0; ok && ph <= PH_NEW; ++ph) {
+                if (ph == PH_LSE) {
+                    for (int t = 0; ok && t < n_tiles; ++t) ok = load(false, ph, t);
+                } else {   // the order kv_pos_k / kv_pos_v describe
+                    ok = load(false, ph, 0);
+                    for (int t = 0; ok && t < n_tiles; ++t) {
+                        if (t + 1 < n_tiles) ok = load(false, ph, t + 1);
+                        if (ok) ok = load(true, ph, t);
                     }
-                    ++vi;
                 }
             }
             if (*abort_flag) {   // let copies already in flight land before the CTA exits
                 volatile int never = 0;
-                for (int g = max(0, kg - kKStages); g < kg; ++g)
-                    wait_bar(bar(BAR_K_FULL + g % kKStages), (g / kKStages) & 1, &never, ERR_K_FULL);
-                for (int v = max(0, vi - kVStages); v < vi; ++v)
-                    wait_bar(bar(BAR_V_FULL + (v & 1)), (v >> 1) & 1, &never, ERR_V_FULL);
+                for (int q = max(0, pos - kStages); q < pos; ++q)
+                    wait_bar(bar(BAR_FULL + q % kStages), (q / kStages) & 1, &never, ERR_FULL);
             }
         }
     } else if (warp == 1 || warp == 2) {
@@ -366,16 +392,25 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             constexpr uint32_t id_pv_neg = idesc_bf16(128, D, false, true, true);    // pass OLD subtracts
             // descriptors are built once; per k-step only the start address moves
             const uint64_t d_q = smem_desc(sbase + C::OFF_Q, 16, 1024, 2);
-            const uint64_t d_k = smem_desc(sbase + C::OFF_K, 16, 1024, 2);
-            const uint64_t d_v = smem_desc(sbase + C::OFF_V, kAtom, 1024, 2);
+            const uint64_t d_k = smem_desc(sbase + C::OFF_KV, 16, 1024, 2);
+            const uint64_t d_v = smem_desc(sbase + C::OFF_KV, kAtom, 1024, 2);
             constexpr uint64_t TB16 = C::TB >> 4, ATOM16 = kAtom >> 4;
+            static_assert(BN / 16 == 8 && (D == 64 || D == 96 || D == 128), "MMA batch shapes");
+            // start-address offset (16-byte units) of k-step kk within a 64-element-atom tile
+            auto kstep_off = [](int kk) -> uint64_t { return (uint64_t)((kk >> 2) * ATOM16 + (kk & 3) * 2); };
+            uint64_t aq[D / 16];   // query-tile descriptors, one per k-step
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) aq[kk] = d_q + kstep_off(kk);
             const int n_old = first ? 0 : n_tiles;   // tiles of pass OLD; pass LSE covers [n_old, n_old + n_tiles)
             const int lse0 = n_old, new0 = n_old + n_tiles;
+            // ring positions of the passes' first loads
+            const int base_lse = 2 * n_old, base_new = base_lse + n_tiles;
             bool q_seen = first;   // the query tile holds this loop's q (passes LSE and NEW)
-            // S = Q K^T for tile g (K slot g % 3) into S buffer g & 1
+            // S = Q K^T for tile g into S buffer g & 1
             auto issue_qk = [&](int g) -> bool {
-                const int ks = g % kKStages, sb = g & 1;
-                if (!wait_bar(bar(BAR_K_FULL + ks), (uint32_t)(g / kKStages) & 1u, abort_flag, ERR_K_FULL)) return false;
+                const int kp = g < lse0 ? kv_pos_k(g) : g < new0 ? base_lse + g - lse0 : base_new + kv_pos_k(g - new0);
+                const int ks = kp % kStages, sb = g & 1;
+                if (!wait_bar(bar(BAR_FULL + ks), (uint32_t)(kp / kStages) & 1u, abort_flag, ERR_FULL)) return false;
                 // the S buffer's previous tile has been read by the softmax
                 if (g >= kSBufs && !wait_bar(bar(BAR_S_READ + sb), ((g >> 1) - 1) & 1, abort_flag, ERR_S_READ))
                     return false;
@@ -385,30 +420,40 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
                 tc_fence_after();
                 const uint64_t dk = d_k + TB16 * (uint32_t)ks;
-                const uint32_t dst = tmem + 128u * (uint32_t)sb;
+                uint64_t bk[D / 16];
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = (kk >> 2) * ATOM16 + (kk & 3) * 2;
-                    mma_bf16_ss(dst, d_q + off, dk + off, id_qk, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk) bk[kk] = dk + kstep_off(kk);
+                const uint32_t dst = tmem + 128u * (uint32_t)sb;
+                if constexpr (D == 128) {
+                    mma_bf16_ss_x8(dst, aq, bk, id_qk, 0u);
+                } else {   // d = 64: one batch of four; d = 96: four, then two
+                    mma_bf16_ss_x4(dst, aq, bk, id_qk, 0u);
+                    if constexpr (D == 96) mma_bf16_ss_x2(dst, aq + 4, bk + 4, id_qk, 1u);
                 }
                 mma_commit(bar(BAR_S_FULL + sb));
-                mma_commit(bar(BAR_K_EMPTY + ks));
+                mma_commit(bar(BAR_EMPTY + ks));
                 return true;
             };
-            // acc (+/-)= P V for the tile with PV index pv (P buffer and V slot pv & 1)
+            // acc (+/-)= P V for the tile with PV index pv (P buffer pv & 1)
             auto issue_pv = [&](int pv, bool old) -> bool {
-                const int vs = pv & 1;
-                const uint32_t vpar = (uint32_t)(pv >> 1) & 1u;
-                if (!wait_bar(bar(BAR_V_FULL + vs), vpar, abort_flag, ERR_V_FULL)) return false;
-                if (!wait_bar(bar(BAR_P_FULL + vs), vpar, abort_flag, ERR_P_FULL)) return false;
+                const int pb = pv & 1;
+                const int vp = pv < n_old ? kv_pos_v(pv, n_tiles) : base_new + kv_pos_v(pv - n_old, n_tiles);
+                const int vs = vp % kStages;
+                if (!wait_bar(bar(BAR_FULL + vs), (uint32_t)(vp / kStages) & 1u, abort_flag, ERR_FULL)) return false;
+                if (!wait_bar(bar(BAR_P_FULL + pb), (uint32_t)(pv >> 1) & 1u, abort_flag, ERR_P_FULL)) return false;
                 tc_fence_after();
                 const uint64_t dv = d_v + TB16 * (uint32_t)vs;
-                const uint32_t pa = tmem + kColP + 64u * (uint32_t)vs;
-                const uint32_t idp = old ? id_pv_neg : id_pv;
+                const uint32_t pa = tmem + kColP + 64u * (uint32_t)pb;
+                uint32_t ap[BN / 16];
+                uint64_t bv[BN / 16];
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)   // acc +-= P[:, 16kk..] * V[16kk.., :]
-                    mma_bf16_ts(tmem + kColAcc, pa + 8u * kk, dv + kk * 128, idp, (pv > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(bar(BAR_PV_DONE + vs));
+                for (int kk = 0; kk < BN / 16; ++kk) {   // acc +-= P[:, 16kk..] * V[16kk.., :]
+                    ap[kk] = pa + 8u * kk;
+                    bv[kk] = dv + kk * 128;
+                }
+                mma_bf16_ts_x8(tmem + kColAcc, ap, bv, old ? id_pv_neg : id_pv, pv > 0 ? 1u : 0u);
+                mma_commit(bar(BAR_PV_DONE + pb));
+                mma_commit(bar(BAR_EMPTY + vs));
                 return true;
             };
             bool ok = true;
@@ -491,9 +536,12 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
 #pragma unroll
             for (int k = 0; k < 4; ++k)
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) v[frag(k, j, e)] = ex2(fmaf(v[frag(k, j, e)], p.sl2, nz[k]));
+                for (int j = 0; j < 4; ++j) {
+                    const float2 x = fma2(make_float2(v[frag(k, j, 0)], v[frag(k, j, 1)]), make_float2(p.sl2, p.sl2),
+                                          make_float2(nz[k], nz[k]));
+                    v[frag(k, j, 0)] = ex2(x.x);
+                    v[frag(k, j, 1)] = ex2(x.y);
+                }
             // P buffer pv & 1 was last read by the PV product of the V tile two before
             const int pb = pv & 1;
             if (pv >= 2 && !wait_bar(bar(BAR_PV_DONE + pb), (uint32_t)((pv >> 1) - 1) & 1u, abort_flag, ERR_PV_DONE))
@@ -516,12 +564,10 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             if constexpr (OLD) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    float a2[2] = {0.f, 0.f};
+                    float2 a2 = make_float2(v[frag(k, 0, 0)], v[frag(k, 0, 1)]);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) a2[e] += v[frag(k, j, e)];
-                    mk[k] += a2[0] + a2[1];
+                    for (int j = 1; j < 4; ++j) a2 = add2(a2, make_float2(v[frag(k, j, 0)], v[frag(k, j, 1)]));
+                    mk[k] += a2.x + a2.y;
                 }
             }
             const float cs = column_sum(v, lane);
@@ -556,12 +602,14 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 const float mnew = max3f(m1, m2, m3);
                 // a row that has seen no key yet keeps M = -inf and L = 0 (every term is 0)
                 const float nb = mnew == -INFINITY ? 0.f : -mnew * p.sl2;
-                float a2[2] = {Lk[k] * ex2(fmaf(Mk[k], p.sl2, nb)), 0.f};
+                float2 a2 = make_float2(Lk[k] * ex2(fmaf(Mk[k], p.sl2, nb)), 0.f);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) a2[e] += ex2(fmaf(v[frag(k, j, e)], p.sl2, nb));
-                Lk[k] = a2[0] + a2[1];
+                for (int j = 0; j < 4; ++j) {
+                    const float2 x = fma2(make_float2(v[frag(k, j, 0)], v[frag(k, j, 1)]), make_float2(p.sl2, p.sl2),
+                                          make_float2(nb, nb));
+                    a2 = add2(a2, make_float2(ex2(x.x), ex2(x.y)));
+                }
+                Lk[k] = a2.x + a2.y;
                 Mk[k] = mnew;
             }
         }
@@ -632,10 +680,10 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         }
         if (ok && wait_bar(bar(BAR_ACC), 0, abort_flag, ERR_ACC)) {
             tc_fence_after();
-            // Epilogue. A thread's accumulator row goes to shared memory (the K ring is idle
+            // Epilogue. A thread's accumulator row goes to shared memory (the ring is idle
             // now); then each warp walks whole rows so that O, Z and qhat move in full lines.
             constexpr int GD = D / kGroups;   // accumulator columns per group (16, 24 or 32)
-            float *xo = reinterpret_cast<float *>(smem + C::OFF_K);
+            float *xo = reinterpret_cast<float *>(smem + C::OFF_KV);
             const uint32_t lane_base = (uint32_t)rq << 16;
 #pragma unroll
             for (int u = 0; u < GD; u += 8) {
@@ -653,6 +701,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 float4 ov[RPW];
                 long long srow[RPW];
                 bool upd[RPW];
+                const uint64_t stream = l2_policy_evict_first();   // O and qhat rows are touched once
                 // all of this warp's O loads first, then the updates
 #pragma unroll
                 for (int i = 0; i < RPW; ++i) {
@@ -660,7 +709,11 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                     upd[i] = rr < rows && row_zn[rr] < INFINITY;
                     srow[i] = upd[i] ? ((long long)b * p.n_state + row_pos_s[rr]) * p.H + h : 0;
                     ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (upd[i] && !first && lane < D / 4) ov[i] = reinterpret_cast<const float4 *>(p.o + srow[i] * D)[lane];
+                    if (upd[i] && !first && lane < D / 4) {
+                        const uint4 u = ld_global_v4_hint(reinterpret_cast<const float4 *>(p.o + srow[i] * D) + lane, stream);
+                        ov[i] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                            __uint_as_float(u.w));
+                    }
                 }
 #pragma unroll
                 for (int i = 0; i < RPW; ++i) {
@@ -673,12 +726,15 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                         o4.y += a4.y;
                         o4.z += a4.z;
                         o4.w += a4.w;
-                        reinterpret_cast<float4 *>(p.o + srow[i] * D)[lane] = o4;
+                        st_global_v4_hint(reinterpret_cast<float4 *>(p.o + srow[i] * D) + lane,
+                                          make_uint4(__float_as_uint(o4.x), __float_as_uint(o4.y), __float_as_uint(o4.z),
+                                                     __float_as_uint(o4.w)),
+                                          stream);
                     }
                     // the query tile holds this loop's q: it becomes qhat
                     if (lane < D / 8)
-                        reinterpret_cast<uint4 *>(p.q_hat + srow[i] * D)[lane] =
-                            *reinterpret_cast<const uint4 *>(smem + C::OFF_Q + swz_off(rr, lane));
+                        st_global_v4_hint(reinterpret_cast<uint4 *>(p.q_hat + srow[i] * D) + lane,
+                                          *reinterpret_cast<const uint4 *>(smem + C::OFF_Q + swz_off(rr, lane)), stream);
                     if (lane == 0) p.z[bh * p.n_state + row_pos_s[rr]] = row_zn[rr] * kLn2;
                 }
             }

@@ -91,6 +91,39 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
 }
+// The same load with an L2 cache policy (from createpolicy) for the tile's lines.
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+        : "memory");
+}
+// L2 cache policies: lines kept in preference to others / evicted first.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// 16-byte global load / store under an L2 cache policy.
+__device__ __forceinline__ uint4 ld_global_v4_hint(const void *ptr, uint64_t policy) {
+    uint4 r;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(ptr), "l"(policy));
+    return r;
+}
+__device__ __forceinline__ void st_global_v4_hint(void *ptr, uint4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -146,6 +179,64 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Batches of MMAs issued back to back from one asm block, so that no other
+// instruction of the issuing thread sits between them: the first accumulates
+// iff acc0 != 0, the rest always accumulate. A operands from shared memory
+// (descriptors a[i]) or from TMEM (addresses a[i]); B from shared memory.
+#define FL_MMA_SS(ai, bi, pr) "tcgen05.mma.cta_group::1.kind::f16 [%0], %" #ai ", %" #bi ", %17, " #pr ";\n\t"
+__device__ __forceinline__ void mma_bf16_ss_x8(uint32_t d_tmem, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                               uint32_t idesc, uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %18, 0;\n\t"
+        "setp.eq.b32 q, %17, %17;\n\t"
+        FL_MMA_SS(1, 9, p) FL_MMA_SS(2, 10, q) FL_MMA_SS(3, 11, q) FL_MMA_SS(4, 12, q)
+        FL_MMA_SS(5, 13, q) FL_MMA_SS(6, 14, q) FL_MMA_SS(7, 15, q) FL_MMA_SS(8, 16, q) "}" ::"r"(d_tmem),
+        "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]),
+        "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc0)
+        : "memory");
+}
+#undef FL_MMA_SS
+#define FL_MMA_SS4(ai, bi, pr) "tcgen05.mma.cta_group::1.kind::f16 [%0], %" #ai ", %" #bi ", %9, " #pr ";\n\t"
+__device__ __forceinline__ void mma_bf16_ss_x4(uint32_t d_tmem, const uint64_t *a, const uint64_t *b, uint32_t idesc,
+                                               uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %10, 0;\n\t"
+        "setp.eq.b32 q, %9, %9;\n\t"
+        FL_MMA_SS4(1, 5, p) FL_MMA_SS4(2, 6, q) FL_MMA_SS4(3, 7, q) FL_MMA_SS4(4, 8, q) "}" ::"r"(d_tmem),
+        "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc),
+        "r"(acc0)
+        : "memory");
+}
+#undef FL_MMA_SS4
+#define FL_MMA_SS2(ai, bi, pr) "tcgen05.mma.cta_group::1.kind::f16 [%0], %" #ai ", %" #bi ", %5, " #pr ";\n\t"
+__device__ __forceinline__ void mma_bf16_ss_x2(uint32_t d_tmem, const uint64_t *a, const uint64_t *b, uint32_t idesc,
+                                               uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.eq.b32 q, %5, %5;\n\t"
+        FL_MMA_SS2(1, 3, p) FL_MMA_SS2(2, 4, q) "}" ::"r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(b[0]), "l"(b[1]),
+        "r"(idesc), "r"(acc0)
+        : "memory");
+}
+#undef FL_MMA_SS2
+#define FL_MMA_TS(ai, bi, pr) "tcgen05.mma.cta_group::1.kind::f16 [%0], [%" #ai "], %" #bi ", %17, " #pr ";\n\t"
+__device__ __forceinline__ void mma_bf16_ts_x8(uint32_t d_tmem, const uint32_t (&a)[8], const uint64_t (&b)[8],
+                                               uint32_t idesc, uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %18, 0;\n\t"
+        "setp.eq.b32 q, %17, %17;\n\t"
+        FL_MMA_TS(1, 9, p) FL_MMA_TS(2, 10, q) FL_MMA_TS(3, 11, q) FL_MMA_TS(4, 12, q)
+        FL_MMA_TS(5, 13, q) FL_MMA_TS(6, 14, q) FL_MMA_TS(7, 15, q) FL_MMA_TS(8, 16, q) "}" ::"r"(d_tmem),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]),
+        "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc0)
+        : "memory");
+}
+#undef FL_MMA_TS
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
