@@ -438,7 +438,8 @@ flashloop_status_t flashloop_reconstruct_keys(const flashloop_kv_cache_t *cache,
     if (K < 1 || K > dm.N_cap) return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad K=%d", K);
     if ((st = check_device()) != FLASHLOOP_OK) return st;
     cudaError_t e = launch_reconstruct_keys(make_view(cache, loop - 1), make_view(cache, loop), key_idx, dm.B, dm.H, K,
-                                            dm.N_cap, dm.d, dm.R_cap, k_old, v_old, k_new, v_new, stream);
+                                            dm.N_cap, dm.d, dm.R_cap, k_old, v_old, k_new, v_new, nullptr, 0,
+                                            nullptr, stream);
     if (e != cudaSuccess) return cuda_fail(e, "reconstruct_keys");
     return FLASHLOOP_OK;
 }
@@ -517,14 +518,17 @@ flashloop_status_t flashloop_lazy_attention(const flashloop_attn_args_t *a, flas
         const size_t one = align_up((size_t)dm.B * dm.H * dm.K * dm.d * 2);
         uint16_t *kv[4];
         for (int i = 0; i < 4; ++i) kv[i] = reinterpret_cast<uint16_t *>(ws + i * one);
+        // both reconstructions of the selected keys, and the keys each row sees
+        int32_t *counts = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(a->workspace) + W.counts);
         e = launch_reconstruct_keys(make_view(c, a->loop - 1), make_view(c, a->loop), a->key_idx, dm.B, dm.H, a->K,
-                                    dm.N_cap, dm.d, dm.R_cap, kv[0], kv[1], kv[2], kv[3], stream);
+                                    dm.N_cap, dm.d, dm.R_cap, kv[0], kv[1], kv[2], kv[3], a->row_pos, a->R, counts,
+                                    stream);
         if (e != cudaSuccess) return cuda_fail(e, "reconstruct_keys");
         p.K = a->K;
         p.key_idx = a->key_idx;
         p.k_old = kv[0]; p.v_old = kv[1]; p.k_new = kv[2]; p.v_new = kv[3];
         p.kv_rows = a->K;
-        p.row_cnt = reinterpret_cast<int32_t *>(static_cast<uint8_t *>(a->workspace) + W.counts);
+        p.row_cnt = counts;
     } else {
         p.K = a->n_keys;
         p.k_new = c->k_dense[a->loop - 1];

@@ -283,7 +283,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const int32_t *A = dense ? nullptr : p.row_pos + (long long)b * p.R + row0;
     // Rows and keys are both ascending, so the keys a row may see are a
     // prefix of the list: row i sees the keys of S that are <= i, counted for
-    // every lazy row by row_key_counts_kernel.
+    // every lazy row before the launch.
     const int32_t *RC = dense ? nullptr : p.row_cnt + bh * p.R + row0;
     const int cnt = dense ? min(row0 + rows, p.n_keys) : __ldg(RC + rows - 1);   // last row
     const int cnt_min = dense ? min(row0 + 1, p.n_keys) : __ldg(RC);             // first row
@@ -749,32 +749,6 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     }
 }
 
-// Keys each lazy row sees, #{j in S_bh : j <= pos_i} for every (b, h, i), with the
-// head's ascending key list staged in shared memory when it fits.
-constexpr int kCountThreads = 256;
-constexpr int kCountStage = 12288;   // keys staged in shared memory (48 KB)
-__global__ void __launch_bounds__(kCountThreads)
-row_key_counts_kernel(const int32_t *__restrict__ key_idx, const int32_t *__restrict__ row_pos, int H, int K, int R,
-                      int32_t *__restrict__ row_cnt) {
-    extern __shared__ int32_t keys_s[];
-    const int h = blockIdx.y, b = blockIdx.z;
-    const long long bh = (long long)b * H + h;
-    const int32_t *S = key_idx + bh * K;
-    const bool staged = K <= kCountStage;
-    if (staged)
-        for (int j = threadIdx.x; j < K; j += kCountThreads) keys_s[j] = __ldg(S + j);
-    __syncthreads();
-    const int i = blockIdx.x * kCountThreads + threadIdx.x;
-    if (i >= R) return;
-    const int x = __ldg(row_pos + (long long)b * R + i);
-    int lo = 0, hi = K;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if ((staged ? keys_s[mid] : __ldg(S + mid)) <= x) lo = mid + 1; else hi = mid;
-    }
-    row_cnt[bh * R + i] = lo;
-}
-
 // ---------------------------------------------------------------------------
 // host side
 
@@ -847,13 +821,7 @@ cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
     kp.c = p.c;
     kp.sl2 = kLog2e / sqrtf((float)D);
     dim3 grid(kp.n_row_tiles * p.H, 1, p.B);
-    if (!dense) {
-        if (!p.row_cnt) return cudaErrorInvalidValue;
-        KernelTimer kt("row_key_counts", s);
-        const int stage = p.K <= kCountStage ? p.K : 0;
-        row_key_counts_kernel<<<dim3(ceil_div(p.R, kCountThreads), p.H, p.B), kCountThreads, stage * 4, s>>>(
-            p.key_idx, p.row_pos, p.H, p.K, p.R, p.row_cnt);
-    }
+    if (!dense && !p.row_cnt) return cudaErrorInvalidValue;
     {
         KernelTimer kt("tc_attention", s);
         tc_attention_kernel<D><<<grid, kThreads, Cf::SMEM, s>>>(kp, maps[0], maps[1], maps[2], maps[3]);

@@ -61,10 +61,14 @@ cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, cons
                                 int B, int N_cap, int H, int d, int R_cap, int32_t *out_idx,
                                 int32_t *out_slot, uint8_t *k_codes, uint16_t *k_scales, uint8_t *v_codes,
                                 uint16_t *v_scales, cudaStream_t s);
+// Reconstruction of the selected keys at the old and the new loop into
+// [B, H, K, d]; with row_cnt set, the same launch also counts the keys each of
+// the R rows at row_pos sees, into row_cnt [B, H, R].
 cudaError_t launch_reconstruct_keys(const DeltaView &old_view, const DeltaView &new_view,
                                     const int32_t *key_idx, int B, int H, int K, int N_cap, int d,
                                     int R_cap, uint16_t *k_old, uint16_t *v_old, uint16_t *k_new,
-                                    uint16_t *v_new, cudaStream_t s);
+                                    uint16_t *v_new, const int32_t *row_pos, int R, int32_t *row_cnt,
+                                    cudaStream_t s);
 // attn_tc.cu (tensor-core prefill / dense attention)
 struct TcAttnParams {
     int mode;            // flashloop_attn_mode_t
@@ -75,7 +79,7 @@ struct TcAttnParams {
     const int32_t *row_pos;   // [B,R] or NULL (dense: row = key position)
     int K;               // key columns per (b,h) (dense: n_keys)
     const int32_t *key_idx;   // [B,H,K] or NULL (dense)
-    int32_t *row_cnt;         // lazy: workspace [B,H,R] for the keys each row sees
+    int32_t *row_cnt;         // lazy: keys each row sees [B,H,R], filled before the launch
     const uint16_t *q;
     uint16_t *q_hat;
     float *o, *z, *c;

@@ -156,12 +156,36 @@ __device__ __forceinline__ void store_group_bf16(const float (&rec)[32], uint16_
 // selected row: its four base chunks load together and each delta layer is
 // one slot lookup, one 16-byte codes load and one scale load for the group.
 // blockIdx.y: 0 = K, 1 = V.
-__global__ void __launch_bounds__(256)
+//
+// The first n_count_blocks blocks of the K half instead count, for every
+// (b, h) and row i, the keys that row sees: #{r : key_idx[b,h,r] <= row_pos[b,i]}
+// (both lists ascending), by binary search over the head's key list.
+constexpr int kRecThreads = 256;
+__global__ void __launch_bounds__(kRecThreads)
 reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const int32_t *__restrict__ key_idx,
                         int H, int K, int d, int N_cap, int R_cap, long long total,
                         uint16_t *__restrict__ k_old, uint16_t *__restrict__ v_old,
-                        uint16_t *__restrict__ k_new, uint16_t *__restrict__ v_new) {
-    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+                        uint16_t *__restrict__ k_new, uint16_t *__restrict__ v_new,
+                        const int32_t *__restrict__ row_pos, int R, long long count_total, int n_count_blocks,
+                        int32_t *__restrict__ row_cnt) {
+    if ((int)blockIdx.x < n_count_blocks) {
+        if (blockIdx.y != 0) return;
+        const long long t = (long long)blockIdx.x * kRecThreads + threadIdx.x;
+        if (t >= count_total) return;
+        const long long bh = t / R;
+        const int i = (int)(t - bh * R);
+        const long long b = bh / H;
+        const int32_t *S = key_idx + bh * K;
+        const int x = __ldg(row_pos + b * R + i);
+        int lo = 0, hi = K;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(S + mid) <= x) lo = mid + 1; else hi = mid;
+        }
+        row_cnt[bh * R + i] = lo;
+        return;
+    }
+    const long long t = (long long)(blockIdx.x - n_count_blocks) * kRecThreads + threadIdx.x;
     if (t >= total) return;
     const bool is_v = blockIdx.y == 1;
     const int gpr = d / 32;
@@ -191,9 +215,8 @@ reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const in
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 8; ++k)
                 rec[8 * c + k] = __fadd_rn(rec[8 * c + k], __fmul_rn(sc, code_f32(w[c], k)));
-            }
     }
     if (new_layers <= old_layers) store_group_bf16(rec, (is_v ? v_old : k_old) + bhr * d + g * 32);
     store_group_bf16(rec, (is_v ? v_new : k_new) + bhr * d + g * 32);
@@ -246,14 +269,18 @@ cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, cons
 cudaError_t launch_reconstruct_keys(const DeltaView &old_view, const DeltaView &new_view,
                                     const int32_t *key_idx, int B, int H, int K, int N_cap, int d,
                                     int R_cap, uint16_t *k_old, uint16_t *v_old, uint16_t *k_new,
-                                    uint16_t *v_new, cudaStream_t s) {
+                                    uint16_t *v_new, const int32_t *row_pos, int R, int32_t *row_cnt,
+                                    cudaStream_t s) {
     const long long total = (long long)B * H * K * (d / 32);
-    if (total == 0) return cudaSuccess;
-    dim3 grid(ceil_div(total, 256), 2);
+    const long long count_total = row_cnt ? (long long)B * H * R : 0;
+    const int n_count = ceil_div(count_total, kRecThreads);
+    if (total == 0 && n_count == 0) return cudaSuccess;
+    dim3 grid(n_count + ceil_div(total, kRecThreads), 2);
     {
         KernelTimer kt("reconstruct_keys", s);
-        reconstruct_keys_kernel<<<grid, 256, 0, s>>>(new_view, old_view.n_layers, new_view.n_layers, key_idx, H, K,
-                                                 d, N_cap, R_cap, total, k_old, v_old, k_new, v_new);
+        reconstruct_keys_kernel<<<grid, kRecThreads, 0, s>>>(new_view, old_view.n_layers, new_view.n_layers, key_idx,
+                                                         H, K, d, N_cap, R_cap, total, k_old, v_old, k_new, v_new,
+                                                         row_pos, R, count_total, n_count, row_cnt);
     }
     return cudaGetLastError();
 }
