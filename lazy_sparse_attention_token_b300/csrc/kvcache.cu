@@ -53,7 +53,10 @@ store_rows_kernel(const uint4 *__restrict__ src, int n_rows, int vecs, uint4 *__
 // loaded together, each earlier delta layer costs one slot lookup, one
 // 16-byte codes load and one scale load for the whole group, and the group's
 // 32 codes (16 bytes) go out in one store. blockIdx.y: 0 = K, 1 = V.
-__global__ void __launch_bounds__(256)
+// Four 256-thread blocks per SM (64 registers): the kernel waits on chains of
+// dependent gathers (one per earlier delta layer), so resident warps matter more
+// than a few spilled registers.
+__global__ void __launch_bounds__(256, 4)
 delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint16_t *__restrict__ v_l,
                     int rows_are_tokens, int src_rows, const int32_t *__restrict__ active, int R, int at,
                     int H, int d, int N_cap, int R_cap, long long total, int32_t *__restrict__ out_idx,
