@@ -63,16 +63,19 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
                     int32_t *__restrict__ out_slot, uint8_t *__restrict__ k_codes,
                     uint16_t *__restrict__ k_scales, uint8_t *__restrict__ v_codes,
                     uint16_t *__restrict__ v_scales) {
-    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= total) return;
+    // 32-bit index arithmetic (the launcher checks that total fits): 64-bit
+    // division and remainder are long instruction sequences
+    const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= (uint32_t)total) return;
     const bool is_v = blockIdx.y == 1;
-    const int gpr = d / 32;   // quantisation groups per (row, head)
-    const int g = (int)(t % gpr);
-    const long long rest = t / gpr;
-    const int h = (int)(rest % H);
-    const long long be = rest / H;   // b * R + e
-    const long long b = be / R;
-    const int e = (int)(be % R);
+    const uint32_t gpr = (uint32_t)d / 32u;   // quantisation groups per (row, head)
+    const uint32_t rest = t / gpr;
+    const int g = (int)(t - rest * gpr);
+    const uint32_t be32 = rest / (uint32_t)H;   // b * R + e
+    const int h = (int)(rest - be32 * (uint32_t)H);
+    const uint32_t b32 = be32 / (uint32_t)R;
+    const int e = (int)(be32 - b32 * (uint32_t)R);
+    const long long be = be32, b = b32;
     const int i = __ldg(active + be);
     const long long src_row = rows_are_tokens ? (long long)i : (long long)e;
 
@@ -173,11 +176,11 @@ reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const in
                         int32_t *__restrict__ row_cnt) {
     if ((int)blockIdx.x < n_count_blocks) {
         if (blockIdx.y != 0) return;
-        const long long t = (long long)blockIdx.x * kRecThreads + threadIdx.x;
-        if (t >= count_total) return;
-        const long long bh = t / R;
-        const int i = (int)(t - bh * R);
-        const long long b = bh / H;
+        const uint32_t t = blockIdx.x * kRecThreads + threadIdx.x;
+        if (t >= (uint32_t)count_total) return;
+        const uint32_t bh32 = t / (uint32_t)R;
+        const int i = (int)(t - bh32 * (uint32_t)R);
+        const long long bh = bh32, b = bh32 / (uint32_t)H;
         const int32_t *S = key_idx + bh * K;
         const int x = __ldg(row_pos + b * R + i);
         int lo = 0, hi = K;
@@ -188,15 +191,16 @@ reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const in
         row_cnt[bh * R + i] = lo;
         return;
     }
-    const long long t = (long long)(blockIdx.x - n_count_blocks) * kRecThreads + threadIdx.x;
-    if (t >= total) return;
+    const uint32_t t = (blockIdx.x - (uint32_t)n_count_blocks) * kRecThreads + threadIdx.x;   // 32-bit, as above
+    if (t >= (uint32_t)total) return;
     const bool is_v = blockIdx.y == 1;
-    const int gpr = d / 32;
-    const int g = (int)(t % gpr);
-    const long long bhr = t / gpr;          // (b * H + h) * K + r
-    const long long bh = bhr / K;
-    const int h = (int)(bh % H);
-    const long long b = bh / H;
+    const uint32_t gpr = (uint32_t)d / 32u;
+    const uint32_t bhr32 = t / gpr;          // (b * H + h) * K + r
+    const int g = (int)(t - bhr32 * gpr);
+    const uint32_t bh32 = bhr32 / (uint32_t)K;
+    const uint32_t b32 = bh32 / (uint32_t)H;
+    const int h = (int)(bh32 - b32 * (uint32_t)H);
+    const long long bhr = bhr32, b = b32;
     const int j = __ldg(key_idx + bhr);
     const uint16_t *base = (is_v ? view.v_base : view.k_base) + ((b * N_cap + j) * H + h) * (long long)d + g * 32;
     uint4 bv[4];
@@ -259,6 +263,7 @@ cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, cons
                                 uint16_t *v_scales, cudaStream_t s) {
     const long long total = (long long)B * R * H * (d / 32);
     if (total == 0) return cudaSuccess;
+    if (total > 0x7fffffffLL - 256) return cudaErrorInvalidValue;   // the kernel indexes in 32 bits
     dim3 grid(ceil_div(total, 256), 2);
     {
         KernelTimer kt("delta_append", s);
@@ -278,6 +283,7 @@ cudaError_t launch_reconstruct_keys(const DeltaView &old_view, const DeltaView &
     const long long count_total = row_cnt ? (long long)B * H * R : 0;
     const int n_count = ceil_div(count_total, kRecThreads);
     if (total == 0 && n_count == 0) return cudaSuccess;
+    if (total + count_total > 0x7fffffffLL - 2 * kRecThreads) return cudaErrorInvalidValue;   // 32-bit indexing
     dim3 grid(n_count + ceil_div(total, kRecThreads), 2);
     {
         KernelTimer kt("reconstruct_keys", s);
