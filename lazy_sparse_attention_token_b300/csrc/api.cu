@@ -358,10 +358,12 @@ flashloop_status_t flashloop_gather(const void *src, int32_t B, int32_t N, int32
     return FLASHLOOP_OK;
 }
 
-flashloop_status_t flashloop_kv_delta_append(flashloop_kv_cache_t *cache, int32_t loop, const uint16_t *k_l,
-                                             const uint16_t *v_l, int32_t rows_are_tokens,
-                                             const int32_t *active_idx, int32_t R, int32_t at,
-                                             flashloop_stream_t stream) {
+namespace fl {
+// slots_cleared: the caller already reset the layer's slot map (at == 0), earlier
+// on the stream, so that the append kernel directly follows the token selection.
+static flashloop_status_t delta_append_impl(flashloop_kv_cache_t *cache, int32_t loop, const uint16_t *k_l,
+                                            const uint16_t *v_l, int32_t rows_are_tokens, const int32_t *active_idx,
+                                            int32_t R, int32_t at, bool slots_cleared, flashloop_stream_t stream) {
     flashloop_status_t st = check_cache(cache);
     if (st != FLASHLOOP_OK) return st;
     const flashloop_dims_t &dm = cache->dims;
@@ -374,7 +376,7 @@ flashloop_status_t flashloop_kv_delta_append(flashloop_kv_cache_t *cache, int32_
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "R=%d at=%d (layer holds %d)", R, at, cache->count[m]);
     if (at + R > dm.R_cap) return set_error(FLASHLOOP_ERR_CAPACITY, "delta layer full (%d + %d > %d)", at, R, dm.R_cap);
     if ((st = check_device()) != FLASHLOOP_OK) return st;
-    if (at == 0) {
+    if (at == 0 && !slots_cleared) {
         cudaError_t e = cudaMemsetAsync(cache->slot[m], 0xFF, (size_t)dm.B * dm.N_cap * 4, stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(slot)");
     }
@@ -388,6 +390,14 @@ flashloop_status_t flashloop_kv_delta_append(flashloop_kv_cache_t *cache, int32_
     if (e != cudaSuccess) return cuda_fail(e, "kv_delta_append");
     cache->count[m] = at + R;
     return FLASHLOOP_OK;
+}
+}  // namespace fl
+
+flashloop_status_t flashloop_kv_delta_append(flashloop_kv_cache_t *cache, int32_t loop, const uint16_t *k_l,
+                                             const uint16_t *v_l, int32_t rows_are_tokens,
+                                             const int32_t *active_idx, int32_t R, int32_t at,
+                                             flashloop_stream_t stream) {
+    return fl::delta_append_impl(cache, loop, k_l, v_l, rows_are_tokens, active_idx, R, at, false, stream);
 }
 
 flashloop_status_t flashloop_kv_dense_store(flashloop_kv_cache_t *cache, int32_t loop, const uint16_t *k,
@@ -611,6 +621,12 @@ flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop
     if (!a->h_prev || !a->h_cur || !a->active_idx || !a->key_idx)
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "lazy loop needs h_prev, h_cur, active_idx and key_idx");
     float *scores = a->scores ? a->scores : reinterpret_cast<float *>(ws + W.scores);
+    {   // this loop's delta layer starts empty; cleared first so that the append
+        // kernel follows the token selection kernel directly
+        const int m = l - dm.T_dense - 1;
+        cudaError_t e = cudaMemsetAsync(c->slot[m], 0xFF, (size_t)dm.B * dm.N_cap * 4, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(slot)");
+    }
     // The key columns depend only on the previous loop's column mass, so their
     // selection runs on a side stream while the token selection and the K/V
     // delta append run on the caller's; the attention waits for both.
@@ -628,7 +644,7 @@ flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop
     if (st == FLASHLOOP_OK)
         st = flashloop_select_tokens(a->h_prev, a->h_cur, dm.B, n, dm.H * dm.d, dm.R, a->active_idx, scores,
                                      nullptr, 0, stream);
-    if (st == FLASHLOOP_OK) st = flashloop_kv_delta_append(c, l, a->k, a->v, 1, a->active_idx, dm.R, 0, stream);
+    if (st == FLASHLOOP_OK) st = delta_append_impl(c, l, a->k, a->v, 1, a->active_idx, dm.R, 0, true, stream);
     if (ss) {   // join (also on failure, so that the caller's stream is never left forked)
         cudaError_t e = cudaEventRecord(ss->join, ss->s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), ss->join, 0);

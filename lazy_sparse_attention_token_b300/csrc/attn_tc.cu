@@ -255,6 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tm_k_old,
                     const __grid_constant__ CUtensorMap tm_v_old, const __grid_constant__ CUtensorMap tm_k_new,
                     const __grid_constant__ CUtensorMap tm_v_new) {
+    pdl_wait();   // every global read below depends on the previous kernel
+    pdl_trigger();
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -824,7 +826,9 @@ cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
     if (!dense && !p.row_cnt) return cudaErrorInvalidValue;
     {
         KernelTimer kt("tc_attention", s);
-        tc_attention_kernel<D><<<grid, kThreads, Cf::SMEM, s>>>(kp, maps[0], maps[1], maps[2], maps[3]);
+        const cudaError_t e = launch_pdl(tc_attention_kernel<D>, grid, dim3(kThreads), (size_t)Cf::SMEM, s, kp,
+                                         maps[0], maps[1], maps[2], maps[3]);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -63,6 +63,8 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
                     int32_t *__restrict__ out_slot, uint8_t *__restrict__ k_codes,
                     uint16_t *__restrict__ k_scales, uint8_t *__restrict__ v_codes,
                     uint16_t *__restrict__ v_scales) {
+    pdl_wait();
+    pdl_trigger();
     // 32-bit index arithmetic (the launcher checks that total fits): 64-bit
     // division and remainder are long instruction sequences
     const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
@@ -174,6 +176,8 @@ reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const in
                         uint16_t *__restrict__ k_new, uint16_t *__restrict__ v_new,
                         const int32_t *__restrict__ row_pos, int R, long long count_total, int n_count_blocks,
                         int32_t *__restrict__ row_cnt) {
+    pdl_wait();
+    pdl_trigger();
     if ((int)blockIdx.x < n_count_blocks) {
         if (blockIdx.y != 0) return;
         const uint32_t t = blockIdx.x * kRecThreads + threadIdx.x;
@@ -267,9 +271,10 @@ cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, cons
     dim3 grid(ceil_div(total, 256), 2);
     {
         KernelTimer kt("delta_append", s);
-        delta_append_kernel<<<grid, 256, 0, s>>>(view, k_l, v_l, rows_are_tokens, src_rows, active, R, at, H, d,
-                                             N_cap, R_cap, total, out_idx, out_slot, k_codes, k_scales,
-                                             v_codes, v_scales);
+        const cudaError_t e = launch_pdl(delta_append_kernel, grid, dim3(256), 0, s, view, k_l, v_l,
+                                         rows_are_tokens, src_rows, active, R, at, H, d, N_cap, R_cap, total,
+                                         out_idx, out_slot, k_codes, k_scales, v_codes, v_scales);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -287,9 +292,11 @@ cudaError_t launch_reconstruct_keys(const DeltaView &old_view, const DeltaView &
     dim3 grid(n_count + ceil_div(total, kRecThreads), 2);
     {
         KernelTimer kt("reconstruct_keys", s);
-        reconstruct_keys_kernel<<<grid, kRecThreads, 0, s>>>(new_view, old_view.n_layers, new_view.n_layers, key_idx,
-                                                         H, K, d, N_cap, R_cap, total, k_old, v_old, k_new, v_new,
-                                                         row_pos, R, count_total, n_count, row_cnt);
+        const cudaError_t e = launch_pdl(reconstruct_keys_kernel, grid, dim3(kRecThreads), 0, s, new_view,
+                                         old_view.n_layers, new_view.n_layers, key_idx, H, K, d, N_cap, R_cap,
+                                         total, k_old, v_old, k_new, v_new, row_pos, R, count_total, n_count,
+                                         row_cnt);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -20,6 +20,8 @@ constexpr int kScoreWarps = 8;
 __global__ void __launch_bounds__(kScoreWarps * 32)
 token_scores_kernel(const uint16_t *__restrict__ h_prev, const uint16_t *__restrict__ h_cur,
                     long long rows, int D, float *__restrict__ score) {
+    pdl_wait();
+    pdl_trigger();
     const long long row = (long long)blockIdx.x * kScoreWarps + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -124,6 +126,8 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
     __shared__ int s_kleft;
     __shared__ unsigned long long warp_tot[kTopkClWarps];
 
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = cl_rank(), ncta = cl_size();
     const int row_id = blockIdx.x / ncta;
@@ -251,7 +255,9 @@ cudaError_t launch_token_scores(const uint16_t *h_prev, const uint16_t *h_cur, i
     const long long rows = (long long)B * N;
     {
         KernelTimer kt("token_scores", s);
-        token_scores_kernel<<<ceil_div(rows, kScoreWarps), kScoreWarps * 32, 0, s>>>(h_prev, h_cur, rows, D, scores);
+        const cudaError_t e = launch_pdl(token_scores_kernel, dim3(ceil_div(rows, kScoreWarps)),
+                                         dim3(kScoreWarps * 32), 0, s, h_prev, h_cur, rows, D, scores);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -271,13 +277,15 @@ cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t 
     cfg.blockDim = dim3(kTopkClThreads);
     cfg.dynamicSmemBytes = staged ? (size_t)seg * 4 : 0;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)ncta;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_wait()
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e;
     {
         KernelTimer kt("topk", s);
