@@ -12,14 +12,15 @@
 //
 // One thread-block cluster per (sequence, head, row); its CTAs split the row's
 // key list into contiguous chunks, so a long list is streamed by several SMs.
-// In a CTA, 16 groups of 16 lanes walk the chunk, kU keys per group at a time:
-// all their base rows, then layer by layer all their slot lookups and then all
-// their delta codes are loaded together, so a key's chain of dependent loads
-// is shared by kU keys. Pass 1 keeps the chunk's old and new logits in shared
-// memory; the row statistics (old mass m, logsumexp lam) are merged across the
-// cluster through distributed shared memory; pass 2 accumulates u and w and
-// updates the column mass; the u and w partials are summed on cluster rank 0,
-// which updates the row's state.
+// In a CTA, 16 groups of 16 lanes walk the chunk, kU keys per group at a time.
+// Every delta layer's entry of every key of the chunk is looked up once, into
+// shared memory, for both passes; a step then loads its kU base rows and the
+// codes of two layers at a time together, with no dependent lookup in front.
+// Pass 1 keeps the chunk's old and new logits in shared memory; the row
+// statistics (old mass m, logsumexp lam) are merged across the cluster through
+// distributed shared memory; pass 2 accumulates u and w and updates the column
+// mass; the u and w partials are summed on cluster rank 0, which updates the
+// row's state.
 #include <float.h>
 #include <mutex>
 
@@ -103,49 +104,58 @@ struct DecKParams {
     float scale;
 };
 
-// Reconstructions of kU cache rows (8-element chunk c8 of head h): `o` at the
-// old view (base + its delta layers), `n` at the new view (o + the new view's
-// further layers); deltas are added in ascending loop order in fp32. Loads
-// are issued in rounds shared by the kU rows: base rows, then per layer the
-// slot lookups and then the codes and scales.
+// Reconstruction (base + delta layers, fp32 in ascending layer order) of the
+// 8-element chunk c8 of kU keys j at the old view's layers (o) and the new
+// view's (n). Every layer's entry of every key of the chunk was looked up once
+// into shared memory (ents[m * chunk + t], t = the key's place in the chunk),
+// so the codes and scales of two layers at a time load together with no
+// dependent lookup in front of them.
+constexpr int kLayerPair = 2;
 template <int D>
 __device__ __forceinline__ void load_rec(const DeltaView &ov, const DeltaView &nv, bool is_v, long long b,
-                                         const int (&j)[kU], int h, int c8, int H, int N_cap, int R_cap,
-                                         float (&o)[kU][8], float (&n)[kU][8]) {
+                                         const int (&j)[kU], const int (&tt)[kU], const int *ents, int chunk, int h,
+                                         int c8, int H, int N_cap, int R_cap, float (&o)[kU][8], float (&n)[kU][8]) {
     const uint16_t *base = is_v ? ov.v_base : ov.k_base;
 #pragma unroll
     for (int u = 0; u < kU; ++u) load_base8(base, b, j[u], h, c8, H, D, N_cap, o[u]);
-    for (int m = 0; m < nv.n_layers; ++m) {
-        if (m == ov.n_layers) {
+    for (int m0 = 0; m0 < nv.n_layers; m0 += kLayerPair) {
+        int ent[kLayerPair][kU];
+        uint32_t w[kLayerPair][kU];
+        float s[kLayerPair][kU];
 #pragma unroll
-            for (int u = 0; u < kU; ++u)
+        for (int mm = 0; mm < kLayerPair; ++mm) {
+            const int m = m0 + mm;
+            const bool live = m < nv.n_layers;
+            const uint8_t *codes = live ? (is_v ? nv.v_codes[m] : nv.k_codes[m]) : nullptr;
+            const uint16_t *scales = live ? (is_v ? nv.v_scales[m] : nv.k_scales[m]) : nullptr;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) n[u][e] = o[u][e];
-        }
-        int ent[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) ent[u] = __ldg(nv.slot[m] + b * N_cap + j[u]);
-        const uint8_t *codes = is_v ? nv.v_codes[m] : nv.k_codes[m];
-        const uint16_t *scales = is_v ? nv.v_scales[m] : nv.k_scales[m];
-        uint32_t w[kU];
-        float s[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            w[u] = 0u;
-            s[u] = 0.f;
-            if (ent[u] >= 0) {
-                const long long e = (b * R_cap + ent[u]) * H + h;
-                w[u] = __ldg(reinterpret_cast<const uint32_t *>(codes + e * (D / 2)) + c8);
-                s[u] = __half2float(__ushort_as_half(__ldg(scales + e * (D / 32) + c8 / 4)));
+            for (int u = 0; u < kU; ++u) {
+                ent[mm][u] = live ? ents[m * chunk + tt[u]] : -1;
+                w[mm][u] = 0u;
+                s[mm][u] = 0.f;
+                if (ent[mm][u] >= 0) {
+                    const long long e = (b * R_cap + ent[mm][u]) * H + h;
+                    w[mm][u] = __ldg(reinterpret_cast<const uint32_t *>(codes + e * (D / 2)) + c8);
+                    s[mm][u] = __half2float(__ushort_as_half(__ldg(scales + e * (D / 32) + c8 / 4)));
+                }
             }
         }
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            if (ent[u] < 0) continue;
-            float *r = m < ov.n_layers ? o[u] : n[u];
+        for (int mm = 0; mm < kLayerPair; ++mm) {
+            const int m = m0 + mm;
+            if (m >= nv.n_layers) break;
+            if (m == ov.n_layers) {
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                r[t] = __fadd_rn(r[t], __fmul_rn(s[u], code_f32(w[u], t)));
+                for (int u = 0; u < kU; ++u)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) n[u][e] = o[u][e];
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                if (ent[mm][u] < 0) continue;
+                float *r = m < ov.n_layers ? o[u] : n[u];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) r[t] = __fadd_rn(r[t], __fmul_rn(s[mm][u], code_f32(w[mm][u], t)));
             }
         }
     }
@@ -158,7 +168,7 @@ __device__ __forceinline__ void load_rec(const DeltaView &ov, const DeltaView &n
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 decode_attention_kernel(const __grid_constant__ DecKParams p) {
     extern __shared__ float sm[];
     constexpr int CH = D / 8;
@@ -199,6 +209,7 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
     float *acc = red + kThreads / 32;                         // [2][kGroups][D]
     float *stats = acc + 2 * kGroups * D;                     // [kMaxCluster][3] (mx, ls, ms) of every rank
     float *uw = stats + kMaxCluster * 3;                      // [2][D] cluster sums of u, w (rank 0)
+    int *ents = reinterpret_cast<int *>(uw + 2 * D);          // lazy: [layers][p.chunk] delta entries
 
     const int grp = threadIdx.x >> 4, gl = threadIdx.x & 15;
     const bool has_chunk = gl < CH;
@@ -212,21 +223,31 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
     if (rank == 0)
         for (int x = threadIdx.x; x < 2 * D; x += kThreads) uw[x] = 0.f;
     __syncthreads();
+    if (p.shared_base) {   // every (layer, key) entry of the chunk, looked up once for both passes
+        const int nl = p.new_view.n_layers;
+        for (int x = threadIdx.x; x < nl * cn; x += kThreads) {
+            const int m = x / cn, t = x - m * cn;
+            ents[m * p.chunk + t] = __ldg(p.new_view.slot[m] + b * p.N_cap + idx[t]);
+        }
+        __syncthreads();
+    }
     auto key_at = [&](int t) { return dense ? k0 + t : idx[t]; };
 
     // pass 1: logits of the chunk's keys. Both 16-lane groups of a warp run the
     // same number of steps (keys past the end recompute the chunk's first key and
     // store nothing) because the sums below shuffle across the whole warp.
     for (int t0 = 0; t0 < cn; t0 += kGroups * kU) {
-        int jj[kU];
+        int jj[kU], tt[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int t = t0 + u * kGroups + grp;
-            jj[u] = key_at(t < cn ? t : 0);
+            tt[u] = t < cn ? t : 0;
+            jj[u] = key_at(tt[u]);
         }
         float kn[kU][8], ko[kU][8];
         if (p.shared_base) {
-            load_rec<D>(p.old_view, p.new_view, false, b, jj, h, c8, p.H, p.N_cap, p.R_cap, ko, kn);
+            load_rec<D>(p.old_view, p.new_view, false, b, jj, tt, ents, p.chunk, h, c8, p.H, p.N_cap, p.R_cap, ko,
+                        kn);
         } else {
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
@@ -297,15 +318,17 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
     float u_[8] = {0, 0, 0, 0, 0, 0, 0, 0}, w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float *cb = p.c + bh * p.n_keys;
     for (int t0 = 0; t0 < cn; t0 += kGroups * kU) {
-        int jj[kU];
+        int jj[kU], tt[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int t = t0 + u * kGroups + grp;
-            jj[u] = key_at(t < cn ? t : 0);
+            tt[u] = t < cn ? t : 0;
+            jj[u] = key_at(tt[u]);
         }
         float vn[kU][8], vo[kU][8];
         if (p.shared_base) {
-            load_rec<D>(p.old_view, p.new_view, true, b, jj, h, c8, p.H, p.N_cap, p.R_cap, vo, vn);
+            load_rec<D>(p.old_view, p.new_view, true, b, jj, tt, ents, p.chunk, h, c8, p.H, p.N_cap, p.R_cap, vo,
+                        vn);
         } else {
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
@@ -368,7 +391,9 @@ cudaError_t launch_d(const DecodeAttnParams &q, cudaStream_t s) {
     const int nk_max = q.mode == FLASHLOOP_ATTN_LAZY ? q.K : q.n_keys;
     const int ncta = max(1, min(kMaxCluster, (nk_max + kKeysPerCta - 1) / kKeysPerCta));
     const int chunk = (nk_max + ncta - 1) / ncta;
-    const size_t smem = (size_t)(3 * chunk + kThreads / 32 + 2 * kGroups * D + kMaxCluster * 3 + 2 * D) * sizeof(float);
+    const int n_ent = q.mode == FLASHLOOP_ATTN_LAZY ? q.new_view.n_layers * chunk : 0;   // delta entries
+    const size_t smem =
+        (size_t)(3 * chunk + kThreads / 32 + 2 * kGroups * D + kMaxCluster * 3 + 2 * D + n_ent) * sizeof(float);
     if (smem > 220 * 1024) return cudaErrorInvalidValue;
     static std::once_flag once;
     std::call_once(once, [] {
