@@ -100,7 +100,6 @@ struct DecKParams {
     uint16_t *q_hat;
     float *o, *z, *c;
     DeltaView old_view, new_view;
-    bool shared_base;   // old and new share the base (lazy): reconstruct incrementally
     float scale;
 };
 
@@ -167,8 +166,12 @@ __device__ __forceinline__ void load_rec(const DeltaView &ov, const DeltaView &n
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+// One instantiation per mode, so that a mode's unused state (the old keys and
+// values of the first dense loop, the delta entries of a dense loop) takes no
+// registers: the first loop, a pure stream of K/V rows, then fits four CTAs per
+// SM and keeps twice the bytes in flight.
+template <int D, int kMode>
+__global__ void __launch_bounds__(kThreads, kMode == FLASHLOOP_ATTN_FIRST_DENSE ? 4 : 2)
 decode_attention_kernel(const __grid_constant__ DecKParams p) {
     extern __shared__ float sm[];
     constexpr int CH = D / 8;
@@ -178,8 +181,9 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
     const long long bh = item / p.R;
     const int h = (int)(bh % p.H);
     const long long b = bh / p.H;
-    const bool dense = p.mode != FLASHLOOP_ATTN_LAZY;
-    const bool first = p.mode == FLASHLOOP_ATTN_FIRST_DENSE;
+    constexpr bool dense = kMode != FLASHLOOP_ATTN_LAZY;
+    constexpr bool first = kMode == FLASHLOOP_ATTN_FIRST_DENSE;
+    constexpr bool shared_base = kMode == FLASHLOOP_ATTN_LAZY;   // old and new share the base: incremental
     const int pos = __ldg(p.row_pos + b * p.R + row);
     const int slot = p.row_slot ? __ldg(p.row_slot + b * p.R + row) : pos;
     const int32_t *S = dense ? nullptr : p.key_idx + bh * p.K;
@@ -223,7 +227,7 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
     if (rank == 0)
         for (int x = threadIdx.x; x < 2 * D; x += kThreads) uw[x] = 0.f;
     __syncthreads();
-    if (p.shared_base) {   // every (layer, key) entry of the chunk, looked up once for both passes
+    if (shared_base) {   // every (layer, key) entry of the chunk, looked up once for both passes
         const int nl = p.new_view.n_layers;
         for (int x = threadIdx.x; x < nl * cn; x += kThreads) {
             const int m = x / cn, t = x - m * cn;
@@ -245,7 +249,7 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
             jj[u] = key_at(tt[u]);
         }
         float kn[kU][8], ko[kU][8];
-        if (p.shared_base) {
+        if constexpr (shared_base) {
             load_rec<D>(p.old_view, p.new_view, false, b, jj, tt, ents, p.chunk, h, c8, p.H, p.N_cap, p.R_cap, ko,
                         kn);
         } else {
@@ -326,7 +330,7 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
             jj[u] = key_at(tt[u]);
         }
         float vn[kU][8], vo[kU][8];
-        if (p.shared_base) {
+        if constexpr (shared_base) {
             load_rec<D>(p.old_view, p.new_view, true, b, jj, tt, ents, p.chunk, h, c8, p.H, p.N_cap, p.R_cap, vo,
                         vn);
         } else {
@@ -397,7 +401,12 @@ cudaError_t launch_d(const DecodeAttnParams &q, cudaStream_t s) {
     if (smem > 220 * 1024) return cudaErrorInvalidValue;
     static std::once_flag once;
     std::call_once(once, [] {
-        cudaFuncSetAttribute(decode_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+        cudaFuncSetAttribute(decode_attention_kernel<D, FLASHLOOP_ATTN_FIRST_DENSE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+        cudaFuncSetAttribute(decode_attention_kernel<D, FLASHLOOP_ATTN_DENSE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+        cudaFuncSetAttribute(decode_attention_kernel<D, FLASHLOOP_ATTN_LAZY>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     });
     DecKParams p;
     p.mode = q.mode;
@@ -419,7 +428,6 @@ cudaError_t launch_d(const DecodeAttnParams &q, cudaStream_t s) {
     p.c = q.c;
     p.old_view = q.old_view;
     p.new_view = q.new_view;
-    p.shared_base = q.mode == FLASHLOOP_ATTN_LAZY;
     p.scale = 1.0f / sqrtf((float)D);
     const long long grid = (long long)q.B * q.H * q.R * ncta;
     cudaLaunchConfig_t cfg = {};
@@ -437,7 +445,10 @@ cudaError_t launch_d(const DecodeAttnParams &q, cudaStream_t s) {
     cudaError_t e;
     {
         KernelTimer kt("decode_attention", s);
-        e = cudaLaunchKernelEx(&cfg, decode_attention_kernel<D>, p);
+        e = q.mode == FLASHLOOP_ATTN_FIRST_DENSE
+                ? cudaLaunchKernelEx(&cfg, decode_attention_kernel<D, FLASHLOOP_ATTN_FIRST_DENSE>, p)
+            : q.mode == FLASHLOOP_ATTN_DENSE ? cudaLaunchKernelEx(&cfg, decode_attention_kernel<D, FLASHLOOP_ATTN_DENSE>, p)
+                                             : cudaLaunchKernelEx(&cfg, decode_attention_kernel<D, FLASHLOOP_ATTN_LAZY>, p);
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }
