@@ -153,8 +153,7 @@ __device__ __forceinline__ void load_rec(const DeltaView &ov, const DeltaView &n
             for (int u = 0; u < kU; ++u) {
                 if (ent[mm][u] < 0) continue;
                 float *r = m < ov.n_layers ? o[u] : n[u];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) r[t] = __fadd_rn(r[t], __fmul_rn(s[mm][u], code_f32(w[mm][u], t)));
+                dequant_add8(r, w[mm][u], s[mm][u]);
             }
         }
     }

@@ -149,6 +149,28 @@ __device__ __forceinline__ float code_f32(uint32_t w, int t) {
     return __fsub_rn(__uint_as_float(((w >> (4 * t)) & 0xFu) ^ 0x4B000008u), 8388616.0f);
 }
 
+// r[t] += s * code t of w (t = 0..7), two elements per packed fp32 instruction:
+// code_f32's exact subtraction, the exact product and the rounded sum, each
+// lane rounded exactly as the scalar __fadd_rn(r, __fmul_rn(s, code_f32(w, t))).
+__device__ __forceinline__ void dequant_add8(float *r, uint32_t w, float s) {
+#pragma unroll
+    for (int t = 0; t < 8; t += 2) {
+        const uint32_t n0 = ((w >> (4 * t)) & 0xFu) ^ 0x4B000008u;
+        const uint32_t n1 = ((w >> (4 * t + 4)) & 0xFu) ^ 0x4B000008u;
+        asm("{\n\t.reg .b64 c, k, m, a;\n\t"
+            "mov.b64 c, {%2, %3};\n\t"
+            "mov.b64 k, {%5, %5};\n\t"
+            "mov.b64 m, {%4, %4};\n\t"
+            "sub.rn.f32x2 c, c, k;\n\t"
+            "mul.rn.f32x2 c, c, m;\n\t"
+            "mov.b64 a, {%0, %1};\n\t"
+            "add.rn.f32x2 a, a, c;\n\t"
+            "mov.b64 {%0, %1}, a;\n\t}"
+            : "+f"(r[t]), "+f"(r[t + 1])
+            : "r"(n0), "r"(n1), "f"(s), "f"(8388616.0f));
+    }
+}
+
 // Adds scale*code of every delta layer of `view` that holds token i to the
 // 8 fp32 values of chunk c8 (elements 8*c8 .. 8*c8+7) of head h.
 __device__ __forceinline__ void apply_deltas(const DeltaView &view, bool is_v, int m0, int m1, long long b,
@@ -162,10 +184,7 @@ __device__ __forceinline__ void apply_deltas(const DeltaView &view, bool is_v, i
         const uint16_t *scales = is_v ? view.v_scales[m] : view.k_scales[m];
         const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(codes + ent * (d / 2)) + c8);
         const float s = __half2float(__ushort_as_half(__ldg(scales + ent * (d / 32) + c8 / 4)));
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            rec[t] = __fadd_rn(rec[t], __fmul_rn(s, code_f32(w, t)));
-        }
+        dequant_add8(rec, w, s);
     }
 }
 

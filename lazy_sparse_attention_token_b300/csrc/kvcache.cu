@@ -105,11 +105,7 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
         const float sc = __half2float(__ushort_as_half(__ldg(scales + ent * (d / 32) + g)));
         const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                rec[8 * c + k] = __fadd_rn(rec[8 * c + k], __fmul_rn(sc, code_f32(w[c], k)));
-            }
+        for (int c = 0; c < 4; ++c) dequant_add8(rec + 8 * c, w[c], sc);
     }
 
     float amax = 0.f;
@@ -224,10 +220,7 @@ reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const in
         const float sc = __half2float(__ushort_as_half(__ldg(scales + ent * (d / 32) + g)));
         const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                rec[8 * c + k] = __fadd_rn(rec[8 * c + k], __fmul_rn(sc, code_f32(w[c], k)));
+        for (int c = 0; c < 4; ++c) dequant_add8(rec + 8 * c, w[c], sc);
     }
     if (new_layers <= old_layers) store_group_bf16(rec, (is_v ? v_old : k_old) + bhr * d + g * 32);
     store_group_bf16(rec, (is_v ? v_new : k_new) + bhr * d + g * 32);
