@@ -176,6 +176,16 @@ def hbm_bytes(w, R, K):
     }
 
 
+def kv_cache_accounting(fl, dims, B, N, H, d, T):
+    """Bytes of this library's KV cache (a bf16 layer per dense loop; int4 delta
+    layers with fp16 group scales, entry lists and slot maps for the lazy loops)
+    against one bf16 K/V cache per loop, the layout a looped model keeps without
+    lazy updates."""
+    ours = fl.flashloop_kv_cache_bytes(dims)
+    per_loop = T * 2 * B * N * H * d * 2
+    return {"bytes": ours, "bf16_cache_per_loop_bytes": per_loop, "ratio": per_loop / ours if ours else None}
+
+
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu record (profiles/traffic.txt),
     or None when there is none or the kernel's source changed since the capture."""
@@ -351,7 +361,7 @@ def native(args, world, rank, local):
                    "launch": launch_mode,
                    "active_tokens_per_s": w.B * R * args.steps * world / secs},
         "roofline": roofline, "step_roofline": step_roofline, "kernels": kernels, "gpu_launches": launches,
-        "clocks": clk, "e2e": e2e,
+        "clocks": clk, "e2e": e2e, "kv_cache": kv_cache_accounting(fl, dims, w.B, w.N, w.H, w.d, w.T),
     }
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, R, K, state1, budget_s=args.cpu_budget)
@@ -480,6 +490,7 @@ def native_decode(args, world, rank, local):
                    "kernel_timing": "per-kernel durations from a second timed pass with a CUDA event pair "
                                     "around every launch"},
         "roofline": roofline, "kernels": kernels, "gpu_launches": launches, "clocks": clk, "e2e": None,
+        "kv_cache": kv_cache_accounting(fl, dims, w.B, Nk, w.H, w.d, w.T),
     }
 
 

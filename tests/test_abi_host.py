@@ -136,3 +136,32 @@ def test_append_and_attention_reject_bad_args(L):
     s.loop = 2
     s.cache = ctypes.pointer(c)
     assert L.flashloop_loop_step(ctypes.byref(s), None) == WORKSPACE
+
+
+def kv_layout_bytes(B, N_cap, H, d, R_cap, T, T_dense):
+    """The cache layout the header documents, summed without alignment padding:
+    a bf16 K and V layer per dense loop; per lazy loop an entry list [B, R_cap]
+    and slot map [B, N_cap] (int32) and, for K and V, int4 codes
+    [B, R_cap, H, d/2] with fp16 scales [B, R_cap, H, d/32]."""
+    dense = B * N_cap * H * d * 2
+    delta = B * R_cap * 4 + B * N_cap * 4 + 2 * (B * R_cap * H * (d // 2) + B * R_cap * H * (d // 32) * 2)
+    return 2 * T_dense * dense + (T - T_dense) * delta
+
+
+@pytest.mark.parametrize("shape, ratio_lo", [
+    # 32K prefill: 1 dense loop + 3 lazy loops of 15% active tokens
+    (dict(B=1, N_cap=32768, H=16, d=128, R=4916, K=3277, T=4, T_dense=1, R_cap=4916), 3.4),
+    # deep recurrence: 2 dense loops + 14 lazy loops of 10% active tokens
+    (dict(B=8, N_cap=16384, H=32, d=96, R=1639, K=820, T=16, T_dense=2, R_cap=1639), 6.5),
+])
+def test_cache_against_a_bf16_cache_per_loop(L, shape, ratio_lo):
+    """The base + int4-delta cache against one bf16 K/V cache per loop (a looped
+    model without lazy updates): the library's size is the documented layout up
+    to 256-byte alignment per section, and the ratio is what the deltas save."""
+    cb = fl.flashloop_kv_cache_bytes(dims(**shape))
+    want = kv_layout_bytes(shape["B"], shape["N_cap"], shape["H"], shape["d"], shape["R_cap"], shape["T"],
+                           shape["T_dense"])
+    sections = 2 * shape["T_dense"] + 6 * (shape["T"] - shape["T_dense"])
+    assert want <= cb <= want + 256 * sections
+    per_loop = shape["T"] * 2 * shape["B"] * shape["N_cap"] * shape["H"] * shape["d"] * 2
+    assert per_loop / cb >= ratio_lo
