@@ -104,19 +104,22 @@ struct DecKParams {
 };
 
 // Reconstruction (base + delta layers, fp32 in ascending layer order) of the
-// 8-element chunk c8 of kU keys j at the old view's layers (o) and the new
-// view's (n). Every layer's entry of every key of the chunk was looked up once
-// into shared memory (ents[m * chunk + t], t = the key's place in the chunk),
-// so the codes and scales of two layers at a time load together with no
-// dependent lookup in front of them.
+// 8-element chunk c8 of kU keys j, handed out twice per key: on_old(u, r) with
+// the old view's layers applied, then on_new(u, r) with the new view's. One
+// 8-float running value per key is live, not an old and a new copy. Every
+// layer's entry of every key of the chunk was looked up once into shared
+// memory (ents[m * chunk + t], t = the key's place in the chunk), so the codes
+// and scales of two layers at a time load together with no dependent lookup in
+// front of them.
 constexpr int kLayerPair = 2;
-template <int D>
-__device__ __forceinline__ void load_rec(const DeltaView &ov, const DeltaView &nv, bool is_v, long long b,
-                                         const int (&j)[kU], const int (&tt)[kU], const int *ents, int chunk, int h,
-                                         int c8, int H, int N_cap, int R_cap, float (&o)[kU][8], float (&n)[kU][8]) {
+template <int D, class OnOld, class OnNew>
+__device__ __forceinline__ void visit_rec(const DeltaView &ov, const DeltaView &nv, bool is_v, long long b,
+                                          const int (&j)[kU], const int (&tt)[kU], const int *ents, int chunk, int h,
+                                          int c8, int H, int N_cap, int R_cap, OnOld &&on_old, OnNew &&on_new) {
     const uint16_t *base = is_v ? ov.v_base : ov.k_base;
+    float r[kU][8];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) load_base8(base, b, j[u], h, c8, H, D, N_cap, o[u]);
+    for (int u = 0; u < kU; ++u) load_base8(base, b, j[u], h, c8, H, D, N_cap, r[u]);
     for (int m0 = 0; m0 < nv.n_layers; m0 += kLayerPair) {
         int ent[kLayerPair][kU];
         uint32_t w[kLayerPair][kU];
@@ -145,24 +148,19 @@ __device__ __forceinline__ void load_rec(const DeltaView &ov, const DeltaView &n
             if (m >= nv.n_layers) break;
             if (m == ov.n_layers) {
 #pragma unroll
-                for (int u = 0; u < kU; ++u)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) n[u][e] = o[u][e];
+                for (int u = 0; u < kU; ++u) on_old(u, r[u]);
             }
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                if (ent[mm][u] < 0) continue;
-                float *r = m < ov.n_layers ? o[u] : n[u];
-                dequant_add8(r, w[mm][u], s[mm][u]);
-            }
+            for (int u = 0; u < kU; ++u)
+                if (ent[mm][u] >= 0) dequant_add8(r[u], w[mm][u], s[mm][u]);
         }
     }
     if (nv.n_layers <= ov.n_layers) {
 #pragma unroll
-        for (int u = 0; u < kU; ++u)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) n[u][e] = o[u][e];
+        for (int u = 0; u < kU; ++u) on_old(u, r[u]);
     }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) on_new(u, r[u]);
 }
 
 // One instantiation per mode, so that a mode's unused state (the old keys and
@@ -247,27 +245,38 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
             tt[u] = t < cn ? t : 0;
             jj[u] = key_at(tt[u]);
         }
-        float kn[kU][8], ko[kU][8];
+        float dot_n[kU], dot_o[kU];   // this lane's part of q.k_new and qhat.k_old
+        // bf16 rounding of a reconstructed chunk, then its dot product with a query chunk
+        auto dot8 = [&](const float (&q8)[8], const float (&r)[8]) {
+            float k8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) k8[e] = r[e];
+            round_bf16x8(k8);
+            float acc8 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc8 = fmaf(q8[e], k8[e], acc8);
+            return acc8;
+        };
         if constexpr (shared_base) {
-            load_rec<D>(p.old_view, p.new_view, false, b, jj, tt, ents, p.chunk, h, c8, p.H, p.N_cap, p.R_cap, ko,
-                        kn);
-        } else {
+            visit_rec<D>(p.old_view, p.new_view, false, b, jj, tt, ents, p.chunk, h, c8, p.H, p.N_cap, p.R_cap,
+                         [&](int u, const float (&r)[8]) { dot_o[u] = dot8(qo, r); },
+                         [&](int u, const float (&r)[8]) { dot_n[u] = dot8(qn, r); });
+        } else {   // dense layers: every key's rows are requested before any is used
+            float kn[kU][8], ko[kU][8];
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 load_base8(p.new_view.k_base, b, jj[u], h, c8, p.H, D, p.N_cap, kn[u]);
                 if (!first) load_base8(p.old_view.k_base, b, jj[u], h, c8, p.H, D, p.N_cap, ko[u]);
             }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                dot_n[u] = dot8(qn, kn[u]);
+                dot_o[u] = first ? 0.f : dot8(qo, ko[u]);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            round_bf16x8(kn[u]);
-            if (!first) round_bf16x8(ko[u]);
-            float so = 0.f, sn = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                sn = fmaf(qn[e], kn[u][e], sn);
-                if (!first) so = fmaf(qo[e], ko[u][e], so);
-            }
+            float sn = dot_n[u], so = first ? 0.f : dot_o[u];
             if (!has_chunk) sn = so = 0.f;
             sn = group16_sum(sn);
             so = group16_sum(so);
@@ -328,33 +337,49 @@ decode_attention_kernel(const __grid_constant__ DecKParams p) {
             tt[u] = t < cn ? t : 0;
             jj[u] = key_at(tt[u]);
         }
-        float vn[kU][8], vo[kU][8];
+        // probabilities of the step's keys: new (a) and old (pj); keys past the end add nothing
+        float a[kU], pj[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int t = t0 + u * kGroups + grp;
+            const bool valid = t < cn;
+            a[u] = valid ? expf(tau[t] - lam) : 0.f;
+            pj[u] = valid && !first ? expf(sig[t] - zo) : 0.f;
+        }
+        // u += pj v_old and w += a v_new with the bf16-rounded reconstructions, key by key
+        auto acc8 = [&](float (&dst)[8], float coef, const float (&r)[8]) {
+            float v8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v8[e] = r[e];
+            round_bf16x8(v8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = fmaf(coef, v8[e], dst[e]);
+        };
         if constexpr (shared_base) {
-            load_rec<D>(p.old_view, p.new_view, true, b, jj, tt, ents, p.chunk, h, c8, p.H, p.N_cap, p.R_cap, vo,
-                        vn);
-        } else {
+            visit_rec<D>(p.old_view, p.new_view, true, b, jj, tt, ents, p.chunk, h, c8, p.H, p.N_cap, p.R_cap,
+                         [&](int u, const float (&r)[8]) {
+                             if (t0 + u * kGroups + grp < cn) acc8(u_, pj[u], r);
+                         },
+                         [&](int u, const float (&r)[8]) {
+                             if (t0 + u * kGroups + grp < cn) acc8(w, a[u], r);
+                         });
+        } else {   // dense layers: every key's rows are requested before any is used
+            float vn[kU][8], vo[kU][8];
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 load_base8(p.new_view.v_base, b, jj[u], h, c8, p.H, D, p.N_cap, vn[u]);
                 if (!first) load_base8(p.old_view.v_base, b, jj[u], h, c8, p.H, D, p.N_cap, vo[u]);
             }
-        }
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int t = t0 + u * kGroups + grp;
-            if (t >= cn) continue;
-            const float a = expf(tau[t] - lam);
-            const float pj = first ? 0.f : expf(sig[t] - zo);
-            round_bf16x8(vn[u]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = fmaf(a, vn[u][e], w[e]);
-            if (!first) {
-                round_bf16x8(vo[u]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) u_[e] = fmaf(pj, vo[u][e], u_[e]);
+            for (int u = 0; u < kU; ++u) {
+                if (t0 + u * kGroups + grp >= cn) continue;
+                acc8(w, a[u], vn[u]);
+                if (!first) acc8(u_, pj[u], vo[u]);
             }
-            if (gl == 0) atomicAdd(cb + jj[u], m * a - pj);
         }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (t0 + u * kGroups + grp < cn && gl == 0) atomicAdd(cb + jj[u], m * a[u] - pj[u]);
     }
     if (has_chunk) {
 #pragma unroll
