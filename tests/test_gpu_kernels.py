@@ -34,7 +34,8 @@ def randn_bf16(shape, seed, scale=1.0):
 # token selection
 
 @pytest.mark.parametrize("B,N,D,R", [(1, 1000, 256, 250), (3, 4097, 2048, 615), (1, 32768, 2048, 4916),
-                                     (2, 50, 64, 50), (1, 7, 8, 1), (2, 70000, 64, 9000)])
+                                     (2, 50, 64, 50), (1, 7, 8, 1), (2, 70000, 64, 9000),
+                                     (1, 400000, 8, 40000)])   # cluster segments too long to stage
 def test_select_tokens(B, N, D, R):
     hp = randn_bf16((B, N, D), 1)
     drift = torch.rand((B, N, 1), generator=gen(2), device="cuda") ** 4
@@ -62,7 +63,9 @@ def test_select_tokens_ties_go_to_lower_index():
 
 
 @pytest.mark.parametrize("B,H,N,K", [(1, 4, 1024, 103), (2, 16, 8192, 820), (1, 3, 129, 129), (4, 2, 5, 1),
-                                     (1, 16, 32768, 3277)])
+                                     (1, 16, 32768, 3277),
+                                     (2, 64, 3001, 300),        # one CTA per row, staged, ragged tail
+                                     (1, 128, 50000, 5000)])    # one CTA per row, row too long to stage
 def test_select_keys_exact(B, H, N, K):
     c = torch.randn(B, H, N, generator=gen(4), device="cuda").abs() * 3
     c = torch.where(torch.rand(B, H, N, generator=gen(5), device="cuda") < 0.2, torch.round(c), c)   # ties

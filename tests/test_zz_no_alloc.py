@@ -43,6 +43,20 @@ def test_no_alloc_selection_matches_workspace_selection_twice():
         assert np.array_equal(out.cpu().numpy(), ref.cpu().numpy()), f"call {call}"
 
 
+def test_no_alloc_selection_at_its_full_scratch():
+    L = fl.lib()
+    B, N, D, R = 4, (1 << 20) // 4, 8, 30000      # B*N exactly fills the fixed scratch
+    hp, hc = _inputs(303, B, N, D)
+    ref = fl.flashloop_select_tokens(hp, hc, R, scores=torch.empty(B, N, device="cuda"))
+    out = torch.full((B, R), -1, dtype=torch.int32, device="cuda")
+    st = L.flashloop_select_tokens_noalloc(ctypes.c_void_p(hp.data_ptr()), ctypes.c_void_p(hc.data_ptr()),
+                                           B, N, D, R, ctypes.c_void_p(out.data_ptr()),
+                                           ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, fl.flashloop._last_error()
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), ref.cpu().numpy())
+
+
 def test_no_alloc_rejects_sizes_beyond_its_scratch():
     L = fl.lib()
     hp, hc = _inputs(7, 1, 8, 8)
