@@ -1,0 +1,79 @@
+"""Host logic of bench.py that sets the roofline numerators: the causal
+(row, key) pair count of the lazy attention, the algorithmic bytes of the
+streaming kernels, and the hash check that keeps a stale ncu traffic record
+out of the report. No GPU needed."""
+import os
+
+import numpy as np
+import torch
+
+import bench
+import synth
+
+
+def test_pair_count_matches_brute_force():
+    rng = np.random.default_rng(11)
+    B, H, N, R, K = 3, 4, 97, 23, 19
+    A = np.stack([np.sort(rng.choice(N, R, replace=False)) for _ in range(B)]).astype(np.int32)
+    S = np.stack([[np.sort(rng.choice(N, K, replace=False)) for _ in range(H)] for _ in range(B)]).astype(np.int32)
+    pool = np.setdiff1d(np.arange(N), A[0, :3])   # keys at exactly a row's position count (causal j <= i)
+    S[0, 0] = np.sort(np.concatenate([A[0, :3], rng.choice(pool, K - 3, replace=False)]))
+    want = sum(1 for b in range(B) for h in range(H) for i in A[b] for j in S[b, h] if j <= i)
+    assert bench.pair_count(torch.from_numpy(A), torch.from_numpy(S)) == want
+
+
+def test_pair_count_edge_sets():
+    A = torch.tensor([[0, 5, 9]], dtype=torch.int32)
+    assert bench.pair_count(A, torch.tensor([[[10, 11]]], dtype=torch.int32)) == 0       # every key after every row
+    assert bench.pair_count(A, torch.tensor([[[0, 1, 2]]], dtype=torch.int32)) == 1 + 3 + 3
+    assert bench.pair_count(A, torch.arange(10, dtype=torch.int32).view(1, 1, 10)) == 1 + 6 + 10
+
+
+def test_streaming_bytes_at_32k_from_tensor_shapes():
+    """Bytes rebuilt from what each kernel reads and writes at B=1, N=32768,
+    H=16, d=128, R=4916, K=3277: bf16 hidden states, int4 codes (two per
+    byte) with one fp16 scale per 32 elements, int32 indices and slots."""
+    w = synth.WORKLOADS["32k"]
+    R, K = synth.active_count(w), synth.key_count(w)
+    assert (R, K) == (4916, 3277)
+    got = bench.hbm_bytes(w, R, K)
+    rows_bf16 = R * 16 * 128 * 2                       # one [R, H, d] bf16 tensor
+    codes, scales = R * 16 * 64, R * 16 * 4 * 2        # [R, H, d/2] u8 and [R, H, d/32] f16
+    assert got["token_scores"] == 2 * (32768 * 2048 * 2) + 32768 * 4 == 268566528
+    # K and V: loop-l rows and base rows read, codes and scales written; entry index and slot
+    assert got["delta_append"] == 2 * (2 * rows_bf16 + codes + scales) + R * 4 * 2 == 91909536
+    sel_bf16 = 16 * K * 128 * 2                        # one [H, K, d] bf16 tensor
+    # K and V: base rows of the selected keys read, old- and new-loop copies written; key list read
+    assert got["reconstruct_keys"] == 2 * (3 * sel_bf16) + 16 * K * 4 == 80745280
+
+
+def test_recorded_traffic_needs_the_captured_source(tmp_path, monkeypatch):
+    import hashlib
+    csrc = tmp_path / "lazy_sparse_attention_token_b300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    src = csrc / "k.cu"
+    src.write_bytes(b"__global__ void k() {}\n")
+    h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles" / "traffic.txt").write_text(
+        "# kernel workload bytes file hash\n"
+        f"k 32k 12345 k.cu {h}\n"
+        f"k 8k 777 k.cu {h}\n"
+        "gone 32k 1 missing.cu 0000000000000000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("k", "32k") == 12345
+    assert bench.recorded_traffic("k", "8k") == 777
+    assert bench.recorded_traffic("k", "deep") is None          # no capture of this workload
+    assert bench.recorded_traffic("gone", "32k") is None        # source file not there
+    src.write_bytes(b"__global__ void k() { }\n")                # kernel changed since the capture
+    assert bench.recorded_traffic("k", "32k") is None
+
+
+def test_committed_traffic_record_names_existing_sources():
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for line in open(os.path.join(root, "profiles", "traffic.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        kernel, workload, nbytes, fname, h = line.split()
+        assert int(nbytes) > 0 and len(h) == 16
+        assert os.path.exists(os.path.join(root, "lazy_sparse_attention_token_b300", "csrc", fname)), fname
