@@ -330,6 +330,93 @@ def test_rows_before_every_selected_key_are_unchanged(orc):
     assert np.array_equal(c[..., :30], st.c[..., :30]) and np.array_equal(c[..., 40:], st.c[..., 40:])
 
 
+def _prefix_softmax(q_rows, k, v, pos):
+    """Per (sequence, head, row): textbook softmax of q.k_j/sqrt(d) over keys
+    j <= pos in float64, giving (o, lse, p) with p over all keys (0 past pos)."""
+    q, k, v = (bits_to_f32(t).astype(np.float64) for t in (q_rows, k, v))
+    B, R, H, d = q.shape
+    Nk = k.shape[1]
+    o = np.zeros((B, R, H, d))
+    lse = np.zeros((B, H, R))
+    p = np.zeros((B, H, R, Nk))
+    for b in range(B):
+        for h in range(H):
+            for r in range(R):
+                n = pos[b, r] + 1
+                x = k[b, :n, h] @ q[b, r, h] / math.sqrt(d)
+                mx = x.max()
+                e = np.exp(x - mx)
+                p[b, h, r, :n] = e / e.sum()
+                lse[b, h, r] = mx + math.log(e.sum())
+                o[b, r, h] = p[b, h, r, :n] @ v[b, :n, h]
+    return o, lse, p
+
+
+def _decode_rows(seed, B=2, N=37, H=2, d=64):
+    """Two state slots per sequence whose rows sit at key positions N - 5 and
+    N (slots stored in the opposite order), over N + 1 keys: the decode form,
+    where a row's state slot is not its key position."""
+    rng = np.random.default_rng(seed)
+    q = bf16_bits(rng.standard_normal((B, 2, H, d)))
+    k, v = (bf16_bits(rng.standard_normal((B, N + 1, H, d))) for _ in range(2))
+    pos = np.tile(np.array([N - 5, N], np.int32), (B, 1))
+    slot = np.tile(np.array([1, 0], np.int32), (B, 1))
+    S = np.tile(np.arange(N + 1, dtype=np.int32), (B, H, 1))
+    return q, k, v, pos, slot, S
+
+
+def _by_slot(x_rows, slot, axis):
+    """Rows of x (row order) placed at their state slots along `axis`."""
+    out = np.empty_like(x_rows)
+    for r in range(slot.shape[1]):
+        idx = [slice(None)] * x_rows.ndim
+        src = list(idx)
+        idx[axis], src[axis] = int(slot[0, r]), r
+        out[tuple(idx)] = x_rows[tuple(src)]
+    return out
+
+
+def test_decode_rows_first_dense_is_prefix_softmax(orc):
+    """First dense loop on rows whose state slot differs from their key
+    position: each row gets softmax attention over its own causal prefix, and
+    c starts afresh as the sum of the rows' probabilities (any earlier c is
+    discarded, as the first dense loop has no previous state)."""
+    q, k, v, pos, slot, S = _decode_rows(21)
+    B, R, H, d = q.shape
+    Nk = k.shape[1]
+    q_slots = _by_slot(q, slot, 1)
+    c0 = np.random.default_rng(3).random((B, H, Nk)).astype(np.float32)
+    qh, o, z, c, m = orc.attention(True, pos, slot, q_slots, q_slots, np.full((B, R, H, d), 9.0, np.float32),
+                                   np.zeros((B, H, R), np.float32), c0, S, None, None, k, v, want_m=True)
+    o_ref, lse_ref, p_ref = _prefix_softmax(q, k, v, pos)
+    np.testing.assert_allclose(o, _by_slot(o_ref, slot, 1), rtol=1e-5, atol=2e-6)
+    np.testing.assert_allclose(z, _by_slot(lse_ref, slot, 2), rtol=0, atol=5e-6)
+    np.testing.assert_allclose(c, p_ref.sum(2), rtol=1e-5, atol=2e-6)
+    np.testing.assert_allclose(m, 1.0, rtol=0, atol=0)
+    assert np.array_equal(qh, q_slots)
+
+
+def test_decode_rows_lazy_full_set_is_softmax_of_new_keys(orc):
+    """A lazy loop over every key, after a dense loop on the previous keys, on
+    the decode-form rows: m = 1 and the result is softmax attention over the
+    new keys, each row over its own prefix."""
+    q1, k1, v1, pos, slot, S = _decode_rows(22)
+    q2, k2, v2, _, _, _ = _decode_rows(23)
+    B, R, H, d = q1.shape
+    Nk = k1.shape[1]
+    q1s, q2s = _by_slot(q1, slot, 1), _by_slot(q2, slot, 1)
+    zeros_c = np.zeros((B, H, Nk), np.float32)
+    qh1, o1, z1, c1, _ = orc.attention(True, pos, slot, q1s, q1s, np.zeros((B, R, H, d), np.float32),
+                                       np.zeros((B, H, R), np.float32), zeros_c, S, None, None, k1, v1)
+    qh2, o2, z2, c2, m = orc.attention(False, pos, slot, q2s, qh1, o1, z1, c1, S, k1, v1, k2, v2, want_m=True)
+    o_ref, lse_ref, p_ref = _prefix_softmax(q2, k2, v2, pos)
+    np.testing.assert_allclose(m, 1.0, rtol=0, atol=2e-6)
+    np.testing.assert_allclose(o2, _by_slot(o_ref, slot, 1), rtol=1e-5, atol=2e-6)
+    np.testing.assert_allclose(z2, _by_slot(lse_ref, slot, 2), rtol=0, atol=5e-6)
+    np.testing.assert_allclose(c2, p_ref.sum(2), rtol=1e-5, atol=2e-6)
+    assert np.array_equal(qh2, q2s)
+
+
 def test_chain_preserves_mass_and_bounds_m(orc):
     """Tiny workload through loops 1..T on the oracle alone: every row keeps
     unit mass, so the column masses always sum to the causal row count N."""
