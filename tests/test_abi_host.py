@@ -81,6 +81,23 @@ def test_select_tokens_rejects_bad_args(L):
     assert b"workspace" in L.flashloop_last_error()
 
 
+def test_select_tokens_noalloc_rejects_bad_args(L):
+    """Checked on the host before any device call: pointers, alignment, sizes,
+    and B*N against the fixed scratch of 1,048,576 scores. Every call here is
+    rejected by the host, so the placeholder pointers never reach a kernel."""
+    a, b, out = P(0x1000), P(0x2000), P(0x3000)
+    f = L.flashloop_select_tokens_noalloc
+    assert f(None, b, 1, 8, 16, 2, out, None) == INVALID
+    assert f(a, b, 1, 8, 16, 2, None, None) == INVALID
+    assert f(a, P(0x2008), 1, 8, 16, 2, out, None) == INVALID      # misaligned
+    assert f(a, b, 1, 8, 12, 2, out, None) == INVALID              # D % 8
+    assert f(a, b, 1, 8, 16, 9, out, None) == INVALID              # R > N
+    assert f(a, b, 0, 8, 16, 2, out, None) == INVALID              # B < 1
+    assert f(a, b, 4, (1 << 18) + 1, 16, 2, out, None) == CAPACITY
+    assert b"fixed scratch" in L.flashloop_last_error()
+    assert f(a, b, 1 << 11, 1 << 11, 16, 2, out, None) == CAPACITY  # 4,194,304 scores
+
+
 def test_gather_and_keys_reject_bad_args(L):
     assert L.flashloop_gather(P(0x1000), 1, 8, 24, P(0x2000), 2, P(0x3000), None) == INVALID      # row_bytes % 16
     assert L.flashloop_gather(P(0x1008), 1, 8, 32, P(0x2000), 2, P(0x3000), None) == INVALID      # misaligned
