@@ -139,6 +139,15 @@ def test_append_and_attention_reject_bad_args(L):
     # dense store of a lazy loop
     assert L.flashloop_kv_dense_store(ctypes.byref(c), 2, k, v, 0, 4, None) == INVALID
     assert L.flashloop_kv_dense_store(ctypes.byref(c), 1, k, v, 1020, 8, None) == CAPACITY
+    # reconstruct-gather of selected keys: lazy loops only, pointers, alignment, K
+    rk = L.flashloop_reconstruct_keys
+    kidx, o1, o2, o3, o4 = P(0x700000), P(0x710000), P(0x720000), P(0x730000), P(0x740000)
+    assert rk(ctypes.byref(c), 1, kidx, 8, o1, o2, o3, o4, None) == INVALID           # loop 1 is dense
+    assert rk(ctypes.byref(c), dm.T + 1, kidx, 8, o1, o2, o3, o4, None) == INVALID    # past the last loop
+    assert rk(ctypes.byref(c), 2, None, 8, o1, o2, o3, o4, None) == INVALID
+    assert rk(ctypes.byref(c), 2, kidx, 8, o1, o2, P(0x730008), o4, None) == INVALID  # misaligned output
+    assert rk(ctypes.byref(c), 2, kidx, 0, o1, o2, o3, o4, None) == INVALID
+    assert rk(ctypes.byref(c), 2, kidx, dm.N_cap + 1, o1, o2, o3, o4, None) == INVALID
     a = fl.AttnArgs()
     a.mode, a.loop, a.n_keys, a.n_state, a.R = fl.LAZY, 2, 1024, 1024, 4
     a.q = a.q_hat = a.o = 0x500000
