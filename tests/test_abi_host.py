@@ -164,6 +164,24 @@ def test_append_and_attention_reject_bad_args(L):
     assert L.flashloop_loop_step(ctypes.byref(s), None) == WORKSPACE
 
 
+def test_rejected_calls_launch_nothing(L):
+    """The launch counter (the source of the bench's launch figure) moves only
+    when a kernel is enqueued: calls the host rejects leave it unchanged."""
+    n0 = fl.flashloop_launch_count()
+    a, b, out = P(0x1000), P(0x2000), P(0x3000)
+    L.flashloop_select_tokens(a, b, 1, 8, 16, 9, out, None, None, 0, None)
+    L.flashloop_select_tokens_noalloc(a, b, 4, (1 << 18) + 1, 16, 2, out, None)
+    L.flashloop_gather(P(0x1000), 1, 8, 24, P(0x2000), 2, P(0x3000), None)
+    L.flashloop_select_keys(P(0x1000), 1, 4, 8, 9, P(0x2000), None, 0, None)
+    c = fake_cache(dims())
+    L.flashloop_kv_delta_append(ctypes.byref(c), 2, P(0x200000), P(0x300000), 1, P(0x400000), 300, 0, None)
+    s = fl.StepArgs()
+    s.loop = 2
+    s.cache = ctypes.pointer(c)
+    L.flashloop_loop_step(ctypes.byref(s), None)
+    assert fl.flashloop_launch_count() == n0
+
+
 def kv_layout_bytes(B, N_cap, H, d, R_cap, T, T_dense):
     """The cache layout the header documents, summed without alignment padding:
     a bf16 K and V layer per dense loop; per lazy loop an entry list [B, R_cap]
