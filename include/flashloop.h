@@ -276,7 +276,14 @@ flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *args, flashl
 
 /* ---- diagnostics -------------------------------------------------------- */
 
+/* Name of a status code ("ok", "invalid argument", ...), or "unknown status"
+ * for a value outside flashloop_status_t. A static string: do not free it. */
 const char *flashloop_status_string(flashloop_status_t status);
+
+/* Message of the most recent failing call made by the calling thread (which
+ * argument, size or CUDA call failed). Successful calls leave it unchanged;
+ * the pointer stays valid until that thread's next failing call. Owned by the
+ * library: do not free it. Empty before the thread's first failure. */
 const char *flashloop_last_error(void);
 
 /* Reads and clears the device-side failure word that kernels set when a

@@ -36,6 +36,17 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) <= set(fl.flashloop.EXPORTS) | set(names)
 
 
+def test_every_declaration_has_its_own_comment():
+    """Each entry point of the header is directly preceded by a comment of its
+    own (its operation, arguments, ownership and errors)."""
+    text = open(HEADER).read()
+    blank = re.sub(r"/\*.*?\*/", lambda m: " " * len(m.group(0)), text, flags=re.S)
+    for n in declared_functions():
+        m = re.search(r"^[^\n]*\b" + n + r"\s*\(", blank, re.M)
+        assert m, n
+        assert text[:m.start()].rstrip().endswith("*/"), f"{n} has no comment of its own"
+
+
 def test_binding_covers_every_entry_point():
     for n in declared_functions():
         assert n in fl.flashloop.EXPORTS, n
