@@ -119,9 +119,15 @@ def _check(status: int, what: str):
 
 
 def _ptr(t: Optional[torch.Tensor]):
+    """Device address of a contiguous CUDA tensor (None passes NULL). The
+    library reads every buffer as dense row-major device memory, so a strided
+    or host tensor is refused here rather than handed to a kernel."""
     if t is None:
         return None
-    assert t.is_contiguous(), "tensors must be contiguous"
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the library must be in CUDA device memory")
     return ctypes.c_void_p(t.data_ptr())
 
 

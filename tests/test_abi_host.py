@@ -109,6 +109,22 @@ def test_select_tokens_noalloc_rejects_bad_args(L):
     assert f(a, b, 1 << 11, 1 << 11, 16, 2, out, None) == CAPACITY  # 4,194,304 scores
 
 
+def test_binding_refuses_strided_and_host_tensors(L):
+    """The binding hands the library only dense CUDA buffers: a strided or a
+    host tensor is refused in Python, before any library call."""
+    import torch
+    from lazy_sparse_attention_token_b300 import flashloop as F
+    assert F._ptr(None) is None
+    with pytest.raises(ValueError, match="contiguous"):
+        F._ptr(torch.zeros(4, 4).t())
+    with pytest.raises(ValueError, match="CUDA"):
+        F._ptr(torch.zeros(4))
+    n0 = fl.flashloop_launch_count()
+    with pytest.raises(ValueError, match="CUDA"):
+        fl.flashloop_select_keys(torch.zeros(1, 2, 8), 2)
+    assert fl.flashloop_launch_count() == n0
+
+
 def test_gather_and_keys_reject_bad_args(L):
     assert L.flashloop_gather(P(0x1000), 1, 8, 24, P(0x2000), 2, P(0x3000), None) == INVALID      # row_bytes % 16
     assert L.flashloop_gather(P(0x1008), 1, 8, 32, P(0x2000), 2, P(0x3000), None) == INVALID      # misaligned
