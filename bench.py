@@ -18,6 +18,8 @@ the data path), value = all ranks' tokens / the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import atexit
+import datetime
 import json
 import math
 import os
@@ -98,13 +100,20 @@ def load_peaks():
 # clocks during the timed region
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms from start() to stop(); only those inside
+    the window between mark_start() and mark_end() (the timed region, with one
+    sampling interval of slack) are summarised. If the timestamps cannot be
+    read, every sample is used and the summary says so."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    SLACK_S = 0.06
 
     def __init__(self, device_index: int):
         self.proc = None
         self.path = None
+        self.out = None
+        self.t0 = self.t1 = None
         try:
             uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
         except Exception:
@@ -115,37 +124,71 @@ class ClockSampler:
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
+            self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-lms", "50", "-i", self.target],
-                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            atexit.register(self._end_proc)   # never leave the sampler running
             time.sleep(0.3)
         except Exception:
             self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def _end_proc(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+                try:
+                    self.proc.wait(timeout=5)
+                except Exception:
+                    pass
+        if self.out is not None:
+            self.out.close()
+            self.out = None
+
+    @staticmethod
+    def _when(text: str):
+        try:
+            return datetime.datetime.strptime(text, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
         if self.proc is None:
             return None
         time.sleep(0.1)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
+        self._end_proc()
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
+            if len(parts) >= 10:
                 rows.append(parts)
         os.unlink(self.path)
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        window = "whole sampler run (no readable timestamps)"
+        if self.t0 is not None and self.t1 is not None:
+            inside = [r for r in rows if (t := self._when(r[0])) is not None
+                      and self.t0 - self.SLACK_S <= t <= self.t1 + self.SLACK_S]
+            if inside:
+                rows, window = inside, "timed region"
+        num = lambda v: v.replace(".", "", 1).isdigit()
+        sm = [float(r[2]) for r in rows if num(r[2])]
+        mx = [float(r[3]) for r in rows if num(r[3])]
+        power = [float(r[4]) for r in rows if num(r[4])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(power) if power else None, "samples": len(rows), "reasons": reasons}
+                "power_w_max": max(power) if power else None, "samples": len(rows), "window": window,
+                "reasons": reasons}
 
 
 # --------------------------------------------------------------------------
@@ -277,6 +320,8 @@ def native(args, world, rank, local):
         clocks.start()
     barrier(world)
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_start()
     ev0.record()
     for i in range(args.steps):
         l = lazy[(args.warmup + i) % len(lazy)]
@@ -286,6 +331,8 @@ def native(args, world, rank, local):
             step_loop(l)
     ev1.record()
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_end()
     barrier(world)
     clk = clocks.stop() if clocks else None
     # launches inside the timed pass (a replayed graph holds the captured step's launches)
@@ -435,6 +482,8 @@ def native_decode(args, world, rank, local):
         clocks.start()
     barrier(world)
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_start()
     ev0.record()
     for _ in range(args.steps):
         if graph is not None:
@@ -443,6 +492,8 @@ def native_decode(args, world, rank, local):
             token_step()
     ev1.record()
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_end()
     barrier(world)
     clk = clocks.stop() if clocks else None
     launches = launches_per_step * args.steps if graph is not None else fl.flashloop_launch_count() - n0

@@ -77,3 +77,58 @@ def test_committed_traffic_record_names_existing_sources():
         kernel, workload, nbytes, fname, h = line.split()
         assert int(nbytes) > 0 and len(h) == 16
         assert os.path.exists(os.path.join(root, "lazy_sparse_attention_token_b300", "csrc", fname)), fname
+
+
+FAKE_SMI = r'''#!/usr/bin/env python3
+# Stand-in for nvidia-smi --query-gpu ... -lms 50: 1000 MHz, no throttle reason,
+# except between 0.35 s and 1.1 s after start: 2032 MHz with sw_power_cap.
+import datetime, sys, time
+t_start = time.time()
+stamps = "{stamps}"
+while True:
+    t = time.time() - t_start
+    hot = 0.35 <= t < 1.1
+    ts = datetime.datetime.now().strftime("%Y/%m/%d %H:%M:%S.%f")[:-3] if stamps == "ok" else "N/A"
+    print(", ".join([ts, "0", "2032" if hot else "1000", "2032", "480.5" if hot else "90.0",
+                     "0x4" if hot else "0x0", "Not Active", "Not Active", "Not Active",
+                     "Active" if hot else "Not Active"]), flush=True)
+    time.sleep(0.05)
+'''
+
+
+def _fake_smi(tmp_path, monkeypatch, stamps):
+    exe = tmp_path / "nvidia-smi"
+    exe.write_text(FAKE_SMI.replace("{stamps}", stamps))
+    exe.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+
+
+def _sample(window_after_start=0.2, window_len=0.4):
+    import time
+    cs = bench.ClockSampler(0)
+    cs.start()                       # returns 0.3 s after the sampler starts
+    time.sleep(window_after_start)
+    cs.mark_start()
+    time.sleep(window_len)
+    cs.mark_end()
+    out = cs.stop()
+    assert cs.proc.poll() is not None    # the sampler process has ended
+    return out
+
+
+def test_clock_sampler_keeps_only_the_timed_window(tmp_path, monkeypatch):
+    _fake_smi(tmp_path, monkeypatch, "ok")
+    out = _sample()
+    assert out["window"] == "timed region"
+    assert out["sm_mhz"] == 2032.0 and out["sm_max_mhz"] == 2032.0
+    assert out["reasons"] == ["sw_power_cap"]
+    assert out["power_w_max"] == 480.5
+    assert 4 <= out["samples"] <= 14     # about 0.4 s + slack at 50 ms, not the whole run
+
+
+def test_clock_sampler_without_timestamps_uses_every_sample(tmp_path, monkeypatch):
+    _fake_smi(tmp_path, monkeypatch, "none")
+    out = _sample()
+    assert out["window"].startswith("whole sampler run")
+    assert out["samples"] >= 12          # the idle samples before and after are included
+    assert out["reasons"] == ["sw_power_cap"]
