@@ -132,3 +132,24 @@ def test_clock_sampler_without_timestamps_uses_every_sample(tmp_path, monkeypatc
     assert out["window"].startswith("whole sampler run")
     assert out["samples"] >= 12          # the idle samples before and after are included
     assert out["reasons"] == ["sw_power_cap"]
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the oracle timed on the host cores) prints
+    exactly one JSON line with the keys the benchmark contract names."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "1",
+                        "--warmup", "3", "--ref-budget", "1"], cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, r.stdout
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference" and j["value"] > 0 and j["unit"] == "tokens/s"
+    assert j["n_gpus"] == 1 and j["steps"] == 1 and j["warmup"] == 3 and j["higher_is_better"] is True
+    assert j["metric"] and j["config"]["workload"].startswith("tiny") and j["data"] == "synthetic"
+    cb = j["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == j["value"]
+    assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
