@@ -23,6 +23,7 @@ import datetime
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -167,10 +168,11 @@ class ClockSampler:
         time.sleep(0.1)
         self._end_proc()
         rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 10:
-                rows.append(parts)
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
         os.unlink(self.path)
         if not rows:
             return None
@@ -236,14 +238,18 @@ def recorded_traffic(kernel: str, workload: str):
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    for line in open(path):
+    with open(path) as f:
+        lines = f.readlines()
+    for line in lines:
         parts = line.split()
         if len(parts) != 5 or line.startswith("#") or parts[0] != kernel or parts[1] != workload:
             continue
         src = os.path.join(ROOT, "lazy_sparse_attention_token_b300", "csrc", parts[3])
         if not os.path.exists(src):
             return None
-        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != parts[4]:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+        if digest != parts[4]:
             return None
         return int(parts[2])
     return None
@@ -646,22 +652,54 @@ def _omp_threads():
     return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
 
 
-def cpu_baseline(w, R, K, gpu_state, budget_s=20.0):
+def _cpu_model():
+    """The host CPU's model name, or None."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or None
+
+
+def _single_thread(w, R, K, inp, n_heads, budget_s):
+    """The same sampled step with the oracle on one thread; the thread count
+    is restored afterwards. A failure here is reported, never raised."""
+    import oracle
+    n0 = oracle.get_threads()
+    try:
+        oracle.set_threads(1)
+        frac = _rows_frac_for(w, R, K, inp, n_heads, budget_s)
+        est, took = _oracle_step(w, R, K, inp, n_heads, frac)
+        return {"value": w.B * w.N / est, "unit": "tokens/s", "cores": 1,
+                "sample": f"{frac:.1%} of the {R} active rows on {n_heads} of {w.H} heads ({took:.1f} s measured)"}
+    except Exception as exc:   # the baseline line must not depend on this extra figure
+        return {"unavailable": str(exc)[:160]}
+    finally:
+        oracle.set_threads(n0)
+
+
+def cpu_baseline(w, R, K, gpu_state, budget_s=20.0, device="cuda"):
     """The oracle as it stands, on the host cores, over a bounded sample of
-    the same lazy step; it starts from the GPU's loop-1 state (sampled heads)."""
+    the same lazy step; it starts from the GPU's loop-1 state (sampled heads).
+    Also times the same sample on one core (about a quarter of the budget)."""
     import oracle
     oracle.build()
     n_heads = 1
-    inp = _oracle_inputs(w, n_heads, "cuda")
+    inp = _oracle_inputs(w, n_heads, device)
     qh, o, z, c = gpu_state
     inp.update(qh1=oracle.bits(qh[:, :, :n_heads].contiguous()), o1=o[:, :, :n_heads].cpu().numpy(),
                z1=z[:, :n_heads].cpu().numpy(), c1=c[:, :n_heads].cpu().numpy())
     frac = _rows_frac_for(w, R, K, inp, n_heads, budget_s)
     est, took = _oracle_step(w, R, K, inp, n_heads, frac)
     return {"value": w.B * w.N / est, "unit": "tokens/s", "cores": _omp_threads(), "kind": "oracle",
+            "cpu_model": _cpu_model(),
             "sample": (f"one lazy step of the {w.name} workload: token scores, top-r and K/V delta append over all "
                        f"{w.N} tokens; key selection, reconstruction and lazy attention on {n_heads} of {w.H} heads "
-                       f"and {frac:.1%} of the {R} active rows, scaled to the whole step ({took:.1f} s measured)")}
+                       f"and {frac:.1%} of the {R} active rows, scaled to the whole step ({took:.1f} s measured)"),
+            "single_thread": _single_thread(w, R, K, inp, n_heads, budget_s / 4)}
 
 
 def reference(args, world, rank):
@@ -698,7 +736,8 @@ def reference(args, world, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": workload_text(w, R, K)},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "cpu_model": _cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

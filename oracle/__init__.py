@@ -60,7 +60,18 @@ def lib():
         _lib.orc_attention.argtypes = [ctypes.c_int, I64, I64, I64, I64, I64, I64, P, P,
                                        P, P, P, P, P, I64, P, P, P, P, P, P, P]
         _lib.orc_softmax_attention.argtypes = [P, P, P, I64, I64, I64, I64, P, P]
+        _lib.orc_set_threads.argtypes = [ctypes.c_int]
+        _lib.orc_get_threads.restype = ctypes.c_int
     return _lib
+
+
+def set_threads(n: int) -> None:
+    """OpenMP threads of the oracle's parallel regions (for timing it)."""
+    lib().orc_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(lib().orc_get_threads())
 
 
 def _c(a: np.ndarray, dtype) -> np.ndarray:

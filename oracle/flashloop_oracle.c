@@ -484,3 +484,9 @@ void orc_softmax_attention(const uint16_t *q, const uint16_t *k, const uint16_t 
         }
     }
 }
+
+/* OpenMP threads of the parallel regions above, for timing the oracle on one
+ * core or on all of them. Results do not depend on it except through the
+ * order in which per-thread column-mass sums are added (in double). */
+void orc_set_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
+int orc_get_threads(void) { return omp_get_max_threads(); }

@@ -22,8 +22,13 @@ def L():
     return fl.lib()
 
 
+def _header_text():
+    with open(HEADER) as f:
+        return f.read()
+
+
 def declared_functions():
-    text = open(HEADER).read()
+    text = _header_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(flashloop_\w+)\s*\(", text)))
 
@@ -39,7 +44,7 @@ def test_every_declared_symbol_is_exported(L):
 def test_every_declaration_has_its_own_comment():
     """Each entry point of the header is directly preceded by a comment of its
     own (its operation, arguments, ownership and errors)."""
-    text = open(HEADER).read()
+    text = _header_text()
     blank = re.sub(r"/\*.*?\*/", lambda m: " " * len(m.group(0)), text, flags=re.S)
     for n in declared_functions():
         m = re.search(r"^[^\n]*\b" + n + r"\s*\(", blank, re.M)

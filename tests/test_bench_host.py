@@ -71,7 +71,9 @@ def test_recorded_traffic_needs_the_captured_source(tmp_path, monkeypatch):
 
 def test_committed_traffic_record_names_existing_sources():
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    for line in open(os.path.join(root, "profiles", "traffic.txt")):
+    with open(os.path.join(root, "profiles", "traffic.txt")) as f:
+        lines = f.readlines()
+    for line in lines:
         if line.startswith("#") or not line.strip():
             continue
         kernel, workload, nbytes, fname, h = line.split()
@@ -153,3 +155,25 @@ def test_reference_arm_prints_one_contract_line():
     cb = j["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == j["value"]
     assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_cpu_baseline_leg_on_host_state():
+    """The bench's cpu_baseline leg, run on the host from an oracle loop-1
+    state (in place of the GPU's): the all-core and one-core figures, the CPU
+    model, and the oracle's thread count restored afterwards."""
+    import numpy as np
+    import oracle
+    w = synth.WORKLOADS["tiny"]
+    R, K = synth.active_count(w), synth.key_count(w)
+    inp = bench._oracle_inputs(w, w.H, "cpu")
+    bench._oracle_loop1(w, inp, w.H)
+    state = (torch.from_numpy(inp["qh1"].view(np.int16)).view(torch.bfloat16), torch.from_numpy(inp["o1"]),
+             torch.from_numpy(inp["z1"]), torch.from_numpy(inp["c1"]))
+    n0 = oracle.get_threads()
+    out = bench.cpu_baseline(w, R, K, state, budget_s=0.4, device="cpu")
+    assert oracle.get_threads() == n0
+    assert out["kind"] == "oracle" and out["unit"] == "tokens/s" and out["value"] > 0 and out["cores"] >= 1
+    assert out["sample"].startswith("one lazy step of the tiny workload")
+    st = out["single_thread"]
+    assert st["cores"] == 1 and st["value"] > 0 and st["unit"] == "tokens/s", st
+    assert out["cpu_model"] is None or isinstance(out["cpu_model"], str)

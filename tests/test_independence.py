@@ -12,6 +12,11 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PKG = os.path.join(ROOT, "lazy_sparse_attention_token_b300")
 
 
+def _read(path):
+    with open(path) as f:
+        return f.read()
+
+
 def _py_files(d):
     for dirpath, _, files in os.walk(d):
         if "__pycache__" in dirpath or "_build" in dirpath:
@@ -22,7 +27,7 @@ def _py_files(d):
 
 
 def _imports(path):
-    tree = ast.parse(open(path).read(), path)
+    tree = ast.parse(_read(path), path)
     out = set()
     for node in ast.walk(tree):
         if isinstance(node, ast.Import):
@@ -38,7 +43,7 @@ def test_package_never_imports_the_oracle():
     for f in files:
         assert "oracle" not in _imports(f), f
     for f in os.listdir(os.path.join(PKG, "csrc")):
-        text = open(os.path.join(PKG, "csrc", f)).read()
+        text = _read(os.path.join(PKG, "csrc", f))
         assert "oracle" not in text.lower(), f
 
 
@@ -49,7 +54,7 @@ def test_oracle_shares_no_code_with_the_cuda_path():
         assert "lazy_sparse_attention_token_b300" not in imps and "synth" not in imps, f
     for f in os.listdir(odir):
         if f.endswith((".c", ".h")):
-            for inc in re.findall(r'#include\s*[<"]([^>"]+)[>"]', open(os.path.join(odir, f)).read()):
+            for inc in re.findall(r'#include\s*[<"]([^>"]+)[>"]', _read(os.path.join(odir, f))):
                 assert "/" not in inc and not inc.endswith((".cuh", ".cu")) and inc != "flashloop.h", (f, inc)
 
 
@@ -71,7 +76,7 @@ def test_bench_reaches_the_oracle_only_through_its_cpu_legs():
     """In bench.py only the cpu_baseline leg and the reference arm may run the
     oracle: every function that uses it (directly, or through a helper that
     does) is called only from those two or from another such helper."""
-    tree = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    tree = ast.parse(_read(os.path.join(ROOT, "bench.py")))
     funcs = {n.name: n for n in tree.body if isinstance(n, ast.FunctionDef)}
 
     def names(fn):

@@ -45,6 +45,8 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_and_barrier_with_gloo():
     world = 2
-    out = mp.Manager().dict()
+    # the result dict's server process is spawned too: forking a process whose
+    # earlier tests left worker threads running can deadlock the child
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     assert out[0] == out[1] == 2.5

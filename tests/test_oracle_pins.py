@@ -19,6 +19,11 @@ import synth
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
 
+def _read(path):
+    with open(path) as f:
+        return f.read()
+
+
 def bf16_bits(x):
     t = torch.as_tensor(np.asarray(x, np.float32)).to(torch.bfloat16)
     return t.view(torch.int16).numpy().view(np.uint16)
@@ -97,7 +102,7 @@ def test_scores_match_library_norm(orc):
 
 def test_topk_golden():
     import oracle
-    g = json.load(open(os.path.join(GOLD, "topk_ties.json")))
+    g = json.loads(_read(os.path.join(GOLD, "topk_ties.json")))
     for case in g["cases"]:
         got = oracle.topk(np.array([g["scores"]]), case["k"])[0]
         assert got.tolist() == case["expect"], case
@@ -123,7 +128,7 @@ def _quant_one(orc, delta):
 
 
 def test_quantiser_golden(orc):
-    g = json.load(open(os.path.join(GOLD, "quantiser_groups.json")))
+    g = json.loads(_read(os.path.join(GOLD, "quantiser_groups.json")))
     for grp in g["groups"]:
         layer = _quant_one(orc, grp["delta"])
         assert int(layer.scales[0, 0, 0, 0]) == grp["scale_bits"], grp["why"]
