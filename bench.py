@@ -649,7 +649,12 @@ def _rows_frac_for(w, R, K, inp, n_heads, budget_s):
 
 
 def _omp_threads():
-    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    """Threads of the oracle's parallel regions (what OpenMP actually runs with)."""
+    import oracle
+    try:
+        return oracle.get_threads()
+    except Exception:
+        return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
 
 
 def _cpu_model():
