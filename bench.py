@@ -673,8 +673,9 @@ def _single_thread(w, R, K, inp, n_heads, budget_s):
     """The same sampled step with the oracle on one thread; the thread count
     is restored afterwards. A failure here is reported, never raised."""
     import oracle
-    n0 = oracle.get_threads()
+    n0 = None
     try:
+        n0 = oracle.get_threads()
         oracle.set_threads(1)
         frac = _rows_frac_for(w, R, K, inp, n_heads, budget_s)
         est, took = _oracle_step(w, R, K, inp, n_heads, frac)
@@ -683,7 +684,8 @@ def _single_thread(w, R, K, inp, n_heads, budget_s):
     except Exception as exc:   # the baseline line must not depend on this extra figure
         return {"unavailable": str(exc)[:160]}
     finally:
-        oracle.set_threads(n0)
+        if n0 is not None:
+            oracle.set_threads(n0)
 
 
 def cpu_baseline(w, R, K, gpu_state, budget_s=20.0, device="cuda"):

@@ -60,8 +60,9 @@ def lib():
         _lib.orc_attention.argtypes = [ctypes.c_int, I64, I64, I64, I64, I64, I64, P, P,
                                        P, P, P, P, P, I64, P, P, P, P, P, P, P]
         _lib.orc_softmax_attention.argtypes = [P, P, P, I64, I64, I64, I64, P, P]
-        _lib.orc_set_threads.argtypes = [ctypes.c_int]
-        _lib.orc_get_threads.restype = ctypes.c_int
+        if hasattr(_lib, "orc_set_threads"):   # timing control; absent from older builds
+            _lib.orc_set_threads.argtypes = [ctypes.c_int]
+            _lib.orc_get_threads.restype = ctypes.c_int
     return _lib
 
 
