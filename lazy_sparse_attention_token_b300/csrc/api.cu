@@ -340,7 +340,7 @@ flashloop_status_t flashloop_select_tokens(const uint16_t *h_prev, const uint16_
     if (st != FLASHLOOP_OK) return st;
     cudaError_t e = launch_token_scores(h_prev, h_cur, B, N, D, sc, stream);
     if (e != cudaSuccess) return cuda_fail(e, "token_scores");
-    e = launch_topk_rows(sc, B, N, R, active_idx, stream);
+    e = launch_topk_rows(sc, B, N, R, active_idx, stream, "topk_tokens");
     if (e != cudaSuccess) return cuda_fail(e, "topk(tokens)");
     return FLASHLOOP_OK;
 }
@@ -375,14 +375,16 @@ static flashloop_status_t delta_append_impl(flashloop_kv_cache_t *cache, int32_t
     if (R < 1 || at < 0 || (at != 0 && at != cache->count[m]))
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "R=%d at=%d (layer holds %d)", R, at, cache->count[m]);
     if (at + R > dm.R_cap) return set_error(FLASHLOOP_ERR_CAPACITY, "delta layer full (%d + %d > %d)", at, R, dm.R_cap);
+    if (rows_are_tokens && (cache->n_tokens < 1 || cache->n_tokens > dm.N_cap))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "rows_are_tokens needs 1 <= cache n_tokens <= N_cap");
+    // every check comes before the slot map is touched: a rejected call leaves
+    // the layer, its slot map and its count as they were
     if ((st = check_device()) != FLASHLOOP_OK) return st;
     if (at == 0 && !slots_cleared) {
         cudaError_t e = cudaMemsetAsync(cache->slot[m], 0xFF, (size_t)dm.B * dm.N_cap * 4, stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(slot)");
     }
     const DeltaView view = make_view(cache, loop - 1);
-    if (rows_are_tokens && (cache->n_tokens < 1 || cache->n_tokens > dm.N_cap))
-        return set_error(FLASHLOOP_ERR_INVALID_ARG, "rows_are_tokens needs 1 <= cache n_tokens <= N_cap");
     const int src_rows = rows_are_tokens ? cache->n_tokens : R;
     cudaError_t e = launch_delta_append(view, k_l, v_l, rows_are_tokens, src_rows, active_idx, R, at, dm.B, dm.N_cap,
                                         dm.H, dm.d, dm.R_cap, cache->idx[m], cache->slot[m], cache->k_codes[m],
@@ -429,7 +431,7 @@ flashloop_status_t flashloop_select_keys(const float *col_stats, int32_t B, int3
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad sizes (B=%d H=%d N=%d K=%d)", B, H, N, K);
     flashloop_status_t st = check_device();
     if (st != FLASHLOOP_OK) return st;
-    cudaError_t e = launch_topk_rows(col_stats, B * H, N, K, key_idx, stream);
+    cudaError_t e = launch_topk_rows(col_stats, B * H, N, K, key_idx, stream, "topk_keys");
     if (e != cudaSuccess) return cuda_fail(e, "topk(keys)");
     return FLASHLOOP_OK;
 }

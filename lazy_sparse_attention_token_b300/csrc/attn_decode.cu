@@ -423,15 +423,20 @@ cudaError_t launch_d(const DecodeAttnParams &q, cudaStream_t s) {
     const size_t smem =
         (size_t)(3 * chunk + kThreads / 32 + 2 * kGroups * D + kMaxCluster * 3 + 2 * D + n_ent) * sizeof(float);
     if (smem > 220 * 1024) return cudaErrorInvalidValue;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        cudaFuncSetAttribute(decode_attention_kernel<D, FLASHLOOP_ATTN_FIRST_DENSE>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-        cudaFuncSetAttribute(decode_attention_kernel<D, FLASHLOOP_ATTN_DENSE>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-        cudaFuncSetAttribute(decode_attention_kernel<D, FLASHLOOP_ATTN_LAZY>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t attr_res[kMaxDevices];
+    const cudaError_t ea = once_per_device(once, attr_res, [] {
+        cudaError_t e = cudaFuncSetAttribute(decode_attention_kernel<D, FLASHLOOP_ATTN_FIRST_DENSE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_attention_kernel<D, FLASHLOOP_ATTN_DENSE>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_attention_kernel<D, FLASHLOOP_ATTN_LAZY>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+        return e;
     });
+    if (ea != cudaSuccess) return ea;
     DecKParams p;
     p.mode = q.mode;
     p.H = q.H;

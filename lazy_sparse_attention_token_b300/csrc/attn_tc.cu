@@ -784,10 +784,12 @@ bool make_map(CUtensorMap *map, const void *base, const cuuint64_t dims[4], cons
 template <int D>
 cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
     using Cf = Cfg<D>;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        cudaFuncSetAttribute(tc_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t attr_res[kMaxDevices];
+    const cudaError_t ea = once_per_device(once, attr_res, [] {
+        return cudaFuncSetAttribute(tc_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     });
+    if (ea != cudaSuccess) return ea;
     const bool dense = p.mode != FLASHLOOP_ATTN_LAZY;
     CUtensorMap maps[4];
     const uint16_t *src[4] = {p.k_old ? p.k_old : p.k_new, p.v_old ? p.v_old : p.v_new, p.k_new, p.v_new};

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "device_once.h"
 #include "flashloop.h"
 
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ != 1030)
@@ -13,6 +14,15 @@
 #endif
 
 namespace fl {
+
+// Kernel attributes belong to one device's context: `set` runs once per
+// device (the current one) and its cudaError_t is returned on every later
+// call from that device (device_once.h).
+template <class Set>
+inline cudaError_t once_per_device(std::once_flag (&once)[kMaxDevices], cudaError_t (&res)[kMaxDevices], Set &&set) {
+    return once_per_device_with(once, res, [](int *dev) { return cudaGetDevice(dev); }, cudaErrorInvalidDevice,
+                                static_cast<Set &&>(set));
+}
 
 // ---- host bookkeeping (api.cu) -------------------------------------------
 void note_launch(int n = 1);
@@ -50,7 +60,9 @@ struct DeltaView {
 // select.cu
 cudaError_t launch_token_scores(const uint16_t *h_prev, const uint16_t *h_cur, int B, int N, int D,
                                 float *scores, cudaStream_t s);
-cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t *out, cudaStream_t s);
+// `name` labels the launch in the per-kernel timing ("topk_tokens", "topk_keys").
+cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t *out, cudaStream_t s,
+                             const char *name);
 // kvcache.cu
 cudaError_t launch_gather_rows(const void *src, int B, int N, int row_bytes, const int32_t *idx, int R,
                                void *dst, cudaStream_t s);

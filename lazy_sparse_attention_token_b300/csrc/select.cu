@@ -262,16 +262,19 @@ cudaError_t launch_token_scores(const uint16_t *h_prev, const uint16_t *h_cur, i
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t *out, cudaStream_t s) {
+cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t *out, cudaStream_t s,
+                             const char *name) {
     if (rows == 0) return cudaSuccess;
     const int ncta = rows >= kTopkRowsForSingle ? 1 : kTopkCluster;
     const int seg = ((n + ncta - 1) / ncta + 31) & ~31;
     const bool staged = seg <= kTopkClStageMax;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        cudaFuncSetAttribute(topk_cluster_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kTopkClStageMax * 4);
+    static std::once_flag once[kMaxDevices];
+    static cudaError_t attr_res[kMaxDevices];
+    const cudaError_t ea = once_per_device(once, attr_res, [] {
+        return cudaFuncSetAttribute(topk_cluster_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kTopkClStageMax * 4);
     });
+    if (ea != cudaSuccess) return ea;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(rows * ncta));
     cfg.blockDim = dim3(kTopkClThreads);
@@ -288,7 +291,7 @@ cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t 
     cfg.numAttrs = 2;
     cudaError_t e;
     {
-        KernelTimer kt("topk", s);
+        KernelTimer kt(name, s);
         e = staged ? cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, vals, n, k, out)
                    : cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, vals, n, k, out);
     }
@@ -352,7 +355,7 @@ extern "C" flashloop_status_t flashloop_select_tokens_noalloc(const uint16_t *h_
     // every score is written before it is read: nothing needs clearing
     e = launch_token_scores(h_prev, h_cur, B, N, D, scores, stream);
     if (e != cudaSuccess) return cuda_fail(e, "token_scores");
-    e = launch_topk_rows(scores, B, N, R, active_idx, stream);
+    e = launch_topk_rows(scores, B, N, R, active_idx, stream, "topk_tokens");
     if (e != cudaSuccess) return cuda_fail(e, "topk(tokens)");
     return FLASHLOOP_OK;
 }

@@ -241,3 +241,21 @@ def test_cache_against_a_bf16_cache_per_loop(L, shape, ratio_lo):
     assert want <= cb <= want + 256 * sections
     per_loop = shape["T"] * 2 * shape["B"] * shape["N_cap"] * shape["H"] * shape["d"] * 2
     assert per_loop / cb >= ratio_lo
+
+
+def test_rejected_append_leaves_the_layer_as_it_was(L):
+    """Every argument check of the delta append runs before its slot map is
+    reset: a call refused for its token count returns INVALID_ARG without a
+    device call (here on a host without a GPU it would otherwise report the
+    missing device), and the layer's count stays where it was."""
+    dm = dims()
+    c = fake_cache(dm)
+    c.count[0] = 5
+    n0 = fl.flashloop_launch_count()
+    for n_tokens in (0, dm.N_cap + 1):
+        c.n_tokens = n_tokens
+        st = L.flashloop_kv_delta_append(ctypes.byref(c), 2, P(0x200000), P(0x300000), 1, P(0x400000), 4, 0, None)
+        assert st == INVALID
+        assert b"n_tokens" in L.flashloop_last_error()
+        assert c.count[0] == 5
+    assert fl.flashloop_launch_count() == n0
