@@ -176,6 +176,32 @@ def test_decode_style_append_at_offset():
         fl.flashloop_kv_delta_append(cache, 2, kn2, kn2, tok, at=51, rows_are_tokens=False)
 
 
+def test_refused_append_leaves_slot_map_and_count():
+    """A delta append refused on the host (here: a token-indexed append while
+    the cache counts no tokens) touches nothing: the layer's slot map, entries
+    and count stay those of the previous append."""
+    B, N, H, d = 2, 300, 2, 64
+    dm = fl.make_dims(B, N, H, d, 40, 20, 2, 1, R_cap=40)
+    cache = fl.Cache(dm)
+    cache.n_tokens = N
+    k1, v1 = randn_bf16((B, N, H, d), 94), randn_bf16((B, N, H, d), 95)
+    fl.flashloop_kv_dense_store(cache, 1, k1, v1)
+    act = torch.stack([torch.arange(3, 300, 8, device="cuda")[:40]] * B).to(torch.int32)
+    k2 = (k1.float() * 1.02).to(torch.bfloat16)
+    fl.flashloop_kv_delta_append(cache, 2, k2, k2, act)
+    torch.cuda.synchronize()
+    idx0, slot0, kc0, *_ = (t.clone() for t in cache.delta_layer(2))
+    cache.n_tokens = 0
+    with pytest.raises(fl.FlashLoopError):
+        fl.flashloop_kv_delta_append(cache, 2, k2, k2, act[:, :10])
+    torch.cuda.synchronize()
+    cache.n_tokens = N
+    assert cache.c.count[0] == 40
+    idx1, slot1, kc1, *_ = cache.delta_layer(2)
+    assert torch.equal(slot0, slot1) and torch.equal(idx0, idx1) and torch.equal(kc0, kc1)
+    check_slot_map(cache, 2, N)
+
+
 # --------------------------------------------------------------------------
 # attention
 

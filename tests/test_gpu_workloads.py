@@ -47,7 +47,31 @@ def _check_append(cache, l, x_l, name, base, prev_layers, A, bsel, rows_are_toke
     assert_layer(g_codes, g_scales, orc.codes, orc.scales, delta_over_scale(xb, rows, orc.scales), f"{name} layer {l}")
 
 
-def run_prefill(name, bsel, hsel, full_dense=False, loops_to_check=None, keep=False):
+def _pick_heads(H, n, seed):
+    """n heads of H for the attention comparison: the first, the last, and a
+    seeded draw of the rest (every head still takes part in the selections
+    and the delta appends, which are compared on all heads)."""
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(1, H - 1), size=max(0, min(n, H) - 2), replace=False).tolist()
+    return sorted({0, H - 1, *mid})
+
+
+def _dense_full_rows(name, l, first, x, bsel, head, before_full, cache, w):
+    """Dense loop l on every row of one (sequence, head): O, Z, q_hat and the
+    column masses c, all of them, against the oracle on the same inputs."""
+    sl = lambda t: bits(t[bsel][:, :, [head]])
+    q, k_new, v_new = sl(x["Q"]), sl(x["K"]), sl(x["V"])
+    k_old = v_old = None
+    if not first:
+        ko, vo = cache.dense_layer(l - 1)
+        k_old, v_old = bits(ko[bsel][:, :w.N][:, :, [head]]), bits(vo[bsel][:, :w.N][:, :, [head]])
+    rows = np.tile(np.arange(w.N, dtype=np.int32), (len(bsel), 1))
+    S = np.tile(np.arange(w.N, dtype=np.int32), (len(bsel), 1, 1))
+    qh, o, z, c, _ = oracle.attention(first, rows, rows, q, *before_full, S, k_old, v_old, k_new, v_new)
+    return qh, o, z, c
+
+
+def run_prefill(name, bsel, hsel, full_dense=False, loops_to_check=None, keep=False, full_rows_loop=None):
     w = synth.WORKLOADS[name]
     extra = 1 if w.decode_after_prefill else 0
     dm = dims_for(w, extra_tokens=extra, R_extra=extra)
@@ -64,6 +88,8 @@ def run_prefill(name, bsel, hsel, full_dense=False, loops_to_check=None, keep=Fa
         l = x["loop"]
         check = loops_to_check is None or l in loops_to_check
         before = st.snapshot(bsel, hsel) if check else None
+        full_rows = check and l == full_rows_loop
+        before_full = st.snapshot(bsel, [hsel[0]]) if full_rows else None
         if check and l > w.T_dense:
             prev_k, prev_v = layers_from_gpu(cache, range(w.T_dense + 1, l), bsel)
             c_full_before = f32(st.c[bsel])
@@ -90,6 +116,15 @@ def run_prefill(name, bsel, hsel, full_dense=False, loops_to_check=None, keep=Fa
                 assert np.array_equal(after[0][:, rows], qh[:, rows])
                 if full_dense:
                     assert_close(after[3], c, C_ATOL, C_RTOL, f"{name} loop {l} c")
+                if full_rows:
+                    # every row of the first sampled head, and its complete column masses
+                    qh1, o1, z1, c1 = _dense_full_rows(name, l, l == 1, x, bsel, hsel[0], before_full, cache, w)
+                    got = st.snapshot(bsel, [hsel[0]])
+                    what = f"{name} loop {l} head {hsel[0]} all {w.N} rows"
+                    assert_close(got[1], o1, O_ATOL, O_RTOL, what + " O")
+                    assert_close(got[2], z1, Z_ATOL, 0, what + " Z")
+                    assert np.array_equal(got[0], qh1), what + " q_hat"
+                    assert_close(got[3], c1, C_ATOL, C_RTOL, what + " c")
             else:
                 # (1) token selection on the full hidden state of each sequence
                 sc = oracle.token_scores(bits(prev[bsel]), bits(x["H"][bsel]))
@@ -133,11 +168,13 @@ def test_tiny_every_output():
 
 
 def test_8k_prefill():
-    run_prefill("8k", [0], [3, 11])
+    w = synth.WORKLOADS["8k"]
+    run_prefill("8k", [0], _pick_heads(w.H, 4, 8), full_rows_loop=1)
 
 
 def test_32k_prefill():
-    run_prefill("32k", [0], [2, 13])
+    w = synth.WORKLOADS["32k"]
+    run_prefill("32k", [0], _pick_heads(w.H, 4, 32), full_rows_loop=1)
 
 
 def _decode_loops(w, dm, cache, ws, bsel, hsel):
@@ -221,6 +258,11 @@ def test_decode():
 
 
 def test_deep_prefill_then_decode():
-    w, dm, cache, ws = run_prefill("deep", [0], [0, 17], loops_to_check={1, 2, 3, 4, 9, 16}, keep=True)
+    """Two sequences x two heads (the first and the last) through the prefill;
+    the second dense loop (previous state in use, m and u computed) on every
+    row of one head; then a decode token on two more sequences and heads."""
+    w = synth.WORKLOADS["deep"]
+    w, dm, cache, ws = run_prefill("deep", [0, 5], [0, w.H - 1], loops_to_check={1, 2, 3, 4, 9, 16}, keep=True,
+                                   full_rows_loop=2)
     cache.n_tokens = w.N + 1
-    _decode_loops(w, dm, cache, ws, [3], [5, 30])
+    _decode_loops(w, dm, cache, ws, [3, 7], [5, 30])

@@ -10,8 +10,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import lazy_sparse_attention_token_b300 as fl
 from lazy_sparse_attention_token_b300 import build as flbuild
+from gpu_helpers import assert_selection, bits
 
 pytestmark = pytest.mark.gpu
 
@@ -41,6 +43,12 @@ def test_no_alloc_selection_matches_workspace_selection_twice():
         assert st == 0, fl.flashloop._last_error()
         torch.cuda.synchronize()
         assert np.array_equal(out.cpu().numpy(), ref.cpu().numpy()), f"call {call}"
+        # and both against the oracle's ranking of the same hidden states
+        sc = oracle.token_scores(bits(hp), bits(hc))
+        A_orc = oracle.topk(sc, R)
+        got = out.cpu().numpy()
+        for b in range(B):
+            assert_selection(got[b], A_orc[b], sc[b], f"call {call}, sequence {b}")
 
 
 def test_no_alloc_selection_at_its_full_scratch():
