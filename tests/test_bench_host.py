@@ -31,41 +31,74 @@ def test_pair_count_edge_sets():
 
 def test_streaming_bytes_at_32k_from_tensor_shapes():
     """Bytes rebuilt from what each kernel reads and writes at B=1, N=32768,
-    H=16, d=128, R=4916, K=3277: bf16 hidden states, int4 codes (two per
-    byte) with one fp16 scale per 32 elements, int32 indices and slots."""
+    H=16, d=128, R=4916, K=3277, in the first lazy loop (no earlier delta
+    layer; every selected key that is also active holds a delta entry): bf16
+    hidden states, int4 codes (two per byte) with one fp16 scale per 32
+    elements, int32 indices and slots."""
     w = synth.WORKLOADS["32k"]
     R, K = synth.active_count(w), synth.key_count(w)
     assert (R, K) == (4916, 3277)
-    got = bench.hbm_bytes(w, R, K)
+    got = bench.hbm_bytes(w, R, K)        # A = the first R tokens, S = the first K tokens of every head
     rows_bf16 = R * 16 * 128 * 2                       # one [R, H, d] bf16 tensor
     codes, scales = R * 16 * 64, R * 16 * 4 * 2        # [R, H, d/2] u8 and [R, H, d/32] f16
     assert got["token_scores"] == 2 * (32768 * 2048 * 2) + 32768 * 4 == 268566528
+    assert got["topk_tokens"] == 32768 * 4 + R * 4
+    assert got["topk_keys"] == 16 * 32768 * 4 + 16 * K * 4
     # K and V: loop-l rows and base rows read, codes and scales written; entry index and slot
     assert got["delta_append"] == 2 * (2 * rows_bf16 + codes + scales) + R * 4 * 2 == 91909536
     sel_bf16 = 16 * K * 128 * 2                        # one [H, K, d] bf16 tensor
-    # K and V: base rows of the selected keys read, old- and new-loop copies written; key list read
-    assert got["reconstruct_keys"] == 2 * (3 * sel_bf16) + 16 * K * 4 == 80745280
+    entry = 64 + 4 * 2                                 # one (token, head) delta entry: codes and scales
+    # K and V: base rows of the selected keys and the entries of the K selected keys
+    # (all active in this layer) read; key list read
+    assert got["reconstruct_keys"] == 2 * (sel_bf16 + 16 * K * entry) + 16 * K * 4
+    assert got["reconstruct_keys_materialised"] == got["reconstruct_keys"] + 4 * sel_bf16
+
+
+def test_loop_bytes_count_earlier_entries_from_the_sets():
+    """In a later lazy loop the append also reads the earlier delta entries of
+    its active tokens, and the reconstruction the entries of its selected keys
+    in every layer up to this loop's: counted from the set intersections."""
+    w = synth.WORKLOADS["tiny"]       # B1 N1024 H4 d64, loops 2..4 lazy
+    R, K = 6, 3
+    act = {2: torch.tensor([[1, 3, 5, 7, 9, 11]], dtype=torch.int32),
+           3: torch.tensor([[3, 4, 5, 6, 7, 8]], dtype=torch.int32)}
+    keys = {2: torch.zeros(1, 4, K, dtype=torch.int32),
+            3: torch.tensor([[[3, 5, 100]] * 4], dtype=torch.int32)}
+    b3 = bench.loop_bytes(w, R, K, act, keys, 3)
+    b2 = bench.loop_bytes(w, R, K, act, keys, 2)
+    E = 4 * (32 + 4)                  # one token's entry per tensor: 4 heads x (d/2 + 2 d/32)
+    assert b3["delta_append"] - b2["delta_append"] == 2 * 3 * E         # tokens 3, 5, 7 hold a loop-2 entry
+    e_head = 32 + 4
+    # loop 3's keys {3, 5, 100}: 3 and 5 hold entries in layers 2 and 3, in all 4 heads
+    assert b3["reconstruct_keys"] == 2 * (4 * K * 64 * 2 + (2 * 4 + 2 * 4) * e_head) + 4 * K * 4
 
 
 def test_recorded_traffic_needs_the_captured_source(tmp_path, monkeypatch):
-    import hashlib
     csrc = tmp_path / "lazy_sparse_attention_token_b300" / "csrc"
     csrc.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
     src = csrc / "k.cu"
-    src.write_bytes(b"__global__ void k() {}\n")
-    h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    hdr = csrc / "h.cuh"
+    hdr2 = csrc / "deep.h"
+    hdr2.write_bytes(b"#define X 1\n")
+    hdr.write_bytes(b'#include "deep.h"\n__device__ int f();\n')
+    src.write_bytes(b'#include "h.cuh"\n#include <cuda.h>\n__global__ void k() {}\n')
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.source_digest("k.cu")
     (tmp_path / "profiles" / "traffic.txt").write_text(
         "# kernel workload bytes file hash\n"
         f"k 32k 12345 k.cu {h}\n"
         f"k 8k 777 k.cu {h}\n"
         "gone 32k 1 missing.cu 0000000000000000\n")
-    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.recorded_traffic("k", "32k") == 12345
     assert bench.recorded_traffic("k", "8k") == 777
     assert bench.recorded_traffic("k", "deep") is None          # no capture of this workload
     assert bench.recorded_traffic("gone", "32k") is None        # source file not there
-    src.write_bytes(b"__global__ void k() { }\n")                # kernel changed since the capture
+    hdr2.write_bytes(b"#define X 2\n")                          # a header two levels down changed
+    assert bench.recorded_traffic("k", "32k") is None
+    hdr2.write_bytes(b"#define X 1\n")
+    assert bench.recorded_traffic("k", "32k") == 12345
+    src.write_bytes(b'#include "h.cuh"\n#include <cuda.h>\n__global__ void k() { }\n')   # kernel changed
     assert bench.recorded_traffic("k", "32k") is None
 
 
@@ -154,6 +187,8 @@ def test_reference_arm_prints_one_contract_line():
     assert j["metric"] and j["config"]["workload"].startswith("tiny") and j["data"] == "synthetic"
     cb = j["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == j["value"]
+    # measured, not scaled: the line's time is the steps it ran
+    assert abs(j["value"] * j["ms_per_step"] / 1e3 - 1024) < 1e-6 * 1024
     assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 
@@ -173,7 +208,22 @@ def test_cpu_baseline_leg_on_host_state():
     out = bench.cpu_baseline(w, R, K, state, budget_s=0.4, device="cpu")
     assert oracle.get_threads() == n0
     assert out["kind"] == "oracle" and out["unit"] == "tokens/s" and out["value"] > 0 and out["cores"] >= 1
-    assert out["sample"].startswith("one lazy step of the tiny workload")
+    # the figure is one complete lazy step, timed as it is
+    assert out["sample"].startswith("one complete lazy step of the tiny workload")
+    assert abs(out["value"] - w.B * w.N / out["seconds"]) <= 1e-6 * out["value"]
     st = out["single_thread"]
     assert st["cores"] == 1 and st["value"] > 0 and st["unit"] == "tokens/s", st
+    assert out["sample_all_cores"]["value"] > 0
     assert out["cpu_model"] is None or isinstance(out["cpu_model"], str)
+
+
+def test_cpu_baseline_falls_back_to_the_sample_when_the_full_step_is_too_long():
+    import numpy as np
+    w = synth.WORKLOADS["tiny"]
+    R, K = synth.active_count(w), synth.key_count(w)
+    inp = bench._oracle_inputs(w, w.H, "cpu")
+    bench._oracle_loop1(w, inp, w.H)
+    state = (torch.from_numpy(inp["qh1"].view(np.int16)).view(torch.bfloat16), torch.from_numpy(inp["o1"]),
+             torch.from_numpy(inp["z1"]), torch.from_numpy(inp["c1"]))
+    out = bench.cpu_baseline(w, R, K, state, budget_s=0.4, device="cpu", full_limit_s=0.0)
+    assert "not run" in out["sample"] and out["value"] == out["sample_all_cores"]["value"]
