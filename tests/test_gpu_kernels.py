@@ -193,7 +193,7 @@ def test_refused_append_leaves_slot_map_and_count():
     idx0, slot0, kc0, *_ = (t.clone() for t in cache.delta_layer(2))
     cache.n_tokens = 0
     with pytest.raises(fl.FlashLoopError):
-        fl.flashloop_kv_delta_append(cache, 2, k2, k2, act[:, :10])
+        fl.flashloop_kv_delta_append(cache, 2, k2, k2, act[:, :10].contiguous())
     torch.cuda.synchronize()
     cache.n_tokens = N
     assert cache.c.count[0] == 40
