@@ -186,7 +186,7 @@ def test_refused_append_leaves_slot_map_and_count():
     cache.n_tokens = N
     k1, v1 = randn_bf16((B, N, H, d), 94), randn_bf16((B, N, H, d), 95)
     fl.flashloop_kv_dense_store(cache, 1, k1, v1)
-    act = torch.stack([torch.arange(3, 300, 8, device="cuda")[:40]] * B).to(torch.int32)
+    act = torch.stack([torch.arange(3, 300, 7, device="cuda")[:40]] * B).to(torch.int32)
     k2 = (k1.float() * 1.02).to(torch.bfloat16)
     fl.flashloop_kv_delta_append(cache, 2, k2, k2, act)
     torch.cuda.synchronize()
