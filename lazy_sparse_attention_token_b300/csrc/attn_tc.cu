@@ -84,11 +84,22 @@ __device__ int g_tc_error;
 enum : int { PH_OLD = 0, PH_LSE = 1, PH_NEW = 2 };
 // PV_DONE[b] completes when the PV product that read P buffer b is done (the
 // softmax may then overwrite it); the product also releases its V tile's slot.
-// FULL[s] / EMPTY[s]: ring slot s holds a landed tile / is free again.
-enum : int { BAR_FULL = 0, BAR_EMPTY = 5, BAR_S_FULL = 10, BAR_S_READ = 12, BAR_P_FULL = 14, BAR_PV_DONE = 16,
-             BAR_ACC = 18, BAR_STATS = 19, BAR_Q_READY = 20, BAR_DRAIN = 21 /* QK, PV */, BAR_ZN = 23, BAR_EPI = 24,
-             N_BARS = 25 };
-static_assert(BAR_EMPTY == BAR_FULL + kStages && BAR_S_FULL == BAR_EMPTY + kStages, "barrier layout");
+// EMPTY[s]: ring slot s is free again (waited by the producer only).
+// FULL[p % (2 kStages)]: the tile of ring position p has landed. The ring's
+// tiles are consumed by two issuing threads, neither of which waits on every
+// position, and a parity wait cannot tell a phase two behind from a completed
+// one. With 2 kStages landed barriers the phase before position p's belongs to
+// position p - 2 kStages, which is always consumed by then: a thread's
+// consecutive waits are at most kStages positions apart, so the producer has
+// issued p - kStages, which it does only once p - 2 kStages is consumed.
+constexpr int kFullBars = 2 * kStages;
+enum : int { BAR_FULL = 0, BAR_EMPTY = kFullBars, BAR_S_FULL = BAR_EMPTY + kStages, BAR_S_READ = BAR_S_FULL + 2,
+             BAR_P_FULL = BAR_S_READ + 2, BAR_PV_DONE = BAR_P_FULL + 2, BAR_ACC = BAR_PV_DONE + 2,
+             BAR_STATS = BAR_ACC + 1, BAR_Q_READY = BAR_STATS + 1, BAR_DRAIN = BAR_Q_READY + 1, BAR_ZN = BAR_DRAIN + 2,
+             BAR_EPI = BAR_ZN + 1, N_BARS = BAR_EPI + 1 };
+// landed barrier and its parity for ring position p
+__device__ __forceinline__ int full_bar_of(int p) { return BAR_FULL + p % kFullBars; }
+__device__ __forceinline__ uint32_t full_parity(int p) { return (uint32_t)(p / kFullBars) & 1u; }
 enum : int { ERR_EMPTY = 1, ERR_FULL = 2, ERR_S_READ = 5, ERR_S_FULL = 6, ERR_P_FULL = 7, ERR_PV_DONE = 8,
              ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11, ERR_ZN = 12, ERR_EPI = 13 };
 
@@ -355,10 +366,11 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 if (!wait_bar(bar(BAR_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_EMPTY)) return false;
                 const CUtensorMap *m = is_v ? (ph == PH_OLD ? &tm_v_old : &tm_v_new) : (ph == PH_OLD ? &tm_k_old : &tm_k_new);
                 const uint32_t dst = sbase + C::OFF_KV + C::TB * s;
-                mbar_arrive_expect_tx(bar(BAR_FULL + s), C::TB);
+                const uint32_t full = bar(full_bar_of(pos));
+                mbar_arrive_expect_tx(full, C::TB);
                 for (int a = 0; a < C::NA; ++a) {
-                    if (dense) tma_load_4d_hint(dst + a * kAtom, m, bar(BAR_FULL + s), a * 64, h, t * BN, b, keep);
-                    else tma_load_4d_hint(dst + a * kAtom, m, bar(BAR_FULL + s), a * 64, t * BN, h, b, keep);
+                    if (dense) tma_load_4d_hint(dst + a * kAtom, m, full, a * 64, h, t * BN, b, keep);
+                    else tma_load_4d_hint(dst + a * kAtom, m, full, a * 64, t * BN, h, b, keep);
                 }
                 ++pos;
                 return true;
@@ -378,7 +390,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             if (*abort_flag) {   // let copies already in flight land before the CTA exits
                 volatile int never = 0;
                 for (int q = max(0, pos - kStages); q < pos; ++q)
-                    wait_bar(bar(BAR_FULL + q % kStages), (q / kStages) & 1, &never, ERR_FULL);
+                    wait_bar(bar(full_bar_of(q)), full_parity(q), &never, ERR_FULL);
             }
         }
     } else if (warp == 1 || warp == 2) {
@@ -412,7 +424,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             auto issue_qk = [&](int g) -> bool {
                 const int kp = g < lse0 ? kv_pos_k(g) : g < new0 ? base_lse + g - lse0 : base_new + kv_pos_k(g - new0);
                 const int ks = kp % kStages, sb = g & 1;
-                if (!wait_bar(bar(BAR_FULL + ks), (uint32_t)(kp / kStages) & 1u, abort_flag, ERR_FULL)) return false;
+                if (!wait_bar(bar(full_bar_of(kp)), full_parity(kp), abort_flag, ERR_FULL)) return false;
                 // the S buffer's previous tile has been read by the softmax
                 if (g >= kSBufs && !wait_bar(bar(BAR_S_READ + sb), ((g >> 1) - 1) & 1, abort_flag, ERR_S_READ))
                     return false;
@@ -441,7 +453,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 const int pb = pv & 1;
                 const int vp = pv < n_old ? kv_pos_v(pv, n_tiles) : base_new + kv_pos_v(pv - n_old, n_tiles);
                 const int vs = vp % kStages;
-                if (!wait_bar(bar(BAR_FULL + vs), (uint32_t)(vp / kStages) & 1u, abort_flag, ERR_FULL)) return false;
+                if (!wait_bar(bar(full_bar_of(vp)), full_parity(vp), abort_flag, ERR_FULL)) return false;
                 if (!wait_bar(bar(BAR_P_FULL + pb), (uint32_t)(pv >> 1) & 1u, abort_flag, ERR_P_FULL)) return false;
                 tc_fence_after();
                 const uint64_t dv = d_v + TB16 * (uint32_t)vs;
