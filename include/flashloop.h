@@ -57,6 +57,9 @@ typedef enum {
 
 #define FLASHLOOP_MAX_LOOPS 32
 
+/* Default limit of every bounded wait inside the attention kernel (ns). */
+#define FLASHLOOP_WAIT_LIMIT_DEFAULT_NS 1000000000ull
+
 /* Problem sizes. B sequences, N_cap key positions per sequence (prefill
  * tokens plus room for decode tokens), H heads of dimension d (64, 96 or
  * 128), D = H*d. R active tokens per sequence and K key columns per
@@ -289,6 +292,17 @@ const char *flashloop_last_error(void);
 /* Reads and clears the device-side failure word that kernels set when a
  * bounded wait gives up (0 = none). SYNCHRONISES the current device. */
 flashloop_status_t flashloop_device_status(int32_t *word);
+
+/* Sets the limit, in ns, of the bounded waits inside the tensor-core
+ * attention kernel on the current device (failure handling, not part of the
+ * method: for tests and diagnosis of the give-up path). A wait that runs past
+ * it makes the CTA record an error word (see flashloop_device_status), stop
+ * issuing work, let its own copies and MMAs land (drains keep the default
+ * limit) and exit; the launch still completes and the context stays usable.
+ * 0 <= ns <= FLASHLOOP_WAIT_LIMIT_DEFAULT_NS (the limit can only be
+ * shortened; pass the default to restore it), else FLASHLOOP_ERR_INVALID_ARG.
+ * Call it between launches: it SYNCHRONISES the current device. */
+flashloop_status_t flashloop_set_wait_limit_ns(uint64_t ns);
 
 /* Number of kernel launches this library has enqueued from the calling
  * process (a counter for benchmarks). */

@@ -661,6 +661,18 @@ flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop
     return flashloop_lazy_attention(&at, stream);
 }
 
+flashloop_status_t flashloop_set_wait_limit_ns(uint64_t ns) {
+    if (ns > FLASHLOOP_WAIT_LIMIT_DEFAULT_NS)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "wait limit %llu ns exceeds the default %llu ns",
+                         (unsigned long long)ns, (unsigned long long)FLASHLOOP_WAIT_LIMIT_DEFAULT_NS);
+    flashloop_status_t st = check_device();
+    if (st != FLASHLOOP_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = static_cast<cudaError_t>(tc_attention_set_wait_limit((unsigned long long)ns));
+    if (e != cudaSuccess) return cuda_fail(e, "set wait limit");
+    return FLASHLOOP_OK;
+}
+
 flashloop_status_t flashloop_device_status(int32_t *word) {
     if (!word) return set_error(FLASHLOOP_ERR_INVALID_ARG, "word is NULL");
     cudaError_t e = cudaDeviceSynchronize();

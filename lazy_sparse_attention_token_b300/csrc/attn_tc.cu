@@ -44,9 +44,10 @@
 // [384,384+d).
 //
 // Waiting threads sleep in a hinted try_wait instead of spinning. Every
-// mbarrier wait is bounded (about one second); on timeout the CTA records an
-// error code, stops issuing work, waits (bounded) for its own copies and
-// MMAs, frees TMEM and exits.
+// mbarrier wait is bounded (one second unless the host shortens it); on
+// timeout the CTA records an error code, stops issuing work, waits (bounded,
+// one second) for its own copies and MMAs, frees TMEM and exits. A softmax
+// warp proceeds past a wait only when all of its lanes saw the phase.
 #include <cudaTypedefs.h>
 #include <float.h>
 #include <mutex>
@@ -80,6 +81,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ int g_tc_error;
+// Limit of every bounded wait on the compute path, in ns (the host may only
+// shorten it, to exercise the failure path). Drains after a failure keep
+// kDrainLimitNs, so that a CTA that gave up still lets its own copies and MMAs
+// land before it frees TMEM and exits.
+constexpr unsigned long long kWaitLimitNs = FLASHLOOP_WAIT_LIMIT_DEFAULT_NS;
+constexpr unsigned long long kDrainLimitNs = FLASHLOOP_WAIT_LIMIT_DEFAULT_NS;
+__device__ unsigned long long g_tc_wait_limit_ns = kWaitLimitNs;
 
 enum : int { PH_OLD = 0, PH_LSE = 1, PH_NEW = 2 };
 // PV_DONE[b] completes when the PV product that read P buffer b is done (the
@@ -171,17 +179,17 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Bounded wait. The thread sleeps inside try_wait (hinted) rather than
-// spinning; it gives up after about one second, or as soon as another role
-// has given up, recording the first failure code.
-__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code) {
+// Bounded wait. The thread sleeps inside try_wait (hinted, at most the limit)
+// rather than spinning; it gives up once `limit_ns` has passed, or as soon as
+// another role has given up, recording the first failure code.
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code,
+                                           unsigned long long limit_ns) {
     const uint64_t t0 = globaltimer_ns();
+    const uint32_t hint = limit_ns < 20000ull ? (uint32_t)limit_ns : 20000u;
     for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 8; ++i)
-            if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > 1000000000ull) {
+        if (globaltimer_ns() - t0 >= limit_ns) {
             *abort_flag = 1;
             atomicCAS(&g_tc_error, 0, code);
             return false;
@@ -191,7 +199,22 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volati
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code) {
     if (mbar_test_wait(bar, parity)) return true;
-    return wait_bar_slow(bar, parity, abort_flag, code);
+    return wait_bar_slow(bar, parity, abort_flag, code, *(volatile unsigned long long *)&g_tc_wait_limit_ns);
+}
+
+// The same wait for a whole warp that goes on to warp-collective instructions
+// (tcgen05.ld/st .sync.aligned, shuffles): every lane waits, and the warp
+// proceeds only if all of them saw the phase complete, so that a lane that
+// gave up never leaves the others alone in a collective.
+__device__ __forceinline__ bool wait_bar_all(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, code));
+}
+
+// Wait of a drain after a failure: not cut short by the abort flag, and held to
+// kDrainLimitNs whatever the compute-path limit is.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int code) {
+    volatile int never = 0;
+    if (!mbar_test_wait(bar, parity)) wait_bar_slow(bar, parity, &never, code, kDrainLimitNs);
 }
 
 // Byte offset of 16-byte chunk `ch` (8 bf16) of row r in a 128-row tile laid
@@ -388,9 +411,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
             }
             if (*abort_flag) {   // let copies already in flight land before the CTA exits
-                volatile int never = 0;
-                for (int q = max(0, pos - kStages); q < pos; ++q)
-                    wait_bar(bar(full_bar_of(q)), full_parity(q), &never, ERR_FULL);
+                for (int q = max(0, pos - kStages); q < pos; ++q) drain_wait(bar(full_bar_of(q)), full_parity(q), ERR_FULL);
             }
         }
     } else if (warp == 1 || warp == 2) {
@@ -485,8 +506,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             }
             if (!ok) {   // drain whatever this thread issued before giving up
                 mma_commit(bar(BAR_DRAIN + (warp - 1)));
-                volatile int never = 0;
-                wait_bar(bar(BAR_DRAIN + (warp - 1)), 0, &never, ERR_ACC);
+                drain_wait(bar(BAR_DRAIN + (warp - 1)), 0, ERR_ACC);
             }
         }
     } else {
@@ -516,7 +536,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         // past a row's prefix count are masked to -inf.
         auto load_s = [&](int t, float (&v)[32]) -> bool {
             const int sb = g & 1;
-            if (!wait_bar(bar(BAR_S_FULL + sb), (g >> 1) & 1, abort_flag, ERR_S_FULL)) return false;
+            if (!wait_bar_all(bar(BAR_S_FULL + sb), (g >> 1) & 1, abort_flag, ERR_S_FULL)) return false;
             tc_fence_after();
             tmem_ld_16x256b_x4(t_lo + 128u * sb + cbase, v);
             tmem_ld_16x256b_x4(t_hi + 128u * sb + cbase, v + 16);
@@ -558,7 +578,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
             // P buffer pv & 1 was last read by the PV product of the V tile two before
             const int pb = pv & 1;
-            if (pv >= 2 && !wait_bar(bar(BAR_PV_DONE + pb), (uint32_t)((pv >> 1) - 1) & 1u, abort_flag, ERR_PV_DONE))
+            if (pv >= 2 && !wait_bar_all(bar(BAR_PV_DONE + pb), (uint32_t)((pv >> 1) - 1) & 1u, abort_flag, ERR_PV_DONE))
                 return false;
             tc_fence_after();
             // bf16 pairs of adjacent keys: register pair (2i, 2i + 1) is one packed P column
@@ -659,7 +679,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
             }
             warp_arrive(bar(BAR_STATS), lane);
-            ok = wait_bar(bar(BAR_STATS), 0, abort_flag, ERR_STATS);
+            ok = wait_bar_all(bar(BAR_STATS), 0, abort_flag, ERR_STATS);
             if (ok && wg == 0) {
                 // rows with an empty key set or no old mass keep their state (Z' = inf)
                 float zn = INFINITY;
@@ -682,7 +702,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             }
             if (ok) {
                 warp_arrive(bar(BAR_ZN), lane);
-                ok = wait_bar(bar(BAR_ZN), 0, abort_flag, ERR_ZN);
+                ok = wait_bar_all(bar(BAR_ZN), 0, abort_flag, ERR_ZN);
             }
         }
         // ---- pass NEW: this loop's probabilities with the merged normaliser, added ----
@@ -692,7 +712,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             for (int k = 0; k < 4; ++k) nz[k] = -row_zn[rlo + 8 * k];
             for (int t = 0; ok && t < n_tiles; ++t) ok = pv_tile(std::false_type{}, t, nz);
         }
-        if (ok && wait_bar(bar(BAR_ACC), 0, abort_flag, ERR_ACC)) {
+        if (ok && wait_bar_all(bar(BAR_ACC), 0, abort_flag, ERR_ACC)) {
             tc_fence_after();
             // Epilogue. A thread's accumulator row goes to shared memory (the ring is idle
             // now); then each warp walks whole rows so that O, Z and qhat move in full lines.
@@ -709,7 +729,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 dst[1] = make_float4(av[4], av[5], av[6], av[7]);
             }
             warp_arrive(bar(BAR_EPI), lane);
-            if (wait_bar(bar(BAR_EPI), 0, abort_flag, ERR_EPI)) {
+            if (wait_bar_all(bar(BAR_EPI), 0, abort_flag, ERR_EPI)) {
                 constexpr int RPW = BM / kSoftmaxWarps;   // rows per warp
                 const int sw = warp - kFirstSoftmaxWarp;
                 float4 ov[RPW];
@@ -857,6 +877,10 @@ cudaError_t launch_tc_attention(const TcAttnParams &p, cudaStream_t s) {
         case 128: return launch_d<128>(p, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+int32_t tc_attention_set_wait_limit(unsigned long long ns) {
+    return (int32_t)cudaMemcpyToSymbol(g_tc_wait_limit_ns, &ns, sizeof ns);
 }
 
 int32_t tc_attention_read_error(bool clear) {

@@ -101,6 +101,7 @@ struct TcAttnParams {
 };
 cudaError_t launch_tc_attention(const TcAttnParams &p, cudaStream_t s);
 int32_t tc_attention_read_error(bool clear);
+int32_t tc_attention_set_wait_limit(unsigned long long ns);   // cudaError_t
 // attn_decode.cu (few-row attention reading the cache directly)
 struct DecodeAttnParams {
     int mode;

@@ -64,7 +64,9 @@ EXPORTS = [
     "flashloop_select_keys", "flashloop_reconstruct_keys", "flashloop_lazy_attention", "flashloop_loop_step",
     "flashloop_status_string", "flashloop_last_error", "flashloop_device_status", "flashloop_launch_count",
     "flashloop_timing_enable", "flashloop_timing_read", "flashloop_select_tokens_noalloc",
+    "flashloop_set_wait_limit_ns",
 ]
+WAIT_LIMIT_DEFAULT_NS = 1_000_000_000
 
 
 def lib() -> ctypes.CDLL:
@@ -92,6 +94,7 @@ def lib() -> ctypes.CDLL:
         L.flashloop_status_string.argtypes = [ctypes.c_int]
         L.flashloop_last_error.restype = ctypes.c_char_p
         L.flashloop_device_status.argtypes = [ctypes.POINTER(I32)]
+        L.flashloop_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.flashloop_launch_count.restype = ctypes.c_int64
         L.flashloop_timing_enable.argtypes = [I32]
         L.flashloop_timing_read.restype = I32
@@ -296,6 +299,11 @@ def flashloop_device_status() -> int:
     w = I32(0)
     lib().flashloop_device_status(ctypes.byref(w))
     return w.value
+
+
+def flashloop_set_wait_limit_ns(ns: int):
+    """Limit of the attention kernel's bounded waits (may only shorten the default; synchronises)."""
+    _check(lib().flashloop_set_wait_limit_ns(int(ns)), "flashloop_set_wait_limit_ns")
 
 
 def flashloop_launch_count() -> int:

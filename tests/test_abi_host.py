@@ -259,3 +259,13 @@ def test_rejected_append_leaves_the_layer_as_it_was(L):
         assert b"n_tokens" in L.flashloop_last_error()
         assert c.count[0] == 5
     assert fl.flashloop_launch_count() == n0
+
+
+def test_wait_limit_can_only_be_shortened(L):
+    """The hook that shortens the attention kernel's bounded waits refuses a
+    limit above the default on the host, before any device call."""
+    n0 = fl.flashloop_launch_count()
+    assert L.flashloop_set_wait_limit_ns(fl.flashloop.WAIT_LIMIT_DEFAULT_NS + 1) == INVALID
+    assert b"exceeds the default" in L.flashloop_last_error()
+    assert L.flashloop_set_wait_limit_ns(2 ** 63) == INVALID
+    assert fl.flashloop_launch_count() == n0

@@ -270,6 +270,59 @@ def test_lazy_attention(B, N, H, d, R, K):
     np.testing.assert_allclose(f32(st.c).sum(-1), N, rtol=1e-4)
 
 
+def _lazy_case(seed):
+    """A small lazy attention call (two row tiles, two key tiles) and its oracle."""
+    B, N, H, d, R, K = 1, 520, 2, 128, 200, 150
+    dm, cache, st, q1, k1, v1 = _setup_first(B, N, H, d, seed)
+    dm2 = fl.make_dims(B, N, H, d, R, K, 2, 1, R_cap=R)
+    cache2 = fl.Cache(dm2)
+    cache2.n_tokens = N
+    fl.flashloop_kv_dense_store(cache2, 1, k1, v1)
+    q2, k2, v2 = ((x.float() + 0.3 * torch.randn(x.shape, generator=gen(seed + 10 + i), device="cuda")).to(torch.bfloat16)
+                  for i, x in enumerate((q1, k1, v1)))
+    A = torch.sort(torch.randperm(N, generator=gen(seed + 20), device="cuda")[:R]).values.to(torch.int32)[None]
+    fl.flashloop_kv_delta_append(cache2, 2, k2, v2, A)
+    S = fl.flashloop_select_keys(st.c, K)
+    torch.cuda.synchronize()
+    return dm2, cache2, st, q2, A, S
+
+
+def test_bounded_wait_gives_up_and_the_context_recovers():
+    """Failure path of the attention kernel's bounded waits, made to run out on
+    purpose by shortening the limit to zero (nothing is withheld: every copy and
+    MMA is still issued and lands). The launch completes, the device status
+    reports the failure with one of the kernel's wait codes, and once the limit
+    is restored the same call on fresh state matches the oracle."""
+    dm2, cache2, st, q2, A, S = _lazy_case(500)
+    ws = fl.workspace_for(dm2)
+    assert fl.flashloop_device_status() == 0
+    fl.flashloop_set_wait_limit_ns(0)
+    try:
+        fl.flashloop_lazy_attention(cache2, fl.LAZY, 2, q2, st.q_hat, st.o, st.z, st.c, row_pos=A, key_idx=S,
+                                    workspace=ws)
+        torch.cuda.synchronize()                    # the launch returned
+        word = fl.flashloop_device_status()
+    finally:
+        fl.flashloop_set_wait_limit_ns(fl.flashloop.WAIT_LIMIT_DEFAULT_NS)
+    assert word in (1, 2, 5, 6, 7, 8, 9, 10, 11, 12, 13), word
+    assert fl.flashloop_device_status() == 0        # read and cleared
+    # a fresh state through the same call, with the default limit
+    dm2, cache2, st, q2, A, S = _lazy_case(500)
+    before = (bits(st.q_hat), f32(st.o), f32(st.z), f32(st.c))
+    fl.flashloop_lazy_attention(cache2, fl.LAZY, 2, q2, st.q_hat, st.o, st.z, st.c, row_pos=A, key_idx=S,
+                                workspace=fl.workspace_for(dm2))
+    torch.cuda.synchronize()
+    assert fl.flashloop_device_status() == 0
+    base_k, base_v = (bits(t) for t in cache2.dense_layer(1))
+    lk, lv = layers_from_gpu(cache2, [2], [0])
+    kn = oracle.reconstruct(base_k, lk, want_f32=False)[1]
+    vn = oracle.reconstruct(base_v, lv, want_f32=False)[1]
+    a, s_ = A.cpu().numpy(), S.cpu().numpy()
+    qh, o, z, c, _ = oracle.attention(False, a, a, bits(q2), *before, s_, base_k, base_v, kn, vn)
+    assert_close(f32(st.o), o, O_ATOL, O_RTOL, "O after recovery")
+    assert_close(f32(st.c), c, C_ATOL, C_RTOL, "c after recovery")
+
+
 def test_lazy_full_sets_match_softmax_of_new_loop():
     """A = all rows, S = all keys: the lazy step is softmax attention over the
     loop-2 reconstruction (compared with torch's attention in float64)."""
