@@ -187,7 +187,9 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volati
     const uint64_t t0 = globaltimer_ns();
     const uint32_t hint = limit_ns < 20000ull ? (uint32_t)limit_ns : 20000u;
     for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i)
+            if (mbar_try_wait_sleep(bar, parity, hint)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 >= limit_ns) {
             *abort_flag = 1;
@@ -197,17 +199,21 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volati
     }
 }
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code) {
+// `limit_ns` is the kernel's copy of g_tc_wait_limit_ns, read once per thread
+// at the start of the kernel.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code,
+                                         unsigned long long limit_ns) {
     if (mbar_test_wait(bar, parity)) return true;
-    return wait_bar_slow(bar, parity, abort_flag, code, *(volatile unsigned long long *)&g_tc_wait_limit_ns);
+    return wait_bar_slow(bar, parity, abort_flag, code, limit_ns);
 }
 
 // The same wait for a whole warp that goes on to warp-collective instructions
 // (tcgen05.ld/st .sync.aligned, shuffles): every lane waits, and the warp
 // proceeds only if all of them saw the phase complete, so that a lane that
 // gave up never leaves the others alone in a collective.
-__device__ __forceinline__ bool wait_bar_all(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code) {
-    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, code));
+__device__ __forceinline__ bool wait_bar_all(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code,
+                                             unsigned long long limit_ns) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, code, limit_ns));
 }
 
 // Wait of a drain after a failure: not cut short by the abort flag, and held to
@@ -291,6 +297,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                     const __grid_constant__ CUtensorMap tm_v_new) {
     pdl_wait();   // every global read below depends on the previous kernel
     pdl_trigger();
+    const unsigned long long wlimit = g_tc_wait_limit_ns;
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -386,7 +393,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             // K or V tile t of pass ph into the next slot, once its previous tile is consumed
             auto load = [&](bool is_v, int ph, int t) -> bool {
                 const int s = pos % kStages, use = pos / kStages;
-                if (!wait_bar(bar(BAR_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_EMPTY)) return false;
+                if (!wait_bar(bar(BAR_EMPTY + s), (use & 1) ^ 1, abort_flag, ERR_EMPTY, wlimit)) return false;
                 const CUtensorMap *m = is_v ? (ph == PH_OLD ? &tm_v_old : &tm_v_new) : (ph == PH_OLD ? &tm_k_old : &tm_k_new);
                 const uint32_t dst = sbase + C::OFF_KV + C::TB * s;
                 const uint32_t full = bar(full_bar_of(pos));
@@ -445,12 +452,12 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             auto issue_qk = [&](int g) -> bool {
                 const int kp = g < lse0 ? kv_pos_k(g) : g < new0 ? base_lse + g - lse0 : base_new + kv_pos_k(g - new0);
                 const int ks = kp % kStages, sb = g & 1;
-                if (!wait_bar(bar(full_bar_of(kp)), full_parity(kp), abort_flag, ERR_FULL)) return false;
+                if (!wait_bar(bar(full_bar_of(kp)), full_parity(kp), abort_flag, ERR_FULL, wlimit)) return false;
                 // the S buffer's previous tile has been read by the softmax
-                if (g >= kSBufs && !wait_bar(bar(BAR_S_READ + sb), ((g >> 1) - 1) & 1, abort_flag, ERR_S_READ))
+                if (g >= kSBufs && !wait_bar(bar(BAR_S_READ + sb), ((g >> 1) - 1) & 1, abort_flag, ERR_S_READ, wlimit))
                     return false;
                 if (g >= lse0 && !q_seen) {   // after pass OLD, once the query tile holds this loop's q
-                    if (!wait_bar(bar(BAR_Q_READY), 0, abort_flag, ERR_Q_READY)) return false;
+                    if (!wait_bar(bar(BAR_Q_READY), 0, abort_flag, ERR_Q_READY, wlimit)) return false;
                     q_seen = true;
                 }
                 tc_fence_after();
@@ -474,8 +481,8 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 const int pb = pv & 1;
                 const int vp = pv < n_old ? kv_pos_v(pv, n_tiles) : base_new + kv_pos_v(pv - n_old, n_tiles);
                 const int vs = vp % kStages;
-                if (!wait_bar(bar(full_bar_of(vp)), full_parity(vp), abort_flag, ERR_FULL)) return false;
-                if (!wait_bar(bar(BAR_P_FULL + pb), (uint32_t)(pv >> 1) & 1u, abort_flag, ERR_P_FULL)) return false;
+                if (!wait_bar(bar(full_bar_of(vp)), full_parity(vp), abort_flag, ERR_FULL, wlimit)) return false;
+                if (!wait_bar(bar(BAR_P_FULL + pb), (uint32_t)(pv >> 1) & 1u, abort_flag, ERR_P_FULL, wlimit)) return false;
                 tc_fence_after();
                 const uint64_t dv = d_v + TB16 * (uint32_t)vs;
                 const uint32_t pa = tmem + kColP + 64u * (uint32_t)pb;
@@ -536,7 +543,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         // past a row's prefix count are masked to -inf.
         auto load_s = [&](int t, float (&v)[32]) -> bool {
             const int sb = g & 1;
-            if (!wait_bar_all(bar(BAR_S_FULL + sb), (g >> 1) & 1, abort_flag, ERR_S_FULL)) return false;
+            if (!wait_bar_all(bar(BAR_S_FULL + sb), (g >> 1) & 1, abort_flag, ERR_S_FULL, wlimit)) return false;
             tc_fence_after();
             tmem_ld_16x256b_x4(t_lo + 128u * sb + cbase, v);
             tmem_ld_16x256b_x4(t_hi + 128u * sb + cbase, v + 16);
@@ -578,7 +585,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
             // P buffer pv & 1 was last read by the PV product of the V tile two before
             const int pb = pv & 1;
-            if (pv >= 2 && !wait_bar_all(bar(BAR_PV_DONE + pb), (uint32_t)((pv >> 1) - 1) & 1u, abort_flag, ERR_PV_DONE))
+            if (pv >= 2 && !wait_bar_all(bar(BAR_PV_DONE + pb), (uint32_t)((pv >> 1) - 1) & 1u, abort_flag, ERR_PV_DONE, wlimit))
                 return false;
             tc_fence_after();
             // bf16 pairs of adjacent keys: register pair (2i, 2i + 1) is one packed P column
@@ -679,7 +686,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 }
             }
             warp_arrive(bar(BAR_STATS), lane);
-            ok = wait_bar_all(bar(BAR_STATS), 0, abort_flag, ERR_STATS);
+            ok = wait_bar_all(bar(BAR_STATS), 0, abort_flag, ERR_STATS, wlimit);
             if (ok && wg == 0) {
                 // rows with an empty key set or no old mass keep their state (Z' = inf)
                 float zn = INFINITY;
@@ -702,7 +709,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             }
             if (ok) {
                 warp_arrive(bar(BAR_ZN), lane);
-                ok = wait_bar_all(bar(BAR_ZN), 0, abort_flag, ERR_ZN);
+                ok = wait_bar_all(bar(BAR_ZN), 0, abort_flag, ERR_ZN, wlimit);
             }
         }
         // ---- pass NEW: this loop's probabilities with the merged normaliser, added ----
@@ -712,7 +719,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             for (int k = 0; k < 4; ++k) nz[k] = -row_zn[rlo + 8 * k];
             for (int t = 0; ok && t < n_tiles; ++t) ok = pv_tile(std::false_type{}, t, nz);
         }
-        if (ok && wait_bar_all(bar(BAR_ACC), 0, abort_flag, ERR_ACC)) {
+        if (ok && wait_bar_all(bar(BAR_ACC), 0, abort_flag, ERR_ACC, wlimit)) {
             tc_fence_after();
             // Epilogue. A thread's accumulator row goes to shared memory (the ring is idle
             // now); then each warp walks whole rows so that O, Z and qhat move in full lines.
@@ -729,7 +736,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 dst[1] = make_float4(av[4], av[5], av[6], av[7]);
             }
             warp_arrive(bar(BAR_EPI), lane);
-            if (wait_bar_all(bar(BAR_EPI), 0, abort_flag, ERR_EPI)) {
+            if (wait_bar_all(bar(BAR_EPI), 0, abort_flag, ERR_EPI, wlimit)) {
                 constexpr int RPW = BM / kSoftmaxWarps;   // rows per warp
                 const int sw = warp - kFirstSoftmaxWarp;
                 float4 ov[RPW];

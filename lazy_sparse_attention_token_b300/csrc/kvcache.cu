@@ -156,74 +156,106 @@ __device__ __forceinline__ void store_group_bf16(const float (&rec)[32], uint16_
 
 // For each selected key j = key_idx[b,h,r]: reconstruction at the old loop
 // (old_layers deltas) and at the new loop (new_layers deltas), bf16 RNE,
-// written densely as [B, H, K, d]. One thread per 32-element group of a
-// selected row: its four base chunks load together and each delta layer is
-// one slot lookup, one 16-byte codes load and one scale load for the group.
-// blockIdx.y: 0 = K, 1 = V.
+// written densely as [B, H, K, d]. A selected key of one head is one lane
+// group of d/4 lanes (a warp for d = 128, 96; two keys per warp for d = 64):
+// each lane owns one 16-byte chunk (8 elements) of the K or the V row, so
+// base rows and the dense copies move as whole rows. The dependent loads run
+// in two rounds per four delta layers: every layer's slot entry of the key at
+// once, then every entry's codes and scale at once, then the fp32 sums in
+// ascending layer order.
 //
-// The first n_count_blocks blocks of the K half instead count, for every
-// (b, h) and row i, the keys that row sees: #{r : key_idx[b,h,r] <= row_pos[b,i]}
-// (both lists ascending), by binary search over the head's key list.
+// The first n_count_blocks blocks instead count, for every (b, h) and row i,
+// the keys that row sees: #{r : key_idx[b,h,r] <= row_pos[b,i]} (both lists
+// ascending), by binary search over the head's key list staged in shared
+// memory (or read from global memory when the list is longer than the stage).
 constexpr int kRecThreads = 256;
+constexpr int kCountSplit = 4;            // counting blocks per (b, h)
+constexpr int kCountStageMax = 12288;     // keys staged in shared memory (48 KB)
+constexpr int kLayerBatch = 4;            // delta layers whose loads are issued together
+template <int D>
 __global__ void __launch_bounds__(kRecThreads)
 reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const int32_t *__restrict__ key_idx,
-                        int H, int K, int d, int N_cap, int R_cap, long long total,
+                        int H, int K, int N_cap, int R_cap, int n_keys_total,
                         uint16_t *__restrict__ k_old, uint16_t *__restrict__ v_old,
                         uint16_t *__restrict__ k_new, uint16_t *__restrict__ v_new,
-                        const int32_t *__restrict__ row_pos, int R, long long count_total, int n_count_blocks,
+                        const int32_t *__restrict__ row_pos, int R, int n_count_blocks,
                         int32_t *__restrict__ row_cnt) {
     pdl_wait();
     pdl_trigger();
+    extern __shared__ int32_t s_keys[];
     if ((int)blockIdx.x < n_count_blocks) {
-        if (blockIdx.y != 0) return;
-        const uint32_t t = blockIdx.x * kRecThreads + threadIdx.x;
-        if (t >= (uint32_t)count_total) return;
-        const uint32_t bh32 = t / (uint32_t)R;
-        const int i = (int)(t - bh32 * (uint32_t)R);
-        const long long bh = bh32, b = bh32 / (uint32_t)H;
-        const int32_t *S = key_idx + bh * K;
-        const int x = __ldg(row_pos + b * R + i);
-        int lo = 0, hi = K;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (__ldg(S + mid) <= x) lo = mid + 1; else hi = mid;
+        const int bh = (int)blockIdx.x / kCountSplit, part = (int)blockIdx.x % kCountSplit;
+        const int b = bh / H;
+        const int32_t *S = key_idx + (long long)bh * K;
+        const bool staged = K <= kCountStageMax;
+        if (staged)
+            for (int i = threadIdx.x; i < K; i += kRecThreads) s_keys[i] = __ldg(S + i);
+        __syncthreads();
+        const int per = (R + kCountSplit - 1) / kCountSplit;
+        const int i0 = part * per, i1 = min(R, i0 + per);
+        for (int i = i0 + (int)threadIdx.x; i < i1; i += kRecThreads) {
+            const int x = __ldg(row_pos + (long long)b * R + i);
+            int lo = 0, hi = K;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if ((staged ? s_keys[mid] : __ldg(S + mid)) <= x) lo = mid + 1; else hi = mid;
+            }
+            row_cnt[(long long)bh * R + i] = lo;
         }
-        row_cnt[bh * R + i] = lo;
         return;
     }
-    const uint32_t t = (blockIdx.x - (uint32_t)n_count_blocks) * kRecThreads + threadIdx.x;   // 32-bit, as above
-    if (t >= (uint32_t)total) return;
-    const bool is_v = blockIdx.y == 1;
-    const uint32_t gpr = (uint32_t)d / 32u;
-    const uint32_t bhr32 = t / gpr;          // (b * H + h) * K + r
-    const int g = (int)(t - bhr32 * gpr);
-    const uint32_t bh32 = bhr32 / (uint32_t)K;
-    const uint32_t b32 = bh32 / (uint32_t)H;
-    const int h = (int)(bh32 - b32 * (uint32_t)H);
-    const long long bhr = bhr32, b = b32;
-    const int j = __ldg(key_idx + bhr);
-    const uint16_t *base = (is_v ? view.v_base : view.k_base) + ((b * N_cap + j) * H + h) * (long long)d + g * 32;
-    uint4 bv[4];
+    constexpr int d = D;
+    constexpr int cpr = D / 8;              // 16-byte chunks per row of one tensor
+    constexpr int lpk = 2 * cpr;            // lanes per key: K chunks, then V chunks
+    constexpr int kpw = 32 / lpk;           // keys per warp
+    const int lane = threadIdx.x & 31, sub = lane / lpk, c = lane - sub * lpk;
+    // 32-bit index arithmetic (the launcher checks that the key count fits):
+    // 64-bit division is a long instruction sequence
+    const uint32_t key = ((uint32_t)(blockIdx.x - n_count_blocks) * (kRecThreads / 32) + threadIdx.x / 32) * kpw + sub;
+    if (sub >= kpw || key >= (uint32_t)n_keys_total) return;
+    const bool is_v = c >= cpr;
+    const int ch = is_v ? c - cpr : c;      // elements 8 ch .. 8 ch + 7, quantisation group ch / 4
+    const uint32_t bh = key / (uint32_t)K;
+    const uint32_t b32 = bh / (uint32_t)H;
+    const int h = (int)(bh - b32 * (uint32_t)H);
+    const long long b = b32;
+    const int j = __ldg(key_idx + key);
+    const long long tok = b * N_cap + j;
+    float rec[8];
+    unpack_bf16x8(ldg_nc_v4((is_v ? view.v_base : view.k_base) + (tok * H + h) * d + ch * 8), rec);
+    uint16_t *o_old = (is_v ? v_old : k_old) + (long long)key * d + ch * 8;
+    uint16_t *o_new = (is_v ? v_new : k_new) + (long long)key * d + ch * 8;
+    auto store8 = [&](uint16_t *dst) {
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(pack_bf16x2_rn(rec[0], rec[1]), pack_bf16x2_rn(rec[2], rec[3]),
+                                                     pack_bf16x2_rn(rec[4], rec[5]), pack_bf16x2_rn(rec[6], rec[7]));
+    };
+    for (int m0 = 0; m0 < new_layers; m0 += kLayerBatch) {
+        int en[kLayerBatch];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) bv[c] = ldg_nc_v4(base + c * 8);
-    float rec[32];
+        for (int u = 0; u < kLayerBatch; ++u) en[u] = m0 + u < new_layers ? __ldg(view.slot[m0 + u] + tok) : -1;
+        uint32_t w[kLayerBatch];
+        float sc[kLayerBatch];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) unpack_bf16x8(bv[c], rec + 8 * c);
-    for (int m = 0; m < new_layers; ++m) {
-        if (m == old_layers) store_group_bf16(rec, (is_v ? v_old : k_old) + bhr * d + g * 32);
-        const int en = __ldg(view.slot[m] + b * N_cap + j);
-        if (en < 0) continue;
-        const long long ent = (b * R_cap + en) * H + h;
-        const uint8_t *codes = is_v ? view.v_codes[m] : view.k_codes[m];
-        const uint16_t *scales = is_v ? view.v_scales[m] : view.k_scales[m];
-        const uint4 w4 = __ldg(reinterpret_cast<const uint4 *>(codes + ent * (d / 2) + g * 16));
-        const float sc = __half2float(__ushort_as_half(__ldg(scales + ent * (d / 32) + g)));
-        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+        for (int u = 0; u < kLayerBatch; ++u) {
+            w[u] = 0u;
+            sc[u] = 0.f;
+            if (en[u] >= 0) {
+                const int m = m0 + u;
+                const long long ent = (b * R_cap + en[u]) * H + h;
+                const uint8_t *codes = is_v ? view.v_codes[m] : view.k_codes[m];
+                const uint16_t *scales = is_v ? view.v_scales[m] : view.k_scales[m];
+                w[u] = __ldg(reinterpret_cast<const uint32_t *>(codes + ent * (d / 2)) + ch);
+                sc[u] = __half2float(__ushort_as_half(__ldg(scales + ent * (d / 32) + ch / 4)));
+            }
+        }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dequant_add8(rec + 8 * c, w[c], sc);
+        for (int u = 0; u < kLayerBatch; ++u) {
+            if (m0 + u == old_layers) store8(o_old);
+            if (en[u] >= 0) dequant_add8(rec, w[u], sc[u]);
+        }
     }
-    if (new_layers <= old_layers) store_group_bf16(rec, (is_v ? v_old : k_old) + bhr * d + g * 32);
-    store_group_bf16(rec, (is_v ? v_new : k_new) + bhr * d + g * 32);
+    if (new_layers <= old_layers) store8(o_old);
+    store8(o_new);
 }
 
 }  // namespace
@@ -277,18 +309,21 @@ cudaError_t launch_reconstruct_keys(const DeltaView &old_view, const DeltaView &
                                     int R_cap, uint16_t *k_old, uint16_t *v_old, uint16_t *k_new,
                                     uint16_t *v_new, const int32_t *row_pos, int R, int32_t *row_cnt,
                                     cudaStream_t s) {
-    const long long total = (long long)B * H * K * (d / 32);
-    const long long count_total = row_cnt ? (long long)B * H * R : 0;
-    const int n_count = ceil_div(count_total, kRecThreads);
-    if (total == 0 && n_count == 0) return cudaSuccess;
-    if (total + count_total > 0x7fffffffLL - 2 * kRecThreads) return cudaErrorInvalidValue;   // 32-bit indexing
-    dim3 grid(n_count + ceil_div(total, kRecThreads), 2);
+    const long long n_keys = (long long)B * H * K;
+    const int n_count = row_cnt && R > 0 ? B * H * kCountSplit : 0;
+    if (n_keys == 0 && n_count == 0) return cudaSuccess;
+    if (n_keys > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (d != 64 && d != 96 && d != 128) return cudaErrorInvalidValue;
+    const int kpw = 32 / (2 * (d / 8));                         // keys per warp
+    const long long keys_per_block = (long long)(kRecThreads / 32) * kpw;
+    const int n_rec = ceil_div(n_keys, keys_per_block);
+    const size_t smem = n_count && K <= kCountStageMax ? (size_t)K * sizeof(int32_t) : 0;
+    auto kern = d == 64 ? reconstruct_keys_kernel<64> : d == 96 ? reconstruct_keys_kernel<96> : reconstruct_keys_kernel<128>;
     {
         KernelTimer kt("reconstruct_keys", s);
-        const cudaError_t e = launch_pdl(reconstruct_keys_kernel, grid, dim3(kRecThreads), 0, s, new_view,
-                                         old_view.n_layers, new_view.n_layers, key_idx, H, K, d, N_cap, R_cap,
-                                         total, k_old, v_old, k_new, v_new, row_pos, R, count_total, n_count,
-                                         row_cnt);
+        const cudaError_t e = launch_pdl(kern, dim3(n_count + n_rec), dim3(kRecThreads), smem, s, new_view,
+                                         old_view.n_layers, new_view.n_layers, key_idx, H, K, N_cap, R_cap,
+                                         (int)n_keys, k_old, v_old, k_new, v_new, row_pos, R, n_count, row_cnt);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
