@@ -483,6 +483,9 @@ def native(args, world, rank, local):
 
     e2e = None if args.no_e2e else e2e_leg(args, w, fl, cache, ws, loops, q_hat, o, z, c, act, keys, scores, lazy,
                                            dev, world)
+    recovery = None
+    if not args.no_recovery and rank == 0:
+        recovery = column_recovery_leg(w, fl, loops, dev)
     out = {
         "metric": metric_for(args.workload), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
@@ -496,6 +499,7 @@ def native(args, world, rank, local):
                    "active_tokens_per_s": w.B * R * args.steps * world / secs},
         "roofline": roofline, "step_roofline": step_roofline, "kernels": kernels, "gpu_launches": launches,
         "clocks": clk, "e2e": e2e, "kv_cache": kv_cache_accounting(fl, dims, w.B, w.N, w.H, w.d, w.T),
+        "column_recovery": recovery,
     }
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, R, K, state1, budget_s=args.cpu_budget)
@@ -630,6 +634,55 @@ def native_decode(args, world, rank, local):
         "roofline": roofline, "kernels": kernels, "gpu_launches": launches, "clocks": clk, "e2e": None,
         "kv_cache": kv_cache_accounting(fl, dims, w.B, Nk, w.H, w.d, w.T),
     }
+
+
+def column_recovery_leg(w, fl, loops, dev, fractions=(0.05, 0.10, 0.20, 0.50)):
+    """The synthetic analogue of the pages' "10% of the attention columns in a
+    late loop recover more than 90% of the exact result": lazy loop 2 of this
+    workload from one starting state (the CUDA path's dense loop 1), its token
+    selection and delta append as the loop step does them, then attention over
+    the top-k key columns (ranked by column mass, and by column mass per
+    causal row) for each k, and over every key (the exact softmax of the loop-2
+    reconstruction). Over the active rows:
+      recovered = 1 - ||O_k - O_all|| / ||O_before - O_all||,
+      rel_err = ||O_k - O_all|| / ||O_all||.
+    Not timed; the inputs are synthetic, so the figures describe this data, not
+    a trained model's attention."""
+    R = synth.active_count(w)
+    dims = fl.make_dims(w.B, w.N, w.H, w.d, R, w.N, w.T, w.T_dense, R_cap=R)
+    cache = fl.Cache(dims, device=dev)
+    cache.n_tokens = w.N
+    ws = fl.workspace_for(dims, device=dev)
+    st = [torch.zeros(w.B, w.N, w.H, w.d, dtype=torch.bfloat16, device=dev),
+          torch.zeros(w.B, w.N, w.H, w.d, dtype=torch.float32, device=dev),
+          torch.zeros(w.B, w.H, w.N, dtype=torch.float32, device=dev),
+          torch.zeros(w.B, w.H, w.N, dtype=torch.float32, device=dev)]
+    x1, x2 = loops[0], loops[1]
+    fl.flashloop_loop_step(cache, 1, x1["Q"], x1["K"], x1["V"], *st, ws)
+    act = fl.flashloop_select_tokens(x1["H"], x2["H"], R, scores=torch.empty(w.B, w.N, device=dev))
+    fl.flashloop_kv_delta_append(cache, 2, x2["K"], x2["V"], act)
+    torch.cuda.synchronize()
+
+    def run(S):
+        q_hat, o, z, c = (t.clone() for t in st)
+        fl.flashloop_lazy_attention(cache, fl.LAZY, 2, x2["Q"], q_hat, o, z, c, row_pos=act, key_idx=S, workspace=ws)
+        torch.cuda.synchronize()
+        return torch.stack([o[b, act[b].long()] for b in range(w.B)]).double()
+
+    full = run(torch.arange(w.N, dtype=torch.int32, device=dev).expand(w.B, w.H, w.N).contiguous())
+    prev = torch.stack([st[1][b, act[b].long()] for b in range(w.B)]).double()
+    change, full_norm = float((prev - full).norm()), float(full.norm())
+    out = {"loop": 2, "rows": f"the {R} active rows of each sequence", "reference": "every key (exact softmax)"}
+    for name, select in (("by_mass", fl.flashloop_select_keys), ("by_mass_per_row", fl.flashloop_select_keys_per_row)):
+        res = {}
+        for f in fractions:
+            k = synth.key_count(w) if abs(f - float(w.k)) < 1e-9 else max(1, math.ceil(f * w.N))
+            miss = float((run(select(st[3], k)) - full).norm())
+            res[f"{f:.0%}"] = {"k": k, "recovered": 1.0 - miss / change if change > 0 else 1.0,
+                               "rel_err": miss / full_norm if full_norm > 0 else 0.0}
+        out[name] = res
+    assert fl.flashloop_device_status() == 0
+    return out
 
 
 def e2e_leg(args, w, fl, cache, ws, loops, q_hat, o, z, c, act, keys, scores, lazy, dev, world):
@@ -860,6 +913,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of replayed CUDA graphs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-recovery", action="store_true", help="skip the column-recovery analysis")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
     args = ap.parse_args()

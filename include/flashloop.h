@@ -100,6 +100,12 @@ typedef struct {
     int32_t count[FLASHLOOP_MAX_LOOPS];
 } flashloop_kv_cache_t;
 
+/* How a lazy prefill loop ranks key columns for its selection. */
+typedef enum {
+    FLASHLOOP_KEYS_BY_MASS = 0,         /* column mass c_j */
+    FLASHLOOP_KEYS_BY_MASS_PER_ROW = 1  /* c_j / (N - j): mass per causal row that sees key j */
+} flashloop_key_rank_t;
+
 typedef enum {
     FLASHLOOP_ATTN_FIRST_DENSE = 0, /* loop 1: every row and key, no previous state (m = 1, u = 0) */
     FLASHLOOP_ATTN_DENSE = 1,       /* a later dense loop: every row and key, previous state used */
@@ -173,6 +179,7 @@ typedef struct {
     float *scores;            /* [B, N] out, or NULL */
     void *workspace;
     size_t workspace_bytes;
+    int32_t key_rank;         /* flashloop_key_rank_t of the key selection (prefill lazy loops) */
 } flashloop_step_args_t;
 
 /* ---- sizes and set-up ------------------------------------------------- */
@@ -259,6 +266,16 @@ flashloop_status_t flashloop_kv_dense_store(flashloop_kv_cache_t *cache, int32_t
 flashloop_status_t flashloop_select_keys(const float *col_stats, int32_t B, int32_t H, int32_t N, int32_t K,
                                          int32_t *key_idx, void *workspace, size_t workspace_bytes,
                                          flashloop_stream_t stream);
+
+/* Key-column selection by column mass per causal row: another reading of
+ * "keys are chosen from the previous loop's statistics" (same page and
+ * section as flashloop_select_keys): the K largest col_stats[b, h, j] / (n_rows - j) per
+ * (b, h), the quotient an IEEE fp32 division, ties to the lower index,
+ * ascending. In a prefill of n_rows tokens, n_rows - j rows see key j, so a
+ * key that late rows see is not outranked only for being seen by fewer rows.
+ * col_stats [B, H, N] fp32; key_idx [B, H, K] out. N <= n_rows. */
+flashloop_status_t flashloop_select_keys_per_row(const float *col_stats, int32_t B, int32_t H, int32_t N, int32_t K,
+                                                 int32_t n_rows, int32_t *key_idx, flashloop_stream_t stream);
 
 /* Reconstruct-gather of the selected keys: for j = key_idx[b, h, r],
  * k_old/v_old[b, h, r, :] = bf16_rne(reconstruction at loop-1) and

@@ -421,19 +421,34 @@ flashloop_status_t flashloop_kv_dense_store(flashloop_kv_cache_t *cache, int32_t
     return FLASHLOOP_OK;
 }
 
+namespace fl {
+static flashloop_status_t select_keys_impl(const float *col_stats, int32_t B, int32_t H, int32_t N, int32_t K,
+                                           int32_t n_rows, int32_t *key_idx, flashloop_stream_t stream) {
+    if (!col_stats || !key_idx) return set_error(FLASHLOOP_ERR_INVALID_ARG, "NULL pointer");
+    if (B < 1 || H < 1 || N < 1 || K < 1 || K > N)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad sizes (B=%d H=%d N=%d K=%d)", B, H, N, K);
+    if (n_rows != 0 && n_rows < N)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "n_rows=%d must cover the N=%d columns", n_rows, N);
+    flashloop_status_t st = check_device();
+    if (st != FLASHLOOP_OK) return st;
+    cudaError_t e = launch_topk_rows(col_stats, B * H, N, K, key_idx, stream, "topk_keys", n_rows);
+    if (e != cudaSuccess) return cuda_fail(e, "topk(keys)");
+    return FLASHLOOP_OK;
+}
+}  // namespace fl
+
 flashloop_status_t flashloop_select_keys(const float *col_stats, int32_t B, int32_t H, int32_t N, int32_t K,
                                          int32_t *key_idx, void *workspace, size_t workspace_bytes,
                                          flashloop_stream_t stream) {
     (void)workspace;
     (void)workspace_bytes;
-    if (!col_stats || !key_idx) return set_error(FLASHLOOP_ERR_INVALID_ARG, "NULL pointer");
-    if (B < 1 || H < 1 || N < 1 || K < 1 || K > N)
-        return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad sizes (B=%d H=%d N=%d K=%d)", B, H, N, K);
-    flashloop_status_t st = check_device();
-    if (st != FLASHLOOP_OK) return st;
-    cudaError_t e = launch_topk_rows(col_stats, B * H, N, K, key_idx, stream, "topk_keys");
-    if (e != cudaSuccess) return cuda_fail(e, "topk(keys)");
-    return FLASHLOOP_OK;
+    return fl::select_keys_impl(col_stats, B, H, N, K, 0, key_idx, stream);
+}
+
+flashloop_status_t flashloop_select_keys_per_row(const float *col_stats, int32_t B, int32_t H, int32_t N, int32_t K,
+                                                 int32_t n_rows, int32_t *key_idx, flashloop_stream_t stream) {
+    if (n_rows < 1) return set_error(FLASHLOOP_ERR_INVALID_ARG, "n_rows=%d", n_rows);
+    return fl::select_keys_impl(col_stats, B, H, N, K, n_rows, key_idx, stream);
 }
 
 flashloop_status_t flashloop_reconstruct_keys(const flashloop_kv_cache_t *cache, int32_t loop, const int32_t *key_idx,
@@ -642,7 +657,11 @@ flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop
         if (e != cudaSuccess) return cuda_fail(e, "fork of the key selection");
         key_stream = ss->s;
     }
-    st = flashloop_select_keys(a->c, dm.B, dm.H, n, dm.K, a->key_idx, nullptr, 0, key_stream);
+    if (a->key_rank != FLASHLOOP_KEYS_BY_MASS && a->key_rank != FLASHLOOP_KEYS_BY_MASS_PER_ROW)
+        st = set_error(FLASHLOOP_ERR_INVALID_ARG, "bad key_rank %d", a->key_rank);
+    else
+        st = fl::select_keys_impl(a->c, dm.B, dm.H, n, dm.K, a->key_rank == FLASHLOOP_KEYS_BY_MASS_PER_ROW ? n : 0,
+                                  a->key_idx, key_stream);
     if (st == FLASHLOOP_OK)
         st = flashloop_select_tokens(a->h_prev, a->h_cur, dm.B, n, dm.H * dm.d, dm.R, a->active_idx, scores,
                                      nullptr, 0, stream);

@@ -61,8 +61,9 @@ struct DeltaView {
 cudaError_t launch_token_scores(const uint16_t *h_prev, const uint16_t *h_cur, int B, int N, int D,
                                 float *scores, cudaStream_t s);
 // `name` labels the launch in the per-kernel timing ("topk_tokens", "topk_keys").
+// norm_n > 0 ranks column i by vals[i] / (norm_n - i) (requires n <= norm_n).
 cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t *out, cudaStream_t s,
-                             const char *name);
+                             const char *name, int norm_n = 0);
 // kvcache.cu
 cudaError_t launch_gather_rows(const void *src, int B, int N, int row_bytes, const int32_t *idx, int R,
                                void *dst, cudaStream_t s);

@@ -113,9 +113,11 @@ __device__ __forceinline__ void cl_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// norm_n > 0 ranks column i of a row by vals[i] / (norm_n - i) (IEEE fp32
+// division) instead of vals[i]: a key's column mass per causal row that sees it.
 template <bool kStaged>
 __global__ void __launch_bounds__(kTopkClThreads)
-topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__restrict__ out) {
+topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__restrict__ out, int norm_n) {
     extern __shared__ uint32_t staged[];
     __shared__ uint32_t whist[kTopkClWarps][256];   // one histogram per warp: keys of similar
                                                     // magnitude share a digit, so a single
@@ -139,9 +141,13 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
 
     if (rank == 0)
         for (int i = tid; i < 4 * 256; i += kTopkClThreads) (&g_hist[0][0])[i] = 0u;
+    auto value_at = [&](int i) -> float {
+        const float v = __ldg(row + lo + i);
+        return norm_n > 0 ? __fdiv_rn(v, (float)(norm_n - (lo + i))) : v;
+    };
     if (kStaged)
-        for (int i = tid; i < len; i += kTopkClThreads) staged[i] = f32_order_key(__ldg(row + lo + i));
-    auto key_at = [&](int i) -> uint32_t { return kStaged ? staged[i] : f32_order_key(__ldg(row + lo + i)); };
+        for (int i = tid; i < len; i += kTopkClThreads) staged[i] = f32_order_key(value_at(i));
+    auto key_at = [&](int i) -> uint32_t { return kStaged ? staged[i] : f32_order_key(value_at(i)); };
     cl_sync();   // rank 0's merged histograms are zero; every CTA of the cluster runs
 
     uint32_t prefix = 0, mask = 0;
@@ -263,7 +269,7 @@ cudaError_t launch_token_scores(const uint16_t *h_prev, const uint16_t *h_cur, i
 }
 
 cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t *out, cudaStream_t s,
-                             const char *name) {
+                             const char *name, int norm_n) {
     if (rows == 0) return cudaSuccess;
     const int ncta = rows >= kTopkRowsForSingle ? 1 : kTopkCluster;
     const int seg = ((n + ncta - 1) / ncta + 31) & ~31;
@@ -292,8 +298,8 @@ cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t 
     cudaError_t e;
     {
         KernelTimer kt(name, s);
-        e = staged ? cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, vals, n, k, out)
-                   : cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, vals, n, k, out);
+        e = staged ? cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, vals, n, k, out, norm_n)
+                   : cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, vals, n, k, out, norm_n);
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }

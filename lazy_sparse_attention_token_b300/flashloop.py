@@ -53,7 +53,8 @@ class AttnArgs(ctypes.Structure):
 class StepArgs(ctypes.Structure):
     _fields_ = [("loop", I32), ("decode", I32), ("h_prev", P), ("h_cur", P), ("q", P), ("k", P), ("v", P),
                 ("q_hat", P), ("o", P), ("z", P), ("c", P), ("cache", ctypes.POINTER(KVCache)),
-                ("active_idx", P), ("key_idx", P), ("scores", P), ("workspace", P), ("workspace_bytes", SZ)]
+                ("active_idx", P), ("key_idx", P), ("scores", P), ("workspace", P), ("workspace_bytes", SZ),
+                ("key_rank", I32)]
 
 
 _lib = None
@@ -64,8 +65,9 @@ EXPORTS = [
     "flashloop_select_keys", "flashloop_reconstruct_keys", "flashloop_lazy_attention", "flashloop_loop_step",
     "flashloop_status_string", "flashloop_last_error", "flashloop_device_status", "flashloop_launch_count",
     "flashloop_timing_enable", "flashloop_timing_read", "flashloop_select_tokens_noalloc",
-    "flashloop_set_wait_limit_ns",
+    "flashloop_set_wait_limit_ns", "flashloop_select_keys_per_row",
 ]
+KEYS_BY_MASS, KEYS_BY_MASS_PER_ROW = 0, 1
 WAIT_LIMIT_DEFAULT_NS = 1_000_000_000
 
 
@@ -87,6 +89,7 @@ def lib() -> ctypes.CDLL:
         L.flashloop_kv_delta_append.argtypes = [ctypes.POINTER(KVCache), I32, P, P, I32, P, I32, I32, P]
         L.flashloop_kv_dense_store.argtypes = [ctypes.POINTER(KVCache), I32, P, P, I32, I32, P]
         L.flashloop_select_keys.argtypes = [P, I32, I32, I32, I32, P, P, SZ, P]
+        L.flashloop_select_keys_per_row.argtypes = [P, I32, I32, I32, I32, I32, P, P]
         L.flashloop_reconstruct_keys.argtypes = [ctypes.POINTER(KVCache), I32, P, I32, P, P, P, P, P]
         L.flashloop_lazy_attention.argtypes = [ctypes.POINTER(AttnArgs), P]
         L.flashloop_loop_step.argtypes = [ctypes.POINTER(StepArgs), P]
@@ -255,6 +258,16 @@ def flashloop_select_keys(col_stats, K: int, key_idx=None, stream=None):
     return key_idx
 
 
+def flashloop_select_keys_per_row(col_stats, K: int, n_rows: Optional[int] = None, key_idx=None, stream=None):
+    """Top-K of col_stats[b, h, j] / (n_rows - j) per (b, h) (n_rows defaults to N)."""
+    B, H, N = col_stats.shape
+    if key_idx is None:
+        key_idx = torch.empty(B, H, K, dtype=torch.int32, device=col_stats.device)
+    _check(lib().flashloop_select_keys_per_row(_ptr(col_stats), B, H, N, K, N if n_rows is None else n_rows,
+                                               _ptr(key_idx), _stream(stream)), "flashloop_select_keys_per_row")
+    return key_idx
+
+
 def flashloop_reconstruct_keys(cache: Cache, loop: int, key_idx, stream=None):
     d = cache.dims
     B, H, K = key_idx.shape
@@ -282,9 +295,11 @@ def flashloop_lazy_attention(cache: Cache, mode: int, loop: int, q, q_hat, o, z,
 
 
 def flashloop_loop_step(cache: Cache, loop: int, q, k, v, q_hat, o, z, c, workspace, h_prev=None, h_cur=None,
-                        active_idx=None, key_idx=None, scores=None, decode: bool = False, stream=None):
+                        active_idx=None, key_idx=None, scores=None, decode: bool = False, key_rank: int = 0,
+                        stream=None):
     a = StepArgs()
     a.loop, a.decode = loop, int(decode)
+    a.key_rank = key_rank
     a.h_prev, a.h_cur = _ptr(h_prev), _ptr(h_cur)
     a.q, a.k, a.v = _ptr(q), _ptr(k), _ptr(v)
     a.q_hat, a.o, a.z, a.c = _ptr(q_hat), _ptr(o), _ptr(z), _ptr(c)

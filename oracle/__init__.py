@@ -218,6 +218,36 @@ def attention(first: bool, pos, slot, q, qhat, o, z, c, S, k_old, v_old, k_new, 
     return qhat, o, z, c, m
 
 
+def key_scores_per_row(c, n_rows: int) -> np.ndarray:
+    """Column mass per causal row that sees the key: c_j / (n_rows - j), as the
+    IEEE fp32 quotient (another reading of "keys chosen from the previous
+    loop's statistics", rit.work page, section "FlashLoop combines three kinds
+    of saving"; in a prefill of n_rows tokens, n_rows - j rows see key j).
+    c [..., N] fp32 -> float64 scores for ``topk``."""
+    c = np.asarray(c, dtype=np.float32)
+    n = c.shape[-1]
+    assert n <= n_rows
+    den = (n_rows - np.arange(n)).astype(np.float32)
+    return (c / den).astype(np.float32).astype(np.float64)
+
+
+def column_recovery(o_lazy, o_full, o_prev):
+    """How much of the exact loop-l attention result the lazy update over a
+    key subset recovers (the synthetic analogue of the rit.work page's
+    observation, section "Later loops change only part of the state", that
+    updating 10% of the attention columns in a late loop recovers more than
+    90% of the exact result), over the rows given (float64):
+      recovered = 1 - ||o_lazy - o_full|| / ||o_prev - o_full||
+      rel_err   = ||o_lazy - o_full|| / ||o_full||
+    with o_full the same rows updated over every key (exact softmax of the
+    loop-l reconstruction) and o_prev the rows before the loop."""
+    a, f, p = (np.asarray(x, dtype=np.float64) for x in (o_lazy, o_full, o_prev))
+    miss = np.linalg.norm((a - f).ravel())
+    change = np.linalg.norm((p - f).ravel())
+    return {"recovered": 1.0 - miss / change if change > 0 else 1.0,
+            "rel_err": miss / np.linalg.norm(f.ravel()) if np.any(f) else 0.0}
+
+
 def softmax_attention(q, k, v):
     """Textbook causal softmax attention in double: (o [B,N,H,d], lse [B,H,N])."""
     q, k, v = (_c(bits(t), np.uint16) for t in (q, k, v))

@@ -1,0 +1,137 @@
+"""Selection variants (the survey's next steps): key columns ranked by column
+mass per causal row, and the synthetic analogue of the rit.work page's "10% of
+the attention columns in a late loop recover more than 90% of the exact
+result" (section "Later loops change only part of the state"), measured on
+the CUDA path and compared with the oracle on the same inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import lazy_sparse_attention_token_b300 as fl
+from lazy_sparse_attention_token_b300 import build as flbuild
+from gpu_helpers import C_ATOL, C_RTOL, O_ATOL, O_RTOL, Z_ATOL, State, assert_close, bits, f32, layers_from_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    flbuild.build()
+    fl.lib()
+    oracle.build()
+
+
+def gen(seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return g
+
+
+@pytest.mark.parametrize("B,H,N,K,extra", [(1, 4, 1024, 103, 0), (2, 16, 8192, 820, 0), (1, 16, 32768, 3277, 0),
+                                           (2, 3, 700, 70, 5), (1, 128, 3000, 300, 0), (4, 2, 5, 1, 0)])
+def test_select_keys_per_row_exact(B, H, N, K, extra):
+    c = torch.rand(B, H, N, generator=gen(30), device="cuda") * 40
+    c = torch.where(torch.rand(B, H, N, generator=gen(31), device="cuda") < 0.3, torch.round(c), c)   # ties
+    n_rows = N + extra
+    idx = fl.flashloop_select_keys_per_row(c, K, n_rows=n_rows).cpu().numpy()
+    orc = oracle.topk(oracle.key_scores_per_row(f32(c), n_rows), K)
+    assert np.array_equal(idx, orc)
+
+
+def _tiny_after_loop1(K_cap):
+    w = synth.WORKLOADS["tiny"]
+    R, K = synth.active_count(w), synth.key_count(w)
+    dm = fl.make_dims(w.B, w.N, w.H, w.d, R, K_cap, w.T, w.T_dense, R_cap=R)
+    cache = fl.Cache(dm)
+    cache.n_tokens = w.N
+    ws = fl.workspace_for(dm)
+    st = State(w.B, w.N, w.H, w.d, w.N)
+    it = synth.prefill_loops(w, device="cuda", last=2)
+    x1, x2 = next(it), next(it)
+    fl.flashloop_loop_step(cache, 1, x1["Q"], x1["K"], x1["V"], st.q_hat, st.o, st.z, st.c, ws)
+    torch.cuda.synchronize()
+    return w, R, K, dm, cache, ws, st, x1, x2
+
+
+def test_loop_step_ranking_keys_per_row():
+    """A lazy loop of the tiny workload with the per-row key ranking: the key
+    columns equal the oracle's selection on the loop's starting column mass,
+    and the attention state matches the oracle on those sets."""
+    w, R, K, dm, cache, ws, st, x1, x2 = _tiny_after_loop1(synth.key_count(synth.WORKLOADS["tiny"]))
+    before = st.snapshot([0], list(range(w.H)))
+    act = torch.empty(w.B, R, dtype=torch.int32, device="cuda")
+    keys = torch.empty(w.B, w.H, K, dtype=torch.int32, device="cuda")
+    fl.flashloop_loop_step(cache, 2, x2["Q"], x2["K"], x2["V"], st.q_hat, st.o, st.z, st.c, ws, h_prev=x1["H"],
+                           h_cur=x2["H"], active_idx=act, key_idx=keys, key_rank=fl.flashloop.KEYS_BY_MASS_PER_ROW)
+    torch.cuda.synchronize()
+    assert fl.flashloop_device_status() == 0
+    S = keys.cpu().numpy()
+    assert np.array_equal(S, oracle.topk(oracle.key_scores_per_row(before[3], w.N), K))
+    assert not np.array_equal(S, oracle.topk(before[3].astype(np.float64), K))   # a different ranking here
+    A = act.cpu().numpy()
+    base_k, base_v = bits(x1["K"]), bits(x1["V"])
+    lk, lv = layers_from_gpu(cache, [2], [0])
+    kn = oracle.reconstruct(base_k, lk, want_f32=False)[1]
+    vn = oracle.reconstruct(base_v, lv, want_f32=False)[1]
+    qh, o, z, c, _ = oracle.attention(False, A, A, bits(x2["Q"]), *before, S, base_k, base_v, kn, vn)
+    after = st.snapshot([0], list(range(w.H)))
+    assert_close(after[1], o, O_ATOL, O_RTOL, "O")
+    assert_close(after[2], z, Z_ATOL, 0, "Z")
+    assert_close(after[3], c, C_ATOL, C_RTOL, "c")
+
+
+def gpu_column_recovery(w, dm, cache, st, x_prev, x_cur, R, ks, key_rank=0):
+    """Lazy loop 2 from the state in `st`: token selection and delta append as
+    the loop step does them, then, from that same starting state, attention
+    over the top-k key columns for each k in ks and over every key. Returns
+    ({k: recovery of the active rows}, active rows, starting state, outputs)."""
+    act = fl.flashloop_select_tokens(x_prev["H"], x_cur["H"], R, scores=torch.empty(w.B, w.N, device="cuda"))
+    fl.flashloop_kv_delta_append(cache, 2, x_cur["K"], x_cur["V"], act)
+    start = tuple(t.clone() for t in (st.q_hat, st.o, st.z, st.c))
+    ws = fl.workspace_for(dm)
+    outs = {}
+    for k in list(ks) + [w.N]:
+        q_hat, o, z, c = (t.clone() for t in start)
+        if k == w.N:
+            S = torch.arange(w.N, dtype=torch.int32, device="cuda").expand(w.B, w.H, w.N).contiguous()
+        elif key_rank:
+            S = fl.flashloop_select_keys_per_row(start[3], k)
+        else:
+            S = fl.flashloop_select_keys(start[3], k)
+        fl.flashloop_lazy_attention(cache, fl.LAZY, 2, x_cur["Q"], q_hat, o, z, c, row_pos=act, key_idx=S,
+                                    workspace=ws)
+        torch.cuda.synchronize()
+        outs[k] = (o, S)
+    A = act.cpu().numpy()
+    rows = lambda t: f32(t)[0][A[0]]
+    full = rows(outs[w.N][0])
+    prev = rows(start[1])
+    rec = {k: oracle.column_recovery(rows(outs[k][0]), full, prev) for k in outs}
+    return rec, A, start, outs
+
+
+def test_column_recovery_matches_the_oracle():
+    """Recovery of the exact loop-2 result over the active rows of the tiny
+    workload, for key subsets of 5%, 10% and 50%: the CUDA path's figures match
+    the oracle's on the same sets (teacher forcing), and every key recovers all."""
+    w, R, K, dm, cache, ws, st, x1, x2 = _tiny_after_loop1(synth.WORKLOADS["tiny"].N)
+    ks = [52, 103, 512]
+    rec, A, start, outs = gpu_column_recovery(w, dm, cache, st, x1, x2, R, ks)
+    assert rec[w.N]["recovered"] == 1.0 and rec[w.N]["rel_err"] == 0.0
+    base_k, base_v = bits(x1["K"]), bits(x1["V"])
+    lk, lv = layers_from_gpu(cache, [2], [0])
+    kn = oracle.reconstruct(base_k, lk, want_f32=False)[1]
+    vn = oracle.reconstruct(base_v, lv, want_f32=False)[1]
+    sb = (bits(start[0]), f32(start[1]), f32(start[2]), f32(start[3]))
+    o_of = lambda S: oracle.attention(False, A, A, bits(x2["Q"]), *sb, S, base_k, base_v, kn, vn)[1][0][A[0]]
+    full = o_of(np.tile(np.arange(w.N, dtype=np.int32), (1, w.H, 1)))
+    prev = sb[1][0][A[0]]
+    for k in ks:
+        S = outs[k][1].cpu().numpy()
+        assert np.array_equal(S, oracle.topk(sb[3].astype(np.float64), k))
+        ref = oracle.column_recovery(o_of(S), full, prev)
+        assert abs(rec[k]["recovered"] - ref["recovered"]) < 1e-2, (k, rec[k], ref)
+        assert abs(rec[k]["rel_err"] - ref["rel_err"]) < 1e-2, (k, rec[k], ref)
+    assert rec[512]["recovered"] > rec[52]["recovered"]

@@ -455,3 +455,62 @@ def test_chain_preserves_mass_and_bounds_m(orc):
             st = st2
         np.testing.assert_allclose(st.c.sum(-1), w.N, rtol=1e-6)
         prev = x["H"]
+
+
+# ---------------------------------------------------------------------------
+# key ranking by column mass per causal row, and the column-recovery measure
+
+def test_key_scores_per_row_hand_worked(orc):
+    """c = [8, 3, 4, 3] over N = 4 rows: rows 4, 3, 2, 1 see keys 0..3, so the
+    scores are [2, 1, 2, 3]; the top two are key 3 and, of the tie at 2, key 0."""
+    s = orc.key_scores_per_row(np.array([[8.0, 3.0, 4.0, 3.0]], np.float32), 4)
+    assert s.tolist() == [[2.0, 1.0, 2.0, 3.0]]
+    assert orc.topk(s, 2).tolist() == [[0, 3]]
+    # more rows than columns (a prefix of a longer prefill): rows 6..3 see keys 0..3
+    s = orc.key_scores_per_row(np.array([6.0, 5.0, 4.0, 3.0], np.float32), 6)
+    assert s.tolist() == [1.0, 1.0, 1.0, 1.0]
+
+
+def test_key_scores_per_row_is_the_fp32_quotient(orc):
+    """The quotient is rounded once to fp32 (as a kernel's IEEE fp32 division
+    would), checked against exact rational arithmetic on random values."""
+    from fractions import Fraction
+    rng = np.random.default_rng(5)
+    c = (rng.random(300) * 50).astype(np.float32)
+    s = orc.key_scores_per_row(c, 1000)
+    for j in range(0, 300, 7):
+        exact = Fraction(float(c[j])) / (1000 - j)
+        # s[j] is the fp32 nearest to the exact quotient: no fp32 lies strictly closer
+        up, dn = np.nextafter(np.float32(s[j]), np.float32(np.inf)), np.nextafter(np.float32(s[j]), np.float32(-np.inf))
+        err = abs(Fraction(float(s[j])) - exact)
+        assert err <= abs(Fraction(float(up)) - exact) and err <= abs(Fraction(float(dn)) - exact)
+
+
+def test_column_recovery_closed_forms(orc):
+    prev = np.zeros((3, 4))
+    full = np.ones((3, 4))
+    assert orc.column_recovery(full, full, prev)["recovered"] == 1.0          # exact result
+    assert orc.column_recovery(prev, full, prev)["recovered"] == 0.0          # no update at all
+    half = orc.column_recovery(0.5 * full, full, prev)
+    assert half["recovered"] == 0.5 and half["rel_err"] == 0.5
+
+
+def test_full_key_set_recovers_everything(orc):
+    """The lazy step over every key of a (tiny) loop is the exact result: its
+    recovery is 1 by the mass-preserving identity, whatever the previous state."""
+    rng = np.random.default_rng(9)
+    B, N, H, d = 1, 40, 1, 64
+    bf = lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    q1, k1, v1, q2, k2, v2 = (bf(rng.standard_normal((B, N, H, d))) for _ in range(6))
+    rows = np.arange(N, dtype=np.int32)[None]
+    S_all = np.arange(N, dtype=np.int32)[None, None]
+    zero = (np.zeros((B, N, H, d), np.uint16), np.zeros((B, N, H, d), np.float32),
+            np.zeros((B, H, N), np.float32), np.zeros((B, H, N), np.float32))
+    st = orc.attention(True, rows, rows, q1, *zero, S_all, None, None, k1, v1)[:4]
+    A = np.array([[3, 10, 22, 39]], np.int32)
+    full = orc.attention(False, A, A, q2, *st, S_all, k1, v1, k2, v2)[1]
+    some = orc.attention(False, A, A, q2, *st, np.array([[[0, 5, 10, 22]]], np.int32), k1, v1, k2, v2)[1]
+    rec_full = orc.column_recovery(full[:, A[0]], full[:, A[0]], st[1][:, A[0]])
+    assert rec_full["recovered"] == 1.0
+    rec = orc.column_recovery(some[:, A[0]], full[:, A[0]], st[1][:, A[0]])
+    assert rec["recovered"] < 1.0 and rec["rel_err"] > 0
