@@ -180,6 +180,16 @@ typedef struct {
     void *workspace;
     size_t workspace_bytes;
     int32_t key_rank;         /* flashloop_key_rank_t of the key selection (prefill lazy loops) */
+    /* Early exit of a sequence by state difference (prefill lazy loops; NULL
+     * seq_exit = off). seq_exit [B] int32 device flags, caller-owned, zero at
+     * the start: a sequence flagged 1 has stopped looping, and every later lazy
+     * loop leaves it unchanged (its delta entries are zero deltas, its rows
+     * keep O, Z and qhat, its column masses stay). With exit_threshold > 0 the
+     * loop first sets the flag of every sequence whose largest token change
+     * score (squared L2 norm of h_cur - h_prev, the one the token selection
+     * ranks by) is below it, in fp32; flags are never cleared by the library. */
+    float exit_threshold;
+    int32_t *seq_exit;
 } flashloop_step_args_t;
 
 /* ---- sizes and set-up ------------------------------------------------- */

@@ -363,7 +363,8 @@ namespace fl {
 // on the stream, so that the append kernel directly follows the token selection.
 static flashloop_status_t delta_append_impl(flashloop_kv_cache_t *cache, int32_t loop, const uint16_t *k_l,
                                             const uint16_t *v_l, int32_t rows_are_tokens, const int32_t *active_idx,
-                                            int32_t R, int32_t at, bool slots_cleared, flashloop_stream_t stream) {
+                                            int32_t R, int32_t at, bool slots_cleared, flashloop_stream_t stream,
+                                            const int32_t *seq_exit = nullptr) {
     flashloop_status_t st = check_cache(cache);
     if (st != FLASHLOOP_OK) return st;
     const flashloop_dims_t &dm = cache->dims;
@@ -388,7 +389,7 @@ static flashloop_status_t delta_append_impl(flashloop_kv_cache_t *cache, int32_t
     const int src_rows = rows_are_tokens ? cache->n_tokens : R;
     cudaError_t e = launch_delta_append(view, k_l, v_l, rows_are_tokens, src_rows, active_idx, R, at, dm.B, dm.N_cap,
                                         dm.H, dm.d, dm.R_cap, cache->idx[m], cache->slot[m], cache->k_codes[m],
-                                        cache->k_scales[m], cache->v_codes[m], cache->v_scales[m], stream);
+                                        cache->k_scales[m], cache->v_codes[m], cache->v_scales[m], stream, seq_exit);
     if (e != cudaSuccess) return cuda_fail(e, "kv_delta_append");
     cache->count[m] = at + R;
     return FLASHLOOP_OK;
@@ -471,7 +472,19 @@ flashloop_status_t flashloop_reconstruct_keys(const flashloop_kv_cache_t *cache,
     return FLASHLOOP_OK;
 }
 
+namespace fl {
+// seq_exit: [B] flags or NULL; the tensor-core path leaves sequences flagged 1 unchanged.
+static flashloop_status_t lazy_attention_impl(const flashloop_attn_args_t *a, flashloop_stream_t stream,
+                                              const int32_t *seq_exit);
+}  // namespace fl
+
 flashloop_status_t flashloop_lazy_attention(const flashloop_attn_args_t *a, flashloop_stream_t stream) {
+    return fl::lazy_attention_impl(a, stream, nullptr);
+}
+
+namespace fl {
+static flashloop_status_t lazy_attention_impl(const flashloop_attn_args_t *a, flashloop_stream_t stream,
+                                              const int32_t *seq_exit) {
     if (!a) return set_error(FLASHLOOP_ERR_INVALID_ARG, "args is NULL");
     flashloop_status_t st = check_cache(a->cache);
     if (st != FLASHLOOP_OK) return st;
@@ -566,10 +579,12 @@ flashloop_status_t flashloop_lazy_attention(const flashloop_attn_args_t *a, flas
         }
         p.kv_rows = dm.N_cap;
     }
+    p.seq_exit = seq_exit;
     e = launch_tc_attention(p, stream);
     if (e != cudaSuccess) return cuda_fail(e, "tc_attention");
     return FLASHLOOP_OK;
 }
+}  // namespace fl
 
 flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop_stream_t stream) {
     if (!a) return set_error(FLASHLOOP_ERR_INVALID_ARG, "args is NULL");
@@ -663,9 +678,22 @@ flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop
         st = fl::select_keys_impl(a->c, dm.B, dm.H, n, dm.K, a->key_rank == FLASHLOOP_KEYS_BY_MASS_PER_ROW ? n : 0,
                                   a->key_idx, key_stream);
     if (st == FLASHLOOP_OK)
-        st = flashloop_select_tokens(a->h_prev, a->h_cur, dm.B, n, dm.H * dm.d, dm.R, a->active_idx, scores,
-                                     nullptr, 0, stream);
-    if (st == FLASHLOOP_OK) st = delta_append_impl(c, l, a->k, a->v, 1, a->active_idx, dm.R, 0, true, stream);
+        {
+        // token selection; with exit flags, the top-k also flags sequences whose
+        // largest change score is below the threshold (sticky)
+        const bool upd = a->seq_exit && a->exit_threshold > 0.f;
+        if (st == FLASHLOOP_OK && (!aligned16(a->h_prev) || !aligned16(a->h_cur) || (dm.H * dm.d) % 8))
+            st = set_error(FLASHLOOP_ERR_INVALID_ARG, "hidden states must be 16-byte aligned rows");
+        if (st == FLASHLOOP_OK) {
+            cudaError_t e = launch_token_scores(a->h_prev, a->h_cur, dm.B, n, dm.H * dm.d, scores, stream);
+            if (e == cudaSuccess)
+                e = launch_topk_rows(scores, dm.B, n, dm.R, a->active_idx, stream, "topk_tokens", 0,
+                                     upd ? a->exit_threshold : 0.f, upd ? a->seq_exit : nullptr);
+            if (e != cudaSuccess) st = cuda_fail(e, "token selection");
+        }
+    }
+    if (st == FLASHLOOP_OK)
+        st = delta_append_impl(c, l, a->k, a->v, 1, a->active_idx, dm.R, 0, true, stream, a->seq_exit);
     if (ss) {   // join (also on failure, so that the caller's stream is never left forked)
         cudaError_t e = cudaEventRecord(ss->join, ss->s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), ss->join, 0);
@@ -677,7 +705,7 @@ flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop
     at.row_pos = a->active_idx;
     at.K = dm.K;
     at.key_idx = a->key_idx;
-    return flashloop_lazy_attention(&at, stream);
+    return fl::lazy_attention_impl(&at, stream, a->seq_exit);
 }
 
 flashloop_status_t flashloop_set_wait_limit_ns(uint64_t ns) {

@@ -144,6 +144,7 @@ struct KParams {
     uint16_t *q_hat;
     float *o, *z, *c;
     float sl2;   // log2(e) / sqrt(d)
+    const int32_t *seq_exit;   // [B] or NULL: a sequence flagged 1 has stopped looping
 };
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -298,6 +299,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     pdl_wait();   // every global read below depends on the previous kernel
     pdl_trigger();
     const unsigned long long wlimit = g_tc_wait_limit_ns;
+    if (p.seq_exit && __ldg(p.seq_exit + blockIdx.z)) return;   // the whole CTA: its sequence stopped looping
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -863,6 +865,7 @@ cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
     kp.z = p.z;
     kp.c = p.c;
     kp.sl2 = kLog2e / sqrtf((float)D);
+    kp.seq_exit = p.seq_exit;
     dim3 grid(kp.n_row_tiles * p.H, 1, p.B);
     if (!dense && !p.row_cnt) return cudaErrorInvalidValue;
     {

@@ -62,8 +62,9 @@ cudaError_t launch_token_scores(const uint16_t *h_prev, const uint16_t *h_cur, i
                                 float *scores, cudaStream_t s);
 // `name` labels the launch in the per-kernel timing ("topk_tokens", "topk_keys").
 // norm_n > 0 ranks column i by vals[i] / (norm_n - i) (requires n <= norm_n).
+// seq_exit != NULL sets seq_exit[row] = 1 when the row's largest value is below exit_thr.
 cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t *out, cudaStream_t s,
-                             const char *name, int norm_n = 0);
+                             const char *name, int norm_n = 0, float exit_thr = 0.f, int32_t *seq_exit = nullptr);
 // kvcache.cu
 cudaError_t launch_gather_rows(const void *src, int B, int N, int row_bytes, const int32_t *idx, int R,
                                void *dst, cudaStream_t s);
@@ -73,7 +74,7 @@ cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, cons
                                 int rows_are_tokens, int src_rows, const int32_t *active, int R, int at,
                                 int B, int N_cap, int H, int d, int R_cap, int32_t *out_idx,
                                 int32_t *out_slot, uint8_t *k_codes, uint16_t *k_scales, uint8_t *v_codes,
-                                uint16_t *v_scales, cudaStream_t s);
+                                uint16_t *v_scales, cudaStream_t s, const int32_t *seq_exit = nullptr);
 // Reconstruction of the selected keys at the old and the new loop into
 // [B, H, K, d]; with row_cnt set, the same launch also counts the keys each of
 // the R rows at row_pos sees, into row_cnt [B, H, R].
@@ -99,6 +100,7 @@ struct TcAttnParams {
     // key/value sources: lazy = dense [B,H,K,d] buffers; dense = cache layers [B,N_cap,H,d]
     const uint16_t *k_old, *v_old, *k_new, *v_new;
     int kv_rows;         // rows of the source arrays per (b[,h]) (K or N_cap)
+    const int32_t *seq_exit;  // [B] or NULL: sequences flagged 1 are left unchanged
 };
 cudaError_t launch_tc_attention(const TcAttnParams &p, cudaStream_t s);
 int32_t tc_attention_read_error(bool clear);

@@ -62,7 +62,7 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
                     int H, int d, int N_cap, int R_cap, long long total, int32_t *__restrict__ out_idx,
                     int32_t *__restrict__ out_slot, uint8_t *__restrict__ k_codes,
                     uint16_t *__restrict__ k_scales, uint8_t *__restrict__ v_codes,
-                    uint16_t *__restrict__ v_scales) {
+                    uint16_t *__restrict__ v_scales, const int32_t *__restrict__ seq_exit) {
     pdl_wait();
     pdl_trigger();
     // 32-bit index arithmetic (the launcher checks that total fits): 64-bit
@@ -114,6 +114,8 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
         x[u] = __fsub_rn(x[u], rec[u]);   // the delta
         amax = fmaxf(amax, fabsf(x[u]));
     }
+    // a sequence that has stopped looping keeps its K/V: its entries are zero deltas
+    if (seq_exit && __ldg(seq_exit + b)) amax = 0.f;
     const __half sh = __float2half_rn(__fdiv_rn(amax, 7.0f));   // the scale is exact: fp16(fp32(amax / 7))
     const float s = __half2float(sh);
     // code = rint(delta / scale): the quotient is taken as delta * (1 / scale), within
@@ -289,7 +291,7 @@ cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, cons
                                 int rows_are_tokens, int src_rows, const int32_t *active, int R, int at,
                                 int B, int N_cap, int H, int d, int R_cap, int32_t *out_idx,
                                 int32_t *out_slot, uint8_t *k_codes, uint16_t *k_scales, uint8_t *v_codes,
-                                uint16_t *v_scales, cudaStream_t s) {
+                                uint16_t *v_scales, cudaStream_t s, const int32_t *seq_exit) {
     const long long total = (long long)B * R * H * (d / 32);
     if (total == 0) return cudaSuccess;
     if (total > 0x7fffffffLL - 256) return cudaErrorInvalidValue;   // the kernel indexes in 32 bits
@@ -298,7 +300,7 @@ cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, cons
         KernelTimer kt("delta_append", s);
         const cudaError_t e = launch_pdl(delta_append_kernel, grid, dim3(256), 0, s, view, k_l, v_l,
                                          rows_are_tokens, src_rows, active, R, at, H, d, N_cap, R_cap, total,
-                                         out_idx, out_slot, k_codes, k_scales, v_codes, v_scales);
+                                         out_idx, out_slot, k_codes, k_scales, v_codes, v_scales, seq_exit);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

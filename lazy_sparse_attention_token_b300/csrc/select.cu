@@ -105,6 +105,13 @@ __device__ __forceinline__ uint32_t cl_ld(uint32_t addr) {
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
+__device__ __forceinline__ void cl_red_max(uint32_t addr, uint32_t v) {
+    asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Inverse of f32_order_key (for keys of finite values; -0 comes back as +0).
+__device__ __forceinline__ float order_key_f32(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
 __device__ __forceinline__ void cl_st(uint32_t addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -115,9 +122,13 @@ __device__ __forceinline__ void cl_sync() {
 
 // norm_n > 0 ranks column i of a row by vals[i] / (norm_n - i) (IEEE fp32
 // division) instead of vals[i]: a key's column mass per causal row that sees it.
+// seq_exit != NULL: the row's largest value (a sequence's largest token change
+// score) is found on the way, and if it is below exit_thr the row's flag is set
+// to 1 (flags are only ever set here, never cleared).
 template <bool kStaged>
 __global__ void __launch_bounds__(kTopkClThreads)
-topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__restrict__ out, int norm_n) {
+topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__restrict__ out, int norm_n,
+                    float exit_thr, int32_t *__restrict__ seq_exit) {
     extern __shared__ uint32_t staged[];
     __shared__ uint32_t whist[kTopkClWarps][256];   // one histogram per warp: keys of similar
                                                     // magnitude share a digit, so a single
@@ -127,6 +138,7 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
     __shared__ uint32_t s_prefix;
     __shared__ int s_kleft;
     __shared__ unsigned long long warp_tot[kTopkClWarps];
+    __shared__ uint32_t s_cta_max, s_row_max;   // largest key of this CTA's segment / of the row (rank 0)
 
     pdl_wait();
     pdl_trigger();
@@ -141,6 +153,10 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
 
     if (rank == 0)
         for (int i = tid; i < 4 * 256; i += kTopkClThreads) (&g_hist[0][0])[i] = 0u;
+    if (tid == 0) {
+        s_cta_max = 0u;
+        s_row_max = 0u;
+    }
     auto value_at = [&](int i) -> float {
         const float v = __ldg(row + lo + i);
         return norm_n > 0 ? __fdiv_rn(v, (float)(norm_n - (lo + i))) : v;
@@ -156,9 +172,15 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
         const int shift = 24 - 8 * pass;
         for (int i = tid; i < kTopkClWarps * 256; i += kTopkClThreads) (&whist[0][0])[i] = 0u;
         __syncthreads();
+        uint32_t kmax = 0u;
         for (int i = tid; i < len; i += kTopkClThreads) {
             const uint32_t key = key_at(i);
             if ((key & mask) == prefix) atomicAdd(&whist[warp][(key >> shift) & 255u], 1u);
+            kmax = max(kmax, key);
+        }
+        if (pass == 0 && seq_exit) {
+            kmax = __reduce_max_sync(0xffffffffu, kmax);
+            if (lane == 0) atomicMax(&s_cta_max, kmax);
         }
         __syncthreads();
         if (tid < 256) {
@@ -167,7 +189,10 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
             for (int w = 0; w < kTopkClWarps; ++w) tot += whist[w][tid];
             if (tot != 0u) cl_red_add(cl_map(&g_hist[pass][tid], 0), tot);
         }
+        if (pass == 0 && seq_exit && tid == 0 && len > 0) cl_red_max(cl_map(&s_row_max, 0), s_cta_max);
         cl_sync();
+        if (pass == 0 && seq_exit && rank == 0 && tid == 0 && order_key_f32(s_row_max) < exit_thr)
+            seq_exit[row_id] = 1;
         if (warp == 0) {
             uint32_t c[8], local = 0;
 #pragma unroll
@@ -269,7 +294,7 @@ cudaError_t launch_token_scores(const uint16_t *h_prev, const uint16_t *h_cur, i
 }
 
 cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t *out, cudaStream_t s,
-                             const char *name, int norm_n) {
+                             const char *name, int norm_n, float exit_thr, int32_t *seq_exit) {
     if (rows == 0) return cudaSuccess;
     const int ncta = rows >= kTopkRowsForSingle ? 1 : kTopkCluster;
     const int seg = ((n + ncta - 1) / ncta + 31) & ~31;
@@ -298,8 +323,8 @@ cudaError_t launch_topk_rows(const float *vals, int rows, int n, int k, int32_t 
     cudaError_t e;
     {
         KernelTimer kt(name, s);
-        e = staged ? cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, vals, n, k, out, norm_n)
-                   : cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, vals, n, k, out, norm_n);
+        e = staged ? cudaLaunchKernelEx(&cfg, topk_cluster_kernel<true>, vals, n, k, out, norm_n, exit_thr, seq_exit)
+                   : cudaLaunchKernelEx(&cfg, topk_cluster_kernel<false>, vals, n, k, out, norm_n, exit_thr, seq_exit);
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -54,7 +54,7 @@ class StepArgs(ctypes.Structure):
     _fields_ = [("loop", I32), ("decode", I32), ("h_prev", P), ("h_cur", P), ("q", P), ("k", P), ("v", P),
                 ("q_hat", P), ("o", P), ("z", P), ("c", P), ("cache", ctypes.POINTER(KVCache)),
                 ("active_idx", P), ("key_idx", P), ("scores", P), ("workspace", P), ("workspace_bytes", SZ),
-                ("key_rank", I32)]
+                ("key_rank", I32), ("exit_threshold", ctypes.c_float), ("seq_exit", P)]
 
 
 _lib = None
@@ -296,10 +296,11 @@ def flashloop_lazy_attention(cache: Cache, mode: int, loop: int, q, q_hat, o, z,
 
 def flashloop_loop_step(cache: Cache, loop: int, q, k, v, q_hat, o, z, c, workspace, h_prev=None, h_cur=None,
                         active_idx=None, key_idx=None, scores=None, decode: bool = False, key_rank: int = 0,
-                        stream=None):
+                        exit_threshold: float = 0.0, seq_exit=None, stream=None):
     a = StepArgs()
     a.loop, a.decode = loop, int(decode)
     a.key_rank = key_rank
+    a.exit_threshold, a.seq_exit = float(exit_threshold), _ptr(seq_exit)
     a.h_prev, a.h_cur = _ptr(h_prev), _ptr(h_cur)
     a.q, a.k, a.v = _ptr(q), _ptr(k), _ptr(v)
     a.q_hat, a.o, a.z, a.c = _ptr(q_hat), _ptr(o), _ptr(z), _ptr(c)

@@ -66,15 +66,35 @@ def dense_loop(loop: int, q, k, v, cache: Cache, state: State, bh_mask=None) -> 
     return State(qh, o, z, c)
 
 
-def lazy_loop(loop: int, h_prev, h_cur, q, k, v, cache: Cache, state: State, R: int, K: int,
-              A: Optional[np.ndarray] = None, S: Optional[np.ndarray] = None, bh_mask=None):
-    """A lazy loop. ``A``/``S`` override the selections (teacher forcing).
+def exit_flags(scores: np.ndarray, threshold: float, exited: Optional[np.ndarray] = None) -> np.ndarray:
+    """Early exit by state difference (the recurrent-depth overview page's
+    dynamic early exit: a sequence stops looping once its state stops
+    changing): a sequence is flagged once its largest token change score
+    falls below ``threshold``, and stays flagged. The comparison is made in
+    fp32, on the fp32 rounding of the largest score."""
+    B = scores.shape[0]
+    ex = np.zeros(B, bool) if exited is None else np.asarray(exited, bool).copy()
+    if threshold > 0:
+        ex |= np.float32(scores.max(axis=-1)) < np.float32(threshold)
+    return ex
 
-    Returns (A, S, scores, new_state, new_k_layer, new_v_layer).
+
+def lazy_loop(loop: int, h_prev, h_cur, q, k, v, cache: Cache, state: State, R: int, K: int,
+              A: Optional[np.ndarray] = None, S: Optional[np.ndarray] = None, bh_mask=None,
+              exit_threshold: float = 0.0, exited: Optional[np.ndarray] = None):
+    """A lazy loop. ``A``/``S`` override the selections (teacher forcing).
+    With ``exited`` (per-sequence flags) or ``exit_threshold`` > 0, a flagged
+    sequence stops looping: its delta entries hold zero deltas (scale 0,
+    codes 0) and its rows keep their state; the flags come back as the last
+    element of the result.
+
+    Returns (A, S, scores, new_state, new_k_layer, new_v_layer[, flags]).
     """
     q, k, v = bits(q), bits(k), bits(v)
     B, N, H, d = q.shape
     scores = token_scores(h_prev, h_cur)
+    use_exit = exited is not None or exit_threshold > 0
+    flags = exit_flags(scores, exit_threshold, exited) if use_exit else np.zeros(B, bool)
     if A is None:
         A = topk(scores, R)
     if S is None:
@@ -82,6 +102,9 @@ def lazy_loop(loop: int, h_prev, h_cur, q, k, v, cache: Cache, state: State, R: 
     td = len(cache.dense_k)
     lk = kv_delta_append(k, cache.dense_k[-1], cache.delta_k[: loop - 1 - td], A)
     lv = kv_delta_append(v, cache.dense_v[-1], cache.delta_v[: loop - 1 - td], A)
+    for lay in (lk, lv):          # a sequence that stopped looping keeps its K/V
+        lay.codes[flags] = 0
+        lay.scales[flags] = 0
     k_old, v_old = cache.rec(loop - 1, "k"), cache.rec(loop - 1, "v")
     del cache.delta_k[loop - 1 - td:], cache.delta_v[loop - 1 - td:]
     cache.delta_k.append(lk)
@@ -89,4 +112,8 @@ def lazy_loop(loop: int, h_prev, h_cur, q, k, v, cache: Cache, state: State, R: 
     k_new, v_new = cache.rec(loop, "k"), cache.rec(loop, "v")
     qh, o, z, c, _ = attention(False, A, A, q, state.qhat, state.o, state.z, state.c, S,
                                k_old, v_old, k_new, v_new, bh_mask=bh_mask)
+    # rows of a sequence that stopped looping keep their state
+    qh[flags], o[flags], z[flags], c[flags] = state.qhat[flags], state.o[flags], state.z[flags], state.c[flags]
+    if use_exit:
+        return A, S, scores, State(qh, o, z, c), lk, lv, flags
     return A, S, scores, State(qh, o, z, c), lk, lv

@@ -514,3 +514,59 @@ def test_full_key_set_recovers_everything(orc):
     assert rec_full["recovered"] == 1.0
     rec = orc.column_recovery(some[:, A[0]], full[:, A[0]], st[1][:, A[0]])
     assert rec["recovered"] < 1.0 and rec["rel_err"] > 0
+
+
+# ---------------------------------------------------------------------------
+# early exit by state difference
+
+def _exit_case(orc, B=3, N=64, H=2, d=64, seed=21):
+    from oracle import loop as oloop
+    rng = np.random.default_rng(seed)
+    bf = lambda a: (np.asarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    h1 = rng.standard_normal((B, N, H * d))
+    h2 = h1 + rng.standard_normal((B, N, H * d)) * np.array([0.5, 0.0, 0.01])[:, None, None]   # seq 1 frozen
+    q1, k1, v1, q2, k2, v2 = (bf(rng.standard_normal((B, N, H, d))) for _ in range(6))
+    cache = oloop.Cache()
+    st = oloop.dense_loop(1, q1, k1, v1, cache, oloop.empty_state(B, N, H, d))
+    return oloop, bf(h1), bf(h2), (q2, k2, v2), cache, st
+
+
+def test_exit_threshold_zero_changes_nothing(orc):
+    oloop, h1, h2, (q2, k2, v2), cache, st = _exit_case(orc)
+    import copy
+    plain = oloop.lazy_loop(2, h1, h2, q2, k2, v2, copy.deepcopy(cache), st, 16, 8)
+    ex = oloop.lazy_loop(2, h1, h2, q2, k2, v2, copy.deepcopy(cache), st, 16, 8, exit_threshold=0.0,
+                         exited=np.zeros(3, bool))
+    assert not ex[6].any()
+    for a, b in zip(plain[3].__dict__.values(), ex[3].__dict__.values()):
+        assert np.array_equal(a, b)
+    assert np.array_equal(plain[4].codes, ex[4].codes) and np.array_equal(plain[4].scales, ex[4].scales)
+
+
+def test_frozen_sequence_exits_and_keeps_its_state(orc):
+    """Sequence 1 did not change between the loops (every score 0), so any
+    positive threshold stops it: its rows keep O, Z, qhat and c bit for bit and
+    its delta entries are zero; the other sequences loop as usual."""
+    oloop, h1, h2, (q2, k2, v2), cache, st = _exit_case(orc)
+    import copy
+    plain = oloop.lazy_loop(2, h1, h2, q2, k2, v2, copy.deepcopy(cache), st, 16, 8)
+    A, S, scores, new, lk, lv, flags = oloop.lazy_loop(2, h1, h2, q2, k2, v2, copy.deepcopy(cache), st, 16, 8,
+                                                       exit_threshold=1e-6)
+    assert flags.tolist() == [False, True, False]
+    assert scores[1].max() == 0.0
+    for name in ("qhat", "o", "z", "c"):
+        assert np.array_equal(getattr(new, name)[1], getattr(st, name)[1])        # exited: unchanged
+        assert np.array_equal(getattr(new, name)[[0, 2]], getattr(plain[3], name)[[0, 2]])   # others: as usual
+    assert not lk.codes[1].any() and not lk.scales[1].any() and not lv.scales[1].any()
+    assert lk.scales[0].any()
+
+
+def test_exit_is_strict_and_sticky(orc):
+    from oracle import loop as oloop
+    scores = np.array([[0.5, 2.0], [1.0, 0.25], [3.0, 3.0]])
+    # largest scores 2.0, 1.0, 3.0: a threshold equal to a maximum does not stop it
+    assert oloop.exit_flags(scores, 1.0).tolist() == [False, False, False]
+    assert oloop.exit_flags(scores, 1.0 + 1e-6).tolist() == [False, True, False]
+    # a flag once set stays set, whatever the scores
+    assert oloop.exit_flags(scores, 0.5, np.array([True, False, False])).tolist() == [True, False, False]
+    assert oloop.exit_flags(scores, float("inf")).tolist() == [True, True, True]
