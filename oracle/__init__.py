@@ -54,9 +54,10 @@ def lib():
         _lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
         _lib.orc_token_scores.argtypes = [P, P, I64, I64, I64, P]
         _lib.orc_topk_rows.argtypes = [P, I64, I64, I64, P]
-        _lib.orc_kv_delta_append.argtypes = [P, P, ctypes.c_int, P, P, P, P,
+        _lib.orc_kv_delta_append.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, P, P, P, P,
                                              I64, I64, I64, I64, P, I64, P, P, P]
-        _lib.orc_reconstruct.argtypes = [P, ctypes.c_int, P, P, P, P, I64, I64, I64, I64, P, P]
+        _lib.orc_reconstruct.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, P, P, P, P, I64, I64, I64, I64, P, P]
+        _lib.orc_quantize_base.argtypes = [P, I64, I64, I64, I64, P, P]
         _lib.orc_attention.argtypes = [ctypes.c_int, I64, I64, I64, I64, I64, I64, P, P,
                                        P, P, P, P, P, I64, P, P, P, P, P, P, P]
         _lib.orc_softmax_attention.argtypes = [P, P, P, I64, I64, I64, I64, P, P]
@@ -135,7 +136,7 @@ def topk(score: np.ndarray, k: int) -> np.ndarray:
 
 
 class DeltaLayer:
-    """One delta layer: idx [B,cnt] i32, codes [B,cnt,H,d/2] u8, scales [B,cnt,H,d/32] u16 (fp16 bits)."""
+    """One delta layer: idx [B,cnt] i32, codes [B,cnt,H,d*bits/8] u8, scales [B,cnt,H,d/32] u16 (fp16 bits)."""
 
     def __init__(self, idx, codes, scales):
         self.idx = _c(np.asarray(idx), np.int32)
@@ -149,6 +150,34 @@ class DeltaLayer:
                           np.concatenate([self.scales, other.scales], 1))
 
 
+class CompressedBase:
+    """An int8 base (the page's compressed base; reading R8 of the C file):
+    codes [B,Nk,H,d] int8 and fp16 scales [B,Nk,H,d/32] (uint16 bits)."""
+
+    def __init__(self, codes, scales):
+        self.codes = _c(np.asarray(codes), np.int8)
+        self.scales = _c(np.asarray(scales), np.uint16)
+        self.shape = self.codes.shape
+
+
+def quantize_base(x) -> CompressedBase:
+    """The int8 compressed base of a bf16 layer x [B,Nk,H,d]."""
+    xb = _c(bits(x), np.uint16)
+    B, Nk, H, d = xb.shape
+    codes = np.empty((B, Nk, H, d), np.int8)
+    scales = np.empty((B, Nk, H, d // 32), np.uint16)
+    lib().orc_quantize_base(_ptr(xb), B, Nk, H, d, _ptr(codes), _ptr(scales))
+    return CompressedBase(codes, scales)
+
+
+def _base_args(base):
+    """(bf16 base, base codes, base scales) pointers and the base's shape."""
+    if isinstance(base, CompressedBase):
+        return None, base, (None, _ptr(base.codes), _ptr(base.scales)), base.shape
+    bs = _c(bits(base), np.uint16)
+    return bs, None, (_ptr(bs), None, None), bs.shape
+
+
 def _layer_arrays(layers: Sequence[DeltaLayer]):
     n = len(layers)
     assert n <= 64
@@ -159,29 +188,34 @@ def _layer_arrays(layers: Sequence[DeltaLayer]):
     return n, idx, codes, scales, cnt
 
 
-def kv_delta_append(x_l, base, layers: Sequence[DeltaLayer], active) -> DeltaLayer:
-    """New delta layer for the active tokens of loop-l tensor ``x_l`` [B,Nk,H,d]."""
-    x, bs = _c(bits(x_l), np.uint16), _c(bits(base), np.uint16)
+def kv_delta_append(x_l, base, layers: Sequence[DeltaLayer], active, code_bits: int = 4) -> DeltaLayer:
+    """New delta layer (``code_bits``-bit codes) for the active tokens of loop-l
+    tensor ``x_l`` [B,Nk,H,d]; ``base`` is a bf16 layer or a CompressedBase."""
+    assert code_bits in (2, 3, 4)
+    x = _c(bits(x_l), np.uint16)
+    keep_bs, keep_cb, (pb, pc, ps), _ = _base_args(base)
     act = _c(np.asarray(active, dtype=np.int32), np.int32)
     B, Nk, H, d = x.shape
     R = act.shape[1]
     idx = np.empty((B, R), np.int32)
-    codes = np.empty((B, R, H, d // 2), np.uint8)
+    codes = np.zeros((B, R, H, d * code_bits // 8), np.uint8)
     scales = np.empty((B, R, H, d // 32), np.uint16)
     n, li, lc, ls, cnt = _layer_arrays(layers)
-    lib().orc_kv_delta_append(_ptr(x), _ptr(bs), n, li, lc, ls, cnt, B, Nk, H, d,
+    lib().orc_kv_delta_append(_ptr(x), pb, pc, ps, code_bits, n, li, lc, ls, cnt, B, Nk, H, d,
                               _ptr(act), R, _ptr(idx), _ptr(codes), _ptr(scales))
     return DeltaLayer(idx, codes, scales)
 
 
-def reconstruct(base, layers: Sequence[DeltaLayer], want_f32: bool = True, want_bf16: bool = True):
-    """(fp32 [B,Nk,H,d] or None, bf16-bits uint16 [B,Nk,H,d] or None)."""
-    bs = _c(bits(base), np.uint16)
-    B, Nk, H, d = bs.shape
-    f = np.empty(bs.shape, np.float32) if want_f32 else None
-    h = np.empty(bs.shape, np.uint16) if want_bf16 else None
+def reconstruct(base, layers: Sequence[DeltaLayer], want_f32: bool = True, want_bf16: bool = True,
+                code_bits: int = 4):
+    """(fp32 [B,Nk,H,d] or None, bf16-bits uint16 [B,Nk,H,d] or None); ``base``
+    is a bf16 layer or a CompressedBase, the layers hold ``code_bits``-bit codes."""
+    keep_bs, keep_cb, (pb, pc, ps), shape = _base_args(base)
+    B, Nk, H, d = shape
+    f = np.empty(shape, np.float32) if want_f32 else None
+    h = np.empty(shape, np.uint16) if want_bf16 else None
     n, li, lc, ls, cnt = _layer_arrays(layers)
-    lib().orc_reconstruct(_ptr(bs), n, li, lc, ls, cnt, B, Nk, H, d, _ptr(f), _ptr(h))
+    lib().orc_reconstruct(pb, pc, ps, code_bits, n, li, lc, ls, cnt, B, Nk, H, d, _ptr(f), _ptr(h))
     return f, h
 
 

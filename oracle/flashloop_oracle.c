@@ -35,6 +35,17 @@
  *       contiguous elements, scale = fp16_rne(amax / 7) (fp32 divide),
  *       code = rint_even(delta / scale) clamped to +-7, zero scale -> zero
  *       codes; element 2t in the low nibble of byte t.
+ *   R6' narrower deltas (the survey's next steps; the page says quality drops
+ *       noticeably below 4 bits): the same quantiser with codes of `bits`
+ *       bits, 2 <= bits <= 4: qmax = 2^(bits-1) - 1, scale =
+ *       fp16_rne(amax / qmax), codes clamped to [-qmax, qmax]; element x of
+ *       an (entry, head) row occupies bits [bits x, bits x + bits) of the row
+ *       read as a little-endian bit string, two's complement (for bits = 4
+ *       this is R6's nibble order).
+ *   R8  compressed base (the page: "a compressed base plus a sequence of
+ *       compressed deltas"): int8 codes with one fp16 scale per 32 elements,
+ *       scale = fp16_rne(amax / 127), code = rint_even(x / scale) clamped to
+ *       [-127, 127], zero scale -> zero codes; the base value is scale * code.
  *   R7  R = ceil(r N), K = ceil(k N), clamped to [1, N]; ties in every
  *       ranking go to the lower index; index lists ascending.
  * Build with gcc -O2 -ffp-contract=off so every fp32 expression rounds
@@ -155,7 +166,14 @@ void orc_topk_rows(const double *score, int64_t rows, int64_t n, int64_t k, int3
 /* ------------------------------------------------------------------ */
 /* KV cache as [P2-three] describes it: a base plus a sequence of deltas.
  * A delta layer holds, per sequence b, `cnt` entries with ascending token
- * indices idx[b][e], int4 codes [b][e][h][d/2] and fp16 scales [b][e][h][d/32]. */
+ * indices idx[b][e], codes [b][e][h][d * bits / 8] (R6') and fp16 scales
+ * [b][e][h][d/32]. The base is bf16 [b][j][h][d], or (R8) int8 codes
+ * [b][j][h][d] with fp16 scales [b][j][h][d/32]. */
+typedef struct {
+    const uint16_t *bf16;        /* bf16 base, or NULL */
+    const int8_t *codes;         /* R8 base codes (when bf16 is NULL) */
+    const uint16_t *scales;
+} orc_base;
 typedef struct {
     const int32_t *idx;
     const uint8_t *codes;
@@ -173,26 +191,44 @@ static int64_t orc_find(const int32_t *idx, int64_t cnt, int64_t j) {
     return -1;
 }
 
-static int orc_code(const uint8_t *codes, int64_t x) {
-    uint8_t byte = codes[x / 2];
-    int v = (x & 1) ? (byte >> 4) : (byte & 0xF);
-    return v >= 8 ? v - 16 : v;
+/* R6': code of element x of a row of `bits`-bit codes (little-endian bit string). */
+static int orc_code(const uint8_t *row, int64_t x, int bits) {
+    int v = 0;
+    for (int k = 0; k < bits; ++k) {
+        int64_t bit = x * bits + k;
+        v |= ((row[bit / 8] >> (bit % 8)) & 1) << k;
+    }
+    return v >= (1 << (bits - 1)) ? v - (1 << bits) : v;
 }
 
-/* R4: fp32 reconstruction of token j, head h: base, then each delta layer
- * in ascending order that holds an entry for j adds scale * code. */
-static void orc_recon(const uint16_t *base, int64_t Nk, int64_t H, int64_t d,
+static void orc_put_code(uint8_t *row, int64_t x, int bits, int v) {
+    for (int k = 0; k < bits; ++k) {
+        int64_t bit = x * bits + k;
+        uint8_t m = (uint8_t)(1u << (bit % 8));
+        if ((v >> k) & 1) row[bit / 8] |= m; else row[bit / 8] &= (uint8_t)~m;
+    }
+}
+
+/* R4: fp32 reconstruction of token j, head h: base (R8: scale * code), then
+ * each delta layer in ascending order that holds an entry for j adds
+ * scale * code. */
+static void orc_recon(const orc_base *base, int64_t Nk, int64_t H, int64_t d, int bits,
                       const orc_layer *L, int nl, int64_t b, int64_t j, int64_t h, float *out) {
-    const uint16_t *src = base + ((b * Nk + j) * H + h) * d;
-    for (int64_t x = 0; x < d; ++x) out[x] = orc_bf16_to_f32(src[x]);
+    const int64_t row = ((b * Nk + j) * H + h);
+    if (base->bf16) {
+        for (int64_t x = 0; x < d; ++x) out[x] = orc_bf16_to_f32(base->bf16[row * d + x]);
+    } else {
+        for (int64_t x = 0; x < d; ++x)
+            out[x] = orc_f16_to_f32(base->scales[row * (d / 32) + x / 32]) * (float)base->codes[row * d + x];
+    }
     for (int m = 0; m < nl; ++m) {
         int64_t e = orc_find(L[m].idx + b * L[m].cnt, L[m].cnt, j);
         if (e < 0) continue;
-        const uint8_t *cd = L[m].codes + ((b * L[m].cnt + e) * H + h) * (d / 2);
+        const uint8_t *cd = L[m].codes + ((b * L[m].cnt + e) * H + h) * (d * bits / 8);
         const uint16_t *sc = L[m].scales + ((b * L[m].cnt + e) * H + h) * (d / 32);
         for (int64_t x = 0; x < d; ++x) {
             float s = orc_f16_to_f32(sc[x / 32]);
-            float t = s * (float)orc_code(cd, x);
+            float t = s * (float)orc_code(cd, x, bits);
             out[x] = out[x] + t;
         }
     }
@@ -206,14 +242,16 @@ static void orc_pack_layers(orc_layer *L, int nl, const int32_t *const *idx,
     }
 }
 
-/* R6 applied to one group of 32 fp32 deltas. */
-static void orc_quant_group(const float *delta, uint16_t *scale_out, int *q) {
+/* R6 / R6' / R8 applied to one group of 32 fp32 values with codes in
+ * [-qmax, qmax]: qmax = 7 for int4 deltas, 3 for int3, 1 for int2, 127 for the
+ * int8 base. */
+static void orc_quant_group(const float *delta, int qmax, uint16_t *scale_out, int *q) {
     float amax = 0.0f;
     for (int e = 0; e < 32; ++e) {
         float a = fabsf(delta[e]);
         if (a > amax) amax = a;
     }
-    float sf = amax / 7.0f;
+    float sf = amax / (float)qmax;
     uint16_t sh = orc_f32_to_f16(sf);
     float s = orc_f16_to_f32(sh);
     *scale_out = sh;
@@ -222,10 +260,26 @@ static void orc_quant_group(const float *delta, uint16_t *scale_out, int *q) {
         if (s > 0.0f) {
             float t = delta[e] / s;
             v = (int)nearbyintf(t);
-            if (v > 7) v = 7;
-            if (v < -7) v = -7;
+            if (v > qmax) v = qmax;
+            if (v < -qmax) v = -qmax;
         }
         q[e] = v;
+    }
+}
+
+/* R8: the compressed base of a bf16 layer x [B,Nk,H,d]: int8 codes [B,Nk,H,d]
+ * and fp16 scales [B,Nk,H,d/32]. */
+void orc_quantize_base(const uint16_t *x, int64_t B, int64_t Nk, int64_t H, int64_t d,
+                       int8_t *codes, uint16_t *scales) {
+#pragma omp parallel for schedule(static)
+    for (int64_t row = 0; row < B * Nk * H; ++row) {
+        float v[512];
+        int q[32];
+        for (int64_t t = 0; t < d; ++t) v[t] = orc_bf16_to_f32(x[row * d + t]);
+        for (int64_t g = 0; g < d / 32; ++g) {
+            orc_quant_group(v + g * 32, 127, &scales[row * (d / 32) + g], q);
+            for (int e = 0; e < 32; ++e) codes[row * d + g * 32 + e] = (int8_t)q[e];
+        }
     }
 }
 
@@ -235,7 +289,8 @@ static void orc_quant_group(const float *delta, uint16_t *scale_out, int *q) {
  * loop-l tensor x_l against the previous loop's reconstruction is quantised
  * per 32-element group (R6). Writes the new layer's entries in the order of
  * `active` (ascending). `x_l` and `base` are [B,Nk,H,d] bf16. */
-void orc_kv_delta_append(const uint16_t *x_l, const uint16_t *base,
+void orc_kv_delta_append(const uint16_t *x_l, const uint16_t *base_bf16, const int8_t *base_codes,
+                         const uint16_t *base_scales, int bits,
                          int nl, const int32_t *const *idx, const uint8_t *const *codes,
                          const uint16_t *const *scales, const int64_t *cnt,
                          int64_t B, int64_t Nk, int64_t H, int64_t d,
@@ -243,6 +298,8 @@ void orc_kv_delta_append(const uint16_t *x_l, const uint16_t *base,
                          int32_t *out_idx, uint8_t *out_codes, uint16_t *out_scales) {
     orc_layer L[64];
     orc_pack_layers(L, nl, idx, codes, scales, cnt);
+    const orc_base base = {base_bf16, base_codes, base_scales};
+    const int qmax = (1 << (bits - 1)) - 1;
 #pragma omp parallel for collapse(2) schedule(static)
     for (int64_t b = 0; b < B; ++b) {
         for (int64_t e = 0; e < R; ++e) {
@@ -251,15 +308,14 @@ void orc_kv_delta_append(const uint16_t *x_l, const uint16_t *base,
             float rec[512], delta[512];
             int q[32];
             for (int64_t h = 0; h < H; ++h) {
-                orc_recon(base, Nk, H, d, L, nl, b, i, h, rec);
+                orc_recon(&base, Nk, H, d, bits, L, nl, b, i, h, rec);
                 const uint16_t *src = x_l + ((b * Nk + i) * H + h) * d;
                 for (int64_t x = 0; x < d; ++x) delta[x] = orc_bf16_to_f32(src[x]) - rec[x];
-                uint8_t *cd = out_codes + ((b * R + e) * H + h) * (d / 2);
+                uint8_t *cd = out_codes + ((b * R + e) * H + h) * (d * bits / 8);
                 uint16_t *sc = out_scales + ((b * R + e) * H + h) * (d / 32);
                 for (int64_t g = 0; g < d / 32; ++g) {
-                    orc_quant_group(delta + g * 32, &sc[g], q);
-                    for (int t = 0; t < 16; ++t)
-                        cd[g * 16 + t] = (uint8_t)((q[2 * t] & 0xF) | ((q[2 * t + 1] & 0xF) << 4));
+                    orc_quant_group(delta + g * 32, qmax, &sc[g], q);
+                    for (int t = 0; t < 32; ++t) orc_put_code(cd, g * 32 + t, bits, q[t]);
                 }
             }
         }
@@ -268,18 +324,20 @@ void orc_kv_delta_append(const uint16_t *x_l, const uint16_t *base,
 
 /* R4: reconstruct every token of the cache (base + `nl` delta layers) as
  * fp32 (out_f32, may be NULL) and rounded RNE to bf16 (out_bf16, may be NULL). */
-void orc_reconstruct(const uint16_t *base, int nl, const int32_t *const *idx,
+void orc_reconstruct(const uint16_t *base_bf16, const int8_t *base_codes, const uint16_t *base_scales, int bits,
+                     int nl, const int32_t *const *idx,
                      const uint8_t *const *codes, const uint16_t *const *scales, const int64_t *cnt,
                      int64_t B, int64_t Nk, int64_t H, int64_t d,
                      float *out_f32, uint16_t *out_bf16) {
     orc_layer L[64];
     orc_pack_layers(L, nl, idx, codes, scales, cnt);
+    const orc_base base = {base_bf16, base_codes, base_scales};
 #pragma omp parallel for collapse(2) schedule(static)
     for (int64_t b = 0; b < B; ++b) {
         for (int64_t j = 0; j < Nk; ++j) {
             float rec[512];
             for (int64_t h = 0; h < H; ++h) {
-                orc_recon(base, Nk, H, d, L, nl, b, j, h, rec);
+                orc_recon(&base, Nk, H, d, bits, L, nl, b, j, h, rec);
                 int64_t off = ((b * Nk + j) * H + h) * d;
                 for (int64_t x = 0; x < d; ++x) {
                     if (out_f32) out_f32[off + x] = rec[x];

@@ -570,3 +570,78 @@ def test_exit_is_strict_and_sticky(orc):
     # a flag once set stays set, whatever the scores
     assert oloop.exit_flags(scores, 0.5, np.array([True, False, False])).tolist() == [True, False, False]
     assert oloop.exit_flags(scores, float("inf")).tolist() == [True, True, True]
+
+
+# ---------------------------------------------------------------------------
+# narrower deltas (int3, int2) and the int8 compressed base
+
+def _bf(a):
+    return (np.asarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _one_group_append(orc, delta32, code_bits, d=32):
+    """A single-token, single-head layer whose delta against a zero base is `delta32`."""
+    x = np.zeros((1, 1, 1, d), np.float32)
+    x[0, 0, 0, :32] = delta32
+    return orc.kv_delta_append(_bf(x), _bf(np.zeros_like(x)), [], np.array([[0]], np.int32), code_bits=code_bits)
+
+
+def test_int3_group_hand_worked(orc):
+    """amax 3 -> scale fp16(3/3) = 1; codes rint(3, -1.5, 0.75, 0) = 3, -2
+    (the tie goes to even), 1, 0; 3-bit two's complement from bit 0 upward:
+    011, 110, 001 -> byte 0 = 0b01110011 = 0x73, byte 1 bit 0 = 0."""
+    delta = np.zeros(32, np.float32)
+    delta[:4] = [3.0, -1.5, 0.75, 0.0]
+    lay = _one_group_append(orc, delta, 3)
+    assert lay.codes.shape == (1, 1, 1, 12) and lay.scales.tolist() == [[[[0x3C00]]]]   # fp16 1.0
+    assert lay.codes[0, 0, 0, 0] == 0x73 and (lay.codes[0, 0, 0, 1] & 1) == 0
+    assert not lay.codes[0, 0, 0, 2:].any()
+
+
+def test_int2_group_hand_worked(orc):
+    """amax 0.625 (exact in bf16 and fp16) -> scale 0.625; codes rint(1, -0.32, -0.8, 0.8) = 1, 0, -1, 1
+    -> 2-bit fields 01, 00, 11, 01 -> byte 0 = 0b01110001 = 0x71."""
+    delta = np.zeros(32, np.float32)
+    delta[:4] = [0.625, -0.2, -0.5, 0.5]
+    lay = _one_group_append(orc, delta, 2)
+    assert lay.codes.shape == (1, 1, 1, 8) and lay.scales.tolist() == [[[[0x3900]]]]   # fp16 0.625
+    assert lay.codes[0, 0, 0, 0] == 0x71 and not lay.codes[0, 0, 0, 1:].any()
+
+
+@pytest.mark.parametrize("code_bits", [2, 3, 4])
+def test_narrow_deltas_round_trip_within_half_a_scale(orc, code_bits):
+    """|delta - s q| <= s/2 wherever the code is not clamped, for every width, and
+    codes stay in [-qmax, qmax]; the reconstruction reads back the same codes."""
+    rng = np.random.default_rng(40 + code_bits)
+    B, N, H, d = 1, 40, 2, 96
+    base = _bf(rng.standard_normal((B, N, H, d)))
+    x = _bf((np.asarray(base, np.uint32) << 16).view(np.float32) + 0.1 * rng.standard_normal((B, N, H, d)))
+    A = np.array([np.sort(rng.choice(N, 15, replace=False))], np.int32)
+    lay = orc.kv_delta_append(x, base, [], A, code_bits=code_bits)
+    qmax = (1 << (code_bits - 1)) - 1
+    rec, _ = orc.reconstruct(base, [lay], want_bf16=False, code_bits=code_bits)
+    xf = (np.asarray(x, np.uint32) << 16).view(np.float32)
+    bf = (np.asarray(base, np.uint32) << 16).view(np.float32)
+    s = np.repeat(lay.scales.view(np.float16).astype(np.float32), 32, axis=-1)[0]
+    delta = (xf - bf)[0][A[0]]
+    q = (rec[0][A[0]] - bf[0][A[0]]) / np.where(s > 0, s, 1)
+    assert np.all(np.abs(np.round(q)) <= qmax) and np.allclose(q, np.round(q))
+    inside = np.abs(delta) <= s * qmax
+    assert np.all(np.abs(delta - s * np.round(q))[inside] <= s[inside] / 2 + 1e-12)
+    others = np.setdiff1d(np.arange(N), A[0])
+    assert np.array_equal(rec[0][others], bf[0][others])
+
+
+def test_int8_base_round_trip_and_reconstruction(orc):
+    rng = np.random.default_rng(44)
+    x = _bf(rng.standard_normal((2, 30, 3, 64)) * 3)
+    cb = orc.quantize_base(x)
+    xf = (np.asarray(x, np.uint32) << 16).view(np.float32)
+    s = np.repeat(cb.scales.view(np.float16).astype(np.float32), 32, axis=-1)
+    assert np.all(np.abs(cb.codes.astype(np.int32)) <= 127)
+    assert np.all(np.abs(xf - s * cb.codes) <= s / 2 + 1e-12)
+    # the group's largest element maps to +-127 exactly when the scale is amax/127 in fp16
+    rec, _ = orc.reconstruct(cb, [], want_bf16=False)
+    assert np.array_equal(rec, (s * cb.codes.astype(np.float32)).astype(np.float32))
+    zero = orc.quantize_base(np.zeros((1, 2, 1, 32), np.uint16))
+    assert not zero.codes.any() and not zero.scales.any()
