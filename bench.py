@@ -483,9 +483,10 @@ def native(args, world, rank, local):
 
     e2e = None if args.no_e2e else e2e_leg(args, w, fl, cache, ws, loops, q_hat, o, z, c, act, keys, scores, lazy,
                                            dev, world)
-    recovery = None
+    recovery = variants = None
     if not args.no_recovery and rank == 0:
         recovery = column_recovery_leg(w, fl, loops, dev)
+        variants = cache_variants_leg(w, fl, loops, dev)
     out = {
         "metric": metric_for(args.workload), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
@@ -499,7 +500,7 @@ def native(args, world, rank, local):
                    "active_tokens_per_s": w.B * R * args.steps * world / secs},
         "roofline": roofline, "step_roofline": step_roofline, "kernels": kernels, "gpu_launches": launches,
         "clocks": clk, "e2e": e2e, "kv_cache": kv_cache_accounting(fl, dims, w.B, w.N, w.H, w.d, w.T),
-        "column_recovery": recovery,
+        "column_recovery": recovery, "cache_variants": variants,
     }
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, R, K, state1, budget_s=args.cpu_budget)
@@ -634,6 +635,61 @@ def native_decode(args, world, rank, local):
         "roofline": roofline, "kernels": kernels, "gpu_launches": launches, "clocks": clk, "e2e": None,
         "kv_cache": kv_cache_accounting(fl, dims, w.B, Nk, w.H, w.d, w.T),
     }
+
+
+def cache_variants_leg(w, fl, loops, dev, formats=((4, 16), (3, 16), (2, 16), (4, 8), (3, 8), (2, 8))):
+    """Cache formats (delta code width, base width) on this workload: the
+    cache's bytes against one bf16 K/V cache per loop (the pages report up to 6x
+    smaller on their models, hardware not stated), and, running loops 1..T
+    through flashloop_loop_step with each format, the error the format adds:
+    K reconstructed at every lazy loop for that loop's active tokens against
+    the exact bf16 K (relative to the change the deltas encode), and the final
+    O against the int4-delta, bf16-base run. Not timed."""
+    R, K = synth.active_count(w), synth.key_count(w)
+    per_loop = w.T * 2 * w.B * w.N * w.H * w.d * 2
+    out, o_ref = {}, None
+    for bits, base_bits in formats:
+        dims = fl.make_dims(w.B, w.N, w.H, w.d, R, K, w.T, w.T_dense, R_cap=R, delta_bits=bits, base_bits=base_bits)
+        cache = fl.Cache(dims, device=dev)
+        cache.n_tokens = w.N
+        ws = fl.workspace_for(dims, device=dev)
+        st = [torch.zeros(w.B, w.N, w.H, w.d, dtype=torch.bfloat16, device=dev),
+              torch.zeros(w.B, w.N, w.H, w.d, dtype=torch.float32, device=dev),
+              torch.zeros(w.B, w.H, w.N, dtype=torch.float32, device=dev),
+              torch.zeros(w.B, w.H, w.N, dtype=torch.float32, device=dev)]
+        act = torch.empty(w.B, R, dtype=torch.int32, device=dev)
+        keys = torch.empty(w.B, w.H, K, dtype=torch.int32, device=dev)
+        err_num = err_den = 0.0
+        for l in range(1, w.T + 1):
+            x = loops[l - 1]
+            if l <= w.T_dense:
+                fl.flashloop_loop_step(cache, l, x["Q"], x["K"], x["V"], *st, ws)
+                continue
+            fl.flashloop_loop_step(cache, l, x["Q"], x["K"], x["V"], *st, ws, h_prev=loops[l - 2]["H"],
+                                   h_cur=x["H"], active_idx=act, key_idx=keys)
+            # K of this loop's active tokens as the cache now reconstructs it, against the exact K
+            sel = act[:, None, :].expand(w.B, w.H, R).contiguous()
+            _, _, k_rec, _ = fl.flashloop_reconstruct_keys(cache, l, sel)
+            exact = torch.stack([x["K"][b, act[b].long()] for b in range(w.B)]).permute(0, 2, 1, 3).double()
+            k_base = torch.stack([loops[w.T_dense - 1]["K"][b, act[b].long()] for b in range(w.B)]).permute(0, 2, 1, 3)
+            err_num += float((k_rec.double() - exact).norm() ** 2)
+            err_den += float((exact - k_base.double()).norm() ** 2)
+        torch.cuda.synchronize()
+        assert fl.flashloop_device_status() == 0
+        o = st[1].double()
+        if o_ref is None:
+            o_ref = o
+        nbytes = fl.flashloop_kv_cache_bytes(dims)
+        dense_bf16 = 2 * w.T_dense * w.B * w.N * w.H * w.d * 2
+        stored = nbytes - (dense_bf16 if base_bits == 8 else 0)   # the int8 base replaces the bf16 layers once stored
+        out[f"int{bits} deltas, {'int8' if base_bits == 8 else 'bf16'} base"] = {
+            "cache_bytes": nbytes, "stored_bytes": stored, "ratio": per_loop / stored,
+            "k_rel_err_of_change": (err_num / err_den) ** 0.5 if err_den else 0.0,
+            "o_rel_err_vs_int4_bf16": float((o - o_ref).norm() / o_ref.norm())}
+        del cache, ws, st
+    return {"bf16_cache_per_loop_bytes": per_loop, "formats": out,
+            "note": "stored_bytes: the base and the delta layers the lazy loops keep; with an int8 base the dense "
+                    "loops' bf16 layers are working memory of those loops"}
 
 
 def column_recovery_leg(w, fl, loops, dev, fractions=(0.05, 0.10, 0.20, 0.50)):

@@ -64,26 +64,41 @@ typedef enum {
  * tokens plus room for decode tokens), H heads of dimension d (64, 96 or
  * 128), D = H*d. R active tokens per sequence and K key columns per
  * (sequence, head) per lazy loop. T loops of which the first T_dense are
- * dense. R_cap = entries per delta layer and sequence (>= R). */
+ * dense. R_cap = entries per delta layer and sequence (>= R).
+ * Cache format ("a compressed base plus a sequence of compressed deltas";
+ * 4-bit deltas in the page's main experiments, lower widths degrade quality):
+ *   delta_bits  width of the delta codes: 4 (or 0), 3 or 2; symmetric codes
+ *               in [-qmax, qmax], qmax = 2^(delta_bits-1) - 1
+ *   base_bits   16 (or 0): the base is the last dense loop's bf16 layer;
+ *               8: the lazy loops read an int8 copy of it instead (one fp16
+ *               scale per 32 elements, scale = fp16(amax/127)), made when
+ *               that layer is stored; the dense loops still attend over bf16. */
 typedef struct {
     int32_t B, N_cap, H, d;
     int32_t R, K;
     int32_t T, T_dense;
     int32_t R_cap;
+    int32_t delta_bits, base_bits;
 } flashloop_dims_t;
 
 /* Per-loop KV cache ("a compressed base plus a sequence of compressed
  * deltas"). Dense loop t (1..T_dense) owns a full bf16 layer; the base is
- * layer T_dense. Lazy loop l (T_dense < l <= T) owns delta layer
- * l - T_dense - 1 holding, per sequence b, count[] entries:
+ * layer T_dense (with base_bits = 8 also held as int8 codes [B, N_cap, H, d]
+ * with fp16 scales [B, N_cap, H, d/32], which the lazy loops read). Lazy
+ * loop l (T_dense < l <= T) owns delta layer l - T_dense - 1 holding, per
+ * sequence b, count[] entries:
  *   idx    [B, R_cap]            token index of each entry, ascending
  *   slot   [B, N_cap]            entry of each token, -1 = no entry
- *   codes  [B, R_cap, H, d/2]    int4 two's-complement codes; element 2t is
- *                                the low nibble of byte t
+ *   codes  [B, R_cap, H, d*w/8]  two's-complement codes of w = delta_bits
+ *                                bits; element x occupies bits [x*w, x*w + w)
+ *                                of its row read as a little-endian bit
+ *                                string (w = 4: element 2t is the low nibble
+ *                                of byte t)
  *   scales [B, R_cap, H, d/32]   fp16 scale of each 32-element group
  * for K and V separately. The reconstruction of token j at loop l is the
- * base plus, in ascending loop order, scale*code of every delta layer up to
- * l that holds j, summed in fp32 without fused multiply-add.
+ * base (scale*code for an int8 base) plus, in ascending loop order,
+ * scale*code of every delta layer up to l that holds j, summed in fp32
+ * without fused multiply-add.
  * All pointers are carved from one caller buffer by flashloop_kv_cache_init;
  * `count` and `n_tokens` are host-side and updated by the calls that append. */
 typedef struct {
@@ -98,6 +113,8 @@ typedef struct {
     uint8_t *v_codes[FLASHLOOP_MAX_LOOPS];
     uint16_t *v_scales[FLASHLOOP_MAX_LOOPS];
     int32_t count[FLASHLOOP_MAX_LOOPS];
+    int8_t *k_base_codes, *v_base_codes;     /* base_bits = 8: [B, N_cap, H, d] */
+    uint16_t *k_base_scales, *v_base_scales; /* base_bits = 8: [B, N_cap, H, d/32] fp16 */
 } flashloop_kv_cache_t;
 
 /* How a lazy prefill loop ranks key columns for its selection. */
@@ -265,7 +282,9 @@ flashloop_status_t flashloop_kv_delta_append(flashloop_kv_cache_t *cache, int32_
                                              flashloop_stream_t stream);
 
 /* Stores K/V rows as (part of) dense layer `loop` (loop <= T_dense):
- * layer[b, pos0 + r] = k[b, r] for r < n_rows. k, v [B, n_rows, H, d]. */
+ * layer[b, pos0 + r] = k[b, r] for r < n_rows. k, v [B, n_rows, H, d].
+ * With base_bits = 8, storing into the base layer (loop = T_dense) also
+ * writes those rows' int8 codes and scales. */
 flashloop_status_t flashloop_kv_dense_store(flashloop_kv_cache_t *cache, int32_t loop,
                                             const uint16_t *k, const uint16_t *v,
                                             int32_t pos0, int32_t n_rows, flashloop_stream_t stream);

@@ -138,6 +138,9 @@ static SideStream *side_stream() {
 }
 
 static bool head_dim_ok(int d) { return d == 64 || d == 96 || d == 128; }
+// width of the delta codes and whether the lazy loops read an int8 base
+static int code_bits_of(const flashloop_dims_t &dm) { return dm.delta_bits ? dm.delta_bits : 4; }
+static bool int8_base(const flashloop_dims_t &dm) { return dm.base_bits == 8; }
 
 static flashloop_status_t check_dims(const flashloop_dims_t *dm) {
     if (!dm) return set_error(FLASHLOOP_ERR_INVALID_ARG, "dims is NULL");
@@ -147,6 +150,10 @@ static flashloop_status_t check_dims(const flashloop_dims_t *dm) {
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad dims (B=%d N_cap=%d H=%d R=%d K=%d T=%d T_dense=%d R_cap=%d)",
                          dm->B, dm->N_cap, dm->H, dm->R, dm->K, dm->T, dm->T_dense, dm->R_cap);
     if (!head_dim_ok(dm->d)) return set_error(FLASHLOOP_ERR_UNSUPPORTED, "head dim %d not in {64, 96, 128}", dm->d);
+    if (dm->delta_bits != 0 && (dm->delta_bits < 2 || dm->delta_bits > 4))
+        return set_error(FLASHLOOP_ERR_UNSUPPORTED, "delta_bits %d not in {2, 3, 4}", dm->delta_bits);
+    if (dm->base_bits != 0 && dm->base_bits != 8 && dm->base_bits != 16)
+        return set_error(FLASHLOOP_ERR_UNSUPPORTED, "base_bits %d not in {8, 16}", dm->base_bits);
     return FLASHLOOP_OK;
 }
 
@@ -172,34 +179,49 @@ static WsLayout ws_layout(const flashloop_dims_t *dm) {
 }
 
 struct CacheLayout {
-    size_t dense_layer, idx, slot, codes, scales, total;
+    size_t dense_layer, base_codes, base_scales, idx, slot, codes, scales, total;
 };
 
 static CacheLayout cache_layout(const flashloop_dims_t *dm) {
     CacheLayout c;
-    c.dense_layer = align_up((size_t)dm->B * dm->N_cap * dm->H * dm->d * 2);
+    const size_t rows = (size_t)dm->B * dm->N_cap * dm->H;
+    c.dense_layer = align_up(rows * dm->d * 2);
+    c.base_codes = int8_base(*dm) ? align_up(rows * dm->d) : 0;
+    c.base_scales = int8_base(*dm) ? align_up(rows * (dm->d / 32) * 2) : 0;
     c.idx = align_up((size_t)dm->B * dm->R_cap * 4);
     c.slot = align_up((size_t)dm->B * dm->N_cap * 4);
-    c.codes = align_up((size_t)dm->B * dm->R_cap * dm->H * (dm->d / 2));
+    c.codes = align_up((size_t)dm->B * dm->R_cap * dm->H * ((size_t)dm->d * code_bits_of(*dm) / 8));
     c.scales = align_up((size_t)dm->B * dm->R_cap * dm->H * (dm->d / 32) * 2);
     const size_t n_delta = (size_t)(dm->T - dm->T_dense);
-    c.total = 2 * dm->T_dense * c.dense_layer + n_delta * (c.idx + c.slot + 2 * c.codes + 2 * c.scales);
+    c.total = 2 * dm->T_dense * c.dense_layer + 2 * (c.base_codes + c.base_scales) +
+              n_delta * (c.idx + c.slot + 2 * c.codes + 2 * c.scales);
     return c;
 }
 
-// Reconstruction of loop `loop` = base (last dense layer) + delta layers up to `loop`.
-static DeltaView make_view(const flashloop_kv_cache_t *c, int loop) {
+// Reconstruction of loop `loop` = base (last dense layer) + delta layers up to
+// `loop`. `lazy` views are those the lazy loops read (appends, reconstructions,
+// decode's lazy attention): with an int8 base they take it in place of the
+// bf16 base layer; the dense loops' own attention reads the bf16 layers.
+static DeltaView make_view(const flashloop_kv_cache_t *c, int loop, bool lazy = true) {
     DeltaView v;
     memset(&v, 0, sizeof v);
     const int td = c->dims.T_dense;
+    v.code_bits = code_bits_of(c->dims);
+    const bool compressed = lazy && int8_base(c->dims) && loop >= td;
+    if (compressed) {
+        v.k_base_codes = c->k_base_codes;
+        v.v_base_codes = c->v_base_codes;
+        v.k_base_scales = c->k_base_scales;
+        v.v_base_scales = c->v_base_scales;
+    }
     if (loop <= td) {
-        v.k_base = c->k_dense[loop - 1];
-        v.v_base = c->v_dense[loop - 1];
+        v.k_base = compressed ? nullptr : c->k_dense[loop - 1];
+        v.v_base = compressed ? nullptr : c->v_dense[loop - 1];
         v.n_layers = 0;
         return v;
     }
-    v.k_base = c->k_dense[td - 1];
-    v.v_base = c->v_dense[td - 1];
+    v.k_base = compressed ? nullptr : c->k_dense[td - 1];
+    v.v_base = compressed ? nullptr : c->v_dense[td - 1];
     v.n_layers = loop - td;
     for (int m = 0; m < v.n_layers; ++m) {
         v.slot[m] = c->slot[m];
@@ -217,6 +239,8 @@ static flashloop_status_t check_cache(const flashloop_kv_cache_t *c) {
     if (st != FLASHLOOP_OK) return st;
     for (int t = 0; t < c->dims.T_dense; ++t)
         if (!c->k_dense[t] || !c->v_dense[t]) return set_error(FLASHLOOP_ERR_INVALID_ARG, "cache is not initialised");
+    if (int8_base(c->dims) && (!c->k_base_codes || !c->v_base_codes || !c->k_base_scales || !c->v_base_scales))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "cache is not initialised (int8 base)");
     return FLASHLOOP_OK;
 }
 
@@ -309,6 +333,12 @@ flashloop_status_t flashloop_kv_cache_init(flashloop_kv_cache_t *cache, void *de
     for (int t = 0; t < dims->T_dense; ++t) {
         cache->k_dense[t] = reinterpret_cast<uint16_t *>(p); p += L.dense_layer;
         cache->v_dense[t] = reinterpret_cast<uint16_t *>(p); p += L.dense_layer;
+    }
+    if (int8_base(*dims)) {
+        cache->k_base_codes = reinterpret_cast<int8_t *>(p); p += L.base_codes;
+        cache->v_base_codes = reinterpret_cast<int8_t *>(p); p += L.base_codes;
+        cache->k_base_scales = reinterpret_cast<uint16_t *>(p); p += L.base_scales;
+        cache->v_base_scales = reinterpret_cast<uint16_t *>(p); p += L.base_scales;
     }
     for (int m = 0; m < dims->T - dims->T_dense; ++m) {
         cache->idx[m] = reinterpret_cast<int32_t *>(p); p += L.idx;
@@ -418,6 +448,13 @@ flashloop_status_t flashloop_kv_dense_store(flashloop_kv_cache_t *cache, int32_t
     const int row = dm.H * dm.d;
     cudaError_t e = launch_store_rows(k, dm.B, n_rows, row, cache->k_dense[loop - 1], dm.N_cap, pos0, stream);
     if (e == cudaSuccess) e = launch_store_rows(v, dm.B, n_rows, row, cache->v_dense[loop - 1], dm.N_cap, pos0, stream);
+    if (e == cudaSuccess && int8_base(dm) && loop == dm.T_dense) {   // the base the lazy loops read, compressed
+        e = launch_quantize_base(k, dm.B, n_rows, dm.H, dm.d, cache->k_base_codes, cache->k_base_scales, dm.N_cap, pos0,
+                                 stream);
+        if (e == cudaSuccess)
+            e = launch_quantize_base(v, dm.B, n_rows, dm.H, dm.d, cache->v_base_codes, cache->v_base_scales, dm.N_cap,
+                                     pos0, stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "kv_dense_store");
     return FLASHLOOP_OK;
 }
@@ -530,8 +567,8 @@ static flashloop_status_t lazy_attention_impl(const flashloop_attn_args_t *a, fl
         p.K = lazy ? a->K : a->n_keys;
         p.key_idx = lazy ? a->key_idx : nullptr;
         p.q = a->q; p.q_hat = a->q_hat; p.o = a->o; p.z = a->z; p.c = a->c;
-        p.new_view = make_view(c, a->loop);
-        if (a->loop > 1) p.old_view = make_view(c, a->loop - 1);
+        p.new_view = make_view(c, a->loop, lazy);
+        if (a->loop > 1) p.old_view = make_view(c, a->loop - 1, lazy);
         p.N_cap = dm.N_cap; p.R_cap = dm.R_cap;
         e = launch_decode_attention(p, stream);
         if (e == cudaErrorInvalidValue)

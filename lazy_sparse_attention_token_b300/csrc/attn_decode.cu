@@ -116,10 +116,9 @@ template <int D, class OnOld, class OnNew>
 __device__ __forceinline__ void visit_rec(const DeltaView &ov, const DeltaView &nv, bool is_v, long long b,
                                           const int (&j)[kU], const int (&tt)[kU], const int *ents, int chunk, int h,
                                           int c8, int H, int N_cap, int R_cap, OnOld &&on_old, OnNew &&on_new) {
-    const uint16_t *base = is_v ? ov.v_base : ov.k_base;
     float r[kU][8];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) load_base8(base, b, j[u], h, c8, H, D, N_cap, r[u]);
+    for (int u = 0; u < kU; ++u) load_base8(ov, is_v, b, j[u], h, c8, H, D, N_cap, r[u]);
     for (int m0 = 0; m0 < nv.n_layers; m0 += kLayerPair) {
         int ent[kLayerPair][kU];
         uint32_t w[kLayerPair][kU];
@@ -137,7 +136,7 @@ __device__ __forceinline__ void visit_rec(const DeltaView &ov, const DeltaView &
                 s[mm][u] = 0.f;
                 if (ent[mm][u] >= 0) {
                     const long long e = (b * R_cap + ent[mm][u]) * H + h;
-                    w[mm][u] = __ldg(reinterpret_cast<const uint32_t *>(codes + e * (D / 2)) + c8);
+                    w[mm][u] = load_codes8(codes + e * (D * nv.code_bits / 8), c8, nv.code_bits);
                     s[mm][u] = __half2float(__ushort_as_half(__ldg(scales + e * (D / 32) + c8 / 4)));
                 }
             }

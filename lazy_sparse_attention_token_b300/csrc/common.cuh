@@ -46,11 +46,16 @@ constexpr int kMaxLoops = FLASHLOOP_MAX_LOOPS;
 
 // Device view of the delta layers needed to reconstruct one loop.
 struct DeltaView {
-    const uint16_t *k_base;            // [B, N_cap, H, d] bf16
+    const uint16_t *k_base;            // [B, N_cap, H, d] bf16, or NULL for an int8 base
     const uint16_t *v_base;
+    const int8_t *k_base_codes;        // int8 base [B, N_cap, H, d] (when k_base is NULL)
+    const int8_t *v_base_codes;
+    const uint16_t *k_base_scales;     // [B, N_cap, H, d/32] fp16
+    const uint16_t *v_base_scales;
+    int code_bits;                     // width of the delta codes: 2, 3 or 4
     int n_layers;                      // delta layers applied, ascending
     const int32_t *slot[kMaxLoops];    // [B, N_cap]
-    const uint8_t *k_codes[kMaxLoops]; // [B, R_cap, H, d/2]
+    const uint8_t *k_codes[kMaxLoops]; // [B, R_cap, H, d * code_bits / 8]
     const uint16_t *k_scales[kMaxLoops];
     const uint8_t *v_codes[kMaxLoops];
     const uint16_t *v_scales[kMaxLoops];
@@ -70,6 +75,11 @@ cudaError_t launch_gather_rows(const void *src, int B, int N, int row_bytes, con
                                void *dst, cudaStream_t s);
 cudaError_t launch_store_rows(const uint16_t *src, int B, int n_rows, int row_elems, uint16_t *dst,
                               int dst_rows, int pos0, cudaStream_t s);
+// int8 base of rows src [B, n_rows, H, d] bf16 at positions pos0.. of codes
+// [B, N_cap, H, d] and scales [B, N_cap, H, d/32]: one fp16 scale per 32
+// elements, scale = fp16_rne(amax / 127), code = rint_even(x / scale) in [-127, 127].
+cudaError_t launch_quantize_base(const uint16_t *src, int B, int n_rows, int H, int d, int8_t *codes,
+                                 uint16_t *scales, int N_cap, int pos0, cudaStream_t s);
 cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, const uint16_t *v_l,
                                 int rows_are_tokens, int src_rows, const int32_t *active, int R, int at,
                                 int B, int N_cap, int H, int d, int R_cap, int32_t *out_idx,
@@ -208,6 +218,50 @@ __device__ __forceinline__ void load_base8(const uint16_t *base, long long b, in
                                            int d, int N_cap, float rec[8]) {
     const uint4 v = ldg_nc_v4(base + ((b * N_cap + i) * H + h) * (long long)d + c8 * 8);
     unpack_bf16x8(v, rec);
+}
+
+// The base's 8 fp32 values of chunk c8 of token i, head h: bf16 rows, or an
+// int8 base's scale * code (exact in fp32: an 8-bit code times an fp16 scale).
+__device__ __forceinline__ void load_base8(const DeltaView &view, bool is_v, long long b, int i, int h, int c8,
+                                           int H, int d, int N_cap, float rec[8]) {
+    const uint16_t *bf = is_v ? view.v_base : view.k_base;
+    if (bf) {
+        load_base8(bf, b, i, h, c8, H, d, N_cap, rec);
+        return;
+    }
+    const long long row = (b * N_cap + i) * H + h;
+    const int8_t *codes = is_v ? view.v_base_codes : view.k_base_codes;
+    const uint16_t *scales = is_v ? view.v_base_scales : view.k_base_scales;
+    const uint2 c = __ldg(reinterpret_cast<const uint2 *>(codes + row * d) + c8);
+    const float s = __half2float(__ushort_as_half(__ldg(scales + row * (d / 32) + c8 / 4)));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int code = (int)(int8_t)(((e < 4 ? c.x : c.y) >> (8 * (e & 3))) & 0xFFu);
+        rec[e] = __fmul_rn(s, (float)code);
+    }
+}
+
+// The 8 codes of chunk c8 (elements 8 c8 .. 8 c8 + 7) of a row of `bits`-bit
+// two's-complement codes (a little-endian bit string), returned as eight 4-bit
+// two's-complement nibbles (code t in bits [4t, 4t + 4)) of the same values, the
+// form dequant_add8 takes. `row` is 4-byte aligned (a row holds d * bits / 8
+// bytes, a multiple of 4 for d a multiple of 32).
+__device__ __forceinline__ uint32_t load_codes8(const uint8_t *row, int c8, int bits) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(row);
+    if (bits == 4) return __ldg(w + c8);
+    const int off = 8 * bits * c8;            // first bit of the chunk
+    const int wi = off >> 5, sh = off & 31;
+    uint32_t v = __ldg(w + wi) >> sh;
+    if (sh + 8 * bits > 32) v |= __ldg(w + wi + 1) << (32 - sh);
+    const uint32_t mask = (1u << bits) - 1u, sign = 1u << (bits - 1);
+    uint32_t out = 0u;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        uint32_t c = (v >> (bits * t)) & mask;
+        if (c & sign) c |= 0xFu & ~mask;      // sign-extend to four bits
+        out |= c << (4 * t);
+    }
+    return out;
 }
 
 inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }

@@ -50,12 +50,13 @@ store_rows_kernel(const uint4 *__restrict__ src, int n_rows, int vecs, uint4 *__
 
 // One thread per (sequence, entry, head, 32-element quantisation group): the
 // group's four 8-element chunks of the loop-l row and of the base row are
-// loaded together, each earlier delta layer costs one slot lookup, one
-// 16-byte codes load and one scale load for the whole group, and the group's
-// 32 codes (16 bytes) go out in one store. blockIdx.y: 0 = K, 1 = V.
+// loaded together, each earlier delta layer costs one slot lookup, one codes
+// load (4 * BITS bytes) and one scale load for the whole group, and the
+// group's 32 codes go out as BITS 32-bit words. blockIdx.y: 0 = K, 1 = V.
 // Four 256-thread blocks per SM (64 registers): the kernel waits on chains of
 // dependent gathers (one per earlier delta layer), so resident warps matter more
 // than a few spilled registers.
+template <int BITS>
 __global__ void __launch_bounds__(256, 4)
 delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint16_t *__restrict__ v_l,
                     int rows_are_tokens, int src_rows, const int32_t *__restrict__ active, int R, int at,
@@ -81,19 +82,17 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
     const int i = __ldg(active + be);
     const long long src_row = rows_are_tokens ? (long long)i : (long long)e;
 
+    constexpr int RB = BITS * 4;              // bytes of one group's codes
+    constexpr float QMAX = (float)((1 << (BITS - 1)) - 1);
     const uint16_t *x_l = (is_v ? v_l : k_l) + ((b * src_rows + src_row) * H + h) * (long long)d + g * 32;
-    const uint16_t *base = (is_v ? view.v_base : view.k_base) + ((b * N_cap + i) * H + h) * (long long)d + g * 32;
-    uint4 xv[4], bv[4];
+    uint4 xv[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) xv[c] = ldg_nc_v4(x_l + c * 8);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) bv[c] = ldg_nc_v4(base + c * 8);
     float x[32], rec[32];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        unpack_bf16x8(xv[c], x + 8 * c);
-        unpack_bf16x8(bv[c], rec + 8 * c);
-    }
+    for (int c = 0; c < 4; ++c) load_base8(view, is_v, b, i, h, 4 * g + c, H, d, N_cap, rec + 8 * c);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) unpack_bf16x8(xv[c], x + 8 * c);
     // the previous loop's reconstruction: base plus each earlier layer's deltas, in order
     for (int m = 0; m < view.n_layers; ++m) {
         const int en = __ldg(view.slot[m] + b * N_cap + i);
@@ -101,9 +100,16 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
         const long long ent = (b * R_cap + en) * H + h;
         const uint8_t *codes = is_v ? view.v_codes[m] : view.k_codes[m];
         const uint16_t *scales = is_v ? view.v_scales[m] : view.k_scales[m];
-        const uint4 w4 = __ldg(reinterpret_cast<const uint4 *>(codes + ent * (d / 2) + g * 16));
+        const uint8_t *crow = codes + ent * (d * BITS / 8);
+        uint32_t w[4];
+        if constexpr (BITS == 4) {
+            const uint4 w4 = __ldg(reinterpret_cast<const uint4 *>(crow + g * RB));
+            w[0] = w4.x; w[1] = w4.y; w[2] = w4.z; w[3] = w4.w;
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) w[c] = load_codes8(crow, 4 * g + c, BITS);
+        }
         const float sc = __half2float(__ushort_as_half(__ldg(scales + ent * (d / 32) + g)));
-        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
         for (int c = 0; c < 4; ++c) dequant_add8(rec + 8 * c, w[c], sc);
     }
@@ -116,30 +122,36 @@ delta_append_kernel(DeltaView view, const uint16_t *__restrict__ k_l, const uint
     }
     // a sequence that has stopped looping keeps its K/V: its entries are zero deltas
     if (seq_exit && __ldg(seq_exit + b)) amax = 0.f;
-    const __half sh = __float2half_rn(__fdiv_rn(amax, 7.0f));   // the scale is exact: fp16(fp32(amax / 7))
+    const __half sh = __float2half_rn(__fdiv_rn(amax, QMAX));   // the scale is exact: fp16(fp32(amax / qmax))
     const float s = __half2float(sh);
     // code = rint(delta / scale): the quotient is taken as delta * (1 / scale), within
     // about one ulp of the divided one, so a code can only differ where the quotient
     // lies within ~1e-6 of a rounding boundary (n + 1/2)
     const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
-    uint32_t packed[4];
+    // the group's codes as a little-endian bit string of BITS-bit fields
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        packed[c] = 0u;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            // rint is monotone and fixes +-7, so clamping before rounding gives the
-            // same integer; adding 1.5 * 2^23 rounds the clamped quotient to an
-            // integer (ties to even) in the low mantissa bits, whose low nibble is
-            // then the code in two's complement
-            const float r = fminf(7.f, fmaxf(-7.f, __fmul_rn(x[8 * c + k], inv)));
-            packed[c] |= (__float_as_uint(__fadd_rn(r, 12582912.0f)) & 0xFu) << (4 * k);
-        }
+    for (int k = 0; k < 32; ++k) {
+        // rint is monotone and fixes +-qmax, so clamping before rounding gives the
+        // same integer; adding 1.5 * 2^23 rounds the clamped quotient to an
+        // integer (ties to even) in the low mantissa bits, whose low BITS bits are
+        // then the code in two's complement
+        const float r = fminf(QMAX, fmaxf(-QMAX, __fmul_rn(x[k], inv)));
+        const uint32_t code = __float_as_uint(__fadd_rn(r, 12582912.0f)) & ((1u << BITS) - 1u);
+        const int bit = BITS * k;
+        packed[bit >> 5] |= code << (bit & 31);
+        if ((bit & 31) + BITS > 32) packed[(bit >> 5) + 1] |= code >> (32 - (bit & 31));
     }
     const long long ent = (b * R_cap + at + e) * H + h;
     uint8_t *codes = is_v ? v_codes : k_codes;
     uint16_t *scales = is_v ? v_scales : k_scales;
-    *reinterpret_cast<uint4 *>(codes + ent * (d / 2) + g * 16) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(codes + ent * (d * BITS / 8) + g * RB);
+    if constexpr (BITS == 4) {
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    } else {
+#pragma unroll
+        for (int w = 0; w < BITS; ++w) dst[w] = packed[w];
+    }
     scales[ent * (d / 32) + g] = __half_as_ushort(sh);
     if (!is_v && h == 0 && g == 0) {
         out_idx[b * R_cap + at + e] = i;
@@ -224,7 +236,7 @@ reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const in
     const int j = __ldg(key_idx + key);
     const long long tok = b * N_cap + j;
     float rec[8];
-    unpack_bf16x8(ldg_nc_v4((is_v ? view.v_base : view.k_base) + (tok * H + h) * d + ch * 8), rec);
+    load_base8(view, is_v, b, j, h, ch, H, d, N_cap, rec);
     uint16_t *o_old = (is_v ? v_old : k_old) + (long long)key * d + ch * 8;
     uint16_t *o_new = (is_v ? v_new : k_new) + (long long)key * d + ch * 8;
     auto store8 = [&](uint16_t *dst) {
@@ -246,7 +258,7 @@ reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const in
                 const long long ent = (b * R_cap + en[u]) * H + h;
                 const uint8_t *codes = is_v ? view.v_codes[m] : view.k_codes[m];
                 const uint16_t *scales = is_v ? view.v_scales[m] : view.k_scales[m];
-                w[u] = __ldg(reinterpret_cast<const uint32_t *>(codes + ent * (d / 2)) + ch);
+                w[u] = load_codes8(codes + ent * (d * view.code_bits / 8), ch, view.code_bits);
                 sc[u] = __half2float(__ushort_as_half(__ldg(scales + ent * (d / 32) + ch / 4)));
             }
         }
@@ -260,7 +272,64 @@ reconstruct_keys_kernel(DeltaView view, int old_layers, int new_layers, const in
     store8(o_new);
 }
 
+// The int8 base of stored rows: one thread per (sequence, row, head, 32-element
+// group), the same quantiser as the deltas with qmax = 127.
+__global__ void __launch_bounds__(256)
+quantize_base_kernel(const uint16_t *__restrict__ src, int n_rows, int H, int d, int8_t *__restrict__ codes,
+                     uint16_t *__restrict__ scales, int N_cap, int pos0, long long total) {
+    pdl_wait();
+    pdl_trigger();
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= total) return;
+    const int gpr = d / 32;
+    const long long rest = t / gpr;
+    const int g = (int)(t - rest * gpr);
+    const long long brh = rest;                 // (b * n_rows + r) * H + h
+    const long long br = brh / H;
+    const int h = (int)(brh - br * H);
+    const long long b = br / n_rows;
+    const int r = (int)(br - b * n_rows);
+    const uint16_t *x = src + brh * d + g * 32;
+    float v[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) unpack_bf16x8(ldg_nc_v4(x + 8 * c), v + 8 * c);
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(v[k]));
+    const __half sh = __float2half_rn(__fdiv_rn(amax, 127.0f));
+    const float s = __half2float(sh);
+    const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
+    uint32_t packed[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        packed[w] = 0u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float q = fminf(127.f, fmaxf(-127.f, __fmul_rn(v[4 * w + k], inv)));
+            packed[w] |= (__float_as_uint(__fadd_rn(q, 12582912.0f)) & 0xFFu) << (8 * k);
+        }
+    }
+    const long long drow = (b * N_cap + pos0 + r) * H + h;
+    uint4 *dst = reinterpret_cast<uint4 *>(codes + drow * d + g * 32);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    scales[drow * (d / 32) + g] = __half_as_ushort(sh);
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_base(const uint16_t *src, int B, int n_rows, int H, int d, int8_t *codes,
+                                 uint16_t *scales, int N_cap, int pos0, cudaStream_t s) {
+    const long long total = (long long)B * n_rows * H * (d / 32);
+    if (total == 0) return cudaSuccess;
+    {
+        KernelTimer kt("quantize_base", s);
+        const cudaError_t e = launch_pdl(quantize_base_kernel, dim3(ceil_div(total, 256)), dim3(256), 0, s, src, n_rows,
+                                         H, d, codes, scales, N_cap, pos0, total);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gather_rows(const void *src, int B, int N, int row_bytes, const int32_t *idx, int R,
                                void *dst, cudaStream_t s) {
@@ -298,7 +367,9 @@ cudaError_t launch_delta_append(const DeltaView &view, const uint16_t *k_l, cons
     dim3 grid(ceil_div(total, 256), 2);
     {
         KernelTimer kt("delta_append", s);
-        const cudaError_t e = launch_pdl(delta_append_kernel, grid, dim3(256), 0, s, view, k_l, v_l,
+        auto kern = view.code_bits == 2 ? delta_append_kernel<2> : view.code_bits == 3 ? delta_append_kernel<3>
+                                                                                         : delta_append_kernel<4>;
+        const cudaError_t e = launch_pdl(kern, grid, dim3(256), 0, s, view, k_l, v_l,
                                          rows_are_tokens, src_rows, active, R, at, H, d, N_cap, R_cap, total,
                                          out_idx, out_slot, k_codes, k_scales, v_codes, v_scales, seq_exit);
         if (e != cudaSuccess) return e;

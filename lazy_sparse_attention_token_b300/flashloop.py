@@ -31,7 +31,7 @@ class FlashLoopError(RuntimeError):
 
 class Dims(ctypes.Structure):
     _fields_ = [("B", I32), ("N_cap", I32), ("H", I32), ("d", I32), ("R", I32), ("K", I32),
-                ("T", I32), ("T_dense", I32), ("R_cap", I32)]
+                ("T", I32), ("T_dense", I32), ("R_cap", I32), ("delta_bits", I32), ("base_bits", I32)]
 
 
 class KVCache(ctypes.Structure):
@@ -40,7 +40,8 @@ class KVCache(ctypes.Structure):
                 ("idx", P * MAX_LOOPS), ("slot", P * MAX_LOOPS),
                 ("k_codes", P * MAX_LOOPS), ("k_scales", P * MAX_LOOPS),
                 ("v_codes", P * MAX_LOOPS), ("v_scales", P * MAX_LOOPS),
-                ("count", I32 * MAX_LOOPS)]
+                ("count", I32 * MAX_LOOPS),
+                ("k_base_codes", P), ("v_base_codes", P), ("k_base_scales", P), ("v_base_scales", P)]
 
 
 class AttnArgs(ctypes.Structure):
@@ -142,8 +143,8 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def make_dims(B, N_cap, H, d, R, K, T, T_dense, R_cap=None) -> Dims:
-    return Dims(B, N_cap, H, d, R, K, T, T_dense, R if R_cap is None else R_cap)
+def make_dims(B, N_cap, H, d, R, K, T, T_dense, R_cap=None, delta_bits=4, base_bits=16) -> Dims:
+    return Dims(B, N_cap, H, d, R, K, T, T_dense, R if R_cap is None else R_cap, delta_bits, base_bits)
 
 
 def flashloop_workspace_bytes(dims: Dims) -> int:
@@ -191,16 +192,30 @@ class Cache:
         return (self._view(self.c.k_dense[loop - 1], shape, torch.bfloat16),
                 self._view(self.c.v_dense[loop - 1], shape, torch.bfloat16))
 
+    @property
+    def code_bits(self) -> int:
+        return self.dims.delta_bits or 4
+
+    def base_int8(self):
+        """(k_codes, k_scales, v_codes, v_scales) of the int8 base (base_bits = 8), or None."""
+        d = self.dims
+        if d.base_bits != 8:
+            return None
+        shape, sshape = (d.B, d.N_cap, d.H, d.d), (d.B, d.N_cap, d.H, d.d // 32)
+        return (self._view(self.c.k_base_codes, shape, torch.int8), self._view(self.c.k_base_scales, sshape, torch.int16),
+                self._view(self.c.v_base_codes, shape, torch.int8), self._view(self.c.v_base_scales, sshape, torch.int16))
+
     def delta_layer(self, loop: int):
         """(idx, slot, k_codes, k_scales, v_codes, v_scales) of lazy loop `loop`, the first count entries."""
         d = self.dims
         m = loop - d.T_dense - 1
         cnt = self.c.count[m]
+        row = d.d * self.code_bits // 8
         idx = self._view(self.c.idx[m], (d.B, d.R_cap), torch.int32)[:, :cnt]
         slot = self._view(self.c.slot[m], (d.B, d.N_cap), torch.int32)
-        kc = self._view(self.c.k_codes[m], (d.B, d.R_cap, d.H, d.d // 2), torch.uint8)[:, :cnt]
+        kc = self._view(self.c.k_codes[m], (d.B, d.R_cap, d.H, row), torch.uint8)[:, :cnt]
         ks = self._view(self.c.k_scales[m], (d.B, d.R_cap, d.H, d.d // 32), torch.int16)[:, :cnt]
-        vc = self._view(self.c.v_codes[m], (d.B, d.R_cap, d.H, d.d // 2), torch.uint8)[:, :cnt]
+        vc = self._view(self.c.v_codes[m], (d.B, d.R_cap, d.H, row), torch.uint8)[:, :cnt]
         vs = self._view(self.c.v_scales[m], (d.B, d.R_cap, d.H, d.d // 32), torch.int16)[:, :cnt]
         return idx, slot, kc, ks, vc, vs
 
