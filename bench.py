@@ -503,7 +503,7 @@ def native(args, world, rank, local):
         "column_recovery": recovery, "cache_variants": variants,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, R, K, state1, budget_s=args.cpu_budget)
+        out["cpu_baseline"] = cpu_baseline(w, R, K, state1, budget_s=args.cpu_budget, force_full=args.cpu_full_step)
     return out
 
 
@@ -887,15 +887,16 @@ def _sample_on(w, R, K, inp, n_heads, rows_frac, threads=None):
             oracle.set_threads(n0)
 
 
-def cpu_baseline(w, R, K, gpu_state, budget_s=20.0, device=None, full_limit_s=120.0):
+def cpu_baseline(w, R, K, gpu_state, budget_s=20.0, device=None, full_limit_s=60.0, force_full=False):
     """The oracle as it stands on the host cores, on the same inputs and the
     same loop-1 state as the CUDA path: one complete lazy step, timed once, is
     the figure (`value`). A bounded sample of the step (one head, a share of
     the active rows) is also timed on every core and on one core, to show
     the oracle's thread scaling; sample figures are tokens of that sample per
-    second, not a full step. If the complete step is predicted (from the
-    sample's per-row cost) to exceed `full_limit_s`, the sample stands in for
-    it and the line says so."""
+    second, not a full step. If the complete step is predicted to exceed
+    `full_limit_s` (and `force_full` is off), the sample stands in for it and
+    the line says so. The prediction separates the attention's cost per head
+    (reconstruction, key selection) from its cost per row, from two probes."""
     import oracle
     oracle.build()
     inp = _oracle_inputs(w, w.H, device or _input_device())
@@ -903,16 +904,19 @@ def cpu_baseline(w, R, K, gpu_state, budget_s=20.0, device=None, full_limit_s=12
     inp.update(qh1=oracle.bits(qh.contiguous()), o1=o.cpu().numpy(), z1=z.cpu().numpy(), c1=c.cpu().numpy())
     # size the sample: one head, a share of the rows that takes about budget_s / 4
     probe, probe_sa = _oracle_step(w, R, K, inp, 1, 0.02)
+    probe2, probe2_sa = _oracle_step(w, R, K, inp, 1, 0.06)
+    per_row = max(0.0, ((probe2 - probe2_sa) - (probe - probe_sa)) / 0.04)      # one head, all rows
+    per_head = max(0.0, (probe - probe_sa) - 0.02 * per_row)                  # one head, no rows
+    predicted = min(probe_sa, probe2_sa) + w.H * (per_head + per_row)
     frac = float(min(1.0, max(0.02, 0.02 * (budget_s / 4) / max(probe, 1e-3))))
     sample_all = _sample_on(w, R, K, inp, 1, frac)
     single = _sample_on(w, R, K, inp, 1, frac, threads=1)
-    # the attention part scales with heads and rows, the selection and append part does not
-    predicted = probe_sa + (probe - probe_sa) * w.H / 0.02
     out = {"unit": "tokens/s", "cores": _omp_threads(), "kind": "oracle", "cpu_model": _cpu_model(),
            "sample_all_cores": sample_all, "single_thread": single}
-    if predicted <= full_limit_s:
+    if force_full or predicted <= full_limit_s:
         took, _ = _oracle_step(w, R, K, inp, w.H, 1.0)
-        out.update(value=w.B * w.N / took, seconds=took, sample=_sample_text(w, R, w.H, 1.0))
+        out.update(value=w.B * w.N / took, seconds=took, sample=_sample_text(w, R, w.H, 1.0),
+                   predicted_seconds=predicted)
     else:
         out.update(value=sample_all.get("value"), seconds=sample_all.get("seconds"),
                    sample=sample_all.get("sample", "") + f"; the complete step was predicted at {predicted:.0f} s "
@@ -971,6 +975,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-recovery", action="store_true", help="skip the column-recovery analysis")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-full-step", action="store_true",
+                    help="time the complete oracle step in cpu_baseline however long it takes")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle work for --impl reference")
     args = ap.parse_args()
     if args.warmup < 3:
