@@ -61,6 +61,7 @@ def lib():
         _lib.orc_attention.argtypes = [ctypes.c_int, I64, I64, I64, I64, I64, I64, P, P,
                                        P, P, P, P, P, I64, P, P, P, P, P, P, P]
         _lib.orc_softmax_attention.argtypes = [P, P, P, I64, I64, I64, I64, P, P]
+        _lib.orc_round_bf16.argtypes = [P, I64, P]
         if hasattr(_lib, "orc_set_threads"):   # timing control; absent from older builds
             _lib.orc_set_threads.argtypes = [ctypes.c_int]
             _lib.orc_get_threads.restype = ctypes.c_int
@@ -103,6 +104,21 @@ def bf16_to_f32(h: int) -> float:
 
 def f32_to_bf16(x: float) -> int:
     return lib().orc_f32_to_bf16(x)
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round float64 values to bf16 bit patterns, nearest even, in one step
+    (reading R9 of the C file)."""
+    a = _c(np.asarray(x, dtype=np.float64), np.float64)
+    out = np.empty(a.shape, np.uint16)
+    lib().orc_round_bf16(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def bf16_values(h) -> np.ndarray:
+    """float64 values of bf16 bit patterns (exact)."""
+    u = np.asarray(bits(h), dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
 
 
 def f16_to_f32(h: int) -> float:

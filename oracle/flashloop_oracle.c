@@ -48,6 +48,14 @@
  *       [-127, 127], zero scale -> zero codes; the base value is scale * code.
  *   R7  R = ceil(r N), K = ceil(k N), clamped to [1, N]; ties in every
  *       ranking go to the lower index; index lists ascending.
+ *   R9  synthetic looped block around the step (the survey's next steps; the
+ *       page says a later loop recomputes only its active tokens but gives
+ *       no block): with x = H_{l-1}[i], q, k, v = bf16(x W_q), bf16(x W_k),
+ *       bf16(x W_v); O from the loop's attention; y = bf16(x + bf16(O) W_o);
+ *       u = bf16(relu(y W_1)); H_l[i] = bf16(y + u W_2). Every output is the
+ *       exact value (products summed in double) rounded ONCE to bf16, nearest
+ *       even (orc_round_bf16 below); tokens a lazy loop leaves inactive keep
+ *       H_l[i] = H_{l-1}[i]. No normalisation layers.
  * Build with gcc -O2 -ffp-contract=off so every fp32 expression rounds
  * exactly as written. Attention and norms accumulate in double.
  */
@@ -540,6 +548,35 @@ void orc_softmax_attention(const uint16_t *q, const uint16_t *k, const uint16_t 
             }
             free(lg);
         }
+    }
+}
+
+/* Round doubles to bfloat16 (8 significant bits, exponent range of binary32),
+ * to nearest, ties to even, in ONE step (no intermediate binary32 rounding,
+ * which could round a value just above a bf16 tie down to the tie and then to
+ * even). Overflow gives infinity; NaN gives the canonical quiet NaN. */
+void orc_round_bf16(const double *x, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i) {
+        const double v = x[i];
+        double r;
+        if (isnan(v)) {
+            out[i] = 0x7FC0u;
+            continue;
+        }
+        if (v == 0.0 || isinf(v)) {
+            r = v;
+        } else if (fabs(v) < ldexp(1.0, -126)) {   /* subnormal range: spacing 2^-133 */
+            r = ldexp(rint(ldexp(v, 133)), -133);
+        } else {
+            int e;
+            const double m = frexp(v, &e);        /* v = m 2^e, 0.5 <= |m| < 1 */
+            r = ldexp(rint(ldexp(m, 8)), e - 8);  /* 8 significant bits */
+            if (fabs(r) >= ldexp(1.0, 128)) r = v > 0 ? INFINITY : -INFINITY;
+        }
+        const float f = (float)r;                 /* exact: every bf16 value is a binary32 value */
+        uint32_t u;
+        memcpy(&u, &f, 4);
+        out[i] = (uint16_t)(u >> 16);
     }
 }
 

@@ -38,7 +38,11 @@ EPS_LO = 0.01
 SEED_BASE = 0xF1A51000
 
 _TAGS = {"H": 1, "Q": 2, "K": 3, "V": 4, "heavy": 5, "carry": 6, "fresh": 7,
-         "dq": 8, "dk": 9, "dv": 10, "ctx": 11}
+         "dq": 8, "dk": 9, "dv": 10, "ctx": 11, "wqkv": 12, "wo": 13, "w1": 14, "w2": 15}
+
+# Synthetic looped block: MLP width and the gains of its random weights.
+BLOCK_FF_MULT = 4
+BLOCK_GAINS = {"wqkv": 1.0, "wo": 0.5, "w1": 1.0, "w2": 0.5}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -205,3 +209,27 @@ def decode_token_loops(w: Workload, device="cpu") -> Iterator[Dict[str, torch.Te
         cur = {n: _drift(cur[n], eps, _gen(w, l, t, device))
                for n, t in (("q", "dq"), ("k", "dk"), ("v", "dv"))}
         yield dict(cur, loop=l)
+
+
+def block_weights(w: Workload, F: Optional[int] = None, device="cpu"):
+    """Random weights of the synthetic looped block, each stored transposed
+    [out features, in features] as bf16: (w_qkv [3D, D], w_o [D, D],
+    w_1 [F, D], w_2 [D, F]), entries N(0, (gain / sqrt(in features))^2)
+    rounded RNE to bf16 (F = 4 D by default). The gains below one on the two
+    projections back into the residual stream keep the state's scale moderate
+    over the loops."""
+    D = w.D
+    F = BLOCK_FF_MULT * D if F is None else F
+    shapes = {"wqkv": (3 * D, D), "wo": (D, D), "w1": (F, D), "w2": (D, F)}
+    out = []
+    for tag in ("wqkv", "wo", "w1", "w2"):
+        n_out, n_in = shapes[tag]
+        z = torch.randn((n_out, n_in), generator=_gen(w, 0, tag, device), device=device, dtype=torch.float32)
+        out.append((z * (BLOCK_GAINS[tag] / math.sqrt(n_in))).to(torch.bfloat16))
+    return tuple(out)
+
+
+def block_input(w: Workload, device="cpu") -> torch.Tensor:
+    """H_0 of the synthetic looped block: [B, N, D], N(0,1) rounded to bf16
+    (the same draw as loop 1's H of the prefill workload)."""
+    return normal_bf16((w.B, w.N, w.D), _gen(w, 1, "H", device), device)
