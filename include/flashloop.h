@@ -209,11 +209,79 @@ typedef struct {
     int32_t *seq_exit;
 } flashloop_step_args_t;
 
+/* Weights of the synthetic looped block (one weight-shared block applied every
+ * loop; random weights stand in for a trained looped model). Each matrix is
+ * stored transposed, [out features, in features] row-major bf16, so that the
+ * weights of one output feature are contiguous:
+ *   w_qkv [3D, D]  rows 0..D-1 give q, D..2D-1 k, 2D..3D-1 v, each in
+ *                  (head, dim) order, the layout of a [B, N, H, d] row
+ *   w_o   [D, D]   attention output projection
+ *   w_1   [F, D]   MLP up projection (ReLU)
+ *   w_2   [D, F]   MLP down projection
+ * D = H*d and F must be multiples of 256. */
+typedef struct {
+    const uint16_t *w_qkv, *w_o, *w_1, *w_2;
+    int32_t F;
+} flashloop_block_weights_t;
+
+/* One loop l of the synthetic looped block around the lazy step (rit.work
+ * page "FlashLoop: Fast and Memory-Efficient Looped Transformers via Lazy
+ * Updates", section "FlashLoop combines three kinds of saving": a later loop
+ * recomputes only its active tokens, the others reuse their state). With
+ * x_i = H_{l-1}[i] (bf16) and bf16() = round to nearest even:
+ *   q_i, k_i, v_i = bf16(x_i W_q), bf16(x_i W_k), bf16(x_i W_v)
+ *   (the loop's attention as in flashloop_loop_step, giving O_i)
+ *   y_i = bf16(x_i + bf16(O_i) W_o)
+ *   u_i = bf16(relu(y_i W_1))
+ *   H_l[i] = bf16(y_i + u_i W_2)
+ * for every token i of a dense loop, and only for the active tokens i of a
+ * lazy loop, whose other tokens keep H_l[i] = H_{l-1}[i]. Products accumulate
+ * in fp32. The active tokens of a lazy loop are the top-R of the change
+ * score on (h_prev = H_{l-2}, h_cur = H_{l-1}) as in flashloop_select_tokens;
+ * its keys the top-K of c as in flashloop_select_keys (key_rank chooses the
+ * ranking as in flashloop_step_args_t). */
+typedef struct {
+    int32_t loop;
+    const uint16_t *h_prev;   /* [B, N, D] H_{l-2} (lazy loops) */
+    const uint16_t *h_cur;    /* [B, N, D] H_{l-1}, the loop's input */
+    /* [B, N, D] out: H_l. In a lazy loop only the rows that can differ from
+     * h_cur are written: on entry every row not listed in stale_idx must
+     * already hold h_cur's value. stale_idx [B, n_stale] (NULL: every row is
+     * stale and is copied from h_cur) is typically the previous lazy loop's
+     * active_idx when h_out is the buffer of h_prev (buffers then alternate:
+     * the next loop's h_prev is this h_cur and its h_out this h_cur's buffer).
+     * h_out may be h_prev; it must not be h_cur. Dense loops write every row. */
+    uint16_t *h_out;
+    const int32_t *stale_idx;
+    int32_t n_stale;
+    uint16_t *q_hat;          /* state, as in flashloop_attn_args_t */
+    float *o;
+    float *z;
+    float *c;                 /* [B, H, n_keys] */
+    flashloop_kv_cache_t *cache;
+    int32_t *active_idx;      /* [B, R] out (in with force_selection) (lazy loops) */
+    int32_t *key_idx;         /* [B, H, K] out (in with force_selection) (lazy loops) */
+    int32_t force_selection;  /* 1: active_idx and key_idx are inputs, no selection runs */
+    int32_t key_rank;         /* flashloop_key_rank_t */
+    float *scores;            /* [B, N] out, or NULL */
+    const flashloop_block_weights_t *weights;
+    /* [B, N, H, d] bf16 each, out, or NULL (then they live in the workspace):
+     * the loop's q, k, v (a lazy loop writes the active tokens' rows only) */
+    uint16_t *q, *k, *v;
+    void *workspace;          /* flashloop_block_workspace_bytes(dims, F), 256-byte aligned */
+    size_t workspace_bytes;
+} flashloop_block_args_t;
+
 /* ---- sizes and set-up ------------------------------------------------- */
 
 /* Bytes of workspace every call below needs for these dims (prefill and
  * decode). Returns 0 for invalid dims. */
 size_t flashloop_workspace_bytes(const flashloop_dims_t *dims);
+
+/* Bytes of workspace flashloop_block_loop needs for these dims and MLP
+ * width F (the step's workspace plus the block's q/k/v and row buffers).
+ * Returns 0 for invalid dims or F. */
+size_t flashloop_block_workspace_bytes(const flashloop_dims_t *dims, int32_t F);
 
 /* Bytes of the single device buffer that holds the whole KV cache. */
 size_t flashloop_kv_cache_bytes(const flashloop_dims_t *dims);
@@ -323,6 +391,29 @@ flashloop_status_t flashloop_lazy_attention(const flashloop_attn_args_t *args, f
  * enqueues kernels and memsets on `stream`. */
 flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *args, flashloop_stream_t stream);
 
+/* bf16 GEMM on the tcgen05 tensor cores, the projections of the synthetic
+ * looped block: for every row m < M,
+ *   C[m, :] = act(A[m, :] W^T + residual[m, :])   act = ReLU if relu else identity,
+ * A [M, K] bf16, w_t = W^T [N, K] bf16, residual [M, N] bf16 or NULL, fp32
+ * accumulation, the residual added in fp32, then one round to bf16 (nearest
+ * even). Columns [s*N/n_split, (s+1)*N/n_split) go to output c[s]
+ * (c: a host array of n_split device pointers), whose rows are N/n_split
+ * elements long. Row m goes to output row m, or with c_rows [M] (device) to
+ * row (m / rows_per_seq) * seq_rows + c_rows[m] (a scatter to token rows of
+ * sequences of seq_rows rows; M % rows_per_seq == 0). An index outside
+ * [0, seq_rows) stores nothing for that row and sets the device status word
+ * (flashloop_device_status) to 0x101. Requires K % 64 == 0, 1 <= n_split <= 3,
+ * N % (256 * n_split) == 0, 16-byte aligned pointers. M = 0 enqueues nothing. */
+flashloop_status_t flashloop_gemm(const uint16_t *a, int32_t M, int32_t K, const uint16_t *w_t, int32_t N,
+                                  const uint16_t *residual, int32_t relu, uint16_t *const *c, int32_t n_split,
+                                  const int32_t *c_rows, int32_t rows_per_seq, int32_t seq_rows,
+                                  flashloop_stream_t stream);
+
+/* One loop of the synthetic looped block, see flashloop_block_args_t.
+ * Prefill only (every token of the cache's n_tokens is a row); no early exit.
+ * Graph-capturable like flashloop_loop_step. */
+flashloop_status_t flashloop_block_loop(const flashloop_block_args_t *args, flashloop_stream_t stream);
+
 /* ---- diagnostics -------------------------------------------------------- */
 
 /* Name of a status code ("ok", "invalid argument", ...), or "unknown status"
@@ -335,8 +426,11 @@ const char *flashloop_status_string(flashloop_status_t status);
  * library: do not free it. Empty before the thread's first failure. */
 const char *flashloop_last_error(void);
 
-/* Reads and clears the device-side failure word that kernels set when a
- * bounded wait gives up (0 = none). SYNCHRONISES the current device. */
+/* Reads and clears the device-side failure word (0 = none) that kernels set
+ * when a bounded wait gives up: codes below 0x100 come from the attention
+ * kernel, 0x100 from the GEMM, 0x101 is the GEMM's out-of-range output row
+ * (the attention's word is reported first when both are set; both are
+ * cleared). SYNCHRONISES the current device. */
 flashloop_status_t flashloop_device_status(int32_t *word);
 
 /* Sets the limit, in ns, of the bounded waits inside the tensor-core

@@ -11,6 +11,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -623,6 +624,81 @@ static flashloop_status_t lazy_attention_impl(const flashloop_attn_args_t *a, fl
 }
 }  // namespace fl
 
+namespace fl {
+// The selection and cache half of a lazy prefill loop, shared by the fused
+// step and the synthetic block: the key selection (on a side stream, forked
+// from and joined back to `stream`), the token selection, then `project` (the
+// block's projections of the active rows; NULL for the step, whose K/V exist
+// already), then the delta append of K/V. forced: active_idx and key_idx are
+// inputs and neither selection runs.
+struct LazyFront {
+    flashloop_kv_cache_t *c;
+    int loop, n;
+    const uint16_t *h_prev, *h_cur;
+    float *scores;
+    int32_t *active_idx, *key_idx;
+    const float *col;
+    int key_rank;
+    bool forced;
+    float exit_threshold;
+    int32_t *seq_exit;
+    const uint16_t *k, *v;
+};
+
+static flashloop_status_t lazy_front(const LazyFront &f, const std::function<flashloop_status_t()> &project,
+                                     flashloop_stream_t stream) {
+    flashloop_kv_cache_t *c = f.c;
+    const flashloop_dims_t &dm = c->dims;
+    flashloop_status_t st = FLASHLOOP_OK;
+    if (f.key_rank != FLASHLOOP_KEYS_BY_MASS && f.key_rank != FLASHLOOP_KEYS_BY_MASS_PER_ROW)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad key_rank %d", f.key_rank);
+    if (!f.forced && (!aligned16(f.h_prev) || !aligned16(f.h_cur) || (dm.H * dm.d) % 8))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "hidden states must be 16-byte aligned rows");
+    {   // this loop's delta layer starts empty; cleared first so that the append
+        // kernel follows the token selection kernel directly
+        const int m = f.loop - dm.T_dense - 1;
+        cudaError_t e = cudaMemsetAsync(c->slot[m], 0xFF, (size_t)dm.B * dm.N_cap * 4, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(slot)");
+    }
+    // The key columns depend only on the previous loop's column mass, so their
+    // selection runs on a side stream while the token selection, projections
+    // and K/V delta append run on the caller's; the attention waits for both.
+    SideStream *ss = f.forced ? nullptr : side_stream();
+    std::unique_lock<std::mutex> side_lock;
+    flashloop_stream_t key_stream = stream;
+    if (ss) {
+        side_lock = std::unique_lock<std::mutex>(ss->mu);
+        cudaError_t e = cudaEventRecord(ss->fork, static_cast<cudaStream_t>(stream));
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "fork of the key selection");
+        key_stream = ss->s;
+    }
+    if (!f.forced)
+        st = select_keys_impl(f.col, dm.B, dm.H, f.n, dm.K, f.key_rank == FLASHLOOP_KEYS_BY_MASS_PER_ROW ? f.n : 0,
+                              f.key_idx, key_stream);
+    if (st == FLASHLOOP_OK && !f.forced) {
+        // token selection; with exit flags, the top-k also flags sequences whose
+        // largest change score is below the threshold (sticky)
+        const bool upd = f.seq_exit && f.exit_threshold > 0.f;
+        cudaError_t e = launch_token_scores(f.h_prev, f.h_cur, dm.B, f.n, dm.H * dm.d, f.scores, stream);
+        if (e == cudaSuccess)
+            e = launch_topk_rows(f.scores, dm.B, f.n, dm.R, f.active_idx, stream, "topk_tokens", 0,
+                                 upd ? f.exit_threshold : 0.f, upd ? f.seq_exit : nullptr);
+        if (e != cudaSuccess) st = cuda_fail(e, "token selection");
+    }
+    if (st == FLASHLOOP_OK && project) st = project();
+    if (st == FLASHLOOP_OK)
+        st = delta_append_impl(c, f.loop, f.k, f.v, 1, f.active_idx, dm.R, 0, true, stream, f.seq_exit);
+    if (ss) {   // join (also on failure, so that the caller's stream is never left forked)
+        cudaError_t e = cudaEventRecord(ss->join, ss->s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), ss->join, 0);
+        side_lock.unlock();
+        if (e != cudaSuccess && st == FLASHLOOP_OK) return cuda_fail(e, "join of the key selection");
+    }
+    return st;
+}
+}  // namespace fl
+
 flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop_stream_t stream) {
     if (!a) return set_error(FLASHLOOP_ERR_INVALID_ARG, "args is NULL");
     flashloop_status_t st = check_cache(a->cache);
@@ -689,60 +765,184 @@ flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop
     }
     if (!a->h_prev || !a->h_cur || !a->active_idx || !a->key_idx)
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "lazy loop needs h_prev, h_cur, active_idx and key_idx");
-    float *scores = a->scores ? a->scores : reinterpret_cast<float *>(ws + W.scores);
-    {   // this loop's delta layer starts empty; cleared first so that the append
-        // kernel follows the token selection kernel directly
-        const int m = l - dm.T_dense - 1;
-        cudaError_t e = cudaMemsetAsync(c->slot[m], 0xFF, (size_t)dm.B * dm.N_cap * 4, static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(slot)");
-    }
-    // The key columns depend only on the previous loop's column mass, so their
-    // selection runs on a side stream while the token selection and the K/V
-    // delta append run on the caller's; the attention waits for both.
-    SideStream *ss = side_stream();
-    std::unique_lock<std::mutex> side_lock;
-    flashloop_stream_t key_stream = stream;
-    if (ss) {
-        side_lock = std::unique_lock<std::mutex>(ss->mu);
-        cudaError_t e = cudaEventRecord(ss->fork, static_cast<cudaStream_t>(stream));
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
-        if (e != cudaSuccess) return cuda_fail(e, "fork of the key selection");
-        key_stream = ss->s;
-    }
-    if (a->key_rank != FLASHLOOP_KEYS_BY_MASS && a->key_rank != FLASHLOOP_KEYS_BY_MASS_PER_ROW)
-        st = set_error(FLASHLOOP_ERR_INVALID_ARG, "bad key_rank %d", a->key_rank);
-    else
-        st = fl::select_keys_impl(a->c, dm.B, dm.H, n, dm.K, a->key_rank == FLASHLOOP_KEYS_BY_MASS_PER_ROW ? n : 0,
-                                  a->key_idx, key_stream);
-    if (st == FLASHLOOP_OK)
-        {
-        // token selection; with exit flags, the top-k also flags sequences whose
-        // largest change score is below the threshold (sticky)
-        const bool upd = a->seq_exit && a->exit_threshold > 0.f;
-        if (st == FLASHLOOP_OK && (!aligned16(a->h_prev) || !aligned16(a->h_cur) || (dm.H * dm.d) % 8))
-            st = set_error(FLASHLOOP_ERR_INVALID_ARG, "hidden states must be 16-byte aligned rows");
-        if (st == FLASHLOOP_OK) {
-            cudaError_t e = launch_token_scores(a->h_prev, a->h_cur, dm.B, n, dm.H * dm.d, scores, stream);
-            if (e == cudaSuccess)
-                e = launch_topk_rows(scores, dm.B, n, dm.R, a->active_idx, stream, "topk_tokens", 0,
-                                     upd ? a->exit_threshold : 0.f, upd ? a->seq_exit : nullptr);
-            if (e != cudaSuccess) st = cuda_fail(e, "token selection");
-        }
-    }
-    if (st == FLASHLOOP_OK)
-        st = delta_append_impl(c, l, a->k, a->v, 1, a->active_idx, dm.R, 0, true, stream, a->seq_exit);
-    if (ss) {   // join (also on failure, so that the caller's stream is never left forked)
-        cudaError_t e = cudaEventRecord(ss->join, ss->s);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), ss->join, 0);
-        side_lock.unlock();
-        if (e != cudaSuccess && st == FLASHLOOP_OK) return cuda_fail(e, "join of the key selection");
-    }
+    LazyFront f;
+    f.c = c; f.loop = l; f.n = n;
+    f.h_prev = a->h_prev; f.h_cur = a->h_cur;
+    f.scores = a->scores ? a->scores : reinterpret_cast<float *>(ws + W.scores);
+    f.active_idx = a->active_idx; f.key_idx = a->key_idx; f.col = a->c;
+    f.key_rank = a->key_rank; f.forced = false;
+    f.exit_threshold = a->exit_threshold; f.seq_exit = a->seq_exit;
+    f.k = a->k; f.v = a->v;
+    st = lazy_front(f, nullptr, stream);
     if (st != FLASHLOOP_OK) return st;
     at.R = dm.R;
     at.row_pos = a->active_idx;
     at.K = dm.K;
     at.key_idx = a->key_idx;
     return fl::lazy_attention_impl(&at, stream, a->seq_exit);
+}
+
+namespace fl {
+static flashloop_status_t gemm_impl(const uint16_t *a, int M, int K, const uint16_t *w_t, int N, const uint16_t *residual,
+                                    int relu, uint16_t *const *c, int n_split, const int32_t *c_rows, int rows_per_seq,
+                                    int seq_rows, flashloop_stream_t stream) {
+    if (M < 0 || K < 64 || K % 64 || n_split < 1 || n_split > 3 || N < 256 * n_split || N % (256 * n_split))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG,
+                         "gemm sizes M=%d K=%d N=%d n_split=%d (K %% 64 == 0, N %% (256 n_split) == 0)", M, K, N, n_split);
+    if (!a || !w_t || !c) return set_error(FLASHLOOP_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(a) || !aligned16(w_t) || (residual && !aligned16(residual)))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "gemm operands must be 16-byte aligned");
+    for (int i = 0; i < n_split; ++i)
+        if (!c[i] || !aligned16(c[i])) return set_error(FLASHLOOP_ERR_INVALID_ARG, "output %d NULL or misaligned", i);
+    if (c_rows && (rows_per_seq < 1 || M % rows_per_seq || seq_rows < 1))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "scatter needs rows_per_seq >= 1 dividing M=%d and seq_rows >= 1", M);
+    if (M == 0) return FLASHLOOP_OK;
+    flashloop_status_t st = check_device();
+    if (st != FLASHLOOP_OK) return st;
+    const cudaError_t e = launch_gemm(a, M, K, w_t, N, residual, relu, c, n_split, (long long)(N / n_split), c_rows,
+                                      rows_per_seq, seq_rows, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gemm");
+    return FLASHLOOP_OK;
+}
+
+struct BlockWs {
+    size_t step, q, k, v, x, a, y, u, total;
+};
+
+// The step's workspace, then q/k/v in token rows, the gathered input rows x,
+// the attention outputs a (bf16), y and the MLP activations u.
+static BlockWs block_ws(const flashloop_dims_t *dm, int F) {
+    BlockWs w;
+    const size_t rows = (size_t)dm->B * dm->N_cap, D = (size_t)dm->H * dm->d;
+    size_t off = ws_layout(dm).total;
+    w.step = 0;
+    w.q = off; off += align_up(rows * D * 2);
+    w.k = off; off += align_up(rows * D * 2);
+    w.v = off; off += align_up(rows * D * 2);
+    w.x = off; off += align_up((size_t)dm->B * dm->R_cap * D * 2);
+    w.a = off; off += align_up(rows * D * 2);
+    w.y = off; off += align_up(rows * D * 2);
+    w.u = off; off += align_up(rows * (size_t)F * 2);
+    w.total = off;
+    return w;
+}
+
+static bool block_sizes_ok(const flashloop_dims_t &dm, int F) {
+    return (dm.H * dm.d) % 256 == 0 && F >= 256 && F % 256 == 0;
+}
+}  // namespace fl
+
+size_t flashloop_block_workspace_bytes(const flashloop_dims_t *dims, int32_t F) {
+    if (check_dims(dims) != FLASHLOOP_OK || !block_sizes_ok(*dims, F)) return 0;
+    return block_ws(dims, F).total;
+}
+
+flashloop_status_t flashloop_gemm(const uint16_t *a, int32_t M, int32_t K, const uint16_t *w_t, int32_t N,
+                                  const uint16_t *residual, int32_t relu, uint16_t *const *c, int32_t n_split,
+                                  const int32_t *c_rows, int32_t rows_per_seq, int32_t seq_rows,
+                                  flashloop_stream_t stream) {
+    return gemm_impl(a, M, K, w_t, N, residual, relu, c, n_split, c_rows, rows_per_seq, seq_rows, stream);
+}
+
+flashloop_status_t flashloop_block_loop(const flashloop_block_args_t *a, flashloop_stream_t stream) {
+    if (!a) return set_error(FLASHLOOP_ERR_INVALID_ARG, "args is NULL");
+    flashloop_status_t st = check_cache(a->cache);
+    if (st != FLASHLOOP_OK) return st;
+    flashloop_kv_cache_t *c = a->cache;
+    const flashloop_dims_t &dm = c->dims;
+    const int l = a->loop;
+    if (l < 1 || l > dm.T) return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad loop %d", l);
+    const flashloop_block_weights_t *wt = a->weights;
+    if (!wt || !wt->w_qkv || !wt->w_o || !wt->w_1 || !wt->w_2)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "block weights missing");
+    const int D = dm.H * dm.d, F = wt->F;
+    if (!block_sizes_ok(dm, F))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "block needs D=%d and F=%d multiples of 256", D, F);
+    const BlockWs BW = block_ws(&dm, F);
+    if (!a->workspace || a->workspace_bytes < BW.total || reinterpret_cast<uintptr_t>(a->workspace) % kAlign)
+        return set_error(FLASHLOOP_ERR_WORKSPACE, "block workspace needs %zu bytes, 256-byte aligned", BW.total);
+    const int n = c->n_tokens;
+    if (n < 1 || n > dm.N_cap) return set_error(FLASHLOOP_ERR_INVALID_ARG, "cache n_tokens=%d", n);
+    if (!a->h_cur || !a->h_out || a->h_out == a->h_cur || !aligned16(a->h_cur) || !aligned16(a->h_out))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "h_cur/h_out NULL, misaligned or the same buffer");
+    const bool dense = l <= dm.T_dense;
+    if (!dense && (!a->active_idx || !a->key_idx || (!a->force_selection && !a->h_prev)))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "lazy loop needs active_idx, key_idx and h_prev");
+    if (!dense && a->stale_idx && (a->n_stale < 0 || a->n_stale > n))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "n_stale=%d outside [0, %d]", a->n_stale, n);
+    uint8_t *ws = static_cast<uint8_t *>(a->workspace);
+    uint16_t *q = a->q ? a->q : reinterpret_cast<uint16_t *>(ws + BW.q),
+             *k = a->k ? a->k : reinterpret_cast<uint16_t *>(ws + BW.k),
+             *v = a->v ? a->v : reinterpret_cast<uint16_t *>(ws + BW.v), *xg = reinterpret_cast<uint16_t *>(ws + BW.x),
+             *ag = reinterpret_cast<uint16_t *>(ws + BW.a), *yg = reinterpret_cast<uint16_t *>(ws + BW.y),
+             *ug = reinterpret_cast<uint16_t *>(ws + BW.u);
+    uint16_t *qkv[3] = {q, k, v};
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "q/k/v outputs must be 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = check_device()) != FLASHLOOP_OK) return st;
+
+    flashloop_attn_args_t at;
+    memset(&at, 0, sizeof at);
+    at.loop = l;
+    at.n_keys = n;
+    at.n_state = n;
+    at.q = q; at.q_hat = a->q_hat; at.o = a->o; at.z = a->z; at.c = a->c;
+    at.cache = c;
+    at.workspace = a->workspace;
+    at.workspace_bytes = a->workspace_bytes;
+    at.mode = l == 1 ? FLASHLOOP_ATTN_FIRST_DENSE : dense ? FLASHLOOP_ATTN_DENSE : FLASHLOOP_ATTN_LAZY;
+
+    if (dense) {   // every token: x = H_{l-1}
+        const int M = dm.B * n;
+        if ((st = gemm_impl(a->h_cur, M, D, wt->w_qkv, 3 * D, nullptr, 0, qkv, 3, nullptr, 0, 0, stream)) != FLASHLOOP_OK)
+            return st;
+        if ((st = flashloop_kv_dense_store(c, l, k, v, 0, n, stream)) != FLASHLOOP_OK) return st;
+        at.R = n;
+        if ((st = lazy_attention_impl(&at, stream, nullptr)) != FLASHLOOP_OK) return st;
+        cudaError_t e = launch_gather_f32_to_bf16(a->o, dm.B, n, D, nullptr, n, ag, s);
+        if (e != cudaSuccess) return cuda_fail(e, "gather of the attention output");
+        if ((st = gemm_impl(ag, M, D, wt->w_o, D, a->h_cur, 0, &yg, 1, nullptr, 0, 0, stream)) != FLASHLOOP_OK) return st;
+        if ((st = gemm_impl(yg, M, D, wt->w_1, F, nullptr, 1, &ug, 1, nullptr, 0, 0, stream)) != FLASHLOOP_OK) return st;
+        uint16_t *ho = a->h_out;
+        return gemm_impl(ug, M, F, wt->w_2, D, yg, 0, &ho, 1, nullptr, 0, 0, stream);
+    }
+
+    // lazy: only the R active tokens of each sequence are recomputed
+    const int R = dm.R, M = dm.B * R;
+    LazyFront f;
+    f.c = c; f.loop = l; f.n = n;
+    f.h_prev = a->h_prev; f.h_cur = a->h_cur;
+    f.scores = a->scores ? a->scores : reinterpret_cast<float *>(ws + ws_layout(&dm).scores);
+    f.active_idx = a->active_idx; f.key_idx = a->key_idx; f.col = a->c;
+    f.key_rank = a->key_rank; f.forced = a->force_selection != 0;
+    f.exit_threshold = 0.f; f.seq_exit = nullptr;
+    f.k = k; f.v = v;
+    st = lazy_front(f, [&]() -> flashloop_status_t {
+        // x = H_{l-1}[A]; q, k, v of the active rows, scattered to their token rows
+        cudaError_t e = launch_gather_rows(a->h_cur, dm.B, n, D * 2, a->active_idx, R, xg, s);
+        if (e != cudaSuccess) return cuda_fail(e, "gather of the active rows");
+        return gemm_impl(xg, M, D, wt->w_qkv, 3 * D, nullptr, 0, qkv, 3, a->active_idx, R, n, stream);
+    }, stream);
+    if (st != FLASHLOOP_OK) return st;
+    at.R = R;
+    at.row_pos = a->active_idx;
+    at.K = dm.K;
+    at.key_idx = a->key_idx;
+    if ((st = lazy_attention_impl(&at, stream, nullptr)) != FLASHLOOP_OK) return st;
+    cudaError_t e = launch_gather_f32_to_bf16(a->o, dm.B, n, D, a->active_idx, R, ag, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gather of the attention output");
+    if ((st = gemm_impl(ag, M, D, wt->w_o, D, xg, 0, &yg, 1, nullptr, 0, 0, stream)) != FLASHLOOP_OK) return st;
+    if ((st = gemm_impl(yg, M, D, wt->w_1, F, nullptr, 1, &ug, 1, nullptr, 0, 0, stream)) != FLASHLOOP_OK) return st;
+    // h_out = h_cur outside the active rows: bring its stale rows up to date
+    // (after the token selection has read h_prev, which h_out may be)
+    if (a->stale_idx)
+        e = launch_copy_rows(a->h_cur, dm.B, n, D * 2, a->stale_idx, a->n_stale, a->h_out, s);
+    else
+        e = cudaMemcpyAsync(a->h_out, a->h_cur, (size_t)dm.B * n * D * 2, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "copy of the stale rows");
+    uint16_t *ho = a->h_out;
+    return gemm_impl(ug, M, F, wt->w_2, D, yg, 0, &ho, 1, a->active_idx, R, n, stream);
 }
 
 flashloop_status_t flashloop_set_wait_limit_ns(uint64_t ns) {
@@ -761,7 +961,8 @@ flashloop_status_t flashloop_device_status(int32_t *word) {
     if (!word) return set_error(FLASHLOOP_ERR_INVALID_ARG, "word is NULL");
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-    *word = tc_attention_read_error(true);
+    const int32_t tc = tc_attention_read_error(true), gm = gemm_read_error(true);
+    *word = tc ? tc : gm;
     return *word ? FLASHLOOP_ERR_DEVICE : FLASHLOOP_OK;
 }
 

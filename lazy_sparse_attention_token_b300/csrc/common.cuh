@@ -131,6 +131,19 @@ struct DecodeAttnParams {
     float *scratch;           // [B, H, R, K] x 2 logits
 };
 cudaError_t launch_decode_attention(const DecodeAttnParams &p, cudaStream_t s);
+// gemm.cu: C = act(A W^T + residual), bf16 in and out, fp32 accumulation (see the file).
+// c_rows (or NULL): A row m is written to row (m / rows_per_seq) * seq_rows + c_rows[m].
+cudaError_t launch_gemm(const uint16_t *a, int M, int K, const uint16_t *wt, int N, const uint16_t *residual, int relu,
+                        uint16_t *const *c, int n_split, long long c_ld, const int32_t *c_rows, int rows_per_seq,
+                        int seq_rows, cudaStream_t s);
+int32_t gemm_read_error(bool clear);
+// kvcache.cu: dst[b, idx[b, r], :] = src[b, idx[b, r], :] for rows of row_bytes (% 16 == 0).
+cudaError_t launch_copy_rows(const void *src, int B, int N, int row_bytes, const int32_t *idx, int R, void *dst,
+                             cudaStream_t s);
+// kvcache.cu: dst[b * R + r, :] = bf16_rne(src[b, idx[b, r], :]) for fp32 rows of `elems`
+// (idx NULL: rows r of src in order, R = rows per sequence).
+cudaError_t launch_gather_f32_to_bf16(const float *src, int B, int N, int elems, const int32_t *idx, int R,
+                                      uint16_t *dst, cudaStream_t s);
 
 // ---- device helpers -------------------------------------------------------
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }

@@ -36,6 +36,39 @@ gather_rows_kernel(const uint4 *__restrict__ src, int N, int vecs, const int32_t
     for (int v = threadIdx.x & 31; v < vecs; v += 32) d[v] = ldg_nc_v4(s + v);
 }
 
+// dst[b, idx[b, r], :] = src[b, idx[b, r], :]; one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(kCopyWarps * 32)
+copy_rows_kernel(const uint4 *__restrict__ src, int N, int vecs, const int32_t *__restrict__ idx, int R,
+                 long long rows, uint4 *__restrict__ dst) {
+    pdl_wait();
+    pdl_trigger();
+    const long long row = (long long)blockIdx.x * kCopyWarps + threadIdx.x / 32;
+    if (row >= rows) return;
+    const long long b = row / R;
+    const long long off = (b * N + __ldg(idx + row)) * (long long)vecs;
+    for (int v = threadIdx.x & 31; v < vecs; v += 32) dst[off + v] = __ldg(src + off + v);
+}
+
+// dst[b * R + r, :] = bf16_rne(src[b, idx[b, r], :]) (idx NULL: src row r): one
+// warp per row, 8 fp32 in, 8 bf16 (16 bytes) out per lane step.
+__global__ void __launch_bounds__(kCopyWarps * 32)
+gather_f32_bf16_kernel(const float *__restrict__ src, int N, int elems, const int32_t *__restrict__ idx, int R,
+                       long long rows, uint16_t *__restrict__ dst) {
+    pdl_wait();
+    pdl_trigger();
+    const long long row = (long long)blockIdx.x * kCopyWarps + threadIdx.x / 32;
+    if (row >= rows) return;
+    const long long b = row / R;
+    const int i = idx ? __ldg(idx + row) : (int)(row - b * R);
+    const float4 *s = reinterpret_cast<const float4 *>(src + (b * N + i) * (long long)elems);
+    uint4 *d = reinterpret_cast<uint4 *>(dst + row * (long long)elems);
+    for (int v = threadIdx.x & 31; v < elems / 8; v += 32) {
+        const float4 a = __ldg(s + 2 * v), c = __ldg(s + 2 * v + 1);
+        d[v] = make_uint4(pack_bf16x2_rn(a.x, a.y), pack_bf16x2_rn(a.z, a.w), pack_bf16x2_rn(c.x, c.y),
+                          pack_bf16x2_rn(c.z, c.w));
+    }
+}
+
 // dst[b, pos0 + r, :] = src[b, r, :] for r < n_rows.
 __global__ void __launch_bounds__(kCopyWarps * 32)
 store_rows_kernel(const uint4 *__restrict__ src, int n_rows, int vecs, uint4 *__restrict__ dst,
@@ -339,6 +372,33 @@ cudaError_t launch_gather_rows(const void *src, int B, int N, int row_bytes, con
         KernelTimer kt("gather", s);
         gather_rows_kernel<<<ceil_div(rows, kCopyWarps), kCopyWarps * 32, 0, s>>>(
         static_cast<const uint4 *>(src), N, row_bytes / 16, idx, R, rows, static_cast<uint4 *>(dst));
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_rows(const void *src, int B, int N, int row_bytes, const int32_t *idx, int R, void *dst,
+                             cudaStream_t s) {
+    const long long rows = (long long)B * R;
+    if (rows == 0) return cudaSuccess;
+    {
+        KernelTimer kt("copy_rows", s);
+        const cudaError_t e = launch_pdl(copy_rows_kernel, dim3(ceil_div(rows, kCopyWarps)), dim3(kCopyWarps * 32), 0,
+                                         s, static_cast<const uint4 *>(src), N, row_bytes / 16, idx, R, rows,
+                                         static_cast<uint4 *>(dst));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_f32_to_bf16(const float *src, int B, int N, int elems, const int32_t *idx, int R,
+                                      uint16_t *dst, cudaStream_t s) {
+    const long long rows = (long long)B * R;
+    if (rows == 0) return cudaSuccess;
+    {
+        KernelTimer kt("gather_f32_bf16", s);
+        const cudaError_t e = launch_pdl(gather_f32_bf16_kernel, dim3(ceil_div(rows, kCopyWarps)), dim3(kCopyWarps * 32),
+                                         0, s, src, N, elems, idx, R, rows, dst);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -58,6 +58,18 @@ class StepArgs(ctypes.Structure):
                 ("key_rank", I32), ("exit_threshold", ctypes.c_float), ("seq_exit", P)]
 
 
+class BlockWeights(ctypes.Structure):
+    _fields_ = [("w_qkv", P), ("w_o", P), ("w_1", P), ("w_2", P), ("F", I32)]
+
+
+class BlockArgs(ctypes.Structure):
+    _fields_ = [("loop", I32), ("h_prev", P), ("h_cur", P), ("h_out", P), ("stale_idx", P), ("n_stale", I32),
+                ("q_hat", P), ("o", P), ("z", P), ("c", P), ("cache", ctypes.POINTER(KVCache)),
+                ("active_idx", P), ("key_idx", P), ("force_selection", I32), ("key_rank", I32), ("scores", P),
+                ("weights", ctypes.POINTER(BlockWeights)), ("q", P), ("k", P), ("v", P),
+                ("workspace", P), ("workspace_bytes", SZ)]
+
+
 _lib = None
 
 EXPORTS = [
@@ -66,7 +78,8 @@ EXPORTS = [
     "flashloop_select_keys", "flashloop_reconstruct_keys", "flashloop_lazy_attention", "flashloop_loop_step",
     "flashloop_status_string", "flashloop_last_error", "flashloop_device_status", "flashloop_launch_count",
     "flashloop_timing_enable", "flashloop_timing_read", "flashloop_select_tokens_noalloc",
-    "flashloop_set_wait_limit_ns", "flashloop_select_keys_per_row",
+    "flashloop_set_wait_limit_ns", "flashloop_select_keys_per_row", "flashloop_block_workspace_bytes",
+    "flashloop_gemm", "flashloop_block_loop",
 ]
 KEYS_BY_MASS, KEYS_BY_MASS_PER_ROW = 0, 1
 WAIT_LIMIT_DEFAULT_NS = 1_000_000_000
@@ -94,6 +107,10 @@ def lib() -> ctypes.CDLL:
         L.flashloop_reconstruct_keys.argtypes = [ctypes.POINTER(KVCache), I32, P, I32, P, P, P, P, P]
         L.flashloop_lazy_attention.argtypes = [ctypes.POINTER(AttnArgs), P]
         L.flashloop_loop_step.argtypes = [ctypes.POINTER(StepArgs), P]
+        L.flashloop_block_workspace_bytes.restype = SZ
+        L.flashloop_block_workspace_bytes.argtypes = [ctypes.POINTER(Dims), I32]
+        L.flashloop_gemm.argtypes = [P, I32, I32, P, I32, P, I32, ctypes.POINTER(P), I32, P, I32, I32, P]
+        L.flashloop_block_loop.argtypes = [ctypes.POINTER(BlockArgs), P]
         L.flashloop_status_string.restype = ctypes.c_char_p
         L.flashloop_status_string.argtypes = [ctypes.c_int]
         L.flashloop_last_error.restype = ctypes.c_char_p
@@ -106,6 +123,7 @@ def lib() -> ctypes.CDLL:
                                             ctypes.POINTER(ctypes.c_int64), I32]
         for name in EXPORTS:
             if name not in ("flashloop_workspace_bytes", "flashloop_kv_cache_bytes", "flashloop_status_string",
+                            "flashloop_block_workspace_bytes",
                             "flashloop_last_error", "flashloop_launch_count", "flashloop_timing_read"):
                 getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -324,6 +342,54 @@ def flashloop_loop_step(cache: Cache, loop: int, q, k, v, q_hat, o, z, c, worksp
     a.workspace = _ptr(workspace)
     a.workspace_bytes = workspace.numel() * workspace.element_size()
     _check(lib().flashloop_loop_step(ctypes.byref(a), _stream(stream)), "flashloop_loop_step")
+
+
+def flashloop_gemm(a, w_t, c: Sequence[torch.Tensor], residual=None, relu: bool = False, c_rows=None,
+                   rows_per_seq: int = 0, seq_rows: int = 0, stream=None):
+    """C = act(a @ w_t.T + residual) into the outputs ``c`` (a column split
+    of N into len(c) parts), rows scattered by ``c_rows`` when given."""
+    M, K = a.shape
+    N = w_t.shape[0]
+    outs = (P * len(c))(*[_ptr(t) for t in c])
+    _check(lib().flashloop_gemm(_ptr(a), M, K, _ptr(w_t), N, _ptr(residual), int(relu), outs, len(c), _ptr(c_rows),
+                                rows_per_seq, seq_rows, _stream(stream)), "flashloop_gemm")
+
+
+def flashloop_block_workspace_bytes(dims: Dims, F: int) -> int:
+    return int(lib().flashloop_block_workspace_bytes(ctypes.byref(dims), F))
+
+
+def block_workspace_for(dims: Dims, F: int, device="cuda") -> torch.Tensor:
+    """A 256-byte aligned workspace of flashloop_block_workspace_bytes(dims, F)."""
+    n = flashloop_block_workspace_bytes(dims, F)
+    if n == 0:
+        raise FlashLoopError(-1, "flashloop_block_workspace_bytes")
+    buf = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-buf.data_ptr()) % 256
+    return buf[off:off + n]
+
+
+def flashloop_block_loop(cache: Cache, loop: int, weights: Sequence[torch.Tensor], h_cur, h_out, q_hat, o, z, c,
+                         workspace, h_prev=None, stale_idx=None, active_idx=None, key_idx=None,
+                         force_selection: bool = False, key_rank: int = 0, scores=None, q=None, k=None, v=None,
+                         stream=None):
+    """One loop of the synthetic looped block; ``weights`` = (w_qkv, w_o, w_1, w_2), each [out, in] bf16."""
+    w_qkv, w_o, w_1, w_2 = weights
+    wt = BlockWeights(_ptr(w_qkv), _ptr(w_o), _ptr(w_1), _ptr(w_2), w_1.shape[0])
+    a = BlockArgs()
+    a.loop = loop
+    a.h_prev, a.h_cur, a.h_out = _ptr(h_prev), _ptr(h_cur), _ptr(h_out)
+    a.stale_idx = _ptr(stale_idx)
+    a.n_stale = 0 if stale_idx is None else stale_idx.shape[-1]
+    a.q_hat, a.o, a.z, a.c = _ptr(q_hat), _ptr(o), _ptr(z), _ptr(c)
+    a.cache = ctypes.pointer(cache.c)
+    a.active_idx, a.key_idx = _ptr(active_idx), _ptr(key_idx)
+    a.force_selection, a.key_rank, a.scores = int(force_selection), key_rank, _ptr(scores)
+    a.weights = ctypes.pointer(wt)
+    a.q, a.k, a.v = _ptr(q), _ptr(k), _ptr(v)
+    a.workspace = _ptr(workspace)
+    a.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().flashloop_block_loop(ctypes.byref(a), _stream(stream)), "flashloop_block_loop")
 
 
 def flashloop_device_status() -> int:

@@ -269,3 +269,48 @@ def test_wait_limit_can_only_be_shortened(L):
     assert b"exceeds the default" in L.flashloop_last_error()
     assert L.flashloop_set_wait_limit_ns(2 ** 63) == INVALID
     assert fl.flashloop_launch_count() == n0
+
+
+def test_gemm_rejects_bad_args(L):
+    """Shapes, pointers and alignment are checked on the host; the placeholder
+    pointers never reach a kernel."""
+    a, w, r = P(0x1000), P(0x2000), P(0x3000)
+    outs = (P * 3)(P(0x10000), P(0x20000), P(0x30000))
+    g = L.flashloop_gemm
+    assert g(a, 8, 96, w, 256, None, 0, outs, 1, None, 0, 0, None) == INVALID       # K % 64
+    assert g(a, 8, 64, w, 384, None, 0, outs, 1, None, 0, 0, None) == INVALID       # N % 256
+    assert g(a, 8, 64, w, 512, None, 0, outs, 3, None, 0, 0, None) == INVALID       # N % (256 * 3)
+    assert g(a, 8, 64, w, 256, None, 0, outs, 4, None, 0, 0, None) == INVALID       # n_split > 3
+    assert g(a, -1, 64, w, 256, None, 0, outs, 1, None, 0, 0, None) == INVALID      # M < 0
+    assert g(P(0x1008), 8, 64, w, 256, None, 0, outs, 1, None, 0, 0, None) == INVALID   # misaligned A
+    assert g(a, 8, 64, w, 256, P(0x3004), 0, outs, 1, None, 0, 0, None) == INVALID   # misaligned residual
+    assert g(a, 8, 64, w, 256, None, 0, None, 1, None, 0, 0, None) == INVALID       # no outputs
+    assert g(a, 8, 64, w, 256, None, 0, outs, 1, r, 3, 16, None) == INVALID         # 3 does not divide M
+    assert g(a, 0, 64, w, 256, None, 0, outs, 1, None, 0, 0, None) == OK            # M = 0: nothing to do
+
+
+def test_block_sizes_and_rejects(L):
+    dm = dims(H=4, d=64)                       # D = 256
+    ws = fl.flashloop_block_workspace_bytes(dm, 1024)
+    D, rows = 256, 1024
+    assert ws >= fl.flashloop_workspace_bytes(dm) + 5 * rows * D * 2 + rows * 1024 * 2 + 256 * D * 2
+    assert L.flashloop_block_workspace_bytes(ctypes.byref(dm), 1000) == 0      # F % 256
+    assert L.flashloop_block_workspace_bytes(ctypes.byref(dims(H=3, d=64)), 1024) == 0   # D % 256
+    assert L.flashloop_block_loop(None, None) == INVALID
+    c = fake_cache(dm)
+    wt = fl.BlockWeights(P(0x1000), P(0x2000), P(0x3000), P(0x4000), 1024)
+    a = fl.BlockArgs()
+    a.loop, a.cache, a.weights = 2, ctypes.pointer(c), ctypes.pointer(wt)
+    a.h_cur, a.h_out, a.h_prev = P(0x5000), P(0x5000), P(0x6000)
+    a.workspace, a.workspace_bytes = P(0x100000), ws
+    a.active_idx, a.key_idx = P(0x7000), P(0x8000)
+    assert L.flashloop_block_loop(ctypes.byref(a), None) == INVALID           # h_out == h_cur
+    a.h_out = P(0x9000)
+    a.workspace_bytes = ws - 1
+    assert L.flashloop_block_loop(ctypes.byref(a), None) == WORKSPACE
+    a.workspace_bytes = ws
+    wt.F = 1000
+    assert L.flashloop_block_loop(ctypes.byref(a), None) == INVALID           # F % 256
+    wt.F = 1024
+    a.h_prev = None
+    assert L.flashloop_block_loop(ctypes.byref(a), None) == INVALID           # lazy loop without h_prev
