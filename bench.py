@@ -483,10 +483,12 @@ def native(args, world, rank, local):
 
     e2e = None if args.no_e2e else e2e_leg(args, w, fl, cache, ws, loops, q_hat, o, z, c, act, keys, scores, lazy,
                                            dev, world)
-    recovery = variants = None
+    recovery = variants = block = None
     if not args.no_recovery and rank == 0:
         recovery = column_recovery_leg(w, fl, loops, dev)
         variants = cache_variants_leg(w, fl, loops, dev)
+    if not args.no_block and rank == 0 and w.D % 256 == 0:
+        block = block_leg(w, fl, dev)
     out = {
         "metric": metric_for(args.workload), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
@@ -500,7 +502,7 @@ def native(args, world, rank, local):
                    "active_tokens_per_s": w.B * R * args.steps * world / secs},
         "roofline": roofline, "step_roofline": step_roofline, "kernels": kernels, "gpu_launches": launches,
         "clocks": clk, "e2e": e2e, "kv_cache": kv_cache_accounting(fl, dims, w.B, w.N, w.H, w.d, w.T),
-        "column_recovery": recovery, "cache_variants": variants,
+        "column_recovery": recovery, "cache_variants": variants, "looped_block": block,
     }
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, R, K, state1, budget_s=args.cpu_budget, force_full=args.cpu_full_step)
@@ -690,6 +692,105 @@ def cache_variants_leg(w, fl, loops, dev, formats=((4, 16), (3, 16), (2, 16), (4
     return {"bf16_cache_per_loop_bytes": per_loop, "formats": out,
             "note": "stored_bytes: the base and the delta layers the lazy loops keep; with an int8 base the dense "
                     "loops' bf16 layers are working memory of those loops"}
+
+
+def block_gemm_flop(M, D, F):
+    """FLOP of the block's four projections on M rows: q/k/v (D -> 3D), the
+    attention output (D -> D), the MLP (D -> F -> D)."""
+    return 2 * M * D * (3 * D + D + F + F)
+
+
+def block_leg(w, fl, dev, reps=5):
+    """The synthetic looped block (seeded random weights, F = 4D) run as a
+    whole forward of the looped model: loops 1..T on this workload's tokens,
+    the projections and MLP of every lazy loop on its active rows only. The
+    same forward with every loop dense is timed beside it. Each timed forward
+    starts from the same H_0 (one device copy inside the timed region).
+    Timed as CUDA-graph replays with CUDA events; per-kernel durations from a
+    second pass with an event pair around every launch."""
+    R, K = synth.active_count(w), synth.key_count(w)
+    D, F = w.D, synth.BLOCK_FF_MULT * w.D
+    weights = [t.contiguous() for t in synth.block_weights(w, device=dev)]
+    h0 = synth.block_input(w, device=dev)
+    peaks, peak_kind = load_peaks()
+
+    def chain(T_dense):
+        dims = fl.make_dims(w.B, w.N, w.H, w.d, R, K, w.T, T_dense, R_cap=R)
+        cache = fl.Cache(dims, device=dev)
+        cache.n_tokens = w.N
+        ws = fl.block_workspace_for(dims, F, device=dev)
+        bufs = [torch.empty_like(h0), torch.empty_like(h0)]
+        q_hat = torch.zeros(w.B, w.N, w.H, w.d, dtype=torch.bfloat16, device=dev)
+        o = torch.zeros(w.B, w.N, w.H, w.d, dtype=torch.float32, device=dev)
+        z = torch.zeros(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+        c = torch.zeros(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+        act = {l: torch.empty(w.B, R, dtype=torch.int32, device=dev) for l in range(1, w.T + 1)}
+        keys = {l: torch.empty(w.B, w.H, K, dtype=torch.int32, device=dev) for l in range(1, w.T + 1)}
+        final = {}
+
+        def run():
+            bufs[0].copy_(h0)
+            cur, prev = 0, None
+            for l in range(1, w.T + 1):
+                out, lazy = 1 - cur, l > T_dense
+                fl.flashloop_block_loop(cache, l, weights, bufs[cur], bufs[out], q_hat, o, z, c, ws,
+                                        h_prev=bufs[out] if lazy else None, stale_idx=prev if lazy else None,
+                                        active_idx=act[l] if lazy else None, key_idx=keys[l] if lazy else None)
+                if lazy:
+                    prev = act[l]
+                cur = out
+            final["h"] = bufs[cur]
+
+        for _ in range(2):
+            run()
+        torch.cuda.synchronize()
+        assert fl.flashloop_device_status() == 0
+        finite = bool(torch.isfinite(final["h"].float()).all())
+        mode = "direct launches"
+        g = None
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                run()
+            g.replay()
+            torch.cuda.synchronize()
+            mode = "CUDA graph of the whole forward, replayed"
+        except Exception as exc:
+            g, mode = None, f"direct launches (graph capture failed: {str(exc)[:60]})"
+            torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        for _ in range(reps):
+            g.replay() if g is not None else run()
+        ev1.record()
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / reps
+        fl.flashloop_timing_read()
+        fl.flashloop_timing_enable(True)
+        run()
+        torch.cuda.synchronize()
+        fl.flashloop_timing_enable(False)
+        per = fl.flashloop_timing_read()
+        assert fl.flashloop_device_status() == 0
+        flop = sum(block_gemm_flop(w.B * (w.N if l <= T_dense else R), D, F) for l in range(1, w.T + 1))
+        gms, gn = per.get("gemm", (0.0, 0))
+        tf = flop / (gms / 1e3) / 1e12 if gms else None
+        tot = sum(v for v, _ in per.values())
+        del cache, ws
+        return {"ms_per_forward": ms, "tokens_per_s": w.B * w.N / (ms / 1e3), "launch": mode, "finite": finite,
+                "gemm": {"flop_per_forward": flop, "ms_per_forward": gms, "launches": gn, "achieved_tflops": tf,
+                         "frac_sustained": tf / peaks["bf16_tflops_sustained"] if tf and "bf16_tflops_sustained" in peaks
+                         else None,
+                         "frac_burst": tf / peaks["bf16_tflops"] if tf else None,
+                         "frac_nominal": tf / NOMINAL_PEAKS["bf16_tflops"] if tf else None},
+                "kernel_share": {k: v / tot for k, (v, _) in sorted(per.items(), key=lambda kv: -kv[1][0])}}
+
+    lazy = chain(w.T_dense)
+    dense = chain(w.T)
+    return {"model": f"one weight-shared block (QKV/O projections, attention, ReLU MLP F={F}) looped T={w.T} times, "
+                     f"seeded random weights",
+            "lazy": lazy, "all_dense": dense, "speedup": dense["ms_per_forward"] / lazy["ms_per_forward"],
+            "peak_source": peak_kind}
 
 
 def column_recovery_leg(w, fl, loops, dev, fractions=(0.05, 0.10, 0.20, 0.50)):
@@ -974,6 +1075,7 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of replayed CUDA graphs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-recovery", action="store_true", help="skip the column-recovery analysis")
+    ap.add_argument("--no-block", action="store_true", help="skip the synthetic looped block forward")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--cpu-full-step", action="store_true",
                     help="time the complete oracle step in cpu_baseline however long it takes")

@@ -8,4 +8,7 @@ from .workloads import (  # noqa: F401
     decode_context,
     decode_token_loops,
     normal_bf16,
+    BLOCK_FF_MULT,
+    block_weights,
+    block_input,
 )
