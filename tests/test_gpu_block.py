@@ -172,6 +172,23 @@ CONFIGS = {
     "tiny": dict(B=2, N=384, H=2, d=128, F=512, T=4, T_dense=1, R=96, K=77),
     "wide": dict(B=1, N=1024, H=16, d=128, F=8192, T=3, T_dense=1, R=160, K=103),
 }
+# the 8K prefill workload's shapes (B=1, N=8192, H=16, d=128, T=4, r=25%,
+# k=10%) with F = 4D; the attention state is compared on 4 seeded heads
+# (the first, the last and two drawn), everything else on all of them
+_W8 = synth.WORKLOADS["8k"]
+CONFIGS["8k"] = dict(B=_W8.B, N=_W8.N, H=_W8.H, d=_W8.d, F=synth.BLOCK_FF_MULT * _W8.D, T=_W8.T,
+                     T_dense=_W8.T_dense, R=synth.active_count(_W8), K=synth.key_count(_W8), heads=4)
+
+
+def _heads(cfg, seed=5):
+    """Heads on which the attention state is compared (all unless cfg["heads"])."""
+    H = cfg["H"]
+    n = cfg.get("heads")
+    if not n or n >= H:
+        return np.arange(H)
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(1, H - 1), size=n - 2, replace=False).tolist()
+    return np.array(sorted({0, H - 1, *mid}))
 
 
 def _weights(cfg, seed):
@@ -282,7 +299,7 @@ def test_block_chain_independent(name):
     assert fl.flashloop_device_status() == 0
 
 
-@pytest.mark.parametrize("name", ["tiny", "wide"])
+@pytest.mark.parametrize("name", ["tiny", "wide", "8k"])
 def test_block_loop_by_loop(name):
     # every loop with the GPU's own selections, each part against the oracle
     # started from the GPU's values before that part (the teacher forcing of
@@ -298,6 +315,9 @@ def test_block_loop_by_loop(name):
     g = GpuBlock(cfg, [_dev(t) for t in w], _dev(h0))
     qkv = [torch.zeros((B, N, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
     bi = np.arange(B)[:, None]
+    hs = _heads(cfg)
+    mask = np.zeros((B, H), bool)
+    mask[:, hs] = True
     for l in range(1, cfg["T"] + 1):
         before = g.state()
         oc = g.oracle_cache(l)
@@ -325,15 +345,16 @@ def test_block_loop_by_loop(name):
         assert_gemm(gotp, want, gemm_bound(x, wb[0]), f"{name}: q/k/v of loop {l}", D)
         # (2) the loop's step on the GPU's projections
         if A is None:
-            st_o = dense_loop(l, q_g, k_g, v_g, oc, before)
+            st_o = dense_loop(l, q_g, k_g, v_g, oc, before, bh_mask=mask)
         else:
-            _, _, _, st_o, lk, lv = lazy_loop(l, h_prev, h_cur, q_g, k_g, v_g, oc, before, R, K, A=A, S=S)
+            _, _, _, st_o, lk, lv = lazy_loop(l, h_prev, h_cur, q_g, k_g, v_g, oc, before, R, K, A=A, S=S,
+                                              bh_mask=mask)
             _check_layers(g.cache, l, lk, lv, oc, k_g, v_g, A, f"{name}: loop {l}")
         after = g.state()
-        assert_close(after.o, st_o.o, O_ATOL, O_RTOL, f"{name}: O after loop {l}")
-        assert_close(after.z, st_o.z, Z_ATOL, 0, f"{name}: Z after loop {l}")
-        assert_close(after.c, st_o.c, C_ATOL, C_RTOL, f"{name}: c after loop {l}")
-        assert np.array_equal(after.qhat, st_o.qhat), f"{name}: q_hat after loop {l}"
+        assert_close(after.o[:, :, hs], st_o.o[:, :, hs], O_ATOL, O_RTOL, f"{name}: O after loop {l}")
+        assert_close(after.z[:, hs], st_o.z[:, hs], Z_ATOL, 0, f"{name}: Z after loop {l}")
+        assert_close(after.c[:, hs], st_o.c[:, hs], C_ATOL, C_RTOL, f"{name}: c after loop {l}")
+        assert np.array_equal(after.qhat[:, :, hs], st_o.qhat[:, :, hs]), f"{name}: q_hat after loop {l}"
         # (3) the MLP on the GPU's attention output; untouched rows keep H_{l-1}
         a = oracle.round_bf16(after.o[bi, rows].astype(np.float64)).reshape(B, rows.shape[1], D)
         h_rows = ob.mlp(x, a, wb)
