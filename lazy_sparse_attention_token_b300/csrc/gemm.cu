@@ -11,15 +11,18 @@
 // bf16 result (round to nearest even) written to row c_rows[m] (or m) of one
 // of n_split outputs of N / n_split columns each.
 //
-// One CTA per 128 x 256 output tile: warp 0 streams K-slices of 64 elements of
-// A (128 rows) and W^T (256 rows) by TMA (128-byte swizzle) into a ring of
-// kStages slots; warp 1 allocates TMEM and one of its threads issues the
-// tcgen05.mma products (M 128, N 256, K 16, both operands K-major in shared
-// memory) into a 256-column fp32 accumulator; warps 2..5 (one per TMEM lane
-// quadrant) read it back 32 columns at a time, add the residual, apply the
-// activation and store bf16. Every mbarrier wait is bounded (one second); a
-// CTA that gives up records an error word, lets its own copies and MMAs land,
-// frees TMEM and exits.
+// A persistent kernel: one CTA per SM walks the 128 x 256 output tiles
+// (column tiles fastest, so CTAs running together share A rows in L2). Warp 0
+// streams K-slices of 64 elements of A (128 rows) and W^T (256 rows) by TMA
+// (128-byte swizzle) through a ring of kStages slots, across tile boundaries;
+// warp 1 allocates TMEM and one of its threads issues the tcgen05.mma products
+// (M 128, N 256, K 16, both operands K-major in shared memory) of each tile
+// into one of two 256-column fp32 accumulators; warps 2..5 (one per TMEM lane
+// quadrant) read a finished accumulator back 32 columns at a time, release it
+// to the next tile's products, add the residual, apply the activation and
+// store bf16, while the products of the next tile run. Every mbarrier wait is
+// bounded (one second); a CTA that gives up records an error word, lets its
+// own copies and MMAs land, frees TMEM and exits.
 #include <cudaTypedefs.h>
 #include <mutex>
 
@@ -40,7 +43,13 @@ constexpr int A_BYTES = GM * GK * 2;     // 16 KB
 constexpr int B_BYTES = GN * GK * 2;     // 32 KB
 constexpr int STAGE = A_BYTES + B_BYTES;
 constexpr int OFF_BAR = kStages * STAGE;
-enum : int { BAR_FULL = 0, BAR_EMPTY = kStages, BAR_ACC = 2 * kStages, BAR_DRAIN = BAR_ACC + 1, N_BARS = BAR_DRAIN + 1 };
+constexpr int kEpiWarps = 4;
+constexpr uint32_t kTmemCols = 2 * GN;   // two accumulators
+// FULL[s]/EMPTY[s]: ring slot s landed / free again; ACC_FULL[b]: accumulator b
+// holds a finished tile; ACC_EMPTY[b]: the epilogue has read it (one arrival
+// per epilogue warp).
+enum : int { BAR_FULL = 0, BAR_EMPTY = kStages, BAR_ACC_FULL = 2 * kStages, BAR_ACC_EMPTY = BAR_ACC_FULL + 2,
+             BAR_DRAIN = BAR_ACC_EMPTY + 2, N_BARS = BAR_DRAIN + 1 };
 constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr int SMEM = OFF_MISC + 16 + 1024;   // + room to align the base to 1024 bytes
 static_assert(SMEM <= 232448, "shared memory budget");
@@ -97,16 +106,16 @@ gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtens
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * GN, m0 = blockIdx.y * GM;
     const int n_k = p.K / GK;
+    const int tiles_n = p.N / GN, tiles = tiles_n * ((p.M + GM - 1) / GM);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < N_BARS; ++i) mbar_init(bar(i), 1u);
+        for (int i = 0; i < N_BARS; ++i) mbar_init(bar(i), (i == BAR_ACC_EMPTY || i == BAR_ACC_EMPTY + 1) ? kEpiWarps : 1u);
         misc[1] = 0;
         mbar_fence_init();
     }
     if (warp == 1) {
-        tmem_alloc(sbase + OFF_MISC, GN);
+        tmem_alloc(sbase + OFF_MISC, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -115,52 +124,65 @@ gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtens
     const uint32_t tmem = misc[0];
 
     if (warp == 0 && lane == 0) {
-        // ---- TMA producer ----
+        // ---- TMA producer: the K-slices of every tile of this CTA, through one ring ----
         prefetch_tmap(&tm_a);
         prefetch_tmap(&tm_b);
-        int issued = 0;
-        for (int kb = 0; kb < n_k; ++kb) {
-            const int s = kb % kStages, use = kb / kStages;
-            if (!gemm_wait(bar(BAR_EMPTY + s), (use & 1) ^ 1, abort_flag, false)) break;
-            const uint32_t dst = sbase + s * STAGE;
-            mbar_arrive_expect_tx(bar(BAR_FULL + s), STAGE);
-            tma_load_2d(dst, &tm_a, bar(BAR_FULL + s), kb * GK, m0);
-            tma_load_2d(dst + A_BYTES, &tm_b, bar(BAR_FULL + s), kb * GK, n0);
-            ++issued;
+        int it = 0;   // slices issued
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+            const int n0 = (tile % tiles_n) * GN, m0 = (tile / tiles_n) * GM;
+            for (int kb = 0; kb < n_k; ++kb, ++it) {
+                const int s = it % kStages, use = it / kStages;
+                if (!(ok = gemm_wait(bar(BAR_EMPTY + s), (use & 1) ^ 1, abort_flag, false))) break;
+                const uint32_t dst = sbase + s * STAGE;
+                mbar_arrive_expect_tx(bar(BAR_FULL + s), STAGE);
+                tma_load_2d(dst, &tm_a, bar(BAR_FULL + s), kb * GK, m0);
+                tma_load_2d(dst + A_BYTES, &tm_b, bar(BAR_FULL + s), kb * GK, n0);
+            }
         }
         if (*abort_flag)   // let copies already in flight land before the CTA exits
-            for (int q = max(0, issued - kStages); q < issued; ++q)
+            for (int q = max(0, it - kStages); q < it; ++q)
                 gemm_wait(bar(BAR_FULL + q % kStages), (q / kStages) & 1, abort_flag, true);
     } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer ----
+        // ---- MMA issuer: tile j of this CTA into accumulator j & 1 ----
         constexpr uint32_t idesc = idesc_bf16(GM, GN, false, false, false);
         bool ok = true;
-        for (int kb = 0; ok && kb < n_k; ++kb) {
-            const int s = kb % kStages;
-            if (!(ok = gemm_wait(bar(BAR_FULL + s), (kb / kStages) & 1, abort_flag, false))) break;
+        int it = 0, j = 0;
+        for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++j) {
+            const int ab = j & 1;
+            // the epilogue has read this accumulator's previous tile
+            if (!(ok = gemm_wait(bar(BAR_ACC_EMPTY + ab), ((j >> 1) & 1) ^ 1, abort_flag, false))) break;
             tc_fence_after();
-            const uint64_t da = smem_desc(sbase + s * STAGE, 16, 1024, 2);
-            const uint64_t db = smem_desc(sbase + s * STAGE + A_BYTES, 16, 1024, 2);
+            const uint32_t acc = tmem + (uint32_t)(ab * GN);
+            for (int kb = 0; kb < n_k; ++kb, ++it) {
+                const int s = it % kStages;
+                if (!(ok = gemm_wait(bar(BAR_FULL + s), (it / kStages) & 1, abort_flag, false))) break;
+                tc_fence_after();
+                const uint64_t da = smem_desc(sbase + s * STAGE, 16, 1024, 2);
+                const uint64_t db = smem_desc(sbase + s * STAGE + A_BYTES, 16, 1024, 2);
 #pragma unroll
-            for (int kk = 0; kk < GK / 16; ++kk)   // K = 16 per product: 32 bytes further along the atom
-                mma_bf16_ss(tmem, da + 2 * kk, db + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(bar(BAR_EMPTY + s));
+                for (int kk = 0; kk < GK / 16; ++kk)   // K = 16 per product: 32 bytes further along the atom
+                    mma_bf16_ss(acc, da + 2 * kk, db + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(BAR_EMPTY + s));
+            }
+            if (ok) mma_commit(bar(BAR_ACC_FULL + ab));
         }
-        if (ok) {
-            mma_commit(bar(BAR_ACC));
-        } else {   // drain whatever was issued before giving up
+        if (!ok) {   // drain whatever was issued before giving up
             mma_commit(bar(BAR_DRAIN));
             gemm_wait(bar(BAR_DRAIN), 0, abort_flag, true);
         }
     } else if (warp >= 2) {
         // ---- epilogue: warp w reads TMEM lane quadrant w % 4 (rows 32 (w % 4) ..) ----
         const int q = warp & 3;
-        const int r = q * 32 + lane, m = m0 + r;
-        bool row_ok = m < p.M;
-        const bool ok = __all_sync(0xffffffffu, gemm_wait(bar(BAR_ACC), 0, abort_flag, false));
-        if (ok) {
+        const int per = p.N / p.n_split;   // columns of each output (a multiple of GN)
+        int j = 0;
+        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++j) {
+            const int ab = j & 1;
+            const int n0 = (tile % tiles_n) * GN, m0 = (tile / tiles_n) * GM;
+            const int r = q * 32 + lane, m = m0 + r;
+            if (!__all_sync(0xffffffffu, gemm_wait(bar(BAR_ACC_FULL + ab), (j >> 1) & 1, abort_flag, false))) break;
             tc_fence_after();
-            const int per = p.N / p.n_split;              // columns of each output (a multiple of GN)
+            bool row_ok = m < p.M;
             const int out = n0 / per, nc = n0 - out * per;
             uint16_t *dst = nullptr;
             if (row_ok) {
@@ -176,11 +198,17 @@ gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtens
                 dst = p.c[out] + orow * p.c_ld + nc;
             }
             const uint16_t *res = row_ok && p.residual ? p.residual + (long long)m * p.N + n0 : nullptr;
+            const uint32_t acc = tmem + (uint32_t)(ab * GN) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
             for (int c = 0; c < GN / 32; ++c) {
                 float v[32];
-                tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + 32u * c, v);
+                tmem_ld_32x32b_x32(acc + 32u * c, v);
                 tmem_wait_ld();
+                if (c == GN / 32 - 1) {   // the accumulator is read: the next tile may use it
+                    tc_fence_before();
+                    __syncwarp();
+                    mbar_arrive_elected(bar(BAR_ACC_EMPTY + ab));
+                }
                 if (!row_ok) continue;
                 if (res) {
                     const uint4 *r4 = reinterpret_cast<const uint4 *>(res + 32 * c);
@@ -209,7 +237,7 @@ gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtens
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, GN);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -259,7 +287,13 @@ cudaError_t launch_gemm(const uint16_t *a, int M, int K, const uint16_t *wt, int
     p.residual = residual; p.c_rows = c_rows;
     p.rows_per_seq = rows_per_seq > 0 ? rows_per_seq : M; p.seq_rows = seq_rows;
     for (int i = 0; i < 3; ++i) p.c[i] = i < n_split ? c[i] : nullptr;
-    dim3 grid(N / GN, ceil_div(M, GM));
+    static int sms[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (sms[dev] == 0 && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
+    const long long tiles = (long long)(N / GN) * ceil_div(M, GM);
+    dim3 grid((unsigned)(tiles < sms[dev] ? tiles : sms[dev]));
     {
         KernelTimer kt("gemm", s);
         const cudaError_t e = launch_pdl(gemm_kernel, grid, dim3(kThreads), (size_t)SMEM, s, p, ma, mb);
