@@ -489,6 +489,12 @@ def native(args, world, rank, local):
         variants = cache_variants_leg(w, fl, loops, dev)
     if not args.no_block and rank == 0 and w.D % 256 == 0:
         block = block_leg(w, fl, dev)
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, R, K, state1, budget_s=args.cpu_budget, force_full=args.cpu_full_step)
+    del cache, ws, loops
+    torch.cuda.empty_cache()
+    others = (other_workloads_leg(args, world, rank, local)
+              if (not args.no_workloads and rank == 0 and args.workload == "32k") else None)
     out = {
         "metric": metric_for(args.workload), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
@@ -503,9 +509,10 @@ def native(args, world, rank, local):
         "roofline": roofline, "step_roofline": step_roofline, "kernels": kernels, "gpu_launches": launches,
         "clocks": clk, "e2e": e2e, "kv_cache": kv_cache_accounting(fl, dims, w.B, w.N, w.H, w.d, w.T),
         "column_recovery": recovery, "cache_variants": variants, "looped_block": block,
+        "other_workloads": others,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, R, K, state1, budget_s=args.cpu_budget, force_full=args.cpu_full_step)
+        out["cpu_baseline"] = cpu
     return out
 
 
@@ -637,6 +644,35 @@ def native_decode(args, world, rank, local):
         "roofline": roofline, "kernels": kernels, "gpu_launches": launches, "clocks": clk, "e2e": None,
         "kv_cache": kv_cache_accounting(fl, dims, w.B, Nk, w.H, w.d, w.T),
     }
+
+
+OTHER_WORKLOADS = (("tiny", 50, 5), ("8k", 50, 5), ("deep", 28, 14), ("decode", 6, 3))
+
+
+def other_workloads_leg(args, world, rank, local):
+    """The other configurations of the same step, short runs (steps, warm-ups as
+    listed), each measured like the main line (CUDA-graph replay, CUDA events,
+    clocks sampled in the timed region), without its e2e, oracle or analysis
+    legs. A summary per workload."""
+    import argparse as _ap
+    out = {}
+    for name, steps, warmup in OTHER_WORKLOADS:
+        sub = _ap.Namespace(**vars(args))
+        sub.workload, sub.steps, sub.warmup = name, steps, warmup
+        sub.no_e2e = sub.no_cpu_baseline = sub.no_recovery = sub.no_block = True
+        sub.no_workloads = True
+        d = native_decode(sub, world, rank, local) if name == "decode" else native(sub, world, rank, local)
+        rf = d["roofline"]
+        out[name] = {"config": d["config"]["workload"], "steps": steps, "warmup": warmup,
+                     "ms_per_step": d["ms_per_step"], "value": d["value"], "unit": d["unit"],
+                     "roofline": {"kernel": rf.get("kernel"), "bound": rf.get("bound"), "frac": rf.get("frac"),
+                                  "achieved": rf.get("achieved"), "unit": rf.get("unit")},
+                     "kernels": {k: {"ms_per_launch": v["ms_per_launch"], "frac": v.get("frac")}
+                                 for k, v in d["kernels"].items()},
+                     "clocks": d.get("clocks"), "launch": d["config"].get("launch")}
+        del d
+        torch.cuda.empty_cache()
+    return out
 
 
 def cache_variants_leg(w, fl, loops, dev, formats=((4, 16), (3, 16), (2, 16), (4, 8), (3, 8), (2, 8))):
@@ -1076,6 +1112,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-recovery", action="store_true", help="skip the column-recovery analysis")
     ap.add_argument("--no-block", action="store_true", help="skip the synthetic looped block forward")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the short runs of the other configurations (tiny, 8k, deep, decode)")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--cpu-full-step", action="store_true",
                     help="time the complete oracle step in cpu_baseline however long it takes")
