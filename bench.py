@@ -1039,13 +1039,16 @@ def cpu_baseline(w, R, K, gpu_state, budget_s=20.0, device=None, full_limit_s=60
     inp = _oracle_inputs(w, w.H, device or _input_device())
     qh, o, z, c = gpu_state
     inp.update(qh1=oracle.bits(qh.contiguous()), o1=o.cpu().numpy(), z1=z.cpu().numpy(), c1=c.cpu().numpy())
-    # size the sample: one head, a share of the rows that takes about budget_s / 4
-    probe, probe_sa = _oracle_step(w, R, K, inp, 1, 0.02)
-    probe2, probe2_sa = _oracle_step(w, R, K, inp, 1, 0.06)
-    per_row = max(0.0, ((probe2 - probe2_sa) - (probe - probe_sa)) / 0.04)      # one head, all rows
-    per_head = max(0.0, (probe - probe_sa) - 0.02 * per_row)                  # one head, no rows
+    # size the sample: one head, a share of the rows that takes about budget_s / 4. The
+    # probes take a quarter and a half of one head's rows, so that the difference that
+    # prices a row is large against the timing noise (small probes overestimated the
+    # complete 32K step fifteenfold)
+    probe, probe_sa = _oracle_step(w, R, K, inp, 1, 0.25)
+    probe2, probe2_sa = _oracle_step(w, R, K, inp, 1, 0.5)
+    per_row = max(0.0, ((probe2 - probe2_sa) - (probe - probe_sa)) / 0.25)      # one head, all rows
+    per_head = max(0.0, (probe - probe_sa) - 0.25 * per_row)                  # one head, no rows
     predicted = min(probe_sa, probe2_sa) + w.H * (per_head + per_row)
-    frac = float(min(1.0, max(0.02, 0.02 * (budget_s / 4) / max(probe, 1e-3))))
+    frac = float(min(1.0, max(0.02, 0.25 * (budget_s / 4) / max(probe, 1e-3))))
     sample_all = _sample_on(w, R, K, inp, 1, frac)
     single = _sample_on(w, R, K, inp, 1, frac, threads=1)
     out = {"unit": "tokens/s", "cores": _omp_threads(), "kind": "oracle", "cpu_model": _cpu_model(),
