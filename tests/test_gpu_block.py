@@ -231,7 +231,7 @@ class GpuBlock:
     def state(self):
         return OState(bits(self.st.q_hat), f32(self.st.o), f32(self.st.z), f32(self.st.c))
 
-    def run(self, l, forced=None, qkv=None):
+    def run(self, l, forced=None, qkv=None, key_rank=0):
         cfg = self.cfg
         B, N, H = cfg["B"], cfg["N"], cfg["H"]
         out = 1 - self.cur
@@ -247,7 +247,7 @@ class GpuBlock:
                                 self.ws, h_prev=self.buf[out] if lazy else None,
                                 stale_idx=self.prev_idx if lazy else None,
                                 active_idx=act if lazy else None, key_idx=keys if lazy else None,
-                                force_selection=forced is not None, scores=sc if lazy else None,
+                                force_selection=forced is not None, key_rank=key_rank, scores=sc if lazy else None,
                                 q=None if qkv is None else qkv[0], k=None if qkv is None else qkv[1],
                                 v=None if qkv is None else qkv[2])
         torch.cuda.synchronize()
@@ -299,8 +299,8 @@ def test_block_chain_independent(name):
     assert fl.flashloop_device_status() == 0
 
 
-@pytest.mark.parametrize("name", ["tiny", "wide", "8k"])
-def test_block_loop_by_loop(name):
+@pytest.mark.parametrize("name, key_rank", [("tiny", 0), ("tiny", 1), ("wide", 0), ("8k", 0)])
+def test_block_loop_by_loop(name, key_rank):
     # every loop with the GPU's own selections, each part against the oracle
     # started from the GPU's values before that part (the teacher forcing of
     # the workload tests): the projections of the loop's input rows, the
@@ -323,7 +323,7 @@ def test_block_loop_by_loop(name):
         oc = g.oracle_cache(l)
         h_prev = g.hs[-2] if l >= 2 else None
         h_cur = g.hs[-1]
-        got = g.run(l, qkv=qkv)
+        got = g.run(l, qkv=qkv, key_rank=key_rank)
         q_g, k_g, v_g = (bits(t) for t in qkv)
         A = S = None
         if got is not None:
@@ -331,12 +331,12 @@ def test_block_loop_by_loop(name):
             sc_o = oracle.token_scores(h_prev, h_cur)
             assert_close(scores, sc_o, 0, 1e-5, f"{name}: change scores of loop {l}")
             A_o = oracle.topk(sc_o, R)
-            S_o = oracle.topk(before.c.astype(np.float64), K)
+            col = before.c.astype(np.float64) if key_rank == 0 else oracle.key_scores_per_row(before.c, N)
+            S_o = oracle.topk(col, K)
             for b in range(B):
                 assert_selection(A[b], A_o[b], sc_o[b], f"{name}: active tokens of loop {l}, sequence {b}")
                 for h in range(H):
-                    assert_selection(S[b, h], S_o[b, h], before.c[b, h].astype(np.float64),
-                                     f"{name}: keys of loop {l}, sequence {b}, head {h}")
+                    assert_selection(S[b, h], S_o[b, h], col[b, h], f"{name}: keys of loop {l}, sequence {b}, head {h}")
         rows = np.tile(np.arange(N), (B, 1)) if A is None else A
         x = h_cur[bi, rows]
         # (1) projections of the loop's input rows
