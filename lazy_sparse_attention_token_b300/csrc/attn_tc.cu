@@ -371,6 +371,11 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         if (is_sm) {   // pass OLD reads qhat; the first dense loop starts with q
             load_query_tile<D>(smem + C::OFF_Q, first ? p.q : p.q_hat, st, b, h, p.H, p.n_state, rows, row0, A);
             fence_proxy_async_smem();
+            // the query tile is reloaded with q after pass OLD: fetch those rows into L2 now
+            if (!first && row_ok && wg * 64 < D) {
+                const uint16_t *qrow = p.q + (((long long)b * p.n_state + pos) * p.H + h) * D + wg * 64;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow));
+            }
             if (wg == 0) {   // per row, shared by the four groups: key count and old normaliser (log2 units)
                 row_cnt[r] = !row_ok ? 0 : cnt_min == cnt ? cnt : dense ? min(pos + 1, p.n_keys) : __ldg(RC + r);
                 row_zo[r] = !row_ok ? INFINITY : first ? 0.f : __ldg(p.z + bh * p.n_state + pos) * kLog2e;
