@@ -185,6 +185,11 @@ def test_reference_arm_prints_one_contract_line():
     assert j["impl"] == "reference" and j["value"] > 0 and j["unit"] == "tokens/s"
     assert j["n_gpus"] == 1 and j["steps"] == 1 and j["warmup"] == 3 and j["higher_is_better"] is True
     assert j["metric"] and j["config"]["workload"].startswith("tiny") and j["data"] == "synthetic"
+    # the same config object as the CUDA arm's line for this workload
+    import bench
+    import synth
+    w = synth.WORKLOADS["tiny"]
+    assert j["config"] == bench.bench_config(w, synth.active_count(w), synth.key_count(w), 1)
     cb = j["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == j["value"]
     # measured, not scaled: the line's time is the steps it ran
