@@ -250,7 +250,8 @@ typedef struct {
      * stale and is copied from h_cur) is typically the previous lazy loop's
      * active_idx when h_out is the buffer of h_prev (buffers then alternate:
      * the next loop's h_prev is this h_cur and its h_out this h_cur's buffer).
-     * h_out may be h_prev; it must not be h_cur. Dense loops write every row. */
+     * h_out may be h_prev; it must not be h_cur. Dense loops write every row.
+     * Indices outside [0, N) in stale_idx are skipped. */
     uint16_t *h_out;
     const int32_t *stale_idx;
     int32_t n_stale;
@@ -327,7 +328,8 @@ flashloop_status_t flashloop_select_tokens_noalloc(const uint16_t *h_prev, const
 /* Gather of selected rows into a dense buffer ("the selected data is
  * gathered into dense buffers"): dst[b, r, :] = src[b, idx[b, r], :].
  * src [B, N, row_bytes], idx [B, R] in [0, N), dst [B, R, row_bytes];
- * row_bytes % 16 == 0. */
+ * row_bytes % 16 == 0. A row whose index lies outside [0, N) is skipped
+ * (its dst row is left as it was). */
 flashloop_status_t flashloop_gather(const void *src, int32_t B, int32_t N, int32_t row_bytes,
                                     const int32_t *idx, int32_t R, void *dst,
                                     flashloop_stream_t stream);

@@ -31,6 +31,7 @@ gather_rows_kernel(const uint4 *__restrict__ src, int N, int vecs, const int32_t
     if (row >= rows) return;
     const long long b = row / R;
     const int i = __ldg(idx + row);
+    if ((unsigned)i >= (unsigned)N) return;   // outside the sequence: the row is not gathered
     const uint4 *s = src + (b * N + i) * (long long)vecs;
     uint4 *d = dst + row * (long long)vecs;
     for (int v = threadIdx.x & 31; v < vecs; v += 32) d[v] = ldg_nc_v4(s + v);
@@ -45,7 +46,9 @@ copy_rows_kernel(const uint4 *__restrict__ src, int N, int vecs, const int32_t *
     const long long row = (long long)blockIdx.x * kCopyWarps + threadIdx.x / 32;
     if (row >= rows) return;
     const long long b = row / R;
-    const long long off = (b * N + __ldg(idx + row)) * (long long)vecs;
+    const int i = __ldg(idx + row);
+    if ((unsigned)i >= (unsigned)N) return;   // outside the sequence: nothing to copy
+    const long long off = (b * N + i) * (long long)vecs;
     for (int v = threadIdx.x & 31; v < vecs; v += 32) dst[off + v] = __ldg(src + off + v);
 }
 
@@ -60,6 +63,7 @@ gather_f32_bf16_kernel(const float *__restrict__ src, int N, int elems, const in
     if (row >= rows) return;
     const long long b = row / R;
     const int i = idx ? __ldg(idx + row) : (int)(row - b * R);
+    if ((unsigned)i >= (unsigned)N) return;   // outside the sequence: the row is not gathered
     const float4 *s = reinterpret_cast<const float4 *>(src + (b * N + i) * (long long)elems);
     uint4 *d = reinterpret_cast<uint4 *>(dst + row * (long long)elems);
     for (int v = threadIdx.x & 31; v < elems / 8; v += 32) {

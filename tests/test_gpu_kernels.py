@@ -93,6 +93,20 @@ def test_gather_is_exact(row_shape, dtype):
     assert torch.equal(out, ref)
 
 
+def test_gather_skips_rows_outside_the_sequence():
+    B, N, R = 2, 100, 5
+    src = torch.randn((B, N, 8), generator=gen(7), device="cuda")
+    idx = torch.tensor([[0, 3, 100, 50, 99], [-1, 2, 4, 1 << 30, 7]], dtype=torch.int32, device="cuda")
+    out = torch.full((B, R, 8), 7.0, device="cuda")
+    fl.flashloop_gather(src, idx, dst=out)
+    torch.cuda.synchronize()
+    for b in range(B):
+        for r in range(R):
+            i = int(idx[b, r])
+            want = src[b, i] if 0 <= i < N else torch.full((8,), 7.0, device="cuda")
+            assert torch.equal(out[b, r], want), (b, r)
+
+
 # --------------------------------------------------------------------------
 # base + int4 delta cache
 
