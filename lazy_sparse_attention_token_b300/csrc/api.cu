@@ -652,6 +652,9 @@ static flashloop_status_t lazy_front(const LazyFront &f, const std::function<fla
     flashloop_status_t st = FLASHLOOP_OK;
     if (f.key_rank != FLASHLOOP_KEYS_BY_MASS && f.key_rank != FLASHLOOP_KEYS_BY_MASS_PER_ROW)
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "bad key_rank %d", f.key_rank);
+    if (dm.R > f.n || dm.K > f.n)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "R=%d and K=%d must not exceed the %d tokens in the cache", dm.R, dm.K,
+                         f.n);
     if (!f.forced && (!aligned16(f.h_prev) || !aligned16(f.h_cur) || (dm.H * dm.d) % 8))
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "hidden states must be 16-byte aligned rows");
     {   // this loop's delta layer starts empty; cleared first so that the append
@@ -765,6 +768,9 @@ flashloop_status_t flashloop_loop_step(const flashloop_step_args_t *a, flashloop
     }
     if (!a->h_prev || !a->h_cur || !a->active_idx || !a->key_idx)
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "lazy loop needs h_prev, h_cur, active_idx and key_idx");
+    if (dm.R > n || dm.K > n)
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "R=%d and K=%d must not exceed the %d tokens in the cache", dm.R,
+                         dm.K, n);
     LazyFront f;
     f.c = c; f.loop = l; f.n = n;
     f.h_prev = a->h_prev; f.h_cur = a->h_cur;
@@ -870,6 +876,9 @@ flashloop_status_t flashloop_block_loop(const flashloop_block_args_t *a, flashlo
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "lazy loop needs active_idx, key_idx and h_prev");
     if (!dense && a->stale_idx && (a->n_stale < 0 || a->n_stale > n))
         return set_error(FLASHLOOP_ERR_INVALID_ARG, "n_stale=%d outside [0, %d]", a->n_stale, n);
+    if (!dense && (dm.R > n || dm.K > n))
+        return set_error(FLASHLOOP_ERR_INVALID_ARG, "R=%d and K=%d must not exceed the %d tokens in the cache", dm.R,
+                         dm.K, n);
     uint8_t *ws = static_cast<uint8_t *>(a->workspace);
     uint16_t *q = a->q ? a->q : reinterpret_cast<uint16_t *>(ws + BW.q),
              *k = a->k ? a->k : reinterpret_cast<uint16_t *>(ws + BW.k),

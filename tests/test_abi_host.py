@@ -314,3 +314,28 @@ def test_block_sizes_and_rejects(L):
     wt.F = 1024
     a.h_prev = None
     assert L.flashloop_block_loop(ctypes.byref(a), None) == INVALID           # lazy loop without h_prev
+
+
+def test_lazy_loop_needs_r_and_k_within_the_tokens(L):
+    """A lazy prefill loop whose R or K exceeds the cache's token count is refused
+    on the host (the selections would have fewer candidates than picks)."""
+    dm = dims(H=4, d=64)                       # R = 256, K = 103
+    c = fake_cache(dm)
+    c.n_tokens = 200                           # fewer tokens than R
+    ws = fl.flashloop_block_workspace_bytes(dm, 1024)
+    wt = fl.BlockWeights(P(0x1000), P(0x2000), P(0x3000), P(0x4000), 1024)
+    a = fl.BlockArgs()
+    a.loop, a.cache, a.weights = 2, ctypes.pointer(c), ctypes.pointer(wt)
+    a.h_cur, a.h_out, a.h_prev = P(0x5000), P(0x9000), P(0x6000)
+    a.workspace, a.workspace_bytes = P(0x100000), ws
+    a.active_idx, a.key_idx = P(0x7000), P(0x8000)
+    assert L.flashloop_block_loop(ctypes.byref(a), None) == INVALID
+    assert b"must not exceed" in L.flashloop_last_error()
+    st = fl.StepArgs()
+    st.loop, st.cache = 2, ctypes.pointer(c)
+    st.h_prev, st.h_cur, st.q, st.k, st.v = P(0x5000), P(0x6000), P(0x7000), P(0x8000), P(0x9000)
+    st.q_hat, st.o, st.z, st.c = P(0xA000), P(0xB000), P(0xC000), P(0xD000)
+    st.active_idx, st.key_idx = P(0xE000), P(0xF000)
+    st.workspace, st.workspace_bytes = P(0x100000), fl.flashloop_workspace_bytes(dm)
+    assert L.flashloop_loop_step(ctypes.byref(st), None) == INVALID
+    assert b"must not exceed" in L.flashloop_last_error()
