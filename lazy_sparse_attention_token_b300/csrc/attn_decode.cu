@@ -15,7 +15,7 @@
 // In a CTA, 16 groups of 16 lanes walk the chunk, kU keys per group at a time.
 // Every delta layer's entry of every key of the chunk is looked up once, into
 // shared memory, for both passes; a step then loads its kU base rows and the
-// codes of two layers at a time together, with no dependent lookup in front.
+// codes of a layer together, with no dependent lookup in front.
 // Pass 1 keeps the chunk's old and new logits in shared memory; the row
 // statistics (old mass m, logsumexp lam) are merged across the cluster through
 // distributed shared memory; pass 2 accumulates u and w and updates the column
@@ -31,7 +31,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kGroups = kThreads / 16;
-constexpr int kU = 4;              // keys per group per step
+constexpr int kU = 2;              // keys per group per step
 constexpr int kMaxCluster = 8;
 constexpr int kKeysPerCta = 1024;  // a CTA per this many keys, up to kMaxCluster
 
@@ -109,9 +109,9 @@ struct DecKParams {
 // 8-float running value per key is live, not an old and a new copy. Every
 // layer's entry of every key of the chunk was looked up once into shared
 // memory (ents[m * chunk + t], t = the key's place in the chunk), so the codes
-// and scales of two layers at a time load together with no dependent lookup in
-// front of them.
-constexpr int kLayerPair = 2;
+// and scales of kLayerPair layers at a time load together with no dependent
+// lookup in front of them.
+constexpr int kLayerPair = 1;
 template <int D, class OnOld, class OnNew>
 __device__ __forceinline__ void visit_rec(const DeltaView &ov, const DeltaView &nv, bool is_v, long long b,
                                           const int (&j)[kU], const int (&tt)[kU], const int *ents, int chunk, int h,
@@ -164,10 +164,13 @@ __device__ __forceinline__ void visit_rec(const DeltaView &ov, const DeltaView &
 
 // One instantiation per mode, so that a mode's unused state (the old keys and
 // values of the first dense loop, the delta entries of a dense loop) takes no
-// registers: the first loop, a pure stream of K/V rows, then fits four CTAs per
-// SM and keeps twice the bytes in flight.
+// registers. Every mode runs five CTAs per SM (48 registers): the kernel waits on
+// gathers of scattered key rows, and on this part more resident warps with a few
+// spilled registers beat fewer warps with more keys in flight each (two keys per
+// group and one delta layer at a time, measured against four keys, two layers and
+// two CTAs per SM: the 64-sequence decode step 5.80 -> 4.37 ms).
 template <int D, int kMode>
-__global__ void __launch_bounds__(kThreads, kMode == FLASHLOOP_ATTN_FIRST_DENSE ? 4 : 2)
+__global__ void __launch_bounds__(kThreads, 5)
 decode_attention_kernel(const __grid_constant__ DecKParams p) {
     extern __shared__ float sm[];
     constexpr int CH = D / 8;
