@@ -164,15 +164,14 @@ __device__ __forceinline__ void visit_rec(const DeltaView &ov, const DeltaView &
 
 // One instantiation per mode, so that a mode's unused state (the old keys and
 // values of the first dense loop, the delta entries of a dense loop) takes no
-// registers. The modes that read two reconstructions run five CTAs per SM (48
-// registers): they wait on gathers of scattered key rows, and on this part more
-// resident warps with a few spilled registers beat fewer warps with more keys in
-// flight each (two keys per group and one delta layer at a time, measured against
-// four keys, two layers and two CTAs per SM: a lazy decode loop of 64 sequences
-// over a 16K context 1.10-1.68 ms -> 0.68-0.98 ms). The first loop, a plain stream
-// of K/V rows, keeps four (4.9 TB/s against 4.4 with five).
+// registers. Every mode runs five CTAs per SM (48 registers): the kernel waits on
+// gathers of scattered key rows, and on this part more resident warps with a few
+// spilled registers beat fewer warps with more keys in flight each (two keys per
+// group and one delta layer at a time, measured against four keys, two layers and
+// two CTAs per SM: the 64-sequence, 16K-context decode token step 5.80 -> 4.37 ms,
+// graph-replayed; four CTAs per SM for the first loop alone: 4.54 ms).
 template <int D, int kMode>
-__global__ void __launch_bounds__(kThreads, kMode == FLASHLOOP_ATTN_FIRST_DENSE ? 4 : 5)
+__global__ void __launch_bounds__(kThreads, 5)
 decode_attention_kernel(const __grid_constant__ DecKParams p) {
     extern __shared__ float sm[];
     constexpr int CH = D / 8;
