@@ -1052,23 +1052,24 @@ def cpu_baseline(w, R, K, gpu_state, budget_s=20.0, device=None, full_limit_s=60
     the oracle's thread scaling; sample figures are tokens of that sample per
     second, not a full step. If the complete step is predicted to exceed
     `full_limit_s` (and `force_full` is off), the sample stands in for it and
-    the line says so. The prediction separates the attention's cost per head
-    (reconstruction, key selection) from its cost per row, from two probes."""
+    the line says so. The prediction prices the rows from two probes that run
+    every head on a tenth and a fifth of the active rows."""
     import oracle
     oracle.build()
     inp = _oracle_inputs(w, w.H, device or _input_device())
     qh, o, z, c = gpu_state
     inp.update(qh1=oracle.bits(qh.contiguous()), o1=o.cpu().numpy(), z1=z.cpu().numpy(), c1=c.cpu().numpy())
-    # size the sample: one head, a share of the rows that takes about budget_s / 4. The
-    # probes take a quarter and a half of one head's rows, so that the difference that
-    # prices a row is large against the timing noise (small probes overestimated the
-    # complete 32K step fifteenfold)
-    probe, probe_sa = _oracle_step(w, R, K, inp, 1, 0.25)
-    probe2, probe2_sa = _oracle_step(w, R, K, inp, 1, 0.5)
-    per_row = max(0.0, ((probe2 - probe2_sa) - (probe - probe_sa)) / 0.25)      # one head, all rows
-    per_head = max(0.0, (probe - probe_sa) - 0.25 * per_row)                  # one head, no rows
-    predicted = min(probe_sa, probe2_sa) + w.H * (per_head + per_row)
-    frac = float(min(1.0, max(0.02, 0.25 * (budget_s / 4) / max(probe, 1e-3))))
+    # The complete step is predicted from two probes over every head and a tenth and a
+    # fifth of the active rows: the oracle parallelises over (sequence, head) pairs when
+    # there are enough of them and over rows otherwise, so a one-head probe runs in
+    # another mode than the complete step (it overestimated the 32K step fifteenfold).
+    probe, _ = _oracle_step(w, R, K, inp, w.H, 0.1)
+    probe2, _ = _oracle_step(w, R, K, inp, w.H, 0.2)
+    per_rows = max(0.0, (probe2 - probe) / 0.1)                  # every head, all rows
+    predicted = probe + 0.9 * per_rows
+    # the thread-scaling sample: one head, a share of the rows that takes about budget_s / 4
+    p1, _ = _oracle_step(w, R, K, inp, 1, 0.02)
+    frac = float(min(1.0, max(0.02, 0.02 * (budget_s / 4) / max(p1, 1e-3))))
     sample_all = _sample_on(w, R, K, inp, 1, frac)
     single = _sample_on(w, R, K, inp, 1, frac, threads=1)
     out = {"unit": "tokens/s", "cores": _omp_threads(), "kind": "oracle", "cpu_model": _cpu_model(),
