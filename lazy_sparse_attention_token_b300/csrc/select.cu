@@ -73,8 +73,10 @@ token_scores_kernel(const uint16_t *__restrict__ h_prev, const uint16_t *__restr
 // up to kTopkCluster CTAs (one row alone would otherwise run on a single SM;
 // with many rows, one CTA per row already fills the GPU): each
 // CTA histograms its own contiguous segment and adds the histogram into a
-// fresh one on cluster rank 0 (distributed shared memory); after one cluster
-// barrier every rank reads the merged histogram and takes the same digit. The
+// fresh one on every rank of the cluster (distributed shared memory: remote
+// additions that need no reply); after one cluster barrier every rank reads the
+// merged histogram from its own shared memory and takes the same digit (reading
+// one rank's copy remotely instead cost about 6 us per 32K-key selection). The
 // output order is rank order, then warp segments, so indices stay ascending.
 constexpr int kTopkCluster = 8;
 constexpr int kTopkClThreads = 512;
@@ -133,8 +135,8 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
     __shared__ uint32_t whist[kTopkClWarps][256];   // one histogram per warp: keys of similar
                                                     // magnitude share a digit, so a single
                                                     // histogram would serialise on one bin
-    __shared__ uint32_t g_hist[4][256];        // merged histograms, used on rank 0
-    __shared__ uint32_t cta_cnt[kTopkCluster][2];   // per-rank (greater, equal) counts, used on rank 0
+    __shared__ uint32_t g_hist[4][256];        // merged histograms: every rank adds its counts into every rank's
+    __shared__ uint32_t cta_cnt[kTopkCluster][2];   // every rank's (greater, equal) counts, on every rank
     __shared__ uint32_t s_prefix;
     __shared__ int s_kleft;
     __shared__ unsigned long long warp_tot[kTopkClWarps];
@@ -151,8 +153,7 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
     const int seg = ((n + (int)ncta - 1) / (int)ncta + 31) & ~31;
     const int lo = min(n, (int)rank * seg), hi = min(n, lo + seg), len = hi - lo;
 
-    if (rank == 0)
-        for (int i = tid; i < 4 * 256; i += kTopkClThreads) (&g_hist[0][0])[i] = 0u;
+    for (int i = tid; i < 4 * 256; i += kTopkClThreads) (&g_hist[0][0])[i] = 0u;
     if (tid == 0) {
         s_cta_max = 0u;
         s_row_max = 0u;
@@ -187,7 +188,8 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
             uint32_t tot = 0;
 #pragma unroll
             for (int w = 0; w < kTopkClWarps; ++w) tot += whist[w][tid];
-            if (tot != 0u) cl_red_add(cl_map(&g_hist[pass][tid], 0), tot);
+            if (tot != 0u)
+                for (uint32_t q = 0; q < ncta; ++q) cl_red_add(cl_map(&g_hist[pass][tid], q), tot);
         }
         if (pass == 0 && seq_exit && tid == 0 && len > 0) cl_red_max(cl_map(&s_row_max, 0), s_cta_max);
         cl_sync();
@@ -197,7 +199,7 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
             uint32_t c[8], local = 0;
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                c[t] = cl_ld(cl_map(&g_hist[pass][255 - 8 * lane - t], 0));
+                c[t] = g_hist[pass][255 - 8 * lane - t];
                 local += c[t];
             }
             uint32_t incl = local;
@@ -246,15 +248,17 @@ topk_cluster_kernel(const float *__restrict__ vals, int n, int k, int32_t *__res
     if (tid == 0) {
         unsigned long long tot = 0;
         for (int w = 0; w < kTopkClWarps; ++w) tot += warp_tot[w];
-        cl_st(cl_map(&cta_cnt[rank][0], 0), (uint32_t)(tot >> 32));
-        cl_st(cl_map(&cta_cnt[rank][1], 0), (uint32_t)(tot & 0xffffffffu));
+        for (uint32_t q = 0; q < ncta; ++q) {
+            cl_st(cl_map(&cta_cnt[rank][0], q), (uint32_t)(tot >> 32));
+            cl_st(cl_map(&cta_cnt[rank][1], q), (uint32_t)(tot & 0xffffffffu));
+        }
     }
     cl_sync();
     // keys before this CTA's segment (lower ranks), then before this warp's part
     uint32_t gt_run = 0, eq_run = 0;
     for (uint32_t q = 0; q < rank; ++q) {
-        gt_run += cl_ld(cl_map(&cta_cnt[q][0], 0));
-        eq_run += cl_ld(cl_map(&cta_cnt[q][1], 0));
+        gt_run += cta_cnt[q][0];
+        eq_run += cta_cnt[q][1];
     }
     for (int w = 0; w < warp; ++w) {
         gt_run += (uint32_t)(warp_tot[w] >> 32);
