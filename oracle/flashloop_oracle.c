@@ -35,7 +35,7 @@
  *       contiguous elements, scale = fp16_rne(amax / 7) (fp32 divide),
  *       code = rint_even(delta / scale) clamped to +-7, zero scale -> zero
  *       codes; element 2t in the low nibble of byte t.
- *   R6' narrower deltas (the survey's next steps; the page says quality drops
+ *   R6' narrower deltas (variants beyond the page's 4-bit setting; it says quality drops
  *       noticeably below 4 bits): the same quantiser with codes of `bits`
  *       bits, 2 <= bits <= 4: qmax = 2^(bits-1) - 1, scale =
  *       fp16_rne(amax / qmax), codes clamped to [-qmax, qmax]; element x of
@@ -48,7 +48,7 @@
  *       [-127, 127], zero scale -> zero codes; the base value is scale * code.
  *   R7  R = ceil(r N), K = ceil(k N), clamped to [1, N]; ties in every
  *       ranking go to the lower index; index lists ascending.
- *   R9  synthetic looped block around the step (the survey's next steps; the
+ *   R9  synthetic looped block around the step (an extension of the step; the
  *       page says a later loop recomputes only its active tokens but gives
  *       no block): with x = H_{l-1}[i], q, k, v = bf16(x W_q), bf16(x W_k),
  *       bf16(x W_v); O from the loop's attention; y = bf16(x + bf16(O) W_o);

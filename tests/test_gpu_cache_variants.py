@@ -1,4 +1,4 @@
-"""Cache variants (the survey's next steps; the rit.work page: "a compressed
+"""Cache variants (beyond the main setting; the rit.work page: "a compressed
 base plus a sequence of compressed deltas", 4-bit deltas in the main
 experiments, quality dropping at lower widths): delta codes of 3 and 2 bits
 and an int8 base, through the C ABI, against the oracle on the same inputs.

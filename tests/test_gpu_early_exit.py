@@ -1,4 +1,4 @@
-"""Early exit by state difference (the survey's next step; the recurrent-depth
+"""Early exit by state difference (beyond the main setting; the recurrent-depth
 overview page's per-sequence dynamic early exit): through flashloop_loop_step,
 a sequence whose largest token change score falls below the threshold stops
 looping, and is compared with the oracle's loop on the same inputs and sets."""

@@ -1,4 +1,4 @@
-"""Selection variants (the survey's next steps): key columns ranked by column
+"""Selection variants (beyond the main setting): key columns ranked by column
 mass per causal row, and the synthetic analogue of the rit.work page's "10% of
 the attention columns in a late loop recover more than 90% of the exact
 result" (section "Later loops change only part of the state"), measured on
