@@ -673,7 +673,7 @@ def other_workloads_leg(args, world, rank, local):
     """The other configurations of the same step, short runs (steps, warm-ups as
     listed), each measured like the main line (CUDA-graph replay, CUDA events,
     clocks sampled in the timed region), without its e2e, oracle or analysis
-    legs. A summary per workload."""
+    legs, on rank 0's GPU alone. A summary per workload."""
     import argparse as _ap
     out = {}
     for name, steps, warmup in OTHER_WORKLOADS:
@@ -681,7 +681,9 @@ def other_workloads_leg(args, world, rank, local):
         sub.workload, sub.steps, sub.warmup = name, steps, warmup
         sub.no_e2e = sub.no_cpu_baseline = sub.no_recovery = sub.no_block = True
         sub.no_workloads = True
-        d = native_decode(sub, world, rank, local) if name == "decode" else native(sub, world, rank, local)
+        # rank 0 alone runs these: a world of one, so that no collective waits for the
+        # other ranks (which have finished their line by then)
+        d = native_decode(sub, 1, 0, local) if name == "decode" else native(sub, 1, 0, local)
         rf = d["roofline"]
         out[name] = {"config": d["config"]["workload"], "steps": steps, "warmup": warmup,
                      "ms_per_step": d["ms_per_step"], "value": d["value"], "unit": d["unit"],
@@ -1157,6 +1159,7 @@ def main():
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist
+        barrier(world)   # rank 0's extra legs run alone; every rank leaves the group together
         dist.destroy_process_group()
 
 
