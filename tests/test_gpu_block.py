@@ -100,19 +100,20 @@ def test_gemm_matches_oracle(M, K, N, with_res, relu):
     assert_gemm(bits(c), want, gemm_bound(bits(a), bits(w), rb), f"gemm {M}x{K}x{N}", K)
 
 
-def test_gemm_split_and_scatter_to_token_rows():
+@pytest.mark.parametrize("n_split", [2, 3])
+def test_gemm_split_and_scatter_to_token_rows(n_split):
     B, R, n_rows, K, D = 2, 150, 400, 256, 256
     g = torch.Generator().manual_seed(17)
     rows = torch.stack([torch.sort(torch.randperm(n_rows, generator=g)[:R]).values for _ in range(B)]).int()
     a = _rand_bf16((B * R, K), 5)
-    w = _rand_bf16((3 * D, K), 6, 1.0 / 16)
+    w = _rand_bf16((n_split * D, K), 6, 1.0 / 16)
     sentinel = torch.tensor(0x7F7F, dtype=torch.int16).view(torch.bfloat16)
-    outs = [torch.full((B * n_rows, D), float(sentinel), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    outs = [torch.full((B * n_rows, D), float(sentinel), dtype=torch.bfloat16, device="cuda") for _ in range(n_split)]
     fl.flashloop_gemm(_dev(a), _dev(w), outs, c_rows=_dev(rows), rows_per_seq=R, seq_rows=n_rows)
     torch.cuda.synchronize()
-    want = ob.project(bits(a), bits(w)).reshape(B, R, 3, D)
-    bound = gemm_bound(bits(a), bits(w)).reshape(B, R, 3, D)
-    for s in range(3):
+    want = ob.project(bits(a), bits(w)).reshape(B, R, n_split, D)
+    bound = gemm_bound(bits(a), bits(w)).reshape(B, R, n_split, D)
+    for s in range(n_split):
         got = bits(outs[s]).reshape(B, n_rows, D)
         listed = np.zeros((B, n_rows), bool)
         for b in range(B):
@@ -171,6 +172,9 @@ def test_gemm_full_size_projection_sampled_rows():
 CONFIGS = {
     "tiny": dict(B=2, N=384, H=2, d=128, F=512, T=4, T_dense=1, R=96, K=77),
     "wide": dict(B=1, N=1024, H=16, d=128, F=8192, T=3, T_dense=1, R=160, K=103),
+    # a ragged sequence (not a multiple of the 128-row tiles), head dim 96, two dense
+    # loops (the second one attends with a previous state)
+    "ragged": dict(B=1, N=300, H=8, d=96, F=1024, T=4, T_dense=2, R=70, K=50),
 }
 # the 8K prefill workload's shapes (B=1, N=8192, H=16, d=128, T=4, r=25%,
 # k=10%) with F = 4D; the attention state is compared on 4 seeded heads
@@ -275,13 +279,29 @@ def _bf16_vals(b):
     return oracle.bf16_values(b)
 
 
-@pytest.mark.parametrize("name", ["tiny", "wide"])
+def assert_mostly_close(gpu, orc, atol, rtol, what, max_frac=1e-3, max_rel=5e-3):
+    """For a loop whose 4-bit codes come from K/V that each side rounded on its
+    own: a code on a rounding boundary may round either way (both correct) and
+    move a reconstructed element by a whole quantisation step, so a few
+    elements may leave the elementwise tolerance; the share of them and the
+    relative Frobenius error stay small."""
+    gpu = np.asarray(gpu, np.float64)
+    orc = np.asarray(orc, np.float64)
+    assert gpu.shape == orc.shape and np.all(np.isfinite(gpu)), what
+    err = np.abs(gpu - orc)
+    frac = float((err > atol + rtol * np.abs(orc)).mean())
+    rel = float(np.linalg.norm(err.ravel()) / np.linalg.norm(orc.ravel()))
+    assert frac <= max_frac, f"{what}: {frac:.2e} of the elements outside tolerance"
+    assert rel <= max_rel, f"{what}: relative Frobenius error {rel:.2e}"
+
+
+@pytest.mark.parametrize("name", ["tiny", "wide", "ragged"])
 def test_block_chain_independent(name):
-    # the dense loop and the first lazy loop, the oracle and the GPU each on
+    # the dense loops and the first lazy loop, the oracle and the GPU each on
     # their own from the same inputs (the lazy loop's selections are the
-    # oracle's, passed in): H_1 and the state after loop 1, then H_2. The
-    # state after the lazy loop is compared in the loop-by-loop test: its
-    # 4-bit codes come from K/V that the two sides round independently.
+    # oracle's, passed in): H of every dense loop and the state after them
+    # elementwise, then the first lazy loop's H (mostly close, see above). The
+    # state after the lazy loop is compared in the loop-by-loop test.
     cfg = CONFIGS[name]
     D, l2 = cfg["H"] * cfg["d"], cfg["T_dense"] + 1
     w = _weights(cfg, 100)
@@ -290,7 +310,8 @@ def test_block_chain_independent(name):
     g = GpuBlock(cfg, [_dev(t) for t in w], _dev(h0))
     for l in range(1, l2 + 1):
         g.run(l, forced=sel_o[l] if l > cfg["T_dense"] else None)
-        assert_close(_bf16_vals(g.hs[l]), _bf16_vals(hs_o[l]), H_ATOL, H_RTOL, f"{name}: H_{l}")
+        check = assert_close if l <= cfg["T_dense"] else assert_mostly_close
+        check(_bf16_vals(g.hs[l]), _bf16_vals(hs_o[l]), H_ATOL, H_RTOL, f"{name}: H_{l}")
         if l == cfg["T_dense"]:
             o = g.state()
             assert_close(o.o, st_o[l].o, O_ATOL, O_RTOL, f"{name}: O after loop {l}")
@@ -299,7 +320,7 @@ def test_block_chain_independent(name):
     assert fl.flashloop_device_status() == 0
 
 
-@pytest.mark.parametrize("name, key_rank", [("tiny", 0), ("tiny", 1), ("wide", 0), ("8k", 0)])
+@pytest.mark.parametrize("name, key_rank", [("tiny", 0), ("tiny", 1), ("wide", 0), ("ragged", 0), ("8k", 0)])
 def test_block_loop_by_loop(name, key_rank):
     # every loop with the GPU's own selections, each part against the oracle
     # started from the GPU's values before that part (the teacher forcing of
@@ -347,9 +368,18 @@ def test_block_loop_by_loop(name, key_rank):
         if A is None:
             st_o = dense_loop(l, q_g, k_g, v_g, oc, before, bh_mask=mask)
         else:
-            _, _, _, st_o, lk, lv = lazy_loop(l, h_prev, h_cur, q_g, k_g, v_g, oc, before, R, K, A=A, S=S,
-                                              bh_mask=mask)
+            # the append against the oracle's own (codes exact except at rounding
+            # boundaries), then the attention over the GPU's layers, as in the workload
+            # tests: a boundary code that rounded the other way would move a
+            # reconstructed element by a whole quantisation step
+            _, _, _, _, lk, lv = lazy_loop(l, h_prev, h_cur, q_g, k_g, v_g, oc, before, R, K, A=A, S=S,
+                                           bh_mask=mask)
             _check_layers(g.cache, l, lk, lv, oc, k_g, v_g, A, f"{name}: loop {l}")
+            og = g.oracle_cache(l + 1)   # the GPU's cache after this loop
+            qh, oo, zz, cc, _ = oracle.attention(False, A, A, q_g, before.qhat, before.o, before.z, before.c, S,
+                                                 og.rec(l - 1, "k"), og.rec(l - 1, "v"), og.rec(l, "k"),
+                                                 og.rec(l, "v"), bh_mask=mask)
+            st_o = OState(qh, oo, zz, cc)
         after = g.state()
         assert_close(after.o[:, :, hs], st_o.o[:, :, hs], O_ATOL, O_RTOL, f"{name}: O after loop {l}")
         assert_close(after.z[:, hs], st_o.z[:, hs], Z_ATOL, 0, f"{name}: Z after loop {l}")
