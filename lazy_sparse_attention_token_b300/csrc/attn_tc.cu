@@ -43,11 +43,23 @@
 // LSE. TMEM columns: S buffers [0,256), P buffers [256,384), accumulator
 // [384,384+d).
 //
+// CTAs run the (row tile, head) items heaviest first, one per SM. A lazy
+// loop's items are of nearly equal size (the keys it selects sit early, so
+// most row tiles see all of them), so the items past the last full wave
+// would keep a few SMs busy for a whole item while the rest idle. Those run
+// in a second launch, each split by key tiles over a cluster of up to four
+// CTAs: every part runs the three passes over its own tiles, the parts'
+// per-row (old mass, maximum, sum) are combined through distributed shared
+// memory before pass NEW (each CTA in the same rank order, so all hold the
+// same Z'), and rank 0 adds the parts' accumulators, in rank order, to O.
+//
 // Waiting threads sleep in a hinted try_wait instead of spinning. Every
 // mbarrier wait is bounded (one second unless the host shortens it); on
 // timeout the CTA records an error code, stops issuing work, waits (bounded,
 // one second) for its own copies and MMAs, frees TMEM and exits. A softmax
-// warp proceeds past a wait only when all of its lanes saw the phase.
+// warp proceeds past a wait only when all of its lanes saw the phase. The CTAs
+// of a split item meet at one cluster barrier after set-up and one before
+// exit, which every CTA reaches because every wait before it is bounded.
 #include <cudaTypedefs.h>
 #include <float.h>
 #include <mutex>
@@ -76,6 +88,7 @@ constexpr int kSBufs = 2;         // logits S: two buffers of 128 fp32 columns, 
 constexpr uint32_t kColP = 256;   // probabilities P: two buffers of 64 columns (128 bf16), [256, 384)
 constexpr uint32_t kColAcc = 384; // accumulator columns [384, 384 + d)
 constexpr int kStages = 5;        // K/V tile slots of the load ring
+constexpr int kMaxParts = 4;      // CTAs that may share one row tile (a cluster)
 static_assert(kSBufs == 2, "S and P buffers are indexed with a parity bit");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -104,12 +117,12 @@ constexpr int kFullBars = 2 * kStages;
 enum : int { BAR_FULL = 0, BAR_EMPTY = kFullBars, BAR_S_FULL = BAR_EMPTY + kStages, BAR_S_READ = BAR_S_FULL + 2,
              BAR_P_FULL = BAR_S_READ + 2, BAR_PV_DONE = BAR_P_FULL + 2, BAR_ACC = BAR_PV_DONE + 2,
              BAR_STATS = BAR_ACC + 1, BAR_Q_READY = BAR_STATS + 1, BAR_DRAIN = BAR_Q_READY + 1, BAR_ZN = BAR_DRAIN + 2,
-             BAR_EPI = BAR_ZN + 1, N_BARS = BAR_EPI + 1 };
+             BAR_EPI = BAR_ZN + 1, BAR_XSTAT = BAR_EPI + 1, BAR_XACC = BAR_XSTAT + 1, N_BARS = BAR_XACC + 1 };
 // landed barrier and its parity for ring position p
 __device__ __forceinline__ int full_bar_of(int p) { return BAR_FULL + p % kFullBars; }
 __device__ __forceinline__ uint32_t full_parity(int p) { return (uint32_t)(p / kFullBars) & 1u; }
 enum : int { ERR_EMPTY = 1, ERR_FULL = 2, ERR_S_READ = 5, ERR_S_FULL = 6, ERR_P_FULL = 7, ERR_PV_DONE = 8,
-             ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11, ERR_ZN = 12, ERR_EPI = 13 };
+             ERR_ACC = 9, ERR_STATS = 10, ERR_Q_READY = 11, ERR_ZN = 12, ERR_EPI = 13, ERR_XSTAT = 14, ERR_XACC = 15 };
 
 // Ring position of a pass's loads. A pass with PV products loads K(0), then
 // K(t+1) before V(t) for every t, and V(n-1) last (2n loads); pass LSE loads
@@ -125,7 +138,8 @@ struct Cfg {
     static constexpr int OFF_KV = TB;               // K/V ring
     static constexpr int OFF_X = OFF_KV + kStages * TB;   // row-statistics exchange: [groups][128][3] fp32
     static constexpr int OFF_ROW = OFF_X + kGroups * 128 * 3 * 4;   // per row: key count, old and new normaliser
-    static constexpr int OFF_BAR = OFF_ROW + 128 * 16;
+    static constexpr int OFF_XCL = OFF_ROW + 128 * 16;   // split items: [part][128] of (m, M, L, 0), written by every rank
+    static constexpr int OFF_BAR = OFF_XCL + kMaxParts * 128 * 16;
     // epilogue: the finished accumulator rows, parked in the (then idle) ring
     static constexpr int XS = D + 4;   // padded row stride in floats
     static_assert(128 * XS * 4 <= kStages * TB, "accumulator rows fit the ring");
@@ -145,6 +159,10 @@ struct KParams {
     float *o, *z, *c;
     float sl2;   // log2(e) / sqrt(d)
     const int32_t *seq_exit;   // [B] or NULL: a sequence flagged 1 has stopped looping
+    // Work item of CTA x: item_base + x / nparts in the heavy-first order (below).
+    // nparts > 1: a cluster of nparts CTAs shares one item, CTA rank p taking key
+    // tiles [p n / nparts, (p + 1) n / nparts) of its n.
+    int item_base, nparts;
 };
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -224,6 +242,60 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int co
     if (!mbar_test_wait(bar, parity)) wait_bar_slow(bar, parity, &never, code, kDrainLimitNs);
 }
 
+// ---- a row tile split over a cluster (distributed shared memory) ----
+// address of the same shared-memory location in cluster CTA `rank`
+__device__ __forceinline__ uint32_t cl_map(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+__device__ __forceinline__ void cl_st4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ float4 cl_ld4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+// arrival on an mbarrier of another CTA of the cluster, releasing this thread's
+// (and, cumulatively, what it has observed of its CTA's) shared-memory writes
+__device__ __forceinline__ void cl_mbar_arrive(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+// Bounded wait for a phase completed by arrivals from the cluster; acquires
+// at cluster scope, so that the arriving CTAs' writes are visible after it.
+__device__ __noinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code,
+                                              unsigned long long limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    const uint32_t hint = limit_ns < 20000ull ? (uint32_t)limit_ns : 20000u;
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
+            uint32_t done;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(done)
+                : "r"(bar), "r"(parity), "r"(hint)
+                : "memory");
+            if (done) return true;
+        }
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 >= limit_ns) {
+            *abort_flag = 1;
+            atomicCAS(&g_tc_error, 0, code);
+            return false;
+        }
+    }
+}
+
 // Byte offset of 16-byte chunk `ch` (8 bf16) of row r in a 128-row tile laid
 // out as 64-element atoms with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t swz_off(int r, int ch) {
@@ -233,20 +305,38 @@ __device__ __forceinline__ uint32_t swz_off(int r, int ch) {
 // Gathers the tile's query rows (qhat or q, [B, n_state, H, D] bf16) into the
 // swizzled query tile. The softmax threads (index st) take consecutive 16-byte
 // chunks, so a warp reads whole rows; rows past the tile's end are zero.
+// Thread st takes chunks st + 512 i (i < D / 32): chunk st % (D / 8) of rows
+// st / (D / 8) + (512 / (D / 8)) i. Their positions are loaded first thing in
+// the kernel (query_positions), as the head of the set-up's longest chain of
+// dependent loads.
+template <int D>
+struct QueryRows {
+    static constexpr int CPR = D / 8;                      // 16-byte chunks per row
+    static constexpr int N = BM * CPR / (32 * kSoftmaxWarps);
+    static_assert(N * 32 * kSoftmaxWarps == BM * CPR, "the gather covers the tile exactly");
+    int pos[N];                                            // -1: row outside the tile
+};
+template <int D>
+__device__ __forceinline__ void query_positions(QueryRows<D> &qr, int st, int rows, int row0, const int32_t *A) {
+#pragma unroll
+    for (int i = 0; i < QueryRows<D>::N; ++i) {
+        const int rr = (st + 32 * kSoftmaxWarps * i) / QueryRows<D>::CPR;
+        qr.pos[i] = rr >= rows ? -1 : A ? __ldg(A + rr) : row0 + rr;
+    }
+}
 template <int D>
 __device__ __forceinline__ void load_query_tile(uint8_t *tile, const uint16_t *src, int st, int b, int h, int H,
-                                                int n_state, int rows, int row0, const int32_t *A) {
-    constexpr int CPR = D / 8;   // 16-byte chunks per row
+                                                int n_state, const QueryRows<D> &qr) {
+    constexpr int CPR = QueryRows<D>::CPR;
     const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
     const uint64_t stream = l2_policy_evict_first();   // each query row is read by one row tile
-#pragma unroll 4
-    for (int c = st; c < BM * CPR; c += 32 * kSoftmaxWarps) {
+#pragma unroll
+    for (int i = 0; i < QueryRows<D>::N; ++i) {
+        const int c = st + 32 * kSoftmaxWarps * i;
         const int rr = c / CPR, ch = c - rr * CPR;
         uint4 val = make_uint4(0, 0, 0, 0);
-        if (rr < rows) {
-            const int pos = A ? __ldg(A + rr) : row0 + rr;
-            val = ld_global_v4_hint(s4 + (((long long)b * n_state + pos) * H + h) * CPR + ch, stream);
-        }
+        if (qr.pos[i] >= 0)
+            val = ld_global_v4_hint(s4 + (((long long)b * n_state + qr.pos[i]) * H + h) * CPR + ch, stream);
         *reinterpret_cast<uint4 *>(tile + swz_off(rr, ch)) = val;
     }
 }
@@ -317,8 +407,12 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     // Work grows with a row tile's last position (later rows see more keys), so the
     // linear CTA order runs every head's heaviest row tiles first and leaves the
     // lightest ones for the last, partial wave.
-    const int b = blockIdx.z, h = (int)(blockIdx.x % p.H);
-    const int rt = p.n_row_tiles - 1 - (int)(blockIdx.x / p.H);
+    // with a cluster of nparts CTAs along x, the CTA's rank in it is x % nparts
+    const bool split = p.nparts > 1;
+    const int part = (int)blockIdx.x % p.nparts;
+    const int item = p.item_base + (int)blockIdx.x / p.nparts;
+    const int b = blockIdx.z, h = item % p.H;
+    const int rt = p.n_row_tiles - 1 - item / p.H;
     const bool dense = p.mode != FLASHLOOP_ATTN_LAZY;
     const bool first = p.mode == FLASHLOOP_ATTN_FIRST_DENSE;
     const int row0 = rt * BM;
@@ -330,10 +424,22 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     // prefix of the list: row i sees the keys of S that are <= i, counted for
     // every lazy row before the launch.
     const int32_t *RC = dense ? nullptr : p.row_cnt + bh * p.R + row0;
+    // row positions first: the query gather and the per-row loads of the set-up depend on them
+    const bool is_sm = warp >= kFirstSoftmaxWarp;
+    const int st = (int)threadIdx.x - 32 * kFirstSoftmaxWarp;   // softmax thread index
+    const int r = (warp & 3) * 32 + lane;          // the row this thread loads and writes back
+    const bool row_ok = is_sm && r < rows;
+    const int pos = row_ok ? (dense ? row0 + r : __ldg(A + r)) : -1;
+    QueryRows<D> qrows;
+    if (is_sm) query_positions<D>(qrows, st, rows, row0, A);
     const int cnt = dense ? min(row0 + rows, p.n_keys) : __ldg(RC + rows - 1);   // last row
     const int cnt_min = dense ? min(row0 + 1, p.n_keys) : __ldg(RC);             // first row
-    const int n_tiles = (cnt + BN - 1) / BN;
-    if (n_tiles == 0) return;   // every row has an empty key set: state unchanged
+    const int n_all = (cnt + BN - 1) / BN;
+    if (n_all == 0) return;   // every row has an empty key set: state unchanged (the whole cluster)
+    // this CTA's key tiles [t0, t0 + n_tiles); a part may get none
+    const int t0 = part * n_all / p.nparts;
+    const int t_end = (part + 1) * n_all / p.nparts;
+    const int n_tiles = t_end - t0;
     const int ph0 = first ? PH_LSE : PH_OLD;
     const int total = (3 - ph0) * n_tiles;
     const int kcols = dense ? p.n_keys : p.K;
@@ -344,23 +450,27 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         for (int i = 0; i < N_BARS; ++i) {
             const bool many = (i >= BAR_S_READ && i < BAR_S_READ + kSBufs) || (i >= BAR_P_FULL && i < BAR_P_FULL + 2) ||
                               i == BAR_STATS || i == BAR_Q_READY || i == BAR_ZN || i == BAR_EPI;
-            mbar_init(bar(i), many ? (uint32_t)kSoftmaxWarps : 1u);
+            const uint32_t cnt_i = i == BAR_XSTAT ? 4u * (uint32_t)p.nparts   // the four group-0 warps of every part
+                                   : i == BAR_XACC ? (uint32_t)p.nparts                  // one arrival per part
+                                   : many ? (uint32_t)kSoftmaxWarps : 1u;
+            mbar_init(bar(i), cnt_i);
         }
         misc[1] = 0;
         mbar_fence_init();
     }
     __syncwarp();
+    // a split item: no CTA touches another's shared memory before every CTA of the
+    // cluster has initialised its barriers (the cluster's CTAs start together)
+    if (split) {
+        cl_arrive();
+        cl_wait();
+    }
     if (warp == 0) {
         tmem_alloc(sbase + C::OFF_MISC, kTmemCols);
         tmem_relinquish();
     }
-    const bool is_sm = warp >= kFirstSoftmaxWarp;
     // softmax group: columns [32 wg, 32 wg + 32) of a tile; its four warps cover the four lane quadrants
     const int wg = is_sm ? (warp - kFirstSoftmaxWarp) >> 2 : 0;
-    const int r = (warp & 3) * 32 + lane;          // the row this thread loads and writes back
-    const bool row_ok = is_sm && r < rows;
-    const int pos = row_ok ? (dense ? row0 + r : __ldg(A + r)) : -1;
-    const int st = (int)threadIdx.x - 32 * kFirstSoftmaxWarp;   // softmax thread index
     // The producer needs only the barriers, so it arrives on the set-up barrier
     // without waiting and starts the K/V copies while the other warps wait for
     // the query tile and the per-row values.
@@ -369,7 +479,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         named_bar_arrive(kSetupBar, kThreads);
     } else {
         if (is_sm) {   // pass OLD reads qhat; the first dense loop starts with q
-            load_query_tile<D>(smem + C::OFF_Q, first ? p.q : p.q_hat, st, b, h, p.H, p.n_state, rows, row0, A);
+            load_query_tile<D>(smem + C::OFF_Q, first ? p.q : p.q_hat, st, b, h, p.H, p.n_state, qrows);
             fence_proxy_async_smem();
             // the query tile is reloaded with q after pass OLD: fetch those rows into L2 now
             if (!first && row_ok && wg * 64 < D) {
@@ -406,14 +516,14 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 const uint32_t full = bar(full_bar_of(pos));
                 mbar_arrive_expect_tx(full, C::TB);
                 for (int a = 0; a < C::NA; ++a) {
-                    if (dense) tma_load_4d_hint(dst + a * kAtom, m, full, a * 64, h, t * BN, b, keep);
-                    else tma_load_4d_hint(dst + a * kAtom, m, full, a * 64, t * BN, h, b, keep);
+                    if (dense) tma_load_4d_hint(dst + a * kAtom, m, full, a * 64, h, (t0 + t) * BN, b, keep);
+                    else tma_load_4d_hint(dst + a * kAtom, m, full, a * 64, (t0 + t) * BN, h, b, keep);
                 }
                 ++pos;
                 return true;
             };
             bool ok = true;
-            for (int ph = ph0; ok && ph <= PH_NEW; ++ph) {
+            for (int ph = ph0; ok && n_tiles > 0 && ph <= PH_NEW; ++ph) {   // a part may have no key tile
                 if (ph == PH_LSE) {
                     for (int t = 0; ok && t < n_tiles; ++t) ok = load(false, ph, t);
                 } else {   // the order kv_pos_k / kv_pos_v describe
@@ -628,17 +738,17 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             float nz[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) nz[k] = -row_zo[rlo + 8 * k];
-            for (int t = 0; ok && t < n_tiles; ++t) ok = pv_tile(std::true_type{}, t, nz);
+            for (int t = t0; ok && t < t_end; ++t) ok = pv_tile(std::true_type{}, t, nz);
             if (ok) {
                 // pass OLD's products are all done (their S tiles were consumed):
                 // reload the query tile with this loop's q
-                load_query_tile<D>(smem + C::OFF_Q, p.q, st, b, h, p.H, p.n_state, rows, row0, A);
+                load_query_tile<D>(smem + C::OFF_Q, p.q, st, b, h, p.H, p.n_state, qrows);
                 fence_proxy_async_smem();
                 warp_arrive(bar(BAR_Q_READY), lane);
             }
         }
         // ---- pass LSE: online logsumexp of the new logits, per fragment row ----
-        for (int t = 0; ok && t < n_tiles; ++t) {
+        for (int t = t0; ok && t < t_end; ++t) {
             float v[32];
             if (!(ok = load_s(t, v))) break;
             ++g;
@@ -664,7 +774,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         // ---- merge the row statistics: Z' = lam - ln m ----
         if (ok) {
             // the epilogue reads this thread's part of its O row: fetch it into L2 now
-            if (row_ok && !first) {
+            if (row_ok && !first && part == 0) {
                 const float *orow = p.o + ((((long long)b * p.n_state + pos) * p.H + h) * D + wg * (D / kGroups));
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(orow));
             }
@@ -695,10 +805,9 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             warp_arrive(bar(BAR_STATS), lane);
             ok = wait_bar_all(bar(BAR_STATS), 0, abort_flag, ERR_STATS, wlimit);
             if (ok && wg == 0) {
-                // rows with an empty key set or no old mass keep their state (Z' = inf)
-                float zn = INFINITY;
+                // this CTA's old mass, maximum and sum of the row
+                float mx = 0.f, Mx = -INFINITY, Lx = 0.f;
                 if (r < rows) {
-                    float mx = 0.f, Mx = -INFINITY, Lx = 0.f;
 #pragma unroll
                     for (int k = 0; k < kGroups; ++k) {
                         mx += ex[(k * 128 + r) * 3 + 0];
@@ -708,9 +817,35 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
 #pragma unroll
                         for (int k = 0; k < kGroups; ++k)
                             Lx += ex[(k * 128 + r) * 3 + 2] * ex2((ex[(k * 128 + r) * 3 + 1] - Mx) * p.sl2);
-                        if (first) mx = 1.f;
-                        if (mx >= FLT_MIN) zn = Mx * p.sl2 + __log2f(Lx) - __log2f(mx);
                     }
+                }
+                if (split) {
+                    // publish them to every CTA of the cluster; each combines all parts
+                    // in rank order, so every part holds the same Z' bits
+                    const uint32_t xa = sbase + C::OFF_XCL + (uint32_t)(part * 128 + r) * 16u;
+                    for (int q = 0; q < p.nparts; ++q) cl_st4(cl_map(xa, (uint32_t)q), make_float4(mx, Mx, Lx, 0.f));
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int q = 0; q < p.nparts; ++q) cl_mbar_arrive(cl_map(bar(BAR_XSTAT), (uint32_t)q));
+                    ok = __all_sync(0xffffffffu, wait_bar_cluster(bar(BAR_XSTAT), 0, abort_flag, ERR_XSTAT, wlimit));
+                    if (ok) {
+                        const float4 *xc = reinterpret_cast<const float4 *>(smem + C::OFF_XCL);
+                        mx = 0.f;
+                        Mx = -INFINITY;
+                        Lx = 0.f;
+                        for (int q = 0; q < p.nparts; ++q) {
+                            mx += xc[q * 128 + r].x;
+                            Mx = fmaxf(Mx, xc[q * 128 + r].y);
+                        }
+                        if (Mx > -INFINITY)
+                            for (int q = 0; q < p.nparts; ++q) Lx += xc[q * 128 + r].z * ex2((xc[q * 128 + r].y - Mx) * p.sl2);
+                    }
+                }
+                // rows with an empty key set or no old mass keep their state (Z' = inf)
+                float zn = INFINITY;
+                if (r < rows && Mx > -INFINITY) {
+                    if (first) mx = 1.f;
+                    if (mx >= FLT_MIN) zn = Mx * p.sl2 + __log2f(Lx) - __log2f(mx);
                 }
                 row_zn[r] = zn;
             }
@@ -724,12 +859,33 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             float nz[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) nz[k] = -row_zn[rlo + 8 * k];
-            for (int t = 0; ok && t < n_tiles; ++t) ok = pv_tile(std::false_type{}, t, nz);
+            for (int t = t0; ok && t < t_end; ++t) ok = pv_tile(std::false_type{}, t, nz);
+        }
+        // Epilogue. Each warp walks whole rows so that O, Z and qhat move in full
+        // lines: first its O rows are loaded (they do not depend on the accumulator,
+        // so the loads overlap the last PV products); then every thread parks its
+        // accumulator row in shared memory (the ring is idle by then), and the rows
+        // are added to O and written back.
+        constexpr int RPW = BM / kSoftmaxWarps;   // rows per warp
+        const int sw = warp - kFirstSoftmaxWarp;
+        const uint64_t stream = l2_policy_evict_first();   // O and qhat rows are touched once
+        float4 ov[RPW];
+        long long srow[RPW];
+        bool upd[RPW];
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+            const int rr = sw + kSoftmaxWarps * i;
+            upd[i] = ok && part == 0 && rr < rows && row_zn[rr] < INFINITY;   // rank 0 writes a split item
+            srow[i] = upd[i] ? ((long long)b * p.n_state + row_pos_s[rr]) * p.H + h : 0;
+            ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (upd[i] && !first && lane < D / 4) {
+                const uint4 u = ld_global_v4_hint(reinterpret_cast<const float4 *>(p.o + srow[i] * D) + lane, stream);
+                ov[i] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                    __uint_as_float(u.w));
+            }
         }
         if (ok && wait_bar_all(bar(BAR_ACC), 0, abort_flag, ERR_ACC, wlimit)) {
             tc_fence_after();
-            // Epilogue. A thread's accumulator row goes to shared memory (the ring is idle
-            // now); then each warp walks whole rows so that O, Z and qhat move in full lines.
             constexpr int GD = D / kGroups;   // accumulator columns per group (16, 24 or 32)
             float *xo = reinterpret_cast<float *>(smem + C::OFF_KV);
             const uint32_t lane_base = (uint32_t)rq << 16;
@@ -738,31 +894,54 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 float av[8];
                 tmem_ld_32x32b_x8(tmem + lane_base + kColAcc + wg * GD + u, av);
                 tmem_wait_ld();
+                if (n_tiles == 0)   // a part without key tiles: no PV product wrote the accumulator
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) av[i] = 0.f;
                 float4 *dst = reinterpret_cast<float4 *>(xo + r * C::XS + wg * GD + u);
                 dst[0] = make_float4(av[0], av[1], av[2], av[3]);
                 dst[1] = make_float4(av[4], av[5], av[6], av[7]);
             }
             warp_arrive(bar(BAR_EPI), lane);
-            if (wait_bar_all(bar(BAR_EPI), 0, abort_flag, ERR_EPI, wlimit)) {
-                constexpr int RPW = BM / kSoftmaxWarps;   // rows per warp
-                const int sw = warp - kFirstSoftmaxWarp;
-                float4 ov[RPW];
-                long long srow[RPW];
-                bool upd[RPW];
-                const uint64_t stream = l2_policy_evict_first();   // O and qhat rows are touched once
-                // all of this warp's O loads first, then the updates
+            bool go = wait_bar_all(bar(BAR_EPI), 0, abort_flag, ERR_EPI, wlimit);
+            if (go && split) {   // rank 0 sums the parts' parked accumulators and writes the rows
+                if (st == 0) cl_mbar_arrive(cl_map(bar(BAR_XACC), 0u));
+                go = part == 0 &&
+                     __all_sync(0xffffffffu, wait_bar_cluster(bar(BAR_XACC), 0, abort_flag, ERR_XACC, wlimit));
+                if (go && lane < D / 4) {
+                    // the other parts' accumulators, added in rank order into the parked rows
+                    // (each thread to the elements it writes back below), two rows at a time
+                    // so that their remote loads are in flight together
 #pragma unroll
-                for (int i = 0; i < RPW; ++i) {
-                    const int rr = sw + kSoftmaxWarps * i;
-                    upd[i] = rr < rows && row_zn[rr] < INFINITY;
-                    srow[i] = upd[i] ? ((long long)b * p.n_state + row_pos_s[rr]) * p.H + h : 0;
-                    ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (upd[i] && !first && lane < D / 4) {
-                        const uint4 u = ld_global_v4_hint(reinterpret_cast<const float4 *>(p.o + srow[i] * D) + lane, stream);
-                        ov[i] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
-                                            __uint_as_float(u.w));
+                    for (int i = 0; i < RPW; i += 2) {
+                        float4 rb[2][kMaxParts - 1];
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const int rr = sw + kSoftmaxWarps * (i + j);
+                            const uint32_t xa = smem_u32(xo + rr * C::XS + 4 * lane);
+#pragma unroll
+                            for (int q = 1; q < kMaxParts; ++q)
+                                if (rr < rows && q < p.nparts) rb[j][q - 1] = cl_ld4(cl_map(xa, (uint32_t)q));
+                        }
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const int rr = sw + kSoftmaxWarps * (i + j);
+                            if (rr >= rows) continue;
+                            float4 *own = reinterpret_cast<float4 *>(xo + rr * C::XS) + lane;
+                            float4 a4 = *own;
+#pragma unroll
+                            for (int q = 1; q < kMaxParts; ++q)
+                                if (q < p.nparts) {
+                                    a4.x += rb[j][q - 1].x;
+                                    a4.y += rb[j][q - 1].y;
+                                    a4.z += rb[j][q - 1].z;
+                                    a4.w += rb[j][q - 1].w;
+                                }
+                            *own = a4;
+                        }
                     }
                 }
+            }
+            if (go) {
 #pragma unroll
                 for (int i = 0; i < RPW; ++i) {
                     if (!upd[i]) continue;
@@ -794,6 +973,12 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(misc[0], kTmemCols);
+    }
+    // a split item: no CTA exits while another may still read its shared memory.
+    // Every wait above is bounded, so every CTA of the cluster gets here.
+    if (split) {
+        cl_arrive();
+        cl_wait();
     }
 }
 
@@ -871,13 +1056,59 @@ cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
     kp.c = p.c;
     kp.sl2 = kLog2e / sqrtf((float)D);
     kp.seq_exit = p.seq_exit;
-    dim3 grid(kp.n_row_tiles * p.H, 1, p.B);
+    kp.item_base = 0;
+    kp.nparts = 1;
     if (!dense && !p.row_cnt) return cudaErrorInvalidValue;
+    // One CTA per (row tile, head) item and sequence, one CTA per SM. Lazy items
+    // are of nearly equal size (the selected keys sit early, so most row tiles
+    // see all of them), and the items past the last full wave would leave the
+    // other SMs idle for a whole item: those go to a second launch that splits
+    // each over a cluster of up to four CTAs by key tiles.
+    const int X = kp.n_row_tiles * p.H;
+    int tail_x = 0, parts = 1;
+    if (!dense) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        static int sms[kMaxDevices];
+        if (sms[dev] == 0 && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaErrorInvalidDevice;
+        const long long total = (long long)X * p.B, rem = total % sms[dev];
+        if (total >= sms[dev] && rem > 0) {
+            tail_x = (int)((rem + p.B - 1) / p.B);
+            parts = (int)std::min<long long>(kMaxParts, sms[dev] / ((long long)tail_x * p.B));
+            if (parts < 2) tail_x = 0, parts = 1;
+        }
+    }
     {
         KernelTimer kt("tc_attention", s);
-        const cudaError_t e = launch_pdl(tc_attention_kernel<D>, grid, dim3(kThreads), (size_t)Cf::SMEM, s, kp,
-                                         maps[0], maps[1], maps[2], maps[3]);
-        if (e != cudaSuccess) return e;
+        if (X - tail_x > 0) {
+            const cudaError_t e = launch_pdl(tc_attention_kernel<D>, dim3(X - tail_x, 1, p.B), dim3(kThreads),
+                                             (size_t)Cf::SMEM, s, kp, maps[0], maps[1], maps[2], maps[3]);
+            if (e != cudaSuccess) return e;
+        }
+        if (tail_x > 0) {
+            KParams kt2 = kp;
+            kt2.item_base = X - tail_x;
+            kt2.nparts = parts;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(tail_x * parts, 1, p.B);
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = (size_t)Cf::SMEM;
+            cfg.stream = s;
+            cudaLaunchAttribute attr[2];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = (unsigned)parts;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 2;
+            const cudaError_t e =
+                cudaLaunchKernelEx(&cfg, tc_attention_kernel<D>, kt2, maps[0], maps[1], maps[2], maps[3]);
+            if (e != cudaSuccess) return e;
+            if (X - tail_x > 0) note_launch(1);   // the timer above counted one of the two
+        }
     }
     return cudaGetLastError();
 }

@@ -249,7 +249,10 @@ def test_first_dense_attention(B, N, H, d):
 
 
 @pytest.mark.parametrize("B,N,H,d,R,K", [(1, 300, 2, 64, 77, 41), (2, 520, 2, 96, 130, 200), (1, 700, 3, 128, 300, 129),
-                                         (1, 256, 2, 128, 256, 256), (1, 300, 1, 128, 5, 300)])
+                                         (1, 256, 2, 128, 256, 256), (1, 300, 1, 128, 5, 300),
+                                         # more (row tile, head) items than SMs: the items past the last full
+                                         # wave are split over clusters by key tiles (some parts get none)
+                                         (1, 2048, 16, 128, 1280, 600), (2, 1024, 16, 64, 640, 90)])
 def test_lazy_attention(B, N, H, d, R, K):
     dm, cache, st, q1, k1, v1 = _setup_first(B, N, H, d, 200)
     dm2 = fl.make_dims(B, N, H, d, R, K, 2, 1, R_cap=R)
