@@ -324,6 +324,26 @@ __device__ __forceinline__ void query_positions(QueryRows<D> &qr, int st, int ro
         qr.pos[i] = rr >= rows ? -1 : A ? __ldg(A + rr) : row0 + rr;
     }
 }
+// The same gather as 16-byte asynchronous copies (no registers held; rows
+// outside the tile are zero-filled): completed by cp.async.wait_all.
+template <int D>
+__device__ __forceinline__ void load_query_tile_async(uint8_t *tile, const uint16_t *src, int st, int b, int h,
+                                                      int H, int n_state, const QueryRows<D> &qr) {
+    constexpr int CPR = QueryRows<D>::CPR;
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+    for (int i = 0; i < QueryRows<D>::N; ++i) {
+        const int c = st + 32 * kSoftmaxWarps * i;
+        const int rr = c / CPR, ch = c - rr * CPR;
+        const bool in = qr.pos[i] >= 0;
+        const uint4 *g = in ? s4 + (((long long)b * n_state + qr.pos[i]) * H + h) * CPR + ch : s4;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(tile + swz_off(rr, ch))), "l"(g),
+                     "r"(in ? 16 : 0)
+                     : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 template <int D>
 __device__ __forceinline__ void load_query_tile(uint8_t *tile, const uint16_t *src, int st, int b, int h, int H,
                                                 int n_state, const QueryRows<D> &qr) {
@@ -432,6 +452,12 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const int pos = row_ok ? (dense ? row0 + r : __ldg(A + r)) : -1;
     QueryRows<D> qrows;
     if (is_sm) query_positions<D>(qrows, st, rows, row0, A);
+    // softmax group: columns [32 wg, 32 wg + 32) of a tile; its four warps cover the four lane quadrants
+    const int wg = is_sm ? (warp - kFirstSoftmaxWarp) >> 2 : 0;
+    // the row's key count and old normaliser (group 0 keeps them in shared memory), issued with the gather
+    const bool row_vals = row_ok && wg == 0;
+    const int rc_r = row_vals && !dense ? __ldg(RC + r) : 0;
+    const float z_r = row_vals && !(p.mode == FLASHLOOP_ATTN_FIRST_DENSE) ? __ldg(p.z + bh * p.n_state + pos) : 0.f;
     const int cnt = dense ? min(row0 + rows, p.n_keys) : __ldg(RC + rows - 1);   // last row
     const int cnt_min = dense ? min(row0 + 1, p.n_keys) : __ldg(RC);             // first row
     const int n_all = (cnt + BN - 1) / BN;
@@ -469,8 +495,6 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         tmem_alloc(sbase + C::OFF_MISC, kTmemCols);
         tmem_relinquish();
     }
-    // softmax group: columns [32 wg, 32 wg + 32) of a tile; its four warps cover the four lane quadrants
-    const int wg = is_sm ? (warp - kFirstSoftmaxWarp) >> 2 : 0;
     // The producer needs only the barriers, so it arrives on the set-up barrier
     // without waiting and starts the K/V copies while the other warps wait for
     // the query tile and the per-row values.
@@ -487,8 +511,8 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow));
             }
             if (wg == 0) {   // per row, shared by the four groups: key count and old normaliser (log2 units)
-                row_cnt[r] = !row_ok ? 0 : cnt_min == cnt ? cnt : dense ? min(pos + 1, p.n_keys) : __ldg(RC + r);
-                row_zo[r] = !row_ok ? INFINITY : first ? 0.f : __ldg(p.z + bh * p.n_state + pos) * kLog2e;
+                row_cnt[r] = !row_ok ? 0 : cnt_min == cnt ? cnt : dense ? min(pos + 1, p.n_keys) : rc_r;
+                row_zo[r] = !row_ok ? INFINITY : first ? 0.f : z_r * kLog2e;
                 row_pos_s[r] = pos;
             }
         }
@@ -738,11 +762,19 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             float nz[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) nz[k] = -row_zo[rlo + 8 * k];
-            for (int t = t0; ok && t < t_end; ++t) ok = pv_tile(std::true_type{}, t, nz);
+            for (int t = t0; ok && t < t_end; ++t) {
+                if (t == t_end - 1) {
+                    // Once the last tile's logits are ready, every QK product of pass OLD
+                    // (one issuing thread, completed in order) has read the query tile:
+                    // start reloading it with this loop's q under the tile's softmax.
+                    ok = wait_bar_all(bar(BAR_S_FULL + (g & 1)), (g >> 1) & 1, abort_flag, ERR_S_FULL, wlimit);
+                    if (ok) load_query_tile_async<D>(smem + C::OFF_Q, p.q, st, b, h, p.H, p.n_state, qrows);
+                }
+                if (ok) ok = pv_tile(std::true_type{}, t, nz);
+            }
+            if (ok && n_tiles == 0) load_query_tile_async<D>(smem + C::OFF_Q, p.q, st, b, h, p.H, p.n_state, qrows);
+            cp_async_wait_all();   // also after a failure: no copy stays in flight
             if (ok) {
-                // pass OLD's products are all done (their S tiles were consumed):
-                // reload the query tile with this loop's q
-                load_query_tile<D>(smem + C::OFF_Q, p.q, st, b, h, p.H, p.n_state, qrows);
                 fence_proxy_async_smem();
                 warp_arrive(bar(BAR_Q_READY), lane);
             }
