@@ -163,6 +163,9 @@ struct KParams {
     // nparts > 1: a cluster of nparts CTAs shares one item, CTA rank p taking key
     // tiles [p n / nparts, (p + 1) n / nparts) of its n.
     int item_base, nparts;
+    // 1: this grid follows the split launch of the same loop, which it does not
+    // depend on: it waits for that grid only before its CTAs exit (see below)
+    int late_wait;
 };
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -406,10 +409,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ CUtensorMap tm_k_old,
                     const __grid_constant__ CUtensorMap tm_v_old, const __grid_constant__ CUtensorMap tm_k_new,
                     const __grid_constant__ CUtensorMap tm_v_new) {
-    pdl_wait();   // every global read below depends on the previous kernel
+    // Every global read below depends on the kernels before this launch. A grid
+    // that follows the split launch starts without waiting: that launch issued
+    // its dependent launch only after all of its CTAs had waited for those
+    // kernels, so their writes are visible here; and waiting for it before
+    // exiting keeps the next kernel's dependency on this grid covering both.
+    if (!p.late_wait) pdl_wait();
     pdl_trigger();
     const unsigned long long wlimit = g_tc_wait_limit_ns;
-    if (p.seq_exit && __ldg(p.seq_exit + blockIdx.z)) return;   // the whole CTA: its sequence stopped looping
+    if (p.seq_exit && __ldg(p.seq_exit + blockIdx.z)) {   // the whole CTA: its sequence stopped looping
+        if (p.late_wait) pdl_wait();
+        return;
+    }
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -461,7 +472,10 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
     const int cnt = dense ? min(row0 + rows, p.n_keys) : __ldg(RC + rows - 1);   // last row
     const int cnt_min = dense ? min(row0 + 1, p.n_keys) : __ldg(RC);             // first row
     const int n_all = (cnt + BN - 1) / BN;
-    if (n_all == 0) return;   // every row has an empty key set: state unchanged (the whole cluster)
+    if (n_all == 0) {   // every row has an empty key set: state unchanged (the whole cluster)
+        if (p.late_wait) pdl_wait();
+        return;
+    }
     // this CTA's key tiles [t0, t0 + n_tiles); a part may get none
     const int t0 = part * n_all / p.nparts;
     const int t_end = (part + 1) * n_all / p.nparts;
@@ -1012,6 +1026,7 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         cl_arrive();
         cl_wait();
     }
+    if (p.late_wait) pdl_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -1090,6 +1105,7 @@ cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
     kp.seq_exit = p.seq_exit;
     kp.item_base = 0;
     kp.nparts = 1;
+    kp.late_wait = 0;
     if (!dense && !p.row_cnt) return cudaErrorInvalidValue;
     // One CTA per (row tile, head) item and sequence, one CTA per SM. Lazy items
     // are of nearly equal size (the selected keys sit early, so most row tiles
@@ -1112,12 +1128,10 @@ cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
         }
     }
     {
+        // The split items go first, on an otherwise idle GPU; the main grid follows
+        // without waiting for them and fills the SMs they leave free.
         KernelTimer kt("tc_attention", s);
-        if (X - tail_x > 0) {
-            const cudaError_t e = launch_pdl(tc_attention_kernel<D>, dim3(X - tail_x, 1, p.B), dim3(kThreads),
-                                             (size_t)Cf::SMEM, s, kp, maps[0], maps[1], maps[2], maps[3]);
-            if (e != cudaSuccess) return e;
-        }
+        kp.late_wait = 0;
         if (tail_x > 0) {
             KParams kt2 = kp;
             kt2.item_base = X - tail_x;
@@ -1139,7 +1153,13 @@ cudaError_t launch_d(const TcAttnParams &p, cudaStream_t s) {
             const cudaError_t e =
                 cudaLaunchKernelEx(&cfg, tc_attention_kernel<D>, kt2, maps[0], maps[1], maps[2], maps[3]);
             if (e != cudaSuccess) return e;
-            if (X - tail_x > 0) note_launch(1);   // the timer above counted one of the two
+            kp.late_wait = 1;
+        }
+        if (X - tail_x > 0) {
+            const cudaError_t e = launch_pdl(tc_attention_kernel<D>, dim3(X - tail_x, 1, p.B), dim3(kThreads),
+                                             (size_t)Cf::SMEM, s, kp, maps[0], maps[1], maps[2], maps[3]);
+            if (e != cudaSuccess) return e;
+            if (tail_x > 0) note_launch(1);   // the timer above counted one of the two
         }
     }
     return cudaGetLastError();
