@@ -287,9 +287,8 @@ def test_lazy_attention(B, N, H, d, R, K):
     np.testing.assert_allclose(f32(st.c).sum(-1), N, rtol=1e-4)
 
 
-def _lazy_case(seed):
-    """A small lazy attention call (two row tiles, two key tiles) and its oracle."""
-    B, N, H, d, R, K = 1, 520, 2, 128, 200, 150
+def _lazy_case(seed, B=1, N=520, H=2, d=128, R=200, K=150):
+    """A lazy attention call (by default small: two row tiles, two key tiles) and its inputs."""
     dm, cache, st, q1, k1, v1 = _setup_first(B, N, H, d, seed)
     dm2 = fl.make_dims(B, N, H, d, R, K, 2, 1, R_cap=R)
     cache2 = fl.Cache(dm2)
@@ -297,7 +296,8 @@ def _lazy_case(seed):
     fl.flashloop_kv_dense_store(cache2, 1, k1, v1)
     q2, k2, v2 = ((x.float() + 0.3 * torch.randn(x.shape, generator=gen(seed + 10 + i), device="cuda")).to(torch.bfloat16)
                   for i, x in enumerate((q1, k1, v1)))
-    A = torch.sort(torch.randperm(N, generator=gen(seed + 20), device="cuda")[:R]).values.to(torch.int32)[None]
+    A = torch.stack([torch.sort(torch.randperm(N, generator=gen(seed + 20 + b), device="cuda")[:R]).values
+                     for b in range(B)]).to(torch.int32)
     fl.flashloop_kv_delta_append(cache2, 2, k2, v2, A)
     S = fl.flashloop_select_keys(st.c, K)
     torch.cuda.synchronize()
@@ -337,6 +337,43 @@ def test_bounded_wait_gives_up_and_the_context_recovers():
     a, s_ = A.cpu().numpy(), S.cpu().numpy()
     qh, o, z, c, _ = oracle.attention(False, a, a, bits(q2), *before, s_, base_k, base_v, kn, vn)
     assert_close(f32(st.o), o, O_ATOL, O_RTOL, "O after recovery")
+    assert_close(f32(st.c), c, C_ATOL, C_RTOL, "c after recovery")
+
+
+def test_bounded_wait_gives_up_on_split_items():
+    """The same failure path with more (row tile, head) items than SMs, so that the
+    items past the last full wave run split over clusters, whose CTAs also wait on
+    one another (bounded, like every other wait) and meet at two cluster barriers
+    that every CTA reaches. The launch completes and reports a wait code; with the
+    limit restored the same call on fresh state matches the oracle."""
+    case = dict(B=1, N=2048, H=16, d=128, R=1280, K=600)
+    dm2, cache2, st, q2, A, S = _lazy_case(510, **case)
+    ws = fl.workspace_for(dm2)
+    assert fl.flashloop_device_status() == 0
+    fl.flashloop_set_wait_limit_ns(0)
+    try:
+        fl.flashloop_lazy_attention(cache2, fl.LAZY, 2, q2, st.q_hat, st.o, st.z, st.c, row_pos=A, key_idx=S,
+                                    workspace=ws)
+        torch.cuda.synchronize()                    # the launches returned
+        word = fl.flashloop_device_status()
+    finally:
+        fl.flashloop_set_wait_limit_ns(fl.flashloop.WAIT_LIMIT_DEFAULT_NS)
+    assert word in (1, 2, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15), word
+    assert fl.flashloop_device_status() == 0
+    dm2, cache2, st, q2, A, S = _lazy_case(510, **case)
+    before = (bits(st.q_hat), f32(st.o), f32(st.z), f32(st.c))
+    fl.flashloop_lazy_attention(cache2, fl.LAZY, 2, q2, st.q_hat, st.o, st.z, st.c, row_pos=A, key_idx=S,
+                                workspace=fl.workspace_for(dm2))
+    torch.cuda.synchronize()
+    assert fl.flashloop_device_status() == 0
+    base_k, base_v = (bits(t) for t in cache2.dense_layer(1))
+    lk, lv = layers_from_gpu(cache2, [2], [0])
+    kn = oracle.reconstruct(base_k, lk, want_f32=False)[1]
+    vn = oracle.reconstruct(base_v, lv, want_f32=False)[1]
+    a, s_ = A.cpu().numpy(), S.cpu().numpy()
+    qh, o, z, c, _ = oracle.attention(False, a, a, bits(q2), *before, s_, base_k, base_v, kn, vn)
+    assert_close(f32(st.o), o, O_ATOL, O_RTOL, "O after recovery")
+    assert_close(f32(st.z), z, Z_ATOL, 0, "Z after recovery")
     assert_close(f32(st.c), c, C_ATOL, C_RTOL, "c after recovery")
 
 
