@@ -443,7 +443,9 @@ flashloop_status_t flashloop_device_status(int32_t *word);
  * limit) and exit; the launch still completes and the context stays usable.
  * 0 <= ns <= FLASHLOOP_WAIT_LIMIT_DEFAULT_NS (the limit can only be
  * shortened; pass the default to restore it), else FLASHLOOP_ERR_INVALID_ARG.
- * Call it between launches: it SYNCHRONISES the current device. */
+ * With 0 a wait does not wait at all: it gives up unless its phase has
+ * already completed when first tested. Call it between launches: it
+ * SYNCHRONISES the current device. */
 flashloop_status_t flashloop_set_wait_limit_ns(uint64_t ns);
 
 /* Number of kernel launches this library has enqueued from the calling

@@ -206,6 +206,11 @@ __device__ __forceinline__ float ex2(float x) {
 // another role has given up, recording the first failure code.
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code,
                                            unsigned long long limit_ns) {
+    if (limit_ns == 0) {   // a zero limit: no waiting at all (the caller has tested the phase once)
+        *abort_flag = 1;
+        atomicCAS(&g_tc_error, 0, code);
+        return false;
+    }
     const uint64_t t0 = globaltimer_ns();
     const uint32_t hint = limit_ns < 20000ull ? (uint32_t)limit_ns : 20000u;
     for (;;) {
@@ -275,6 +280,20 @@ __device__ __forceinline__ void cl_mbar_arrive(uint32_t remote_bar) {
 // at cluster scope, so that the arriving CTAs' writes are visible after it.
 __device__ __noinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code,
                                               unsigned long long limit_ns) {
+    if (limit_ns == 0) {   // a zero limit: the phase is tested once, without waiting
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        *abort_flag = 1;
+        atomicCAS(&g_tc_error, 0, code);
+        return false;
+    }
     const uint64_t t0 = globaltimer_ns();
     const uint32_t hint = limit_ns < 20000ull ? (uint32_t)limit_ns : 20000u;
     for (;;) {
@@ -298,6 +317,69 @@ __device__ __noinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, vol
         }
     }
 }
+
+// ---- MMA issue from a whole (converged) warp: one elected lane issues ----
+// The issuing warps run their loops with all 32 lanes (so that the loop and
+// descriptor arithmetic is warp-uniform) and predicate each tcgen05 instruction
+// on one elected lane, always the same one (the lowest), which therefore also
+// commits: a commit tracks the MMAs of the thread that executes it.
+#define FL_EL "elect.sync _|e, 0xffffffff;\n\t"
+#define FL_MMA_SS_E(ai, bi, n, pr) "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %" #ai ", %" #bi ", %" #n ", " #pr ";\n\t"
+__device__ __forceinline__ void mma_ss_x8_el(uint32_t d_tmem, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                             uint32_t idesc, uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t" FL_EL
+        "setp.ne.b32 p, %18, 0;\n\t"
+        "setp.eq.b32 q, %17, %17;\n\t"
+        FL_MMA_SS_E(1, 9, 17, p) FL_MMA_SS_E(2, 10, 17, q) FL_MMA_SS_E(3, 11, 17, q) FL_MMA_SS_E(4, 12, 17, q)
+        FL_MMA_SS_E(5, 13, 17, q) FL_MMA_SS_E(6, 14, 17, q) FL_MMA_SS_E(7, 15, 17, q) FL_MMA_SS_E(8, 16, 17, q) "}"
+        ::"r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]),
+        "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc0)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ss_x4_el(uint32_t d_tmem, const uint64_t *a, const uint64_t *b, uint32_t idesc,
+                                             uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t" FL_EL
+        "setp.ne.b32 p, %10, 0;\n\t"
+        "setp.eq.b32 q, %9, %9;\n\t"
+        FL_MMA_SS_E(1, 5, 9, p) FL_MMA_SS_E(2, 6, 9, q) FL_MMA_SS_E(3, 7, 9, q) FL_MMA_SS_E(4, 8, 9, q) "}"
+        ::"r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+        "r"(idesc), "r"(acc0)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ss_x2_el(uint32_t d_tmem, const uint64_t *a, const uint64_t *b, uint32_t idesc,
+                                             uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t" FL_EL
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.eq.b32 q, %5, %5;\n\t"
+        FL_MMA_SS_E(1, 3, 5, p) FL_MMA_SS_E(2, 4, 5, q) "}"
+        ::"r"(d_tmem), "l"(a[0]), "l"(a[1]), "l"(b[0]), "l"(b[1]), "r"(idesc), "r"(acc0)
+        : "memory");
+}
+#define FL_MMA_TS_E(ai, bi, pr) "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%" #ai "], %" #bi ", %17, " #pr ";\n\t"
+__device__ __forceinline__ void mma_ts_x8_el(uint32_t d_tmem, const uint32_t (&a)[8], const uint64_t (&b)[8],
+                                             uint32_t idesc, uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t" FL_EL
+        "setp.ne.b32 p, %18, 0;\n\t"
+        "setp.eq.b32 q, %17, %17;\n\t"
+        FL_MMA_TS_E(1, 9, p) FL_MMA_TS_E(2, 10, q) FL_MMA_TS_E(3, 11, q) FL_MMA_TS_E(4, 12, q)
+        FL_MMA_TS_E(5, 13, q) FL_MMA_TS_E(6, 14, q) FL_MMA_TS_E(7, 15, q) FL_MMA_TS_E(8, 16, q) "}"
+        ::"r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
+        "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc0)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_el(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t" FL_EL
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+#undef FL_MMA_TS_E
+#undef FL_MMA_SS_E
+#undef FL_EL
 
 // Byte offset of 16-byte chunk `ch` (8 bf16) of row r in a 128-row tile laid
 // out as 64-element atoms with the 128-byte swizzle.
@@ -582,8 +664,9 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
         // products (no PV there) are split by tile parity between the two: the tensor
         // pipe buffers only about two MMAs, and each issuer's barrier tests between
         // its batches are covered by the other's MMAs. Tile g's logits go to S buffer
-        // g & 1, so each buffer of pass LSE has a single issuer.
-        if (lane == 0) {
+        // g & 1, so each buffer of pass LSE has a single issuer. The whole warp runs
+        // the loop; one elected lane issues (see mma_ss_x8_el).
+        {
             constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false, false);
             constexpr uint32_t id_pv = idesc_bf16(128, D, false, true, false);       // A = P from TMEM
             constexpr uint32_t id_pv_neg = idesc_bf16(128, D, false, true, true);    // pass OLD subtracts
@@ -607,12 +690,13 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
             auto issue_qk = [&](int g) -> bool {
                 const int kp = g < lse0 ? kv_pos_k(g) : g < new0 ? base_lse + g - lse0 : base_new + kv_pos_k(g - new0);
                 const int ks = kp % kStages, sb = g & 1;
-                if (!wait_bar(bar(full_bar_of(kp)), full_parity(kp), abort_flag, ERR_FULL, wlimit)) return false;
+                if (!wait_bar_all(bar(full_bar_of(kp)), full_parity(kp), abort_flag, ERR_FULL, wlimit)) return false;
                 // the S buffer's previous tile has been read by the softmax
-                if (g >= kSBufs && !wait_bar(bar(BAR_S_READ + sb), ((g >> 1) - 1) & 1, abort_flag, ERR_S_READ, wlimit))
+                if (g >= kSBufs &&
+                    !wait_bar_all(bar(BAR_S_READ + sb), ((g >> 1) - 1) & 1, abort_flag, ERR_S_READ, wlimit))
                     return false;
                 if (g >= lse0 && !q_seen) {   // after pass OLD, once the query tile holds this loop's q
-                    if (!wait_bar(bar(BAR_Q_READY), 0, abort_flag, ERR_Q_READY, wlimit)) return false;
+                    if (!wait_bar_all(bar(BAR_Q_READY), 0, abort_flag, ERR_Q_READY, wlimit)) return false;
                     q_seen = true;
                 }
                 tc_fence_after();
@@ -622,13 +706,13 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 for (int kk = 0; kk < D / 16; ++kk) bk[kk] = dk + kstep_off(kk);
                 const uint32_t dst = tmem + 128u * (uint32_t)sb;
                 if constexpr (D == 128) {
-                    mma_bf16_ss_x8(dst, aq, bk, id_qk, 0u);
+                    mma_ss_x8_el(dst, aq, bk, id_qk, 0u);
                 } else {   // d = 64: one batch of four; d = 96: four, then two
-                    mma_bf16_ss_x4(dst, aq, bk, id_qk, 0u);
-                    if constexpr (D == 96) mma_bf16_ss_x2(dst, aq + 4, bk + 4, id_qk, 1u);
+                    mma_ss_x4_el(dst, aq, bk, id_qk, 0u);
+                    if constexpr (D == 96) mma_ss_x2_el(dst, aq + 4, bk + 4, id_qk, 1u);
                 }
-                mma_commit(bar(BAR_S_FULL + sb));
-                mma_commit(bar(BAR_EMPTY + ks));
+                mma_commit_el(bar(BAR_S_FULL + sb));
+                mma_commit_el(bar(BAR_EMPTY + ks));
                 return true;
             };
             // acc (+/-)= P V for the tile with PV index pv (P buffer pv & 1)
@@ -636,8 +720,9 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 const int pb = pv & 1;
                 const int vp = pv < n_old ? kv_pos_v(pv, n_tiles) : base_new + kv_pos_v(pv - n_old, n_tiles);
                 const int vs = vp % kStages;
-                if (!wait_bar(bar(full_bar_of(vp)), full_parity(vp), abort_flag, ERR_FULL, wlimit)) return false;
-                if (!wait_bar(bar(BAR_P_FULL + pb), (uint32_t)(pv >> 1) & 1u, abort_flag, ERR_P_FULL, wlimit)) return false;
+                if (!wait_bar_all(bar(full_bar_of(vp)), full_parity(vp), abort_flag, ERR_FULL, wlimit)) return false;
+                if (!wait_bar_all(bar(BAR_P_FULL + pb), (uint32_t)(pv >> 1) & 1u, abort_flag, ERR_P_FULL, wlimit))
+                    return false;
                 tc_fence_after();
                 const uint64_t dv = d_v + TB16 * (uint32_t)vs;
                 const uint32_t pa = tmem + kColP + 64u * (uint32_t)pb;
@@ -648,9 +733,9 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                     ap[kk] = pa + 8u * kk;
                     bv[kk] = dv + kk * 128;
                 }
-                mma_bf16_ts_x8(tmem + kColAcc, ap, bv, old ? id_pv_neg : id_pv, pv > 0 ? 1u : 0u);
-                mma_commit(bar(BAR_PV_DONE + pb));
-                mma_commit(bar(BAR_EMPTY + vs));
+                mma_ts_x8_el(tmem + kColAcc, ap, bv, old ? id_pv_neg : id_pv, pv > 0 ? 1u : 0u);
+                mma_commit_el(bar(BAR_PV_DONE + pb));
+                mma_commit_el(bar(BAR_EMPTY + vs));
                 return true;
             };
             bool ok = true;
@@ -664,10 +749,10 @@ tc_attention_kernel(const __grid_constant__ KParams p, const __grid_constant__ C
                 for (int g = lse0; ok && g < new0; ++g)
                     if ((g & 1) == 1) ok = issue_qk(g);
                 for (int t = 0; ok && t < n_tiles; ++t) ok = issue_pv(n_old + t, false);
-                if (ok) mma_commit(bar(BAR_ACC));
+                if (ok) mma_commit_el(bar(BAR_ACC));
             }
-            if (!ok) {   // drain whatever this thread issued before giving up
-                mma_commit(bar(BAR_DRAIN + (warp - 1)));
+            if (!ok) {   // drain whatever the warp's elected lane issued before giving up
+                mma_commit_el(bar(BAR_DRAIN + (warp - 1)));
                 drain_wait(bar(BAR_DRAIN + (warp - 1)), 0, ERR_ACC);
             }
         }

@@ -306,8 +306,9 @@ def _lazy_case(seed, B=1, N=520, H=2, d=128, R=200, K=150):
 
 def test_bounded_wait_gives_up_and_the_context_recovers():
     """Failure path of the attention kernel's bounded waits, made to run out on
-    purpose by shortening the limit to zero (nothing is withheld: every copy and
-    MMA is still issued and lands). The launch completes, the device status
+    purpose by setting the limit to zero (a wait then gives up unless its phase
+    has already completed; nothing is withheld, and every copy and MMA issued
+    before the give-up still lands). The launch completes, the device status
     reports the failure with one of the kernel's wait codes, and once the limit
     is restored the same call on fresh state matches the oracle."""
     dm2, cache2, st, q2, A, S = _lazy_case(500)
