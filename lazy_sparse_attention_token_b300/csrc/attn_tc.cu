@@ -231,9 +231,9 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volati
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int code,
                                          unsigned long long limit_ns) {
     if (mbar_test_wait(bar, parity)) return true;
-    // one hinted sleep inline (most waits end within it), the bounded loop out of line
-    if (limit_ns != 0 && mbar_try_wait_sleep(bar, parity, limit_ns < 20000ull ? (uint32_t)limit_ns : 20000u))
-        return true;
+    // one try_wait inline (it suspends for up to a hardware-chosen time, and most
+    // waits end within it), the bounded loop out of line
+    if (limit_ns != 0 && mbar_try_wait(bar, parity)) return true;
     return wait_bar_slow(bar, parity, abort_flag, code, limit_ns);
 }
 
