@@ -25,10 +25,12 @@
 // tile slots, in the order the products consume them (a pass with PV products
 // loads K(0), then K(t+1) before V(t); pass LSE loads keys only and so keeps
 // five key tiles in flight); warp 1 issues the QK
-// products and warp 2 the PV products (one thread each): the tensor pipe
-// buffers only about two MMAs, and a second issuing thread covers the
-// barrier tests the first makes between its batches. The QK issuer runs up
-// to two tiles ahead of the softmax. Warps 3..18 are four softmax groups of
+// products and warp 2 the PV products: the tensor pipe buffers only about two
+// MMAs, and a second issuer covers the barrier tests the first makes between
+// its batches. Each issuing warp runs its loop with all 32 lanes and one
+// elected lane issues (the arithmetic stays warp-uniform instead of taking
+// issue slots from the softmax warps on the same scheduler). The QK issuer
+// runs up to two tiles ahead of the softmax. Warps 3..18 are four softmax groups of
 // four warps, a group owning 32 of a tile's 128 columns and a warp owning one
 // 32-lane quadrant (32 rows) of TMEM.
 // A softmax thread holds 4 rows x 8 columns of its group's block (two
@@ -39,21 +41,26 @@
 // its A operand, so P never touches shared memory; pass OLD's subtraction is
 // the instruction descriptor's negate-A bit. Column masses are formed after
 // P has been handed over and added to c with one atomic per column and warp.
-// The query tile holds qhat for pass OLD and is reloaded with q before pass
-// LSE. TMEM columns: S buffers [0,256), P buffers [256,384), accumulator
+// The query tile holds qhat for pass OLD and is reloaded with q (asynchronous
+// copies issued under the last OLD tile's softmax) before pass LSE. TMEM columns: S buffers [0,256), P buffers [256,384), accumulator
 // [384,384+d).
 //
 // CTAs run the (row tile, head) items heaviest first, one per SM. A lazy
 // loop's items are of nearly equal size (the keys it selects sit early, so
 // most row tiles see all of them), so the items past the last full wave
 // would keep a few SMs busy for a whole item while the rest idle. Those run
-// in a second launch, each split by key tiles over a cluster of up to four
-// CTAs: every part runs the three passes over its own tiles, the parts'
+// in a launch of their own, each split by key tiles over a cluster of up to
+// four CTAs: every part runs the three passes over its own tiles, the parts'
 // per-row (old mass, maximum, sum) are combined through distributed shared
 // memory before pass NEW (each CTA in the same rank order, so all hold the
 // same Z'), and rank 0 adds the parts' accumulators, in rank order, to O.
+// That launch goes first; the main grid follows without waiting for it and
+// fills the SMs it leaves free (it waits for it only before its CTAs exit).
 //
-// Waiting threads sleep in a hinted try_wait instead of spinning. Every
+// A wait tests the phase, then makes one try_wait inline (the thread is
+// suspended until the phase completes or a hardware limit passes) before the
+// out-of-line loop of hinted try_waits: the call would otherwise sit on the
+// critical path of every hand-off. Every
 // mbarrier wait is bounded (one second unless the host shortens it); on
 // timeout the CTA records an error code, stops issuing work, waits (bounded,
 // one second) for its own copies and MMAs, frees TMEM and exits. A softmax
